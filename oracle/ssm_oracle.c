@@ -1,0 +1,147 @@
+/*
+ * ssm_oracle.c -- plain, sequential float64 reference for the Mamba selective
+ * scan and its single-token decode step.
+ *
+ * TEST INFRASTRUCTURE.  Only the tests, the smoke check and the benchmark's
+ * CPU-baseline leg load this library; the product path never does.  It shares
+ * no code with the CUDA path.  Every input is taken as the exact (already
+ * rounded) value the GPU reads, widened to double; everything is computed in
+ * double, in the order the equations are written, one channel at a time.
+ *
+ * What is computed, and where the pages state it:
+ *  - Discretisation: dA = exp(delta * A), dBu = delta * B * u
+ *      youngju.dev, "Mamba: Linear-Time Sequence Modeling with Selective State
+ *      Spaces 论文分析", section "解决方案：Kernel Fusion + Recomputation"
+ *      (selective_scan concept code: deltaA, deltaB_x); ai-lab.club
+ *      "机器学习基础算法", section "状态空间模型：连续系统的离散化".
+ *  - Recurrence h_t = dA_t * h_{t-1} + dBu_t from h = 0, readout with the
+ *      updated state y_t = sum_n C_{t,n} h_{t,n}: same concept code.
+ *  - Skip term D * u: d9bl.com "Mamba 深度解读", equation (1b) and section
+ *      "理解 SSM 矩阵"; ai-lab.club, discrete equations (y_k = C h_k + D x_k).
+ *  - Gate y * silu(z): youngju.dev, section "Mamba 模块架构" (the block's
+ *      forward multiplies the SSM output by F.silu(z)).
+ *  - delta = softplus(delta_raw + bias) when softplus_flag is set, else
+ *      delta_raw + bias: the pages show a biased delta projection (youngju.dev,
+ *      "Mamba 模块架构", dt_proj with bias=True) but no positivity map; the
+ *      softplus reading is the workload's statement of the problem.
+ *  - Decode: one step of the same recurrence on a carried state (ai-lab.club,
+ *      "核心优势": constant work per generated token).
+ * Readings where the pages are silent: D and the gate act on the output only
+ * (last_state is the pre-readout h); B and C are per (batch, time) and shared
+ * by every channel (concept code B.unsqueeze(2)); the state starts at zero.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* softplus(x) = log(1 + e^x), written so that neither branch overflows. */
+double oracle_softplus(double x) {
+  if (x > 0.0) return x + log1p(exp(-x));
+  return log1p(exp(x));
+}
+
+/* silu(z) = z * sigmoid(z) = z / (1 + e^-z). */
+static double oracle_silu(double z) { return z / (1.0 + exp(-z)); }
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+/* Step size for one element. */
+static double step_size(double delta_raw, const double* delta_bias, int64_t d, int softplus_flag) {
+  double x = delta_raw + (delta_bias ? delta_bias[d] : 0.0);
+  return softplus_flag ? oracle_softplus(x) : x;
+}
+
+/*
+ * Full-sequence forward.
+ * u, delta, z, y: [batch][L][d_inner]; B, C: [batch][L][d_state];
+ * A: [d_inner][d_state]; D, delta_bias: [d_inner]; last_state: [batch][d_inner][d_state].
+ * D, z, delta_bias, last_state may be NULL (no skip term, no gate, zero bias, not returned).
+ * Returns 0, or -1 for a bad argument.
+ */
+int oracle_scan_fwd(const double* u, const double* delta, const double* A, const double* B,
+                    const double* C, const double* D, const double* z,
+                    const double* delta_bias, int softplus_flag, double* y, double* last_state,
+                    int64_t batch, int64_t L, int64_t d_inner, int64_t d_state, int nthreads) {
+  if (batch < 0 || L < 0 || d_inner < 0 || d_state < 1) return -1;
+  if ((L > 0 && (!u || !delta || !B || !C || !y)) || !A) return -1;
+  if (nthreads < 1) nthreads = 1;
+  int64_t channels = batch * d_inner;
+  int bad = 0;
+#pragma omp parallel num_threads(nthreads)
+  {
+    double* h = (double*)malloc(sizeof(double) * (size_t)d_state);
+    if (!h) {
+#pragma omp atomic write
+      bad = 1;
+    }
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t ch = 0; ch < channels; ch++) {
+      if (!h) continue;
+      int64_t b = ch / d_inner, d = ch % d_inner;
+      for (int64_t n = 0; n < d_state; n++) h[n] = 0.0;
+      for (int64_t t = 0; t < L; t++) {
+        int64_t e = (b * L + t) * d_inner + d;        /* element (b, t, d) */
+        const double* Bt = B + (b * L + t) * d_state;  /* row B[b, t, :] */
+        const double* Ct = C + (b * L + t) * d_state;
+        double dt = step_size(delta[e], delta_bias, d, softplus_flag);
+        double s = 0.0;
+        for (int64_t n = 0; n < d_state; n++) {
+          double dA = exp(dt * A[d * d_state + n]);
+          double dBu = dt * Bt[n] * u[e];
+          h[n] = dA * h[n] + dBu;
+          s += Ct[n] * h[n];
+        }
+        if (D) s += D[d] * u[e];
+        if (z) s *= oracle_silu(z[e]);
+        y[e] = s;
+      }
+      if (last_state)
+        for (int64_t n = 0; n < d_state; n++) last_state[(b * d_inner + d) * d_state + n] = h[n];
+    }
+    free(h);
+  }
+  return bad ? -1 : 0;
+}
+
+/*
+ * One decode step on a carried state, updated in place.
+ * state: [batch][d_inner][d_state]; u, delta, z, y: [batch][d_inner];
+ * B, C: [batch][d_state]; A: [d_inner][d_state]; D, delta_bias: [d_inner].
+ */
+int oracle_state_update(double* state, const double* u, const double* delta, const double* A,
+                        const double* B, const double* C, const double* D, const double* z,
+                        double* y, const double* delta_bias, int softplus_flag, int64_t batch,
+                        int64_t d_inner, int64_t d_state, int nthreads) {
+  if (batch < 0 || d_inner < 0 || d_state < 1) return -1;
+  if (batch * d_inner > 0 && (!state || !u || !delta || !A || !B || !C || !y)) return -1;
+  if (nthreads < 1) nthreads = 1;
+  int64_t channels = batch * d_inner;
+#pragma omp parallel for num_threads(nthreads) schedule(static)
+  for (int64_t ch = 0; ch < channels; ch++) {
+    int64_t b = ch / d_inner, d = ch % d_inner;
+    double* h = state + ch * d_state;
+    const double* Bb = B + b * d_state;
+    const double* Cb = C + b * d_state;
+    double dt = step_size(delta[ch], delta_bias, d, softplus_flag);
+    double s = 0.0;
+    for (int64_t n = 0; n < d_state; n++) {
+      double dA = exp(dt * A[d * d_state + n]);
+      double dBu = dt * Bb[n] * u[ch];
+      h[n] = dA * h[n] + dBu;
+      s += Cb[n] * h[n];
+    }
+    if (D) s += D[d] * u[ch];
+    if (z) s *= oracle_silu(z[ch]);
+    y[ch] = s;
+  }
+  return 0;
+}

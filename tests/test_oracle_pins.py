@@ -1,0 +1,315 @@
+"""Pins for the float64 oracle, each against something other than the oracle
+itself: a worked expansion from the pages, brute-force unrolled sums, the LTI
+convolution closed form, exact special cases, associativity of the chunk
+composition, linearity, and high-precision softplus values.  CPU only."""
+import decimal
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+RNG = np.random.default_rng(12345)
+
+
+def _softplus_ref(x):
+    return math.log1p(math.exp(x)) if x <= 0 else x + math.log1p(math.exp(-x))
+
+
+def _rand_problem(batch=2, L=6, d_inner=3, d_state=3, gate=True, seed=0):
+    r = np.random.default_rng(seed)
+    p = dict(
+        u=r.normal(size=(batch, L, d_inner)),
+        delta=r.normal(scale=0.7, size=(batch, L, d_inner)),
+        A=-r.uniform(0.3, 2.5, size=(d_inner, d_state)),
+        B=r.normal(size=(batch, L, d_state)),
+        C=r.normal(size=(batch, L, d_state)),
+        D=r.normal(size=d_inner),
+        z=r.normal(size=(batch, L, d_inner)) if gate else None,
+        delta_bias=r.normal(scale=0.5, size=d_inner),
+    )
+    return p
+
+
+def _brute_force(p, softplus_flag=True):
+    """y_t = sum_{s<=t} sum_n C_{t,n} (prod_{s<k<=t} exp(dt_k A_n)) dt_s B_{s,n} u_s + D u_t,
+    times silu(z_t); last_state_n = the same inner sum at t = L-1 without C."""
+    u, A, B, C = p["u"], p["A"], p["B"], p["C"]
+    batch, L, d_inner = u.shape
+    d_state = A.shape[1]
+    dt = np.zeros_like(u)
+    for b in range(batch):
+        for t in range(L):
+            for d in range(d_inner):
+                x = p["delta"][b, t, d] + (p["delta_bias"][d] if p["delta_bias"] is not None else 0.0)
+                dt[b, t, d] = _softplus_ref(x) if softplus_flag else x
+    y = np.zeros_like(u)
+    last = np.zeros((batch, d_inner, d_state))
+    for b in range(batch):
+        for d in range(d_inner):
+            for t in range(L):
+                acc = 0.0
+                for s in range(t + 1):
+                    for n in range(d_state):
+                        decay = 1.0
+                        for k in range(s + 1, t + 1):
+                            decay *= math.exp(dt[b, k, d] * A[d, n])
+                        acc += C[b, t, n] * decay * dt[b, s, d] * B[b, s, n] * u[b, s, d]
+                if p["D"] is not None:
+                    acc += p["D"][d] * u[b, t, d]
+                if p["z"] is not None:
+                    zz = p["z"][b, t, d]
+                    acc *= zz / (1.0 + math.exp(-zz))
+                y[b, t, d] = acc
+            for n in range(d_state):
+                tot = 0.0
+                for s in range(L):
+                    decay = 1.0
+                    for k in range(s + 1, L):
+                        decay *= math.exp(dt[b, k, d] * A[d, n])
+                    tot += decay * dt[b, s, d] * B[b, s, n] * u[b, s, d]
+                last[b, d, n] = tot
+    return y, last, dt
+
+
+def _rel(a, b):
+    scale = max(np.max(np.abs(b)), 1e-300)
+    return float(np.max(np.abs(a - b)) / scale)
+
+
+# ---- worked expansion from the pages -------------------------------------------------------
+
+def test_golden_lti_expansion():
+    with open(os.path.join(GOLDEN, "lti_expansion.json")) as f:
+        g = json.load(f)
+    ln2 = math.log(2.0)
+    for case in g["cases"]:
+        A = np.array(case["A"])
+        L = len(case["u"])
+        u = np.array(case["u"]).reshape(1, L, 1)
+        delta = np.full((1, L, 1), case["delta_over_ln2"] * ln2)
+        B = np.array(case["B"]).reshape(1, L, -1)
+        C = np.array(case["C"]).reshape(1, L, -1)
+        y, last = oracle.scan_fwd(u, delta, A, B, C, softplus_flag=False)
+        np.testing.assert_allclose(y.ravel() / ln2, case["y_over_ln2"], rtol=1e-14, atol=0)
+        np.testing.assert_allclose(last.ravel() / ln2, case["last_state_over_ln2"], rtol=1e-14)
+
+
+# ---- brute force -----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("gate,softplus_flag,seed", [(True, True, 0), (False, True, 1),
+                                                      (True, False, 2)])
+def test_brute_force_unrolled_sum(gate, softplus_flag, seed):
+    p = _rand_problem(gate=gate, seed=seed)
+    if not softplus_flag:  # keep delta positive so the sums stay bounded
+        p["delta"] = np.abs(p["delta"])
+        p["delta_bias"] = np.abs(p["delta_bias"])
+    y, last = oracle.scan_fwd(**p, softplus_flag=softplus_flag)
+    y_ref, last_ref, _ = _brute_force(p, softplus_flag)
+    assert _rel(y, y_ref) < 1e-12
+    assert _rel(last, last_ref) < 1e-12
+
+
+def test_brute_force_no_skip_no_bias():
+    p = _rand_problem(gate=False, seed=7)
+    p["D"] = None
+    p["delta_bias"] = None
+    y, last = oracle.scan_fwd(**p, softplus_flag=True)
+    y_ref, last_ref, _ = _brute_force(p, True)
+    assert _rel(y, y_ref) < 1e-12 and _rel(last, last_ref) < 1e-12
+
+
+def test_empty_sequence():
+    p = _rand_problem(L=0, seed=3)
+    y, last = oracle.scan_fwd(**p)
+    assert y.shape == (2, 0, 3) and np.all(last == 0.0)
+
+
+# ---- LTI closed forms --------------------------------------------------------------------------
+
+def test_lti_convolution_closed_form():
+    """Constant delta, B, C over time: y = causal conv(u, K) + D u with
+    K_k = sum_n C_n exp(delta A_n)^k delta B_n."""
+    r = np.random.default_rng(5)
+    batch, L, d_inner, d_state = 2, 50, 3, 4
+    dt = r.uniform(0.05, 0.6, size=(batch, d_inner))
+    A = -r.uniform(0.2, 3.0, size=(d_inner, d_state))
+    B0 = r.normal(size=(batch, d_state))
+    C0 = r.normal(size=(batch, d_state))
+    D = r.normal(size=d_inner)
+    u = r.normal(size=(batch, L, d_inner))
+    delta = np.broadcast_to(dt[:, None, :], (batch, L, d_inner)).copy()
+    B = np.broadcast_to(B0[:, None, :], (batch, L, d_state)).copy()
+    C = np.broadcast_to(C0[:, None, :], (batch, L, d_state)).copy()
+    y, _ = oracle.scan_fwd(u, delta, A, B, C, D=D, softplus_flag=False)
+    k = np.arange(L)
+    for b in range(batch):
+        for d in range(d_inner):
+            Abar = np.exp(dt[b, d] * A[d])
+            K = (C0[b][None, :] * np.power(Abar[None, :], k[:, None]) * dt[b, d] * B0[b][None, :]).sum(1)
+            ref = np.convolve(u[b, :, d], K)[:L] + D[d] * u[b, :, d]
+            np.testing.assert_allclose(y[b, :, d], ref, rtol=1e-11, atol=1e-12)
+
+
+def test_lti_steady_state_geometric_series():
+    """Constant input: h converges to Bbar u / (1 - Abar)."""
+    L, d_state = 3000, 4
+    dt, uu = 0.05, 0.8
+    A = -np.arange(1, d_state + 1, dtype=np.float64)[None, :]
+    Bn = np.array([0.5, -1.0, 2.0, 0.25])
+    Cn = np.array([1.0, 0.5, -0.25, 2.0])
+    u = np.full((1, L, 1), uu)
+    y, last = oracle.scan_fwd(u, np.full((1, L, 1), dt), A, np.tile(Bn, (1, L, 1)),
+                              np.tile(Cn, (1, L, 1)), D=np.array([0.3]), softplus_flag=False)
+    Abar = np.exp(dt * A[0])
+    h_inf = dt * Bn * uu / (1.0 - Abar)
+    np.testing.assert_allclose(last[0, 0], h_inf, rtol=1e-12)
+    np.testing.assert_allclose(y[0, -1, 0], Cn @ h_inf + 0.3 * uu, rtol=1e-12)
+
+
+# ---- exact special cases -------------------------------------------------------------------------
+
+def test_zero_step_size_is_skip_only():
+    """delta = 0 (softplus off, zero bias): h stays 0 and y = D u silu(z) exactly."""
+    p = _rand_problem(batch=2, L=9, d_inner=4, d_state=5, seed=11)
+    p["delta"] = np.zeros_like(p["u"])
+    p["delta_bias"] = np.zeros(4)
+    y, last = oracle.scan_fwd(**p, softplus_flag=False)
+    z = p["z"]
+    ref = p["D"][None, None, :] * p["u"] * (z / (1.0 + np.exp(-z)))
+    np.testing.assert_array_equal(last, 0.0)
+    np.testing.assert_allclose(y, ref, rtol=1e-15, atol=0)
+
+
+def test_large_step_forgets_history():
+    """delta >> 1 with A < 0: dA ~ 0, so y_t = delta_t u_t (C_t . B_t) + D u_t."""
+    p = _rand_problem(batch=1, L=7, d_inner=3, d_state=4, gate=False, seed=13)
+    p["delta"] = np.full_like(p["u"], 60.0)
+    p["delta_bias"] = np.zeros(3)
+    p["A"] = -np.random.default_rng(14).uniform(1.0, 2.5, size=p["A"].shape)  # exp(-60) ~ 1e-26
+    y, last = oracle.scan_fwd(**p, softplus_flag=True)
+    dt = 60.0 + math.log1p(math.exp(-60.0))
+    cb = (p["C"] * p["B"]).sum(-1)  # [1, L]
+    ref = dt * p["u"] * cb[:, :, None] + p["D"][None, None, :] * p["u"]
+    np.testing.assert_allclose(y, ref, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(last[0], dt * p["u"][0, -1][:, None] * p["B"][0, -1][None, :],
+                               rtol=1e-13)
+
+
+# ---- associativity / chunk composition ------------------------------------------------------------
+
+@pytest.mark.parametrize("L1", [1, 17, 40])
+def test_chunk_composition(L1):
+    """Splitting the sequence: last = exp(A sum(dt_seg2)) * last_seg1 + last_seg2, and for t in
+    segment 2, y_t = y_seg2_alone_t + sum_n C_t,n exp(A_n sum_{s<=t in seg2} dt_s) last_seg1_n."""
+    r = np.random.default_rng(21 + L1)
+    batch, L, d_inner, d_state = 2, 57, 3, 4
+    p = dict(u=r.normal(size=(batch, L, d_inner)), delta=r.uniform(0.01, 0.3, size=(batch, L, d_inner)),
+             A=-r.uniform(0.2, 2.0, size=(d_inner, d_state)), B=r.normal(size=(batch, L, d_state)),
+             C=r.normal(size=(batch, L, d_state)), D=r.normal(size=d_inner))
+    y, last = oracle.scan_fwd(**p, softplus_flag=False)
+    seg1 = {k: (v[:, :L1] if k in ("u", "delta", "B", "C") else v) for k, v in p.items()}
+    seg2 = {k: (v[:, L1:] if k in ("u", "delta", "B", "C") else v) for k, v in p.items()}
+    y1, last1 = oracle.scan_fwd(**seg1, softplus_flag=False)
+    y2, last2 = oracle.scan_fwd(**seg2, softplus_flag=False)
+    cum = np.cumsum(p["delta"][:, L1:], axis=1)  # [batch, L2, d_inner]
+    decay = np.exp(cum[..., None] * p["A"][None, None])  # [batch, L2, d_inner, d_state]
+    np.testing.assert_allclose(last, decay[:, -1] * last1 + last2, rtol=1e-12, atol=1e-14)
+    corr = np.einsum("btn,btdn,bdn->btd", p["C"][:, L1:], decay, last1)
+    np.testing.assert_allclose(y[:, L1:], y2 + corr, rtol=1e-12, atol=1e-13)
+    np.testing.assert_array_equal(y[:, :L1], y1)
+
+
+# ---- structure ---------------------------------------------------------------------------------------
+
+def test_linear_in_u_without_gate():
+    p = _rand_problem(batch=2, L=12, d_inner=3, d_state=4, gate=False, seed=31)
+    u1, u2 = p["u"], RNG.normal(size=p["u"].shape)
+    a, b = 0.7, -1.3
+    ya, la = oracle.scan_fwd(**{**p, "u": u1})
+    yb, lb = oracle.scan_fwd(**{**p, "u": u2})
+    yc, lc = oracle.scan_fwd(**{**p, "u": a * u1 + b * u2})
+    np.testing.assert_allclose(yc, a * ya + b * yb, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(lc, a * la + b * lb, rtol=1e-11, atol=1e-12)
+
+
+def test_channels_independent_under_permutation():
+    p = _rand_problem(batch=2, L=10, d_inner=5, d_state=3, seed=41)
+    perm = np.array([3, 0, 4, 1, 2])
+    q = dict(p)
+    for k in ("u", "delta", "z"):
+        q[k] = p[k][:, :, perm]
+    for k in ("A", "D", "delta_bias"):
+        q[k] = p[k][perm]
+    y, last = oracle.scan_fwd(**p)
+    yq, lq = oracle.scan_fwd(**q)
+    np.testing.assert_array_equal(yq, y[:, :, perm])
+    np.testing.assert_array_equal(lq, last[:, perm])
+
+
+def test_batches_independent():
+    p = _rand_problem(batch=3, L=8, d_inner=2, d_state=3, seed=43)
+    y, last = oracle.scan_fwd(**p)
+    q = {k: (v[1:2] if k in ("u", "delta", "z", "B", "C") else v) for k, v in p.items()}
+    y1, l1 = oracle.scan_fwd(**q)
+    np.testing.assert_array_equal(y1[0], y[1])
+    np.testing.assert_array_equal(l1[0], last[1])
+
+
+# ---- decode step ---------------------------------------------------------------------------------------
+
+def test_decode_step_explicit():
+    """One step from a nonzero state, written out per element."""
+    r = np.random.default_rng(51)
+    batch, d_inner, d_state = 3, 4, 5
+    st = r.normal(scale=0.1, size=(batch, d_inner, d_state))
+    u, dr, z = (r.normal(size=(batch, d_inner)) for _ in range(3))
+    A = -r.uniform(0.5, 3, size=(d_inner, d_state))
+    B, C = r.normal(size=(batch, d_state)), r.normal(size=(batch, d_state))
+    D, bias = r.normal(size=d_inner), r.normal(size=d_inner)
+    y, new = oracle.state_update(st, u, dr, A, B, C, D=D, z=z, delta_bias=bias, softplus_flag=True)
+    for b in range(batch):
+        for d in range(d_inner):
+            dt = _softplus_ref(dr[b, d] + bias[d])
+            h = [math.exp(dt * A[d, n]) * st[b, d, n] + dt * B[b, n] * u[b, d] for n in range(d_state)]
+            yy = sum(C[b, n] * h[n] for n in range(d_state)) + D[d] * u[b, d]
+            yy *= z[b, d] / (1 + math.exp(-z[b, d]))
+            assert abs(y[b, d] - yy) <= 1e-13 * max(1.0, abs(yy))
+            np.testing.assert_allclose(new[b, d], h, rtol=1e-13, atol=1e-15)
+
+
+def test_decode_steps_reproduce_scan():
+    p = _rand_problem(batch=2, L=9, d_inner=3, d_state=4, seed=61)
+    y, last = oracle.scan_fwd(**p)
+    st = np.zeros((2, 3, 4))
+    for t in range(9):
+        yt, st = oracle.state_update(st, p["u"][:, t], p["delta"][:, t], p["A"], p["B"][:, t],
+                                     p["C"][:, t], D=p["D"], z=p["z"][:, t],
+                                     delta_bias=p["delta_bias"])
+        np.testing.assert_allclose(yt, y[:, t], rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(st, last, rtol=1e-14, atol=1e-15)
+
+
+# ---- softplus ------------------------------------------------------------------------------------------
+
+def _softplus_decimal(x):
+    with decimal.localcontext() as ctx:
+        ctx.prec = 50
+        X = decimal.Decimal(x)
+        return float((decimal.Decimal(1) + X.exp()).ln())
+
+
+@pytest.mark.parametrize("x", [-40.0, -12.5, -6.9, -1.0, -1e-3, 0.0, 1e-3, 0.5, 3.0, 19.0, 35.0])
+def test_softplus_high_precision(x):
+    ref = _softplus_decimal(x)
+    assert abs(oracle.softplus(x) - ref) <= 2e-16 * abs(ref)
+
+
+def test_softplus_identity():
+    for x in (-5.0, -0.3, 0.0, 0.7, 8.0):
+        assert abs(oracle.softplus(x) - oracle.softplus(-x) - x) < 1e-15 * max(1.0, abs(x))
+    assert oracle.softplus(0.0) == math.log(2.0)
