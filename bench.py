@@ -1,0 +1,418 @@
+#!/usr/bin/env python
+"""Benchmark: selective-scan forward (and the decode step) on B300.
+
+One "step" is one pass of the whole hot path over one batch of synthetic input
+already resident in HBM: a single ``ssm_scan_fwd`` call over the workload
+(softplus step size, discretisation, recurrence, readout, gate, last state),
+or, for the decode workload, the 1024 sequential ``ssm_state_update`` calls.
+Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload KEY] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs the same per-GPU workload on its own
+GPU (weak scaling: the channels of a model shard independently, with no
+exchange) and the slowest rank's time is reported.  ``--impl reference`` times
+the float64 CPU oracle on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from inputgen import workloads as W  # noqa: E402
+
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6400.0
+SM_MAX_MHZ_NOMINAL = 2032.0
+# Per-SM issue rates of the pipes the scan uses (operations per clock), measured on B300
+# with a throughput probe: FP32 FFMA/FMUL/FADD 128, MUFU.EX2 32, MUFU.LG2 / MUFU.RCP 16.
+FP32_PER_CLK, EX2_PER_CLK, MUFU_SLOW_PER_CLK = 128.0, 32.0, 16.0
+L2_FLUSH_BYTES = 512 << 20
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="mamba130m", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------------------------
+# Algorithmic work per workload (the roofline numerators).
+
+def algorithmic_bytes(w: W.Workload) -> float:
+    """HBM bytes a perfect implementation must move for one step."""
+    s = 2 if w.bf16 else 4
+    N = w.d_state
+    params = w.d_inner * (N + 2) * 4                      # A, D, delta_bias (fp32)
+    if w.decode:
+        per_tok = w.batch * w.d_inner * (4 * s + 2 * N * 4)   # u, delta, z, y + state read/write
+        per_tok += w.batch * 2 * N * s                       # B, C rows
+        return float(w.L * (per_tok + params))
+    acts = w.batch * w.L * w.d_inner * 4 * s             # u, delta, z read; y write
+    bc = w.batch * w.L * 2 * N * s                       # B, C rows
+    last = w.batch * w.d_inner * N * 4                   # last_state write
+    return float(acts + bc + params + last)
+
+
+def alu_clocks_per_element(N: int) -> float:
+    """Lower bound on SM clocks per (b, t, d) element from the arithmetic the method needs:
+    per state n: delta*A, exp, (delta u)*B_n, the FMA of the recurrence and the FMA of the
+    readout (4 FP32 + 1 ex2); per element: delta*u, bias add, D*u, gate multiply, the sigmoid's
+    1 + e^-z and z * (.) (6 FP32), the exps of softplus and sigmoid (2 ex2), softplus's log and
+    the sigmoid's reciprocal (2 slow MUFU).  Each pipe is taken as independent."""
+    fp32 = 4 * N + 6
+    ex2 = N + 2
+    slow = 2
+    return max(fp32 / FP32_PER_CLK, ex2 / EX2_PER_CLK, slow / MUFU_SLOW_PER_CLK)
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p.get("sm_max_mhz", SM_MAX_MHZ_NOMINAL)), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, SM_MAX_MHZ_NOMINAL, "fallback"
+
+
+# ---------------------------------------------------------------------------------------------
+# Clock sampling (NVML, read-only) during the timed region.
+
+class ClockSampler:
+    REASONS = {
+        0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+        0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+        0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting",
+    }
+
+    def __init__(self, index: int, period_s: float = 0.005):
+        self.samples, self.reasons, self.max_mhz = [], 0, None
+        self.period, self.index = period_s, index
+        self._stop = threading.Event()
+        self._thread = None
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self._nv = pynvml
+            self._h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
+        except Exception:  # noqa: BLE001 - clocks are reported as unavailable
+            self._nv = None
+
+    def _sample(self):
+        nv = self._nv
+        self.samples.append(nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM))
+        try:
+            self.reasons |= nv.nvmlDeviceGetCurrentClocksEventReasons(self._h)
+        except AttributeError:
+            self.reasons |= nv.nvmlDeviceGetCurrentClocksThrottleReasons(self._h)
+
+    def _loop(self):
+        while not self._stop.is_set():
+            self._sample()
+            time.sleep(self.period)
+
+    def start(self):
+        if self._nv is not None:
+            self._thread = threading.Thread(target=self._loop, daemon=True)
+            self._thread.start()
+
+    def stop(self):
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join()
+            self._sample()
+
+    def summary(self):
+        if self._nv is None or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unavailable"]}
+        names = [n for bit, n in self.REASONS.items() if self.reasons & bit and n != "gpu_idle"]
+        return {"sm_mhz": float(np.median(self.samples)), "sm_max_mhz": self.max_mhz,
+                "samples": len(self.samples), "reasons": names}
+
+
+# ---------------------------------------------------------------------------------------------
+# Our implementation.
+
+class ScanStep:
+    """One step = one ssm_scan_fwd call over the whole workload."""
+
+    def __init__(self, w, dev, ssm, torch):
+        self.w, self.dev, self.ssm, self.torch = w, dev, ssm, torch
+        self.y = torch.empty_like(dev["u"])
+        self.last = torch.empty((w.batch, w.d_inner, w.d_state), dtype=torch.float32, device="cuda")
+        io = ssm.SSM_BF16 if w.bf16 else ssm.SSM_F32
+        nbytes = ssm.ssm_scan_fwd_workspace_size(w.batch, w.L, w.d_inner, w.d_state, io)
+        self.ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda") if nbytes else None
+        self.launches = 2 if nbytes else 1  # summary pass + main pass when time is chunked
+
+    def __call__(self, stream=None):
+        d = self.dev
+        self.ssm.ssm_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"],
+                              d["delta_bias"], True, self.y, self.last, self.ws, stream)
+
+
+class DecodeStep:
+    """One step = the workload's sequential single-token decode steps."""
+
+    def __init__(self, w, dev, ssm, torch):
+        self.w, self.dev, self.ssm = w, dev, ssm
+        self.state = dev["state0"].clone()
+        self.y = torch.empty((w.batch, w.d_inner), dtype=dev["u"].dtype, device="cuda")
+        self.launches = w.L
+
+    def __call__(self, stream=None):
+        d = self.dev
+        for s in range(self.w.L):
+            self.ssm.ssm_state_update(self.state, d["u"][s], d["delta"][s], d["A"], d["B"][s],
+                                      d["C"][s], d["D"], d["z"][s], self.y, d["delta_bias"], True,
+                                      stream)
+
+
+def run_e2e(w, dev, ssm, torch, steps):
+    """Same metric through the public call with pinned host buffers: every step copies the
+    inputs host->device, runs the scan, and copies y and last_state back."""
+    if w.decode:
+        return None
+    names = ["u", "delta", "z", "B", "C", "A", "D", "delta_bias"]
+    host = {k: dev[k].cpu().pin_memory() for k in names}
+    dbuf = {k: torch.empty_like(dev[k]) for k in names}
+    y = torch.empty_like(dev["u"])
+    last = torch.empty((w.batch, w.d_inner, w.d_state), dtype=torch.float32, device="cuda")
+    y_h = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+    last_h = torch.empty(last.shape, dtype=last.dtype, pin_memory=True)
+    io = ssm.SSM_BF16 if w.bf16 else ssm.SSM_F32
+    nbytes = ssm.ssm_scan_fwd_workspace_size(w.batch, w.L, w.d_inner, w.d_state, io)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda") if nbytes else None
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = y.numel() * y.element_size() + last.numel() * 4
+
+    def one():
+        for k in names:
+            dbuf[k].copy_(host[k], non_blocking=True)
+        ssm.ssm_scan_fwd(dbuf["u"], dbuf["delta"], dbuf["A"], dbuf["B"], dbuf["C"], dbuf["D"],
+                         dbuf["z"], dbuf["delta_bias"], True, y, last, ws)
+        y_h.copy_(y, non_blocking=True)
+        last_h.copy_(last, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        one()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return {"value": w.elements / (ms * 1e-3), "unit": "elements/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def oracle_sample_rate(w, budget_s: float, threads: int | None = None):
+    """Elements/s of the float64 oracle on a bounded sample of the workload: a subset of
+    channels over the full sequence (all batches), sized to roughly budget_s of work."""
+    import oracle
+    oracle.build()
+    threads = threads or oracle.max_threads()
+    if w.decode:
+        steps = 8
+        probe = W.host_decode_inputs(w, steps, d_sel=np.arange(64))
+        t0 = time.perf_counter()
+        st = probe["state0"]
+        for s in range(steps):
+            _, st = oracle.state_update(st, probe["u"][s], probe["delta"][s], probe["A"],
+                                        probe["B"][s], probe["C"][s], D=probe["D"], z=probe["z"][s],
+                                        delta_bias=probe["delta_bias"], nthreads=threads)
+        el = steps * w.batch * 64
+        return el / (time.perf_counter() - t0), threads, \
+            f"{steps} decode steps x {w.batch} batch x 64 of {w.d_inner} channels"
+    T = min(w.L, 1 << 16)
+    d_try = max(1, min(w.d_inner, threads))
+    x = W.host_scan_inputs(w, d_sel=np.arange(d_try), t_count=T)
+    t0 = time.perf_counter()
+    oracle.scan_fwd(x["u"], x["delta"], x["A"], x["B"], x["C"], D=x["D"], z=x["z"],
+                    delta_bias=x["delta_bias"], nthreads=threads)
+    rate = w.batch * T * d_try / (time.perf_counter() - t0)
+    d_cnt = int(min(w.d_inner, max(d_try, rate * budget_s / (w.batch * T))))
+    x = W.host_scan_inputs(w, d_sel=np.arange(d_cnt), t_count=T)
+    t0 = time.perf_counter()
+    oracle.scan_fwd(x["u"], x["delta"], x["A"], x["B"], x["C"], D=x["D"], z=x["z"],
+                    delta_bias=x["delta_bias"], nthreads=threads)
+    dt = time.perf_counter() - t0
+    return w.batch * T * d_cnt / dt, threads, \
+        f"{w.batch} batch x {T} steps x {d_cnt} of {w.d_inner} channels (float64, {dt:.1f} s)"
+
+
+def roofline(w, ms_per_step, hbm_gbs, sm_mhz, sms, peak_src):
+    el_rate = w.elements / (ms_per_step * 1e-3)
+    t_hbm = algorithmic_bytes(w) / (hbm_gbs * 1e9)
+    t_alu = w.elements * alu_clocks_per_element(w.d_state) / (sms * sm_mhz * 1e6)
+    if t_hbm >= t_alu:
+        achieved = algorithmic_bytes(w) / (ms_per_step * 1e-3) / 1e9
+        return {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                "frac": achieved / hbm_gbs, "traffic": None,
+                "peak_source": f"{peak_src} copy bandwidth",
+                "alu_frac": el_rate * t_alu / w.elements}
+    peak = w.elements / t_alu / 1e9
+    return {"bound": "alu", "achieved": el_rate / 1e9, "peak": peak, "unit": "Gelem/s",
+            "frac": el_rate / 1e9 / peak, "traffic": None,
+            "peak_source": f"{sms} SMs x {sm_mhz:.0f} MHz, per-element FP32/EX2/MUFU op counts",
+            "hbm_frac": algorithmic_bytes(w) / (ms_per_step * 1e-3) / 1e9 / hbm_gbs}
+
+
+def main_ours(args, rank, world, local_rank):
+    import torch
+    import selective_state_space_161_b300 as ssm
+
+    torch.cuda.set_device(local_rank)
+    ssm.load_library()
+    w = W.WORKLOADS[args.workload]
+    dev = W.device_inputs(w)
+    step = DecodeStep(w, dev, ssm, torch) if w.decode else ScanStep(w, dev, ssm, torch)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    sms = torch.cuda.get_device_properties(local_rank).multi_processor_count
+
+    for _ in range(max(args.warmup, 0)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = ClockSampler(local_rank)
+    events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    clocks.start()
+    for e0, e1 in events:
+        flush.zero_()            # evict the previous step's data from L2 (untimed)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    clocks.stop()
+    ms = float(np.mean([e0.elapsed_time(e1) for e0, e1 in events]))
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        torch.distributed.barrier()
+        ms = float(t.item())
+
+    e2e = None
+    if not args.no_e2e and not w.decode:
+        e2e = run_e2e(w, dev, ssm, torch, args.e2e_steps)
+        if e2e is not None and world > 1:
+            t = torch.tensor([e2e["ms_per_step"]], dtype=torch.float64, device="cuda")
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e2e["ms_per_step"] = float(t.item())
+            e2e["value"] = world * w.elements / (e2e["ms_per_step"] * 1e-3)
+
+    if rank != 0:
+        return
+    hbm_gbs, _, peak_src = load_peaks()
+    clk = clocks.summary()
+    sm_mhz_peak = float(clk["sm_max_mhz"] or SM_MAX_MHZ_NOMINAL)
+    out = {
+        "metric": "scan elements/s (B*L*d_inner)" if not w.decode
+        else "decode elements/s (B*d_inner*steps)",
+        "value": world * w.elements / (ms * 1e-3),
+        "unit": "elements/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16 I/O, f32 state and arithmetic" if w.bf16 else "f32",
+        "data": "synthetic (seeded; recipe in inputgen/workloads.py)",
+        "config": {"workload": w.desc, "batch": w.batch,
+                   ("steps" if w.decode else "seq_len"): w.L, "d_inner": w.d_inner,
+                   "d_state": w.d_state, "io_dtype": "bf16" if w.bf16 else "f32",
+                   "parallelism": f"replica per GPU x{world}" if world > 1 else "single GPU",
+                   "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write)"},
+        "roofline": roofline(w, ms, hbm_gbs, sm_mhz_peak, sms, peak_src),
+        "gpu_launches": step.launches * args.steps,
+        "clocks": clk,
+    }
+    if e2e is not None:
+        out["e2e"] = e2e
+    if not args.no_cpu_baseline:
+        rate, cores, sample = oracle_sample_rate(w, budget_s=12.0)
+        out["cpu_baseline"] = {"value": rate, "unit": "elements/s", "cores": cores,
+                               "kind": "oracle", "sample": sample}
+    print(json.dumps(out), flush=True)
+
+
+def main_reference(args, rank, world):
+    """The float64 oracle on the host cores: each step is a bounded sample of the workload."""
+    if rank != 0:
+        return
+    w = W.WORKLOADS[args.workload]
+    rates = []
+    info = None
+    for i in range(args.warmup + args.steps):
+        rate, cores, sample = oracle_sample_rate(w, budget_s=1.5)
+        if i >= args.warmup:
+            rates.append(rate)
+            info = (cores, sample)
+    value = float(np.median(rates))
+    out = {
+        "impl": "reference",
+        "metric": "scan elements/s (B*L*d_inner)" if not w.decode
+        else "decode elements/s (B*d_inner*steps)",
+        "value": value, "unit": "elements/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": w.elements / value * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; recipe in inputgen/workloads.py)",
+        "config": {"workload": w.desc, "batch": w.batch,
+                   ("steps" if w.decode else "seq_len"): w.L, "d_inner": w.d_inner,
+                   "d_state": w.d_state, "io_dtype": "bf16" if w.bf16 else "f32"},
+        "cpu_baseline": {"value": value, "unit": "elements/s", "cores": info[0], "kind": "oracle",
+                         "sample": info[1]},
+        "e2e": {"value": value, "unit": "elements/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        main_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        main_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,121 @@
+/*
+ * ssm.h -- C ABI of libssm: the Mamba selective-scan forward pass and its
+ * single-token decode step, as CUDA kernels for NVIDIA B300 (sm_103a).
+ *
+ * The operation (citations are page title + section):
+ *   delta_t = softplus(delta_raw_t + delta_bias)          (or without softplus)
+ *   dA_t    = exp(delta_t * A)                             per (channel, state)
+ *   dBu_t   = delta_t * B_t * u_t
+ *   h_t     = dA_t * h_{t-1} + dBu_t,  h_{-1} = 0
+ *   y_t     = (sum_n C_{t,n} h_{t,n} + D * u_t) * silu(z_t)
+ * - discretisation, recurrence and readout: youngju.dev, "Mamba: Linear-Time
+ *   Sequence Modeling with Selective State Spaces 论文分析", section
+ *   "解决方案：Kernel Fusion + Recomputation" (selective_scan concept code);
+ *   ai-lab.club "机器学习基础算法", section "状态空间模型：连续系统的离散化"
+ *   (h_k = Abar h_{k-1} + Bbar x_k, y_k = C h_k + D x_k);
+ * - selection (B, C, delta per token): youngju.dev, section
+ *   "Mamba 的解决方案：Selection Mechanism";
+ * - gate y * silu(z) and the biased delta projection: youngju.dev, section
+ *   "Mamba 模块架构";
+ * - the single-step (decode) form: ai-lab.club, section "核心优势"
+ *   (constant work per generated token, like an RNN).
+ *
+ * Conventions shared by every entry point
+ * - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *   never allocates, frees or keeps them.  Every call is asynchronous on
+ *   `stream` (a cudaStream_t; NULL = the legacy default stream).
+ * - Layouts are row-major, channels (d_inner) innermost:
+ *     u, delta, z, y  [batch][L][d_inner]      (I/O dtype)
+ *     B, C            [batch][L][d_state]      (I/O dtype)
+ *     A               [d_inner][d_state]       fp32
+ *     D, delta_bias   [d_inner]                fp32
+ *     last_state      [batch][d_inner][d_state] fp32
+ *   The I/O dtype (`io`) is fp32 or bf16; the state and all arithmetic are
+ *   fp32, bf16 outputs are rounded to nearest even.
+ * - Requirements: every non-NULL pointer 16-byte aligned; d_inner a multiple
+ *   of 8 (bf16) or 4 (fp32); 1 <= d_state <= 16; batch, L, d_inner >= 0.
+ *   Outputs must not overlap inputs.
+ * - The return value reports argument validation and launch errors only
+ *   (kernels have no device-side failure mode: there are no inter-block waits).
+ * - Calls on different streams are independent if their outputs and
+ *   workspaces are distinct.
+ */
+#ifndef SSM_H
+#define SSM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SSM_API __attribute__((visibility("default")))
+#else
+#define SSM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype_t;
+
+typedef enum {
+  SSM_OK = 0,
+  SSM_ERR_NULL = 1,       /* a required pointer is NULL */
+  SSM_ERR_SHAPE = 2,      /* negative size, d_state outside 1..16, bad d_inner multiple */
+  SSM_ERR_DTYPE = 3,      /* io is neither SSM_F32 nor SSM_BF16 */
+  SSM_ERR_ALIGN = 4,      /* a pointer is not 16-byte aligned */
+  SSM_ERR_WORKSPACE = 5,  /* workspace NULL or smaller than the size query says */
+  SSM_ERR_CUDA = 6        /* no usable CUDA device, or a launch failed */
+} ssm_status_t;
+
+/*
+ * Bytes of scratch memory ssm_scan_fwd needs for these sizes on the current
+ * device (0 when the sequence is processed in a single chunk).  The scratch
+ * holds one (sum of delta, end state) pair per time chunk and channel; its
+ * contents need no initialisation and are dead after the call completes.
+ */
+SSM_API size_t ssm_scan_fwd_workspace_size(int64_t batch, int64_t L, int64_t d_inner, int d_state,
+                                   ssm_dtype_t io);
+
+/*
+ * Selective-scan forward over whole sequences.
+ *   u, delta, B, C : inputs (io dtype), required when batch*L*d_inner > 0.
+ *   A              : fp32 [d_inner][d_state], required.
+ *   D, z, delta_bias: optional (NULL = no skip term / no gate / zero bias).
+ *   softplus_flag  : nonzero -> delta = softplus(delta_raw + bias), else delta_raw + bias.
+ *   y              : output (io dtype), required when batch*L*d_inner > 0.
+ *   last_state     : optional fp32 output, h after the last step (before D and the gate);
+ *                    zeros when L == 0.
+ *   workspace      : device scratch of workspace_bytes >= ssm_scan_fwd_workspace_size(...);
+ *                    may be NULL when that size is 0.
+ */
+SSM_API ssm_status_t ssm_scan_fwd(const void* u, const void* delta, const float* A, const void* B,
+                          const void* C, const float* D, const void* z, const float* delta_bias,
+                          int softplus_flag, void* y, float* last_state, int64_t batch, int64_t L,
+                          int64_t d_inner, int d_state, ssm_dtype_t io, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
+/*
+ * One decode step on a carried state, in place:
+ *   state [batch][d_inner][d_state] fp32 (read, then overwritten with h_t);
+ *   u, delta, z, y [batch][d_inner] (io dtype); B, C [batch][d_state] (io dtype);
+ *   A [d_inner][d_state], D, delta_bias [d_inner] fp32.
+ * D, z, delta_bias are optional (NULL); softplus_flag as for ssm_scan_fwd.
+ * L calls from a zero state reproduce ssm_scan_fwd's y and last_state.
+ */
+SSM_API ssm_status_t ssm_state_update(float* state, const void* u, const void* delta, const float* A,
+                              const void* B, const void* C, const float* D, const void* z,
+                              void* y, const float* delta_bias, int softplus_flag, int64_t batch,
+                              int64_t d_inner, int d_state, ssm_dtype_t io, void* stream);
+
+/* Human-readable name of a status code (static string). */
+SSM_API const char* ssm_status_string(ssm_status_t status);
+
+/* Library ABI version (major * 100 + minor). */
+SSM_API int ssm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSM_H */

@@ -1,0 +1,190 @@
+"""Python binding of libssm, the B300 (sm_103a) selective-scan library.
+
+The functions named like the C ABI (``ssm_scan_fwd``, ``ssm_state_update``,
+``ssm_scan_fwd_workspace_size``, ``ssm_status_string``) only marshal
+arguments: every step of the computation runs in the library's CUDA kernels.
+PyTorch supplies device memory and streams.  There is no fallback: if the
+compiled library is missing or cannot be loaded, every call raises.
+
+``selective_scan`` is the convenience entry a user calls: it allocates the
+outputs and the scratch workspace with PyTorch and accepts either CUDA tensors
+or host tensors (which it copies to the current device and back).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .build import LIB_PATH, build
+
+__all__ = ["SsmError", "ssm_scan_fwd", "ssm_state_update", "ssm_scan_fwd_workspace_size",
+           "ssm_status_string", "ssm_version", "selective_scan", "selective_state_update",
+           "load_library", "build", "SSM_F32", "SSM_BF16", "EXPORTED_SYMBOLS"]
+
+SSM_F32, SSM_BF16 = 0, 1
+EXPORTED_SYMBOLS = ("ssm_scan_fwd_workspace_size", "ssm_scan_fwd", "ssm_state_update",
+                    "ssm_status_string", "ssm_version")
+
+_lib = None
+
+
+class SsmError(RuntimeError):
+    def __init__(self, func: str, status: int):
+        self.status = status
+        super().__init__(f"{func} failed: status {status} ({ssm_status_string(status)})")
+
+
+def load_library() -> ctypes.CDLL:
+    """Load the compiled library (building it first if the sources are newer)."""
+    global _lib
+    if _lib is None:
+        path = build()
+        if not os.path.exists(path):
+            raise RuntimeError(f"libssm not found at {path}")
+        lib = ctypes.CDLL(path)
+        vp, i64, c_int = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        lib.ssm_scan_fwd_workspace_size.argtypes = [i64, i64, i64, c_int, c_int]
+        lib.ssm_scan_fwd_workspace_size.restype = ctypes.c_size_t
+        lib.ssm_scan_fwd.argtypes = [vp] * 8 + [c_int, vp, vp, i64, i64, i64, c_int, c_int, vp,
+                                              ctypes.c_size_t, vp]
+        lib.ssm_scan_fwd.restype = c_int
+        lib.ssm_state_update.argtypes = [vp] * 10 + [c_int, i64, i64, c_int, c_int, vp]
+        lib.ssm_state_update.restype = c_int
+        lib.ssm_status_string.argtypes = [c_int]
+        lib.ssm_status_string.restype = ctypes.c_char_p
+        lib.ssm_version.restype = c_int
+        _lib = lib
+    return _lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _io_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return SSM_F32
+    if t.dtype == torch.bfloat16:
+        return SSM_BF16
+    raise TypeError(f"I/O tensors must be float32 or bfloat16, got {t.dtype}")
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check_dev(name, t, dtype=None, shape=None):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def ssm_status_string(status: int) -> str:
+    return load_library().ssm_status_string(int(status)).decode()
+
+
+def ssm_version() -> int:
+    return int(load_library().ssm_version())
+
+
+def ssm_scan_fwd_workspace_size(batch: int, L: int, d_inner: int, d_state: int, io: int) -> int:
+    return int(load_library().ssm_scan_fwd_workspace_size(batch, L, d_inner, d_state, io))
+
+
+def ssm_scan_fwd(u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, last_state,
+                 workspace=None, stream=None) -> None:
+    """C-ABI ``ssm_scan_fwd`` on CUDA tensors (shapes as documented in include/ssm.h)."""
+    batch, L, d_inner = u.shape
+    d_state = A.shape[1]
+    io = _io_code(u)
+    dt = u.dtype
+    for name, t, shp in (("u", u, (batch, L, d_inner)), ("delta", delta, (batch, L, d_inner)),
+                         ("z", z, (batch, L, d_inner)), ("y", y, (batch, L, d_inner)),
+                         ("B", B, (batch, L, d_state)), ("C", C, (batch, L, d_state))):
+        _check_dev(name, t, dt, shp)
+    _check_dev("A", A, torch.float32, (d_inner, d_state))
+    _check_dev("D", D, torch.float32, (d_inner,))
+    _check_dev("delta_bias", delta_bias, torch.float32, (d_inner,))
+    _check_dev("last_state", last_state, torch.float32, (batch, d_inner, d_state))
+    _check_dev("workspace", workspace)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load_library().ssm_scan_fwd(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                     _ptr(z), _ptr(delta_bias), int(bool(softplus_flag)), _ptr(y),
+                                     _ptr(last_state), batch, L, d_inner, d_state, io,
+                                     _ptr(workspace), ws_bytes, _stream_handle(stream))
+    if rc != 0:
+        raise SsmError("ssm_scan_fwd", rc)
+
+
+def ssm_state_update(state, u, delta, A, B, C, D, z, y, delta_bias, softplus_flag,
+                     stream=None) -> None:
+    """C-ABI ``ssm_state_update`` on CUDA tensors; ``state`` is updated in place."""
+    batch, d_inner = u.shape
+    d_state = A.shape[1]
+    io = _io_code(u)
+    dt = u.dtype
+    _check_dev("state", state, torch.float32, (batch, d_inner, d_state))
+    for name, t, shp in (("u", u, (batch, d_inner)), ("delta", delta, (batch, d_inner)),
+                         ("z", z, (batch, d_inner)), ("y", y, (batch, d_inner)),
+                         ("B", B, (batch, d_state)), ("C", C, (batch, d_state))):
+        _check_dev(name, t, dt, shp)
+    _check_dev("A", A, torch.float32, (d_inner, d_state))
+    _check_dev("D", D, torch.float32, (d_inner,))
+    _check_dev("delta_bias", delta_bias, torch.float32, (d_inner,))
+    rc = load_library().ssm_state_update(_ptr(state), _ptr(u), _ptr(delta), _ptr(A), _ptr(B),
+                                         _ptr(C), _ptr(D), _ptr(z), _ptr(y), _ptr(delta_bias),
+                                         int(bool(softplus_flag)), batch, d_inner, d_state, io,
+                                         _stream_handle(stream))
+    if rc != 0:
+        raise SsmError("ssm_state_update", rc)
+
+
+def _to_device(t, device):
+    if t is None:
+        return None
+    return t if t.is_cuda else t.to(device, non_blocking=True)
+
+
+def selective_scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True,
+                   return_last_state=True, stream=None):
+    """Selective scan forward.  Returns (y, last_state) on the inputs' device.
+
+    Host tensors (pinned for asynchronous copies) are copied to the current
+    CUDA device, processed there, and the results copied back."""
+    on_host = not u.is_cuda
+    device = torch.device("cuda", torch.cuda.current_device()) if on_host else u.device
+    ins = [_to_device(t, device) for t in (u, delta, A, B, C, D, z, delta_bias)]
+    u_d, delta_d, A_d, B_d, C_d, D_d, z_d, bias_d = ins
+    batch, L, d_inner = u_d.shape
+    d_state = A_d.shape[1]
+    y = torch.empty_like(u_d)
+    last = (torch.empty((batch, d_inner, d_state), dtype=torch.float32, device=device)
+            if return_last_state else None)
+    nbytes = ssm_scan_fwd_workspace_size(batch, L, d_inner, d_state, _io_code(u_d))
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device) if nbytes else None
+    ssm_scan_fwd(u_d, delta_d, A_d, B_d, C_d, D_d, z_d, bias_d, softplus, y, last, ws, stream)
+    if on_host:
+        y = y.to("cpu", non_blocking=False)
+        last = last.to("cpu") if last is not None else None
+    return y, last
+
+
+def selective_state_update(state, u, delta, A, B, C, D=None, z=None, delta_bias=None,
+                           softplus=True, stream=None):
+    """One decode step on CUDA tensors; updates ``state`` in place and returns y."""
+    y = torch.empty_like(u)
+    ssm_state_update(state, u, delta, A, B, C, D, z, y, delta_bias, softplus, stream)
+    return y

@@ -1,0 +1,141 @@
+// C ABI of libssm (declared in include/ssm.h): argument validation, the
+// chunking plan, and dispatch to the kernels on the caller's stream.
+
+#include "ssm.h"
+#include "ssm_internal.h"
+
+#include <cuda_runtime.h>
+
+namespace {
+
+constexpr int kMaxState = 16;
+constexpr int kMaxDevices = 64;
+int g_sm_count[kMaxDevices] = {0};
+
+// SM count of the current device (cached per device), or 0 if there is no usable device.
+int current_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+  if (dev < kMaxDevices && g_sm_count[dev] > 0) return g_sm_count[dev];
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev < kMaxDevices) g_sm_count[dev] = sms;
+  return sms;
+}
+
+bool aligned16(const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+ssm_status_t check_common(int64_t batch, int64_t L, int64_t d_inner, int d_state, ssm_dtype_t io) {
+  if (io != SSM_F32 && io != SSM_BF16) return SSM_ERR_DTYPE;
+  if (batch < 0 || L < 0 || d_inner < 0) return SSM_ERR_SHAPE;
+  if (d_state < 1 || d_state > kMaxState) return SSM_ERR_SHAPE;
+  if (d_inner % (io == SSM_BF16 ? 8 : 4) != 0) return SSM_ERR_SHAPE;
+  // Keep every flat index below 2^62 and every grid below 2^31 blocks.
+  const int64_t lim = (int64_t)1 << 62;
+  if (batch > 0 && d_inner > 0 && (batch > lim / d_inner || (L > 0 && batch * d_inner > lim / L)))
+    return SSM_ERR_SHAPE;
+  if (batch * d_inner * kMaxState > lim) return SSM_ERR_SHAPE;
+  return SSM_OK;
+}
+
+size_t scan_workspace_bytes(int64_t batch, int64_t L, int64_t d_inner, int d_state, int sms,
+                            int64_t* chunk_len, int* n_chunks) {
+  ssm::plan_scan_chunks(batch, L, d_inner, sms, chunk_len, n_chunks);
+  if (*n_chunks <= 1) return 0;
+  return (size_t)batch * (size_t)(*n_chunks - 1) * (size_t)d_inner * (size_t)(d_state + 1) *
+         sizeof(float);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ssm_scan_fwd_workspace_size(int64_t batch, int64_t L, int64_t d_inner, int d_state,
+                                   ssm_dtype_t io) {
+  if (check_common(batch, L, d_inner, d_state, io) != SSM_OK) return 0;
+  const int sms = current_sm_count();
+  if (sms <= 0) return 0;
+  int64_t len;
+  int G;
+  return scan_workspace_bytes(batch, L, d_inner, d_state, sms, &len, &G);
+}
+
+ssm_status_t ssm_scan_fwd(const void* u, const void* delta, const float* A, const void* B,
+                          const void* C, const float* D, const void* z, const float* delta_bias,
+                          int softplus_flag, void* y, float* last_state, int64_t batch, int64_t L,
+                          int64_t d_inner, int d_state, ssm_dtype_t io, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  ssm_status_t st = check_common(batch, L, d_inner, d_state, io);
+  if (st != SSM_OK) return st;
+  const int64_t channels = batch * d_inner;
+  if (channels == 0) return SSM_OK;
+  if (A == nullptr) return SSM_ERR_NULL;
+  if (L > 0 && (!u || !delta || !B || !C || !y)) return SSM_ERR_NULL;
+  const void* ptrs[] = {u, delta, A, B, C, D, z, delta_bias, y, last_state, workspace};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return SSM_ERR_ALIGN;
+  const int sms = current_sm_count();
+  if (sms <= 0) return SSM_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  if (L == 0) {
+    if (last_state &&
+        cudaMemsetAsync(last_state, 0, (size_t)channels * d_state * sizeof(float), s) != cudaSuccess)
+      return SSM_ERR_CUDA;
+    return SSM_OK;
+  }
+
+  ssm::ScanParams p{};
+  const size_t need = scan_workspace_bytes(batch, L, d_inner, d_state, sms, &p.chunk_len, &p.n_chunks);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return SSM_ERR_WORKSPACE;
+  const int64_t n_dtiles = (d_inner + 127) / 128;
+  if (n_dtiles * p.n_chunks * batch >= ((int64_t)1 << 31)) return SSM_ERR_SHAPE;
+  p.u = u; p.delta = delta; p.A = A; p.B = B; p.C = C; p.D = D; p.z = z;
+  p.delta_bias = delta_bias; p.softplus = softplus_flag != 0; p.y = y; p.last_state = last_state;
+  p.batch = batch; p.L = L; p.d_inner = d_inner; p.d_state = d_state;
+  if (p.n_chunks > 1) {
+    p.ws_S = static_cast<float*>(workspace);
+    p.ws_h = p.ws_S + (size_t)batch * (p.n_chunks - 1) * d_inner;
+  }
+  return ssm::launch_scan(p, io == SSM_BF16, s) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+ssm_status_t ssm_state_update(float* state, const void* u, const void* delta, const float* A,
+                              const void* B, const void* C, const float* D, const void* z,
+                              void* y, const float* delta_bias, int softplus_flag, int64_t batch,
+                              int64_t d_inner, int d_state, ssm_dtype_t io, void* stream) {
+  ssm_status_t st = check_common(batch, 1, d_inner, d_state, io);
+  if (st != SSM_OK) return st;
+  const int64_t channels = batch * d_inner;
+  if (channels == 0) return SSM_OK;
+  if (!state || !u || !delta || !A || !B || !C || !y) return SSM_ERR_NULL;
+  const void* ptrs[] = {state, u, delta, A, B, C, D, z, y, delta_bias};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return SSM_ERR_ALIGN;
+  if (current_sm_count() <= 0) return SSM_ERR_CUDA;
+  if ((channels + 255) / 256 >= ((int64_t)1 << 31)) return SSM_ERR_SHAPE;
+  ssm::DecodeParams p{};
+  p.state = state; p.u = u; p.delta = delta; p.A = A; p.B = B; p.C = C; p.D = D; p.z = z; p.y = y;
+  p.delta_bias = delta_bias; p.softplus = softplus_flag != 0;
+  p.batch = batch; p.d_inner = d_inner; p.d_state = d_state;
+  return ssm::launch_state_update(p, io == SSM_BF16, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? SSM_OK
+             : SSM_ERR_CUDA;
+}
+
+const char* ssm_status_string(ssm_status_t status) {
+  switch (status) {
+    case SSM_OK: return "ok";
+    case SSM_ERR_NULL: return "a required pointer is NULL";
+    case SSM_ERR_SHAPE: return "unsupported or inconsistent sizes";
+    case SSM_ERR_DTYPE: return "unknown I/O dtype";
+    case SSM_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+    case SSM_ERR_WORKSPACE: return "workspace missing or too small";
+    case SSM_ERR_CUDA: return "CUDA error (no device or launch failure)";
+  }
+  return "unknown status";
+}
+
+int ssm_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,68 @@
+"""The C ABI library: it loads, exports every symbol include/ssm.h declares,
+and rejects bad arguments on the host (no GPU needed for any of this)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import selective_state_space_161_b300 as ssm
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names |= set(re.findall(r"SSM_API\s+[\w\s\*]+?\b(ssm_\w+)\s*\(", text))
+    return names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ssm.load_library()
+    declared = _declared()
+    assert {"ssm_scan_fwd", "ssm_state_update", "ssm_scan_fwd_workspace_size"} <= declared
+    for name in declared:
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+    assert set(ssm.EXPORTED_SYMBOLS) <= declared
+
+
+def test_version_and_status_strings():
+    assert ssm.ssm_version() >= 100
+    assert ssm.ssm_status_string(0) == "ok"
+    assert "aligned" in ssm.ssm_status_string(4)
+
+
+def _scan_rc(**kw):
+    lib = ssm.load_library()
+    args = dict(u=None, delta=None, A=None, B=None, C=None, D=None, z=None, bias=None, sp=1, y=None,
+                last=None, batch=1, L=8, d_inner=8, d_state=4, io=0, ws=None, ws_bytes=0, stream=None)
+    args.update(kw)
+    return lib.ssm_scan_fwd(*args.values())
+
+
+def test_host_validation_before_any_device_call():
+    assert _scan_rc(io=7) == 3                     # dtype
+    assert _scan_rc(d_state=0) == 2                # d_state range
+    assert _scan_rc(d_state=17) == 2
+    assert _scan_rc(d_inner=6) == 2                # fp32 needs d_inner % 4 == 0
+    assert _scan_rc(d_inner=12, io=1) == 2         # bf16 needs d_inner % 8 == 0
+    assert _scan_rc(batch=-1) == 2
+    assert _scan_rc(L=-3) == 2
+    assert _scan_rc(batch=0) == 0                  # empty problem: nothing to do
+    assert _scan_rc(d_inner=0) == 0
+    lib = ssm.load_library()
+    assert lib.ssm_state_update(*([None] * 10), 1, 2, 8, 0, 0, None) == 2
+
+
+def test_product_path_does_not_import_oracle():
+    """The package never imports, links or loads the oracle (test infrastructure)."""
+    src_dir = os.path.join(ROOT, "selective_state_space_161_b300")
+    for dirpath, _, files in os.walk(src_dir):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
+                assert "liboracle" not in text, f
