@@ -104,29 +104,39 @@ class ClockSampler:
 
     def __init__(self, index: int, period_s: float = 0.005):
         self.samples, self.reasons, self.max_mhz = [], 0, None
-        self.period, self.index = period_s, index
+        self.period, self.index, self.error = period_s, index, None
         self._stop = threading.Event()
         self._thread = None
+        self._nv = None
         try:
             import pynvml
             pynvml.nvmlInit()
-            self._nv = pynvml
             self._h = pynvml.nvmlDeviceGetHandleByIndex(index)
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
-        except Exception:  # noqa: BLE001 - clocks are reported as unavailable
+            self._nv = pynvml
+            self._sample()
+        except Exception as e:  # noqa: BLE001 - clocks are then reported as unavailable
+            self.error = f"{type(e).__name__}: {e}"
             self._nv = None
 
     def _sample(self):
         nv = self._nv
         self.samples.append(nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM))
-        try:
-            self.reasons |= nv.nvmlDeviceGetCurrentClocksEventReasons(self._h)
-        except AttributeError:
-            self.reasons |= nv.nvmlDeviceGetCurrentClocksThrottleReasons(self._h)
+        for fn in ("nvmlDeviceGetCurrentClocksEventReasons", "nvmlDeviceGetCurrentClocksThrottleReasons"):
+            if hasattr(nv, fn):
+                try:
+                    self.reasons |= getattr(nv, fn)(self._h)
+                    break
+                except Exception:  # noqa: BLE001
+                    continue
 
     def _loop(self):
         while not self._stop.is_set():
-            self._sample()
+            try:
+                self._sample()
+            except Exception as e:  # noqa: BLE001
+                self.error = f"{type(e).__name__}: {e}"
+                return
             time.sleep(self.period)
 
     def start(self):
@@ -138,11 +148,15 @@ class ClockSampler:
         if self._thread is not None:
             self._stop.set()
             self._thread.join()
-            self._sample()
+            try:
+                self._sample()
+            except Exception as e:  # noqa: BLE001
+                self.error = f"{type(e).__name__}: {e}"
 
     def summary(self):
         if self._nv is None or not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unavailable"]}
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unavailable"],
+                    "error": self.error}
         names = [n for bit, n in self.REASONS.items() if self.reasons & bit and n != "gpu_idle"]
         return {"sm_mhz": float(np.median(self.samples)), "sm_max_mhz": self.max_mhz,
                 "samples": len(self.samples), "reasons": names}

@@ -88,7 +88,8 @@ ssm_status_t ssm_scan_fwd(const void* u, const void* delta, const float* A, cons
   ssm::ScanParams p{};
   const size_t need = scan_workspace_bytes(batch, L, d_inner, d_state, sms, &p.chunk_len, &p.n_chunks);
   if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return SSM_ERR_WORKSPACE;
-  const int64_t n_dtiles = (d_inner + 127) / 128;
+  const int64_t cpc = ssm::scan_channels_per_cta();
+  const int64_t n_dtiles = (d_inner + cpc - 1) / cpc;
   if (n_dtiles * p.n_chunks * batch >= ((int64_t)1 << 31)) return SSM_ERR_SHAPE;
   p.u = u; p.delta = delta; p.A = A; p.B = B; p.C = C; p.D = D; p.z = z;
   p.delta_bias = delta_bias; p.softplus = softplus_flag != 0; p.y = y; p.last_state = last_state;

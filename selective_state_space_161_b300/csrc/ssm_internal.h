@@ -46,6 +46,9 @@ struct DecodeParams {
   int d_state;
 };
 
+// Channels handled by one CTA of the scan kernels.
+int scan_channels_per_cta();
+
 // Chunking plan for a scan of these sizes on a device with `sms` SMs.
 void plan_scan_chunks(int64_t batch, int64_t L, int64_t d_inner, int sms, int64_t* chunk_len,
                       int* n_chunks);
