@@ -95,40 +95,67 @@ def load_peaks():
 # ---------------------------------------------------------------------------------------------
 # Clock sampling (NVML, read-only) during the timed region.
 
+class _Nvml:
+    """Read-only NVML queries through ctypes (libnvidia-ml ships with the driver)."""
+
+    def __init__(self, index: int):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(self.h)) != 0:
+            raise RuntimeError("nvmlDeviceGetHandleByIndex failed")
+        self._reasons = (getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+                         or self.lib.nvmlDeviceGetCurrentClocksThrottleReasons)
+
+    def _uint(self, fn, *args):
+        v = self.ct.c_uint()
+        if fn(self.h, *args, self.ct.byref(v)) != 0:
+            raise RuntimeError(f"{fn.__name__} failed")
+        return v.value
+
+    def sm_clock(self):
+        return self._uint(self.lib.nvmlDeviceGetClockInfo, 1)  # NVML_CLOCK_SM
+
+    def sm_max_clock(self):
+        return self._uint(self.lib.nvmlDeviceGetMaxClockInfo, 1)
+
+    def power_w(self):
+        return self._uint(self.lib.nvmlDeviceGetPowerUsage) / 1000.0
+
+    def reasons(self):
+        v = self.ct.c_ulonglong()
+        if self._reasons(self.h, self.ct.byref(v)) != 0:
+            return 0
+        return v.value
+
+
 class ClockSampler:
+    """Samples SM clock, power and clock-event reasons in a thread during the timed region."""
     REASONS = {
         0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
         0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
         0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting",
     }
 
-    def __init__(self, index: int, period_s: float = 0.005):
-        self.samples, self.reasons, self.max_mhz = [], 0, None
-        self.period, self.index, self.error = period_s, index, None
+    def __init__(self, index: int, period_s: float = 0.002):
+        self.samples, self.power, self.reasons, self.max_mhz = [], [], 0, None
+        self.period, self.error = period_s, None
         self._stop = threading.Event()
         self._thread = None
-        self._nv = None
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            self._h = pynvml.nvmlDeviceGetHandleByIndex(index)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
-            self._nv = pynvml
-            self._sample()
+            self._nv = _Nvml(index)
+            self.max_mhz = self._nv.sm_max_clock()
         except Exception as e:  # noqa: BLE001 - clocks are then reported as unavailable
             self.error = f"{type(e).__name__}: {e}"
             self._nv = None
 
     def _sample(self):
-        nv = self._nv
-        self.samples.append(nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM))
-        for fn in ("nvmlDeviceGetCurrentClocksEventReasons", "nvmlDeviceGetCurrentClocksThrottleReasons"):
-            if hasattr(nv, fn):
-                try:
-                    self.reasons |= getattr(nv, fn)(self._h)
-                    break
-                except Exception:  # noqa: BLE001
-                    continue
+        self.samples.append(self._nv.sm_clock())
+        self.power.append(self._nv.power_w())
+        self.reasons |= self._nv.reasons()
 
     def _loop(self):
         while not self._stop.is_set():
@@ -148,10 +175,6 @@ class ClockSampler:
         if self._thread is not None:
             self._stop.set()
             self._thread.join()
-            try:
-                self._sample()
-            except Exception as e:  # noqa: BLE001
-                self.error = f"{type(e).__name__}: {e}"
 
     def summary(self):
         if self._nv is None or not self.samples:
@@ -159,6 +182,7 @@ class ClockSampler:
                     "error": self.error}
         names = [n for bit, n in self.REASONS.items() if self.reasons & bit and n != "gpu_idle"]
         return {"sm_mhz": float(np.median(self.samples)), "sm_max_mhz": self.max_mhz,
+                "sm_mhz_min": float(min(self.samples)), "power_w_max": float(max(self.power)),
                 "samples": len(self.samples), "reasons": names}
 
 

@@ -39,10 +39,10 @@ ssm_status_t check_common(int64_t batch, int64_t L, int64_t d_inner, int d_state
 }
 
 size_t scan_workspace_bytes(int64_t batch, int64_t L, int64_t d_inner, int d_state, int sms,
-                            int64_t* chunk_len, int* n_chunks) {
-  ssm::plan_scan_chunks(batch, L, d_inner, sms, chunk_len, n_chunks);
-  if (*n_chunks <= 1) return 0;
-  return (size_t)batch * (size_t)(*n_chunks - 1) * (size_t)d_inner * (size_t)(d_state + 1) *
+                            ssm::ScanPlan* plan) {
+  ssm::plan_scan(batch, L, d_inner, sms, plan);
+  if (plan->n_chunks <= 1) return 0;
+  return (size_t)batch * (size_t)(plan->n_chunks - 1) * (size_t)d_inner * (size_t)(d_state + 1) *
          sizeof(float);
 }
 
@@ -55,9 +55,8 @@ size_t ssm_scan_fwd_workspace_size(int64_t batch, int64_t L, int64_t d_inner, in
   if (check_common(batch, L, d_inner, d_state, io) != SSM_OK) return 0;
   const int sms = current_sm_count();
   if (sms <= 0) return 0;
-  int64_t len;
-  int G;
-  return scan_workspace_bytes(batch, L, d_inner, d_state, sms, &len, &G);
+  ssm::ScanPlan plan;
+  return scan_workspace_bytes(batch, L, d_inner, d_state, sms, &plan);
 }
 
 ssm_status_t ssm_scan_fwd(const void* u, const void* delta, const float* A, const void* B,
@@ -86,7 +85,11 @@ ssm_status_t ssm_scan_fwd(const void* u, const void* delta, const float* A, cons
   }
 
   ssm::ScanParams p{};
-  const size_t need = scan_workspace_bytes(batch, L, d_inner, d_state, sms, &p.chunk_len, &p.n_chunks);
+  ssm::ScanPlan plan;
+  const size_t need = scan_workspace_bytes(batch, L, d_inner, d_state, sms, &plan);
+  p.chunk_len = plan.chunk_len;
+  p.n_chunks = plan.n_chunks;
+  p.lanes = plan.lanes;
   if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return SSM_ERR_WORKSPACE;
   const int64_t cpc = ssm::scan_channels_per_cta();
   const int64_t n_dtiles = (d_inner + cpc - 1) / cpc;

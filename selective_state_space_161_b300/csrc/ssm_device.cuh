@@ -42,6 +42,28 @@ __device__ __forceinline__ float softplus(float x) {
   return fmaxf(x, 0.f) + (e < 0.0625f ? series : viaLog);
 }
 
+// softplus on two values at once (packed fp32x2 arithmetic; same steps as above,
+// with the log1p series as Horner in e: e * (1 + e(-1/2 + e(1/3 + e(-1/4 + e/5))))).
+__device__ __forceinline__ float2 softplus2(float2 x) {
+  const float2 e = make_float2(ex2(-fabsf(x.x) * kLog2e), ex2(-fabsf(x.y) * kLog2e));
+  float2 q = __ffma2_rn(e, make_float2(0.2f, 0.2f), make_float2(-0.25f, -0.25f));
+  q = __ffma2_rn(e, q, make_float2(1.f / 3.f, 1.f / 3.f));
+  q = __ffma2_rn(e, q, make_float2(-0.5f, -0.5f));
+  q = __ffma2_rn(e, q, make_float2(1.f, 1.f));
+  const float2 series = __fmul2_rn(e, q);
+  const float2 ope = __fadd2_rn(e, make_float2(1.f, 1.f));
+  const float2 viaLog = __fmul2_rn(make_float2(lg2(ope.x), lg2(ope.y)), make_float2(kLn2, kLn2));
+  const float2 l = make_float2(e.x < 0.0625f ? series.x : viaLog.x, e.y < 0.0625f ? series.y : viaLog.y);
+  return __fadd2_rn(make_float2(fmaxf(x.x, 0.f), fmaxf(x.y, 0.f)), l);
+}
+
+// silu on two values at once.
+__device__ __forceinline__ float2 silu2(float2 z) {
+  const float2 e = make_float2(ex2(-z.x * kLog2e), ex2(-z.y * kLog2e));
+  const float2 d = __fadd2_rn(e, make_float2(1.f, 1.f));
+  return __fmul2_rn(z, make_float2(rcp(d.x), rcp(d.y)));
+}
+
 // silu(z) = z * sigmoid(z) = z / (1 + e^-z).
 __device__ __forceinline__ float silu(float z) { return z * rcp(1.f + ex2(-z * kLog2e)); }
 

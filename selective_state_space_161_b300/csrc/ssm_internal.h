@@ -26,6 +26,7 @@ struct ScanParams {
   // state started from zero.
   int64_t chunk_len;
   int n_chunks;
+  int lanes;  // 1 or 2 lanes per channel (which kernel runs)
   float* ws_S;  // [batch][n_chunks-1][d_inner]
   float* ws_h;  // [batch][n_chunks-1][d_inner][d_state]
 };
@@ -49,9 +50,14 @@ struct DecodeParams {
 // Channels handled by one CTA of the scan kernels.
 int scan_channels_per_cta();
 
-// Chunking plan for a scan of these sizes on a device with `sms` SMs.
-void plan_scan_chunks(int64_t batch, int64_t L, int64_t d_inner, int sms, int64_t* chunk_len,
-                      int* n_chunks);
+// How a scan of these sizes runs on a device with `sms` SMs: the kernel (lanes per
+// channel) and the time chunking.
+struct ScanPlan {
+  int lanes;
+  int64_t chunk_len;
+  int n_chunks;
+};
+void plan_scan(int64_t batch, int64_t L, int64_t d_inner, int sms, ScanPlan* plan);
 
 cudaError_t launch_scan(const ScanParams& p, bool bf16, cudaStream_t stream);
 cudaError_t launch_state_update(const DecodeParams& p, bool bf16, cudaStream_t stream);

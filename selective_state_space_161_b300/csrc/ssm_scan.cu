@@ -10,30 +10,49 @@
 // The pages' kernel keeps every intermediate (dA, dBu, h) out of HBM; here
 // they live in registers and only u, delta, z, B, C in and y out touch HBM.
 //
-// Parallel structure.  One thread owns one (batch, channel) and all d_state
-// states of it in registers, and walks its time chunk sequentially; a warp
-// covers 32 consecutive channels, so the per-step loads of u, delta, z and
-// the store of y are coalesced along d_inner, and the per-step rows B_t, C_t
-// (shared by every channel) are staged once per CTA in shared memory and read
-// as broadcasts.  When batch * d_inner is too small to fill the GPU, time is
-// cut into chunks.  The recurrence is associative in the pairs (a, b) with
-// (a2, b2) o (a1, b1) = (a2 a1, a2 b1 + b2), so a chunk is summarised by its
-// decay prod_t dA_t = exp(A * sum_t delta_t) and its end state from zero.
-// Pass 1 writes those summaries; pass 2 composes the summaries of the chunks
-// before its own to get its start state, then runs the exact recurrence and
-// writes y.  No kernel waits on another block.
+// Parallel structure.  A CTA covers 32 consecutive channels (d_inner) of one batch row
+// over one time chunk and walks the chunk sequentially; the recurrence state never
+// leaves registers.  Two kernels:
+//  - one lane per channel (32-thread CTAs): a thread keeps all d_state states of its
+//    channel as fp32 pairs and updates them with packed fp32x2 instructions;
+//  - two lanes per channel (64-thread CTAs): each lane keeps half of the states, and the
+//    per-step work that does not touch the state (step size, input, skip term, gate,
+//    output) is split between the two lanes by step parity and exchanged by shuffles.
+//    It doubles the warps for problems with few channels and short sequences.
+// Per tile of 16 steps, delta, u (and z) are staged in shared memory by cp.async
+// (16-byte pieces, coalesced along d_inner) one tile ahead, and the B_t/C_t rows (shared
+// by every channel) are fetched a tile ahead and read as shared-memory broadcasts.
+//
+// Time chunks.  When batch * d_inner cannot fill the GPU, time is cut into chunks.  The
+// recurrence is associative in the pairs (a, b) with (a2, b2) o (a1, b1) =
+// (a2 a1, a2 b1 + b2), so a chunk is summarised by its decay prod_t dA_t =
+// exp(A * sum_t delta_t) and its end state from zero.  Pass 1 writes those summaries
+// for every chunk but the last; pass 2 folds the summaries of the chunks before its own
+// into its start state, then runs the exact recurrence and writes y.  No block waits on
+// another block.
 
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
 
 #include <algorithm>
 #include <cstdlib>
+#include <type_traits>
 
 namespace ssm {
 
-constexpr int kScanCh = 64;    // channels (threads) per CTA
-constexpr int kScanTile = 16;  // time steps per pipelined tile
+constexpr int kScanCh = 32;                          // channels per CTA
+constexpr int kScanThreads = 2 * kScanCh;            // two lanes per channel
+constexpr int kScanTile = 16;                        // time steps per pipelined tile
 constexpr int kChunkAlign = 32;
+
+// How a channel's d_state states are split over its two lanes: each lane owns an
+// even number kHalf of them (padding states, if any, have A = B = C = 0 and stay 0).
+template <int N>
+struct StateSplit {
+  static constexpr int kHalf = ((N + 1) / 2 + 1) / 2 * 2;
+  static constexpr int kPad = 2 * kHalf;
+  static constexpr int kPairs = kHalf / 2;
+};
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {
   const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
@@ -43,25 +62,43 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool va
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
 __device__ __forceinline__ void cp_async_wait_prev() { asm volatile("cp.async.wait_group 1;\n" ::); }
 
-// One CTA: kScanCh consecutive channels of one batch row, one time chunk.
-// kSummary: write the chunk's (sum of delta, end state from zero) instead of y.
-//
-// Per tile of kScanTile steps, the activations delta, u (and z) arrive in
-// shared memory by cp.async (16-byte, coalesced along d_inner) one tile
-// ahead of use, and the B/C rows of the next tile are fetched into registers
-// while the current tile is computed; so no step waits on HBM latency.
+// 16 raw bytes of B/C -> fp32 values in shared memory.
+__device__ __forceinline__ void store_bc_chunk(float* dst, uint4 v, float) {
+  *reinterpret_cast<float4*>(dst) = make_float4(__uint_as_float(v.x), __uint_as_float(v.y),
+                                                __uint_as_float(v.z), __uint_as_float(v.w));
+}
+__device__ __forceinline__ void store_bc_chunk(float* dst, uint4 v, __nv_bfloat16) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int q = 0; q < 2; q++)
+    *reinterpret_cast<float4*>(dst + 4 * q) = make_float4(
+        __uint_as_float(w[2 * q] << 16), __uint_as_float(w[2 * q] & 0xFFFF0000u),
+        __uint_as_float(w[2 * q + 1] << 16), __uint_as_float(w[2 * q + 1] & 0xFFFF0000u));
+}
+
+__device__ __forceinline__ float shfl_pair(float v) { return __shfl_xor_sync(0xFFFFFFFFu, v, 1); }
+
+// One lane per channel: a 32-thread CTA covers kScanCh channels of one batch row over one
+// time chunk; each thread keeps all of its channel's states (as fp32 pairs) in registers.
 template <int N, typename T, bool kSummary>
 __global__ void __launch_bounds__(kScanCh)
-scan_chunk_kernel(const ScanParams p) {
-  constexpr int kVec = 16 / sizeof(T);            // elements per 16-byte copy
-  constexpr int kCopiesPerRow = kScanCh / kVec;
-  constexpr int kNX = kSummary ? 2 : 3;           // delta, u (, z)
-  constexpr int kNBC = kSummary ? 1 : 2;          // B (, C)
-  constexpr int kBCVals = kScanTile * N * kNBC;
-  constexpr int kBCPerThread = (kBCVals + kScanCh - 1) / kScanCh;
+scan_chunk_kernel_1lane(const ScanParams p) {
+  constexpr int kS = sizeof(T);
+  constexpr int kVec = 16 / kS;
+  constexpr int kCPR = kScanCh / kVec;
+  constexpr int kRowsPerPass = kScanCh / kCPR;
+  constexpr int kPasses = kScanTile / kRowsPerPass;
+  constexpr int kNX = kSummary ? 2 : 3;
+  constexpr int kNBC = kSummary ? 1 : 2;
+  constexpr int NP = (N + 1) / 2;
+  constexpr int NPAD = 2 * NP;
+  constexpr bool kVecBC = (N * kS) % 16 == 0;
+  constexpr int kBCChunks = kNBC * kScanTile * N / kVec;
+  constexpr int kBCChunksPerThread = kVecBC ? (kBCChunks + kScanCh - 1) / kScanCh : 1;
+  constexpr int kBCVals = kNBC * kScanTile * N;
+  constexpr int kBCValsPerThread = kVecBC ? 1 : (kBCVals + kScanCh - 1) / kScanCh;
   __shared__ __align__(16) T sX[2][kNX][kScanTile][kScanCh];
-  __shared__ __align__(16) float sBC[2][kNBC][kScanTile][N];
-
+  __shared__ __align__(16) float sBC[2][kNBC][kScanTile][NPAD];
   const int64_t n_dtiles = (p.d_inner + kScanCh - 1) / kScanCh;
   const int chunks = kSummary ? p.n_chunks - 1 : p.n_chunks;
   int64_t blk = blockIdx.x;
@@ -77,57 +114,322 @@ scan_chunk_kernel(const ScanParams p) {
   const int64_t t0 = (int64_t)c * p.chunk_len;
   const int64_t t1 = min(t0 + p.chunk_len, L);
   const int ntiles = (int)((t1 - t0 + kScanTile - 1) / kScanTile);
-
-  const T* __restrict__ u = static_cast<const T*>(p.u);
-  const T* __restrict__ dl = static_cast<const T*>(p.delta);
   const T* __restrict__ Bg = static_cast<const T*>(p.B);
   const T* __restrict__ Cg = static_cast<const T*>(p.C);
-  const T* __restrict__ zg = static_cast<const T*>(p.z);
-  T* __restrict__ yg = static_cast<T*>(p.y);
-  const bool has_z = !kSummary && zg != nullptr;
-
+  const bool has_z = !kSummary && p.z != nullptr;
+  const int nx = kSummary ? 2 : (has_z ? 3 : 2);
+  const int ci = tid % kCPR, rb = tid / kCPR;
+  const bool dvalid = d0 + (int64_t)ci * kVec < Dn;
+  const int64_t row_bytes = Dn * kS;
+  const char* xsrc[3] = {static_cast<const char*>(p.delta), static_cast<const char*>(p.u), static_cast<const char*>(p.z)};
+  const int64_t x_off0 = ((b * L + t0 + rb) * Dn + d0 + (int64_t)ci * kVec) * kS;
   auto issue_x = [&](int tile, int stage) {
-    const int64_t ts = t0 + (int64_t)tile * kScanTile;
-    const int nx = kSummary ? 2 : (has_z ? 3 : 2);
-    for (int i = tid; i < nx * kScanTile * kCopiesPerRow; i += kScanCh) {
-      const int x = i / (kScanTile * kCopiesPerRow);
-      const int r = (i / kCopiesPerRow) % kScanTile;
-      const int ci = i % kCopiesPerRow;
-      const int64_t t = ts + r;
-      const int64_t dd = d0 + (int64_t)ci * kVec;
-      const bool valid = t < t1 && dd < Dn;
-      const T* src = x == 0 ? dl : (x == 1 ? u : zg);
-      cp_async16(&sX[stage][x][r][ci * kVec], valid ? src + (b * L + t) * Dn + dd : src, valid);
+    const int64_t rows0 = (int64_t)tile * kScanTile + rb;
+    const int64_t off = x_off0 + (int64_t)tile * kScanTile * row_bytes;
+#pragma unroll
+    for (int x = 0; x < kNX; x++) {
+      if (x >= nx) break;
+#pragma unroll
+      for (int m = 0; m < kPasses; m++) {
+        const bool valid = dvalid && t0 + rows0 + m * kRowsPerPass < t1;
+        const char* g = xsrc[x] + off + (int64_t)m * kRowsPerPass * row_bytes;
+        cp_async16(&sX[stage][x][rb + m * kRowsPerPass][ci * kVec], valid ? g : xsrc[x], valid);
+      }
     }
   };
-  float bc[kBCPerThread];
+  uint4 bcv[kBCChunksPerThread];
+  float bcs[kBCValsPerThread];
+  const int64_t bc_elems = p.batch * L * N;
   auto load_bc = [&](int tile) {
-    const int64_t ts = t0 + (int64_t)tile * kScanTile;
+    const int64_t e_row0 = (b * L + t0 + (int64_t)tile * kScanTile) * N;
+    const int64_t rows_left = t1 - (t0 + (int64_t)tile * kScanTile);
+    if constexpr (kVecBC) {
 #pragma unroll
-    for (int j = 0; j < kBCPerThread; j++) {
-      const int i = tid + j * kScanCh;
-      float v = 0.f;
-      if (i < kBCVals) {
-        const int which = i / (kScanTile * N), r = (i / N) % kScanTile, n = i % N;
-        const int64_t t = ts + r;
-        if (t < t1) v = to_f32((which ? Cg : Bg)[(b * L + t) * N + n]);
+      for (int j = 0; j < kBCChunksPerThread; j++) {
+        const int q = tid + j * kScanCh;
+        const int which = q / (kScanTile * N / kVec);
+        const int e = (q % (kScanTile * N / kVec)) * kVec;
+        bcv[j] = make_uint4(0, 0, 0, 0);
+        if (q < kBCChunks && e / N < rows_left && e_row0 + e + kVec <= bc_elems)
+          bcv[j] = *reinterpret_cast<const uint4*>((which ? Cg : Bg) + e_row0 + e);
       }
-      bc[j] = v;
+    } else {
+#pragma unroll
+      for (int j = 0; j < kBCValsPerThread; j++) {
+        const int i = tid + j * kScanCh;
+        const int which = i / (kScanTile * N), e = i % (kScanTile * N);
+        bcs[j] = 0.f;
+        if (i < kBCVals && e / N < rows_left) bcs[j] = to_f32((which ? Cg : Bg)[e_row0 + e]);
+      }
     }
   };
   auto store_bc = [&](int stage) {
+    if constexpr (kVecBC) {
 #pragma unroll
-    for (int j = 0; j < kBCPerThread; j++) {
-      const int i = tid + j * kScanCh;
-      if (i < kBCVals) sBC[stage][i / (kScanTile * N)][(i / N) % kScanTile][i % N] = bc[j];
+      for (int j = 0; j < kBCChunksPerThread; j++) {
+        const int q = tid + j * kScanCh;
+        if (q < kBCChunks) {
+          const int which = q / (kScanTile * N / kVec);
+          const int e = (q % (kScanTile * N / kVec)) * kVec;
+          store_bc_chunk(&sBC[stage][which][0][0] + e, bcv[j], T());
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < kBCValsPerThread; j++) {
+        const int i = tid + j * kScanCh;
+        if (i < kBCVals) {
+          const int which = i / (kScanTile * N), e = i % (kScanTile * N);
+          sBC[stage][which][e / N][e % N] = bcs[j];
+        }
+      }
+    }
+  };
+  if constexpr (NPAD != N) {
+    for (int i = tid; i < 2 * kNBC * kScanTile; i += kScanCh) (&sBC[0][0][0][0])[i * NPAD + N] = 0.f;
+  }
+  float2 A2[NP], h[NP];
+#pragma unroll
+  for (int j = 0; j < NP; j++) {
+    const float a0 = active ? p.A[d * N + 2 * j] * kLog2e : 0.f;
+    const float a1 = (active && 2 * j + 1 < N) ? p.A[d * N + 2 * j + 1] * kLog2e : 0.f;
+    A2[j] = make_float2(a0, a1);
+    h[j] = make_float2(0.f, 0.f);
+  }
+  const float Dd = (active && p.D) ? p.D[d] : 0.f;
+  const float bias = (active && p.delta_bias) ? p.delta_bias[d] : 0.f;
+  const bool sp = p.softplus != 0;
+  if (ntiles > 0) { issue_x(0, 0); cp_async_commit(); load_bc(0); store_bc(0); }
+  if (!kSummary && c > 0 && active) {
+    const int64_t base = b * (p.n_chunks - 1);
+    for (int j = 0; j < c; j++) {
+      const float S = p.ws_S[(base + j) * Dn + d];
+      const float* hj = p.ws_h + ((base + j) * Dn + d) * N;
+#pragma unroll
+      for (int q = 0; q < NP; q++) {
+        const float e0 = hj[2 * q];
+        const float e1 = (2 * q + 1 < N) ? hj[2 * q + 1] : 0.f;
+        h[q].x = fmaf(ex2(A2[q].x * S), h[q].x, e0);
+        h[q].y = fmaf(ex2(A2[q].y * S), h[q].y, e1);
+      }
+    }
+  }
+  float S = 0.f, S_comp = 0.f;
+  T* __restrict__ yg = static_cast<T*>(p.y);
+  auto step = [&](int stage, int k, T* yrow) {
+    const float x = to_f32(sX[stage][0][k][tid]) + bias;
+    const float dt = sp ? softplus(x) : x;
+    const float uu = to_f32(sX[stage][1][k][tid]);
+    const float w = dt * uu;
+    if (kSummary) { const float yk = dt - S_comp; const float tk = S + yk; S_comp = (tk - S) - yk; S = tk; }
+    const float2 dt2 = make_float2(dt, dt), w2 = make_float2(w, w);
+    const float* Bk = sBC[stage][0][k];
+    const float* Ck = sBC[stage][kNBC - 1][k];
+    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < NP; j++) {
+      float2 Bv, Cv;
+      if constexpr (NPAD % 4 == 0) {
+        const float4 b4 = *reinterpret_cast<const float4*>(Bk + 4 * (j / 2));
+        Bv = (j & 1) ? make_float2(b4.z, b4.w) : make_float2(b4.x, b4.y);
+        if (!kSummary) { const float4 c4 = *reinterpret_cast<const float4*>(Ck + 4 * (j / 2)); Cv = (j & 1) ? make_float2(c4.z, c4.w) : make_float2(c4.x, c4.y); }
+      } else {
+        Bv = *reinterpret_cast<const float2*>(Bk + 2 * j);
+        if (!kSummary) Cv = *reinterpret_cast<const float2*>(Ck + 2 * j);
+      }
+      const float2 xa = __fmul2_rn(dt2, A2[j]);
+      const float2 dA = make_float2(ex2(xa.x), ex2(xa.y));
+      h[j] = __ffma2_rn(dA, h[j], __fmul2_rn(w2, Bv));
+      if (!kSummary) { if (j & 1) acc1 = __ffma2_rn(Cv, h[j], acc1); else acc0 = __ffma2_rn(Cv, h[j], acc0); }
+    }
+    if (!kSummary) {
+      const float2 a = __fadd2_rn(acc0, acc1);
+      float yv = fmaf(Dd, uu, a.x + a.y);
+      if (has_z) yv *= silu(to_f32(sX[stage][kNX - 1][k][tid]));
+      *yrow = from_f32<T>(yv);
+    }
+  };
+  for (int tile = 0; tile < ntiles; tile++) {
+    const int stage = tile & 1;
+    if (tile + 1 < ntiles) { issue_x(tile + 1, stage ^ 1); load_bc(tile + 1); }
+    cp_async_commit();
+    cp_async_wait_prev();
+    __syncthreads();
+    const int64_t ts = t0 + (int64_t)tile * kScanTile;
+    T* yrow = yg + (b * L + ts) * Dn + d;
+    if (active) {
+      if (ts + kScanTile <= t1) {
+#pragma unroll
+        for (int k = 0; k < kScanTile; k++) step(stage, k, yrow + k * Dn);
+      } else {
+        const int steps = (int)(t1 - ts);
+        for (int k = 0; k < steps; k++) step(stage, k, yrow + k * Dn);
+      }
+    }
+    __syncthreads();
+    if (tile + 1 < ntiles) store_bc(stage ^ 1);
+  }
+  if (!active) return;
+  if (kSummary) {
+    const int64_t slot = (b * (p.n_chunks - 1) + c) * Dn + d;
+    p.ws_S[slot] = S;
+#pragma unroll
+    for (int j = 0; j < NP; j++) { p.ws_h[slot * N + 2 * j] = h[j].x; if (2 * j + 1 < N) p.ws_h[slot * N + 2 * j + 1] = h[j].y; }
+  } else if (c == p.n_chunks - 1 && p.last_state) {
+    float* ls = p.last_state + (b * Dn + d) * N;
+#pragma unroll
+    for (int j = 0; j < NP; j++) { ls[2 * j] = h[j].x; if (2 * j + 1 < N) ls[2 * j + 1] = h[j].y; }
+  }
+}
+
+
+// One CTA: kScanCh consecutive channels of one batch row over one time chunk.
+// Lanes 2c and 2c+1 of a warp share channel c: each owns half of its states,
+// and the per-step work that does not involve the state (step size, input,
+// skip term, gate, output) is split between them by step parity and exchanged
+// with one shuffle per value.  kSummary: the CTA writes the chunk's (sum of
+// delta, end state from zero) instead of y.
+//
+// Data movement per tile of kScanTile steps: delta, u (and z) arrive in shared
+// memory by cp.async (16-byte pieces, coalesced along d_inner) one tile ahead
+// of use; the next tile's B/C rows are fetched into registers while the current
+// tile is computed and converted to fp32 in shared memory.  So no step waits on
+// HBM latency.  State pairs are updated with packed fp32x2 instructions.
+template <int N, typename T, bool kSummary>
+__global__ void __launch_bounds__(kScanThreads)
+scan_chunk_kernel_2lane(const ScanParams p) {
+  using SS = StateSplit<N>;
+  constexpr int kHalf = SS::kHalf, NPAD = SS::kPad, kPairs = SS::kPairs;
+  constexpr int kS = sizeof(T);
+  constexpr int kVec = 16 / kS;                       // elements per 16-byte copy
+  constexpr int kRow = kScanCh + (kS == 4 ? 16 : 0);  // fp32 rows padded: no bank conflict
+  constexpr int kCPR = kScanCh / kVec;                // copies per activation row
+  constexpr int kRowsPerPass = kScanThreads / kCPR;
+  constexpr int kPasses = kScanTile / kRowsPerPass;
+  constexpr int kNX = kSummary ? 2 : 3;               // delta, u (, z)
+  constexpr int kNBC = kSummary ? 1 : 2;              // B (, C)
+  constexpr int kHalfSteps = kScanTile / 2;
+  // B/C rows move as 16-byte vectors when a row is a whole number of them and unpadded.
+  constexpr bool kVecBC = (N * kS) % 16 == 0 && NPAD == N;
+  constexpr int kBCChunks = kNBC * kScanTile * N / kVec;
+  constexpr int kBCChunksPerThread = kVecBC ? (kBCChunks + kScanThreads - 1) / kScanThreads : 1;
+  constexpr int kBCVals = kNBC * kScanTile * N;
+  constexpr int kBCValsPerThread = kVecBC ? 1 : (kBCVals + kScanThreads - 1) / kScanThreads;
+  static_assert(kScanTile % kRowsPerPass == 0 && kPasses >= 1, "tile rows must split evenly");
+  __shared__ __align__(16) T sX[2][kNX][kScanTile][kRow];
+  __shared__ __align__(16) float sBC[2][kNBC][kScanTile][NPAD];
+
+  const int64_t n_dtiles = (p.d_inner + kScanCh - 1) / kScanCh;
+  const int chunks = kSummary ? p.n_chunks - 1 : p.n_chunks;
+  int64_t blk = blockIdx.x;
+  const int64_t dtile = blk % n_dtiles;
+  blk /= n_dtiles;
+  const int c = (int)(blk % chunks);
+  const int64_t b = blk / chunks;
+  const int tid = threadIdx.x;
+  const int cl = ((tid >> 5) << 4) | ((tid & 31) >> 1);  // channel within the CTA
+  const int par = tid & 1;                                // this lane's half / step parity
+  const int64_t Dn = p.d_inner, L = p.L;
+  const int64_t d0 = dtile * kScanCh;
+  const int64_t d = d0 + cl;
+  const bool active = d < Dn;
+  const int64_t t0 = (int64_t)c * p.chunk_len;
+  const int64_t t1 = min(t0 + p.chunk_len, L);
+  const int ntiles = (int)((t1 - t0 + kScanTile - 1) / kScanTile);
+
+  const T* __restrict__ Bg = static_cast<const T*>(p.B);
+  const T* __restrict__ Cg = static_cast<const T*>(p.C);
+  const bool has_z = !kSummary && p.z != nullptr;
+  const int nx = kSummary ? 2 : (has_z ? 3 : 2);
+
+  // Activation copies: thread moves 16-byte piece ci of rows rb, rb + kRowsPerPass, ...
+  const int ci = tid % kCPR, rb = tid / kCPR;
+  const bool dvalid = d0 + (int64_t)ci * kVec < Dn;
+  const int64_t row_bytes = Dn * kS;
+  const char* xsrc[3] = {static_cast<const char*>(p.delta), static_cast<const char*>(p.u),
+                         static_cast<const char*>(p.z)};
+  const int64_t x_off0 = ((b * L + t0 + rb) * Dn + d0 + (int64_t)ci * kVec) * kS;
+  auto issue_x = [&](int tile, int stage) {
+    const int64_t rows0 = (int64_t)tile * kScanTile + rb;
+    const int64_t off = x_off0 + (int64_t)tile * kScanTile * row_bytes;
+#pragma unroll
+    for (int x = 0; x < kNX; x++) {
+      if (x >= nx) break;
+#pragma unroll
+      for (int m = 0; m < kPasses; m++) {
+        const bool valid = dvalid && t0 + rows0 + m * kRowsPerPass < t1;
+        const char* g = xsrc[x] + off + (int64_t)m * kRowsPerPass * row_bytes;
+        cp_async16(&sX[stage][x][rb + m * kRowsPerPass][ci * kVec], valid ? g : xsrc[x], valid);
+      }
     }
   };
 
-  float A2[N], h[N];
+  // B/C rows of a tile: global -> registers (a tile ahead) -> fp32 shared memory.
+  uint4 bcv[kBCChunksPerThread];
+  float bcs[kBCValsPerThread];
+  const int64_t bc_elems = p.batch * L * N;
+  auto load_bc = [&](int tile) {
+    const int64_t e_row0 = (b * L + t0 + (int64_t)tile * kScanTile) * N;
+    const int64_t rows_left = t1 - (t0 + (int64_t)tile * kScanTile);
+    if constexpr (kVecBC) {
 #pragma unroll
-  for (int n = 0; n < N; n++) {
-    A2[n] = active ? p.A[d * N + n] * kLog2e : 0.f;  // exp(x) = 2^(x log2 e)
-    h[n] = 0.f;
+      for (int j = 0; j < kBCChunksPerThread; j++) {
+        const int q = tid + j * kScanThreads;
+        const int which = q / (kScanTile * N / kVec);
+        const int e = (q % (kScanTile * N / kVec)) * kVec;  // element within the tile
+        bcv[j] = make_uint4(0, 0, 0, 0);
+        if (q < kBCChunks && e / N < rows_left && e_row0 + e + kVec <= bc_elems)
+          bcv[j] = *reinterpret_cast<const uint4*>((which ? Cg : Bg) + e_row0 + e);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < kBCValsPerThread; j++) {
+        const int i = tid + j * kScanThreads;
+        const int which = i / (kScanTile * N), e = i % (kScanTile * N);
+        bcs[j] = 0.f;
+        if (i < kBCVals && e / N < rows_left) bcs[j] = to_f32((which ? Cg : Bg)[e_row0 + e]);
+      }
+    }
+  };
+  auto store_bc = [&](int stage) {
+    if constexpr (kVecBC) {
+#pragma unroll
+      for (int j = 0; j < kBCChunksPerThread; j++) {
+        const int q = tid + j * kScanThreads;
+        if (q < kBCChunks) {
+          const int which = q / (kScanTile * N / kVec);
+          const int e = (q % (kScanTile * N / kVec)) * kVec;
+          store_bc_chunk(&sBC[stage][which][0][0] + e, bcv[j], T());
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < kBCValsPerThread; j++) {
+        const int i = tid + j * kScanThreads;
+        if (i < kBCVals) {
+          const int which = i / (kScanTile * N), e = i % (kScanTile * N);
+          sBC[stage][which][e / N][e % N] = bcs[j];
+        }
+      }
+    }
+  };
+
+  if constexpr (NPAD != N) {
+    // padding states read B = C = 0 from columns that are never overwritten
+    for (int i = tid; i < 2 * kNBC * kScanTile * (NPAD - N); i += kScanThreads)
+      (&sBC[0][0][0][0])[(i / (NPAD - N)) * NPAD + N + i % (NPAD - N)] = 0.f;
+  }
+
+  // This lane's states: par * kHalf + 2j, +1 (j < kPairs).
+  const int n0 = par * kHalf;
+  float2 A2[kPairs], h[kPairs];
+#pragma unroll
+  for (int j = 0; j < kPairs; j++) {
+    const int na = n0 + 2 * j, nb = na + 1;
+    const float a0 = (active && na < N) ? p.A[d * N + na] * kLog2e : 0.f;  // e^x = 2^(x log2 e)
+    const float a1 = (active && nb < N) ? p.A[d * N + nb] * kLog2e : 0.f;
+    A2[j] = make_float2(a0, a1);
+    h[j] = make_float2(0.f, 0.f);
   }
   const float Dd = (active && p.D) ? p.D[d] : 0.f;
   const float bias = (active && p.delta_bias) ? p.delta_bias[d] : 0.f;
@@ -147,38 +449,16 @@ scan_chunk_kernel(const ScanParams p) {
       const float S = p.ws_S[(base + j) * Dn + d];
       const float* hj = p.ws_h + ((base + j) * Dn + d) * N;
 #pragma unroll
-      for (int n = 0; n < N; n++) h[n] = fmaf(ex2(A2[n] * S), h[n], hj[n]);
+      for (int q = 0; q < kPairs; q++) {
+        const int na = n0 + 2 * q, nb = na + 1;
+        h[q].x = fmaf(ex2(A2[q].x * S), h[q].x, na < N ? hj[na] : 0.f);
+        h[q].y = fmaf(ex2(A2[q].y * S), h[q].y, nb < N ? hj[nb] : 0.f);
+      }
     }
   }
 
   float S = 0.f, S_comp = 0.f;  // compensated (Kahan) sum of delta over the chunk
-
-  // One time step of the recurrence for this thread's channel.
-  auto step = [&](int stage, int k, int64_t t) {
-    const float x = to_f32(sX[stage][0][k][tid]) + bias;
-    const float dt = sp ? softplus(x) : x;
-    const float uu = to_f32(sX[stage][1][k][tid]);
-    const float w = dt * uu;
-    if (kSummary) {
-      const float yk = dt - S_comp;
-      const float tk = S + yk;
-      S_comp = (tk - S) - yk;
-      S = tk;
-    }
-    const float* Bk = sBC[stage][0][k];
-    float acc = 0.f;
-#pragma unroll
-    for (int n = 0; n < N; n++) {
-      const float dA = ex2(dt * A2[n]);
-      h[n] = fmaf(dA, h[n], w * Bk[n]);
-      if (!kSummary) acc = fmaf(sBC[stage][kNBC - 1][k][n], h[n], acc);
-    }
-    if (!kSummary) {
-      acc = fmaf(Dd, uu, acc);
-      if (has_z) acc *= silu(to_f32(sX[stage][kNX - 1][k][tid]));
-      yg[(b * L + t) * Dn + d] = from_f32<T>(acc);
-    }
-  };
+  T* __restrict__ yg = static_cast<T*>(p.y);
 
   for (int tile = 0; tile < ntiles; tile++) {
     const int stage = tile & 1;
@@ -190,13 +470,101 @@ scan_chunk_kernel(const ScanParams p) {
     cp_async_wait_prev();  // this tile's copies have landed (only the newest group may pend)
     __syncthreads();
     const int64_t ts = t0 + (int64_t)tile * kScanTile;
-    if (active) {
-      if (ts + kScanTile <= t1) {
-#pragma unroll 4
-        for (int k = 0; k < kScanTile; k++) step(stage, k, ts + k);
-      } else {
-        const int steps = (int)(t1 - ts);
-        for (int k = 0; k < steps; k++) step(stage, k, ts + k);
+    const int steps = (int)min((int64_t)kScanTile, t1 - ts);
+
+    // (1) Own steps k = 2i + par: step size, input, skip term, gate (packed over i, i+1).
+    float odt[kHalfSteps], ow[kHalfSteps], odu[kHalfSteps], og[kHalfSteps];
+#pragma unroll
+    for (int i = 0; i < kHalfSteps; i += 2) {
+      const int k0 = 2 * i + par, k1 = k0 + 2;
+      const float2 x = __fadd2_rn(make_float2(to_f32(sX[stage][0][k0][cl]), to_f32(sX[stage][0][k1][cl])),
+                                  make_float2(bias, bias));
+      const float2 dt = sp ? softplus2(x) : x;
+      const float2 uu = make_float2(to_f32(sX[stage][1][k0][cl]), to_f32(sX[stage][1][k1][cl]));
+      const float2 w = __fmul2_rn(dt, uu);
+      odt[i] = dt.x; odt[i + 1] = dt.y;
+      ow[i] = w.x; ow[i + 1] = w.y;
+      if (!kSummary) {
+        const float2 du = __fmul2_rn(make_float2(Dd, Dd), uu);
+        odu[i] = du.x; odu[i + 1] = du.y;
+        if (has_z) {
+          const float2 g = silu2(make_float2(to_f32(sX[stage][kNX - 1][k0][cl]),
+                                             to_f32(sX[stage][kNX - 1][k1][cl])));
+          og[i] = g.x; og[i + 1] = g.y;
+        }
+      }
+    }
+
+    // (2) The recurrence over every step of the tile on this lane's states.  Full tiles take
+    // the unguarded copy (straight-line code the scheduler can overlap across steps).
+    float part[kScanTile];
+    auto recur_tile = [&](auto guarded) {
+      constexpr bool kGuard = decltype(guarded)::value;
+#pragma unroll
+      for (int i = 0; i < kHalfSteps; i++) {
+        const float rdt = shfl_pair(odt[i]), rw = shfl_pair(ow[i]);
+#pragma unroll
+        for (int e = 0; e < 2; e++) {
+          const int k = 2 * i + e;
+          const bool mine = (e == par);
+          const float dt = mine ? odt[i] : rdt;
+          const float w = mine ? ow[i] : rw;
+          if (!kGuard || k < steps) {
+            if (kSummary) {
+              const float yk = dt - S_comp;
+              const float tk = S + yk;
+              S_comp = (tk - S) - yk;
+              S = tk;
+            }
+            const float2 dt2 = make_float2(dt, dt), w2 = make_float2(w, w);
+            const float* Bk = &sBC[stage][0][k][n0];
+            const float* Ck = &sBC[stage][kNBC - 1][k][n0];
+            float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < kPairs; j++) {
+              float2 Bv, Cv;
+              if constexpr (kHalf % 4 == 0) {
+                const float4 b4 = *reinterpret_cast<const float4*>(Bk + 4 * (j / 2));
+                Bv = (j & 1) ? make_float2(b4.z, b4.w) : make_float2(b4.x, b4.y);
+                if (!kSummary) {
+                  const float4 c4 = *reinterpret_cast<const float4*>(Ck + 4 * (j / 2));
+                  Cv = (j & 1) ? make_float2(c4.z, c4.w) : make_float2(c4.x, c4.y);
+                }
+              } else {
+                Bv = *reinterpret_cast<const float2*>(Bk + 2 * j);
+                if (!kSummary) Cv = *reinterpret_cast<const float2*>(Ck + 2 * j);
+              }
+              const float2 xa = __fmul2_rn(dt2, A2[j]);
+              const float2 dA = make_float2(ex2(xa.x), ex2(xa.y));
+              h[j] = __ffma2_rn(dA, h[j], __fmul2_rn(w2, Bv));
+              if (!kSummary) {
+                if (j & 1) acc1 = __ffma2_rn(Cv, h[j], acc1);
+                else acc0 = __ffma2_rn(Cv, h[j], acc0);
+              }
+            }
+            if (!kSummary) {
+              const float2 a = __fadd2_rn(acc0, acc1);
+              part[k] = a.x + a.y;
+            }
+          } else if (!kSummary) {
+            part[k] = 0.f;
+          }
+        }
+      }
+    };
+    if (steps == kScanTile) recur_tile(std::false_type{});
+    else recur_tile(std::true_type{});
+
+    // (3) Own output steps: add the partner lane's half of C.h, skip term and gate.
+    if (!kSummary) {
+      T* yrow = yg + (b * L + ts + par) * Dn + d;
+#pragma unroll
+      for (int i = 0; i < kHalfSteps; i++) {
+        const float give = par ? part[2 * i] : part[2 * i + 1];
+        const float keep = par ? part[2 * i + 1] : part[2 * i];
+        float v = keep + shfl_pair(give) + odu[i];
+        if (has_z) v *= og[i];
+        if (active && 2 * i + par < steps) yrow[(int64_t)2 * i * Dn] = from_f32<T>(v);
       }
     }
     __syncthreads();  // stage is free for the tile after next
@@ -206,49 +574,70 @@ scan_chunk_kernel(const ScanParams p) {
   if (!active) return;
   if (kSummary) {
     const int64_t slot = (b * (p.n_chunks - 1) + c) * Dn + d;
-    p.ws_S[slot] = S;
+    if (par == 0) p.ws_S[slot] = S;
 #pragma unroll
-    for (int n = 0; n < N; n++) p.ws_h[slot * N + n] = h[n];
+    for (int j = 0; j < kPairs; j++) {
+      const int na = n0 + 2 * j, nb = na + 1;
+      if (na < N) p.ws_h[slot * N + na] = h[j].x;
+      if (nb < N) p.ws_h[slot * N + nb] = h[j].y;
+    }
   } else if (c == p.n_chunks - 1 && p.last_state) {
+    float* ls = p.last_state + (b * Dn + d) * N;
 #pragma unroll
-    for (int n = 0; n < N; n++) p.last_state[(b * Dn + d) * N + n] = h[n];
+    for (int j = 0; j < kPairs; j++) {
+      const int na = n0 + 2 * j, nb = na + 1;
+      if (na < N) ls[na] = h[j].x;
+      if (nb < N) ls[nb] = h[j].y;
+    }
   }
 }
 
 int scan_channels_per_cta() { return kScanCh; }
 
-void plan_scan_chunks(int64_t batch, int64_t L, int64_t d_inner, int sms, int64_t* chunk_len,
-                      int* n_chunks) {
-  // Aim for at least `target` resident threads (channels x chunks); chunking
-  // costs a second pass over all but the last chunk, so split only when the
-  // channels alone leave the GPU short of warps.
-  int64_t target_threads_per_sm = 256;
-  if (const char* env = std::getenv("SSM_SCAN_THREADS_PER_SM")) {
-    const long v = std::atol(env);
-    if (v > 0) target_threads_per_sm = v;
+static int64_t env_int(const char* name, int64_t fallback) {
+  if (const char* v = std::getenv(name)) {
+    const long long x = std::atoll(v);
+    if (x > 0) return x;
   }
+  return fallback;
+}
+
+void plan_scan(int64_t batch, int64_t L, int64_t d_inner, int sms, ScanPlan* plan) {
+  // Kernel choice: two lanes per channel doubles the warps for short sequences over few
+  // channels; long sequences get their parallelism from time chunks instead.
   const int64_t channels = batch * d_inner;
-  const int64_t target = (int64_t)sms * target_threads_per_sm;
+  int lanes = (L <= 16384 && channels < (int64_t)sms * 128) ? 2 : 1;
+  lanes = (int)env_int("SSM_SCAN_LANES", lanes) == 2 ? 2 : 1;
+  // Time chunks: none when the channels alone give each SM >= 8 warps; otherwise, since
+  // chunking costs a summary pass over all but the last chunk whatever their number,
+  // cut enough chunks for ~32 warps per SM (at least 64 steps per chunk).
+  const int64_t threads = channels * lanes;
+  const int64_t full = (int64_t)sms * env_int("SSM_SCAN_THREADS_PER_SM", 1024);
   int64_t G = 1;
-  if (channels > 0 && channels < target) G = (target + channels - 1) / channels;
-  const int64_t min_chunk = 64;
-  G = std::min<int64_t>(G, std::max<int64_t>(1, L / min_chunk));
+  if (threads > 0 && threads < (int64_t)sms * 256) G = (full + threads - 1) / threads;
+  G = std::min<int64_t>(G, std::max<int64_t>(1, L / 64));
   G = std::min<int64_t>(G, 4096);
   int64_t len = L > 0 ? (L + G - 1) / G : 1;
   len = (len + kChunkAlign - 1) / kChunkAlign * kChunkAlign;
-  *chunk_len = len;
-  *n_chunks = L > 0 ? (int)((L + len - 1) / len) : 1;
+  plan->lanes = lanes;
+  plan->chunk_len = len;
+  plan->n_chunks = L > 0 ? (int)((L + len - 1) / len) : 1;
 }
 
 template <int N, typename T>
 static cudaError_t launch_scan_t(const ScanParams& p, cudaStream_t stream) {
   const int64_t n_dtiles = (p.d_inner + kScanCh - 1) / kScanCh;
-  if (p.n_chunks > 1) {
-    const int64_t blocks = n_dtiles * (p.n_chunks - 1) * p.batch;
-    scan_chunk_kernel<N, T, true><<<(unsigned)blocks, kScanCh, 0, stream>>>(p);
+  const int64_t sblocks = n_dtiles * (p.n_chunks - 1) * p.batch;
+  const int64_t mblocks = n_dtiles * p.n_chunks * p.batch;
+  if (p.lanes == 2) {
+    if (p.n_chunks > 1)
+      scan_chunk_kernel_2lane<N, T, true><<<(unsigned)sblocks, kScanThreads, 0, stream>>>(p);
+    scan_chunk_kernel_2lane<N, T, false><<<(unsigned)mblocks, kScanThreads, 0, stream>>>(p);
+  } else {
+    if (p.n_chunks > 1)
+      scan_chunk_kernel_1lane<N, T, true><<<(unsigned)sblocks, kScanCh, 0, stream>>>(p);
+    scan_chunk_kernel_1lane<N, T, false><<<(unsigned)mblocks, kScanCh, 0, stream>>>(p);
   }
-  const int64_t blocks = n_dtiles * p.n_chunks * p.batch;
-  scan_chunk_kernel<N, T, false><<<(unsigned)blocks, kScanCh, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

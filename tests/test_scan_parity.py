@@ -165,3 +165,13 @@ def test_bad_arguments_raise():
         # offset view: data pointer no longer 16-byte aligned
         xs = torch.zeros(1 * 4 * 8 + 1, device="cuda")[1:].view(1, 4, 8)
         ssm.ssm_scan_fwd(xs, x, A, Bm, Bm, None, None, None, True, y, None, None)
+
+
+@pytest.mark.parametrize("lanes", ["1", "2"])
+@pytest.mark.parametrize("bf16,d_state,batch,L,d_inner", [
+    (False, 16, 2, 3000, 96), (True, 16, 1, 4100, 64), (False, 5, 3, 700, 40), (True, 1, 2, 257, 24)])
+def test_both_kernels(lanes, bf16, d_state, batch, L, d_inner, monkeypatch):
+    """Both kernels (one or two lanes per channel), chunked and ragged, against the oracle."""
+    monkeypatch.setenv("SSM_SCAN_LANES", lanes)
+    w, raw = _random_case(batch, L, d_inner, d_state, bf16, seed=900 + d_state + int(lanes))
+    _check(w, raw)
