@@ -65,7 +65,8 @@ typedef enum {
   SSM_ERR_DTYPE = 3,      /* io is neither SSM_F32 nor SSM_BF16 */
   SSM_ERR_ALIGN = 4,      /* a pointer is not 16-byte aligned */
   SSM_ERR_WORKSPACE = 5,  /* workspace NULL or smaller than the size query says */
-  SSM_ERR_CUDA = 6        /* no usable CUDA device, or a launch failed */
+  SSM_ERR_CUDA = 6,       /* no usable CUDA device, or a launch failed */
+  SSM_ERR_SCRATCH_LIMIT = 7 /* ssm_scan_fwd_noalloc: the problem needs more scratch than it holds */
 } ssm_status_t;
 
 /*
@@ -107,6 +108,38 @@ SSM_API ssm_status_t ssm_state_update(float* state, const void* u, const void* d
                               const void* B, const void* C, const float* D, const void* z,
                               void* y, const float* delta_bias, int softplus_flag, int64_t batch,
                               int64_t d_inner, int d_state, ssm_dtype_t io, void* stream);
+
+/*
+ * ssm_scan_fwd without a caller-supplied workspace, for callers that cannot allocate
+ * device memory at the point of the call: code that runs under an allocator it does not
+ * own (a framework plugin or custom operator whose host forbids allocations while it
+ * executes), latency-critical loops where a cudaMalloc/cudaFree would synchronise the
+ * device, or embedded callers held to a fixed memory budget.  (The pages have no
+ * counterpart to this entry point; it exists for such callers only.)
+ *
+ * Same arguments, results and requirements as ssm_scan_fwd, minus the workspace.  The
+ * scratch it needs (one delta sum and one end state per time chunk and channel) comes
+ * from an array of SSM_NOALLOC_SCRATCH_BYTES (8 MiB) that the library places in device
+ * memory at load time; every GPU that loads the library keeps that array until the
+ * process exits.  Problems whose scratch need, as reported by
+ * ssm_scan_fwd_workspace_size, exceeds it return SSM_ERR_SCRATCH_LIMIT without launching
+ * anything (an fp32 scan of 2 x 2048 x 1536 x 16 needs 5 MiB; a single 1,048,576-token
+ * sequence over 2048 channels needs about 10 MiB and is rejected).
+ * - The first call on each device looks up the array's device address (with that device
+ *   current) and caches it; make that first call before any stream capture.
+ * - All calls share the one array: calls whose executions overlap on the GPU (on
+ *   different streams, or from different threads) race on it and give wrong results.
+ *   Serialise them.  The array needs no clearing: every value a call reads was written
+ *   earlier in the same call.
+ * - It allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ */
+#define SSM_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+SSM_API ssm_status_t ssm_scan_fwd_noalloc(const void* u, const void* delta, const float* A,
+                                          const void* B, const void* C, const float* D,
+                                          const void* z, const float* delta_bias,
+                                          int softplus_flag, void* y, float* last_state,
+                                          int64_t batch, int64_t L, int64_t d_inner,
+                                          int d_state, ssm_dtype_t io, void* stream);
 
 /* Human-readable name of a status code (static string). */
 SSM_API const char* ssm_status_string(ssm_status_t status);

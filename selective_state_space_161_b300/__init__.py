@@ -19,13 +19,15 @@ import torch
 
 from .build import LIB_PATH, build
 
-__all__ = ["SsmError", "ssm_scan_fwd", "ssm_state_update", "ssm_scan_fwd_workspace_size",
+__all__ = ["SsmError", "ssm_scan_fwd", "ssm_scan_fwd_noalloc", "ssm_state_update",
+           "ssm_scan_fwd_workspace_size",
            "ssm_status_string", "ssm_version", "selective_scan", "selective_state_update",
            "load_library", "build", "SSM_F32", "SSM_BF16", "EXPORTED_SYMBOLS"]
 
 SSM_F32, SSM_BF16 = 0, 1
-EXPORTED_SYMBOLS = ("ssm_scan_fwd_workspace_size", "ssm_scan_fwd", "ssm_state_update",
-                    "ssm_status_string", "ssm_version")
+EXPORTED_SYMBOLS = ("ssm_scan_fwd_workspace_size", "ssm_scan_fwd", "ssm_scan_fwd_noalloc",
+                    "ssm_state_update", "ssm_status_string", "ssm_version")
+SSM_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 _lib = None
 
@@ -50,6 +52,9 @@ def load_library() -> ctypes.CDLL:
         lib.ssm_scan_fwd.argtypes = [vp] * 8 + [c_int, vp, vp, i64, i64, i64, c_int, c_int, vp,
                                               ctypes.c_size_t, vp]
         lib.ssm_scan_fwd.restype = c_int
+        lib.ssm_scan_fwd_noalloc.argtypes = [vp] * 8 + [c_int, vp, vp, i64, i64, i64, c_int, c_int,
+                                                       vp]
+        lib.ssm_scan_fwd_noalloc.restype = c_int
         lib.ssm_state_update.argtypes = [vp] * 10 + [c_int, i64, i64, c_int, c_int, vp]
         lib.ssm_state_update.restype = c_int
         lib.ssm_status_string.argtypes = [c_int]
@@ -127,6 +132,32 @@ def ssm_scan_fwd(u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, last_sta
                                      _ptr(workspace), ws_bytes, _stream_handle(stream))
     if rc != 0:
         raise SsmError("ssm_scan_fwd", rc)
+
+
+def ssm_scan_fwd_noalloc(u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, last_state,
+                         stream=None) -> None:
+    """C-ABI ``ssm_scan_fwd_noalloc``: ``ssm_scan_fwd`` with the library's own fixed scratch
+    instead of a caller workspace, for callers that cannot allocate device memory where they
+    call it.  Calls that overlap on the GPU share that scratch and must be serialised."""
+    batch, L, d_inner = u.shape
+    d_state = A.shape[1]
+    io = _io_code(u)
+    dt = u.dtype
+    for name, t, shp in (("u", u, (batch, L, d_inner)), ("delta", delta, (batch, L, d_inner)),
+                         ("z", z, (batch, L, d_inner)), ("y", y, (batch, L, d_inner)),
+                         ("B", B, (batch, L, d_state)), ("C", C, (batch, L, d_state))):
+        _check_dev(name, t, dt, shp)
+    _check_dev("A", A, torch.float32, (d_inner, d_state))
+    _check_dev("D", D, torch.float32, (d_inner,))
+    _check_dev("delta_bias", delta_bias, torch.float32, (d_inner,))
+    _check_dev("last_state", last_state, torch.float32, (batch, d_inner, d_state))
+    rc = load_library().ssm_scan_fwd_noalloc(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
+                                             _ptr(D), _ptr(z), _ptr(delta_bias),
+                                             int(bool(softplus_flag)), _ptr(y), _ptr(last_state),
+                                             batch, L, d_inner, d_state, io,
+                                             _stream_handle(stream))
+    if rc != 0:
+        raise SsmError("ssm_scan_fwd_noalloc", rc)
 
 
 def ssm_state_update(state, u, delta, A, B, C, D, z, y, delta_bias, softplus_flag,

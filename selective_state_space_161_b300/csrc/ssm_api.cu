@@ -6,6 +6,8 @@
 
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 namespace {
 
 constexpr int kMaxState = 16;
@@ -136,10 +138,66 @@ const char* ssm_status_string(ssm_status_t status) {
     case SSM_ERR_ALIGN: return "a pointer is not 16-byte aligned";
     case SSM_ERR_WORKSPACE: return "workspace missing or too small";
     case SSM_ERR_CUDA: return "CUDA error (no device or launch failure)";
+    case SSM_ERR_SCRATCH_LIMIT:
+      return "problem needs more scratch than ssm_scan_fwd_noalloc holds (use ssm_scan_fwd)";
   }
   return "unknown status";
 }
 
 int ssm_version(void) { return 100; }
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------------------
+// No-allocation variant of ssm_scan_fwd.  Its scratch is this file-scope device array;
+// host code must not hand the symbol itself to a kernel (on the host it only names a
+// host-side shadow), so its device address is looked up per device, once, below.
+
+static __device__ __align__(256) float g_noalloc_scratch[SSM_NOALLOC_SCRATCH_BYTES / sizeof(float)];
+
+namespace {
+
+std::mutex g_noalloc_mutex;
+float* g_noalloc_addr[kMaxDevices] = {nullptr};
+
+// Device address of g_noalloc_scratch on the current device (looked up on first use).
+float* noalloc_scratch_address() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (g_noalloc_addr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
+      return nullptr;
+    g_noalloc_addr[dev] = static_cast<float*>(ptr);
+  }
+  return g_noalloc_addr[dev];
+}
+
+}  // namespace
+
+extern "C" {
+
+ssm_status_t ssm_scan_fwd_noalloc(const void* u, const void* delta, const float* A,
+                                  const void* B, const void* C, const float* D, const void* z,
+                                  const float* delta_bias, int softplus_flag, void* y,
+                                  float* last_state, int64_t batch, int64_t L, int64_t d_inner,
+                                  int d_state, ssm_dtype_t io, void* stream) {
+  ssm_status_t st = check_common(batch, L, d_inner, d_state, io);
+  if (st != SSM_OK) return st;
+  if (batch * d_inner == 0) return SSM_OK;
+  const int sms = current_sm_count();
+  if (sms <= 0) return SSM_ERR_CUDA;
+  ssm::ScanPlan plan;
+  const size_t need = L > 0 ? scan_workspace_bytes(batch, L, d_inner, d_state, sms, &plan) : 0;
+  if (need > SSM_NOALLOC_SCRATCH_BYTES) return SSM_ERR_SCRATCH_LIMIT;
+  float* scratch = nullptr;
+  if (need > 0) {
+    scratch = noalloc_scratch_address();
+    if (scratch == nullptr) return SSM_ERR_CUDA;
+  }
+  return ssm_scan_fwd(u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, last_state, batch, L,
+                      d_inner, d_state, io, scratch, need, stream);
+}
 
 }  // extern "C"
