@@ -32,6 +32,8 @@ if ROOT not in sys.path:
 from inputgen import workloads as W  # noqa: E402
 
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
+KERNEL_SOURCES = ("ssm_scan.cu", "ssm_decode.cu", "ssm_device.cuh")
 FALLBACK_HBM_GBS = 6400.0
 SM_MAX_MHZ_NOMINAL = 2032.0
 # Per-SM issue rates of the pipes the scan uses (operations per clock), measured on B300
@@ -50,6 +52,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--decode-steps", type=int, default=None,
+                    help="decode steps per bench step (default: the workload's 1024); "
+                         "only for small profiling captures")
     return ap.parse_args()
 
 
@@ -81,6 +86,29 @@ def alu_clocks_per_element(N: int) -> float:
     ex2 = N + 2
     slow = 2
     return max(fp32 / FP32_PER_CLK, ex2 / EX2_PER_CLK, slow / MUFU_SLOW_PER_CLK)
+
+
+def kernel_source_hash() -> str:
+    """Hash of the kernel sources; DRAM counters recorded for another hash are stale."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "selective_state_space_161_b300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload_key: str):
+    """DRAM bytes (read + write) per step from the committed ncu capture of this workload,
+    or None if there is none or the kernels changed since it was taken."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f).get(workload_key)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("kernel_hash") != kernel_source_hash():
+        return None
+    return float(rec["dram_bytes_per_step"])
 
 
 def load_peaks():
@@ -214,11 +242,12 @@ class DecodeStep:
         self.w, self.dev, self.ssm = w, dev, ssm
         self.state = dev["state0"].clone()
         self.y = torch.empty((w.batch, w.d_inner), dtype=dev["u"].dtype, device="cuda")
-        self.launches = w.L
+        self.steps = dev["u"].shape[0]
+        self.launches = self.steps
 
     def __call__(self, stream=None):
         d = self.dev
-        for s in range(self.w.L):
+        for s in range(self.steps):
             self.ssm.ssm_state_update(self.state, d["u"][s], d["delta"][s], d["A"], d["B"][s],
                                       d["C"][s], d["D"], d["z"][s], self.y, d["delta_bias"], True,
                                       stream)
@@ -298,19 +327,38 @@ def oracle_sample_rate(w, budget_s: float, threads: int | None = None):
         f"{w.batch} batch x {T} steps x {d_cnt} of {w.d_inner} channels (float64, {dt:.1f} s)"
 
 
-def roofline(w, ms_per_step, hbm_gbs, sm_mhz, sms, peak_src):
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest value across ranks (barrier included); the value itself on one rank."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.barrier()
+    return float(t.item())
+
+
+def whole_job_rate(elements_per_rank: int, world: int, ms_max: float) -> float:
+    """Weak scaling: every rank processed its own workload; the slowest rank sets the time."""
+    return world * elements_per_rank / (ms_max * 1e-3)
+
+
+def roofline(w, ms_per_step, hbm_gbs, sm_mhz, sms, peak_src, traffic=None):
     el_rate = w.elements / (ms_per_step * 1e-3)
     t_hbm = algorithmic_bytes(w) / (hbm_gbs * 1e9)
     t_alu = w.elements * alu_clocks_per_element(w.d_state) / (sms * sm_mhz * 1e6)
     if t_hbm >= t_alu:
         achieved = algorithmic_bytes(w) / (ms_per_step * 1e-3) / 1e9
         return {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
-                "frac": achieved / hbm_gbs, "traffic": None,
+                "frac": achieved / hbm_gbs, "traffic": traffic,
+                "algorithmic_bytes": algorithmic_bytes(w),
                 "peak_source": f"{peak_src} copy bandwidth",
                 "alu_frac": el_rate * t_alu / w.elements}
     peak = w.elements / t_alu / 1e9
     return {"bound": "alu", "achieved": el_rate / 1e9, "peak": peak, "unit": "Gelem/s",
-            "frac": el_rate / 1e9 / peak, "traffic": None,
+            "frac": el_rate / 1e9 / peak, "traffic": traffic,
+            "algorithmic_bytes": algorithmic_bytes(w),
             "peak_source": f"{sms} SMs x {sm_mhz:.0f} MHz, per-element FP32/EX2/MUFU op counts",
             "hbm_frac": algorithmic_bytes(w) / (ms_per_step * 1e-3) / 1e9 / hbm_gbs}
 
@@ -322,6 +370,9 @@ def main_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     ssm.load_library()
     w = W.WORKLOADS[args.workload]
+    if w.decode and args.decode_steps:
+        import dataclasses
+        w = dataclasses.replace(w, L=args.decode_steps)
     dev = W.device_inputs(w)
     step = DecodeStep(w, dev, ssm, torch) if w.decode else ScanStep(w, dev, ssm, torch)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
@@ -346,21 +397,14 @@ def main_ours(args, rank, world, local_rank):
         e1.record(stream)
     torch.cuda.synchronize()
     clocks.stop()
-    ms = float(np.mean([e0.elapsed_time(e1) for e0, e1 in events]))
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        torch.distributed.barrier()
-        ms = float(t.item())
+    ms = max_over_ranks(float(np.mean([e0.elapsed_time(e1) for e0, e1 in events])), world, "cuda")
 
     e2e = None
     if not args.no_e2e and not w.decode:
         e2e = run_e2e(w, dev, ssm, torch, args.e2e_steps)
         if e2e is not None and world > 1:
-            t = torch.tensor([e2e["ms_per_step"]], dtype=torch.float64, device="cuda")
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e["ms_per_step"] = float(t.item())
-            e2e["value"] = world * w.elements / (e2e["ms_per_step"] * 1e-3)
+            e2e["ms_per_step"] = max_over_ranks(e2e["ms_per_step"], world, "cuda")
+            e2e["value"] = whole_job_rate(w.elements, world, e2e["ms_per_step"])
 
     if rank != 0:
         return
@@ -370,7 +414,7 @@ def main_ours(args, rank, world, local_rank):
     out = {
         "metric": "scan elements/s (B*L*d_inner)" if not w.decode
         else "decode elements/s (B*d_inner*steps)",
-        "value": world * w.elements / (ms * 1e-3),
+        "value": whole_job_rate(w.elements, world, ms),
         "unit": "elements/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -386,7 +430,8 @@ def main_ours(args, rank, world, local_rank):
                    "d_state": w.d_state, "io_dtype": "bf16" if w.bf16 else "f32",
                    "parallelism": f"replica per GPU x{world}" if world > 1 else "single GPU",
                    "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write)"},
-        "roofline": roofline(w, ms, hbm_gbs, sm_mhz_peak, sms, peak_src),
+        "roofline": roofline(w, ms, hbm_gbs, sm_mhz_peak, sms, peak_src,
+                             measured_traffic(w.key)),
         "gpu_launches": step.launches * args.steps,
         "clocks": clk,
     }

@@ -119,7 +119,7 @@ ssm_status_t ssm_state_update(float* state, const void* u, const void* delta, co
   for (const void* q : ptrs)
     if (!aligned16(q)) return SSM_ERR_ALIGN;
   if (current_sm_count() <= 0) return SSM_ERR_CUDA;
-  if ((channels + 255) / 256 >= ((int64_t)1 << 31)) return SSM_ERR_SHAPE;
+  if ((channels * 4 + 255) / 256 >= ((int64_t)1 << 31)) return SSM_ERR_SHAPE;
   ssm::DecodeParams p{};
   p.state = state; p.u = u; p.delta = delta; p.A = A; p.B = B; p.C = C; p.D = D; p.z = z; p.y = y;
   p.delta_bias = delta_bias; p.softplus = softplus_flag != 0;

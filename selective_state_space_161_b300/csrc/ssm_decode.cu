@@ -8,9 +8,7 @@
 // Recomputation".
 //
 // The step is bound by HBM: per (batch, channel) it reads and writes d_state
-// fp32 states and touches only a few bytes of activations.  One thread owns
-// one channel's states; the state row is moved with 16-byte accesses when
-// d_state is a multiple of 4.
+// fp32 states and touches only a few bytes of activations.
 
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
@@ -19,59 +17,97 @@ namespace ssm {
 
 constexpr int kDecodeThreads = 256;
 
-template <int N, typename T>
-__global__ void __launch_bounds__(kDecodeThreads) state_update_kernel(const DecodeParams p) {
-  const int64_t i = (int64_t)blockIdx.x * kDecodeThreads + threadIdx.x;  // b * d_inner + d
-  if (i >= p.batch * p.d_inner) return;
-  const int64_t b = i / p.d_inner, d = i % p.d_inner;
-  const T* u = static_cast<const T*>(p.u);
-  const T* dl = static_cast<const T*>(p.delta);
-  const T* Bg = static_cast<const T*>(p.B) + b * N;
-  const T* Cg = static_cast<const T*>(p.C) + b * N;
-  const T* zg = static_cast<const T*>(p.z);
-
-  const float x = to_f32(dl[i]) + (p.delta_bias ? p.delta_bias[d] : 0.f);
-  const float dt = p.softplus ? softplus(x) : x;
-  const float uu = to_f32(u[i]);
-  const float w = dt * uu;
-
-  float h[N];
-  float* st = p.state + i * N;
-  if constexpr (N % 4 == 0) {
+// SPL consecutive I/O elements -> fp32; multiples of 4 move as 16-byte (fp32) or 8-byte
+// (bf16) pieces.
+template <int SPL>
+__device__ __forceinline__ void load_vals(const float* g, float* v) {
+  if constexpr (SPL % 4 == 0) {
 #pragma unroll
-    for (int q = 0; q < N / 4; q++) {
-      const float4 v = reinterpret_cast<const float4*>(st)[q];
-      h[4 * q] = v.x; h[4 * q + 1] = v.y; h[4 * q + 2] = v.z; h[4 * q + 3] = v.w;
+    for (int k = 0; k < SPL / 4; k++) {
+      const float4 q = reinterpret_cast<const float4*>(g)[k];
+      v[4 * k] = q.x; v[4 * k + 1] = q.y; v[4 * k + 2] = q.z; v[4 * k + 3] = q.w;
     }
   } else {
 #pragma unroll
-    for (int n = 0; n < N; n++) h[n] = st[n];
+    for (int n = 0; n < SPL; n++) v[n] = g[n];
   }
-  float acc = 0.f;
+}
+template <int SPL>
+__device__ __forceinline__ void load_vals(const __nv_bfloat16* g, float* v) {
+  if constexpr (SPL % 4 == 0) {
 #pragma unroll
-  for (int n = 0; n < N; n++) {
-    const float dA = ex2(dt * (p.A[d * N + n] * kLog2e));
-    h[n] = fmaf(dA, h[n], w * to_f32(Bg[n]));
-    acc = fmaf(to_f32(Cg[n]), h[n], acc);
-  }
-  if constexpr (N % 4 == 0) {
-#pragma unroll
-    for (int q = 0; q < N / 4; q++)
-      reinterpret_cast<float4*>(st)[q] = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+    for (int k = 0; k < SPL / 4; k++) {
+      const uint2 q = reinterpret_cast<const uint2*>(g)[k];
+      v[4 * k] = __uint_as_float(q.x << 16); v[4 * k + 1] = __uint_as_float(q.x & 0xFFFF0000u);
+      v[4 * k + 2] = __uint_as_float(q.y << 16); v[4 * k + 3] = __uint_as_float(q.y & 0xFFFF0000u);
+    }
   } else {
 #pragma unroll
-    for (int n = 0; n < N; n++) st[n] = h[n];
+    for (int n = 0; n < SPL; n++) v[n] = __bfloat162float(g[n]);
   }
-  if (p.D) acc = fmaf(p.D[d], uu, acc);
-  if (zg) acc *= silu(to_f32(zg[i]));
-  static_cast<T*>(p.y)[i] = from_f32<T>(acc);
+}
+
+// LPC lanes per (batch, channel), each owning SPL = N / LPC consecutive states, so that
+// the state row, A row and B/C rows move as coalesced 16-byte (or 8-byte) pieces; the
+// readout sum over states is finished with log2(LPC) shuffles.
+template <int N, typename T, int LPC>
+__global__ void __launch_bounds__(kDecodeThreads) state_update_kernel(const DecodeParams p) {
+  constexpr int SPL = N / LPC;
+  const int64_t gid = (int64_t)blockIdx.x * kDecodeThreads + threadIdx.x;
+  const int64_t i = gid / LPC;  // channel index b * d_inner + d
+  const int q = (int)(gid % LPC);
+  const bool valid = i < p.batch * p.d_inner;
+  const int64_t ic = valid ? i : 0;  // lanes past the end still join the shuffles
+  const int64_t b = ic / p.d_inner, d = ic % p.d_inner;
+  const T* u = static_cast<const T*>(p.u);
+  const T* dl = static_cast<const T*>(p.delta);
+  const T* zg = static_cast<const T*>(p.z);
+
+  const float x = to_f32(dl[ic]) + (p.delta_bias ? p.delta_bias[d] : 0.f);
+  const float dt = p.softplus ? softplus(x) : x;
+  const float uu = to_f32(u[ic]);
+  const float w = dt * uu;
+
+  float h[SPL], A[SPL], Bv[SPL], Cv[SPL];
+  float* st = p.state + ic * N + q * SPL;
+  load_vals<SPL>(st, h);
+  load_vals<SPL>(p.A + d * N + q * SPL, A);
+  load_vals<SPL>(static_cast<const T*>(p.B) + b * N + q * SPL, Bv);
+  load_vals<SPL>(static_cast<const T*>(p.C) + b * N + q * SPL, Cv);
+  float acc = 0.f;
+#pragma unroll
+  for (int n = 0; n < SPL; n++) {
+    const float dA = ex2(dt * (A[n] * kLog2e));
+    h[n] = fmaf(dA, h[n], w * Bv[n]);
+    acc = fmaf(Cv[n], h[n], acc);
+  }
+#pragma unroll
+  for (int o = 1; o < LPC; o <<= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+  if (!valid) return;
+  if constexpr (SPL % 4 == 0) {
+#pragma unroll
+    for (int k = 0; k < SPL / 4; k++)
+      reinterpret_cast<float4*>(st)[k] = make_float4(h[4 * k], h[4 * k + 1], h[4 * k + 2], h[4 * k + 3]);
+  } else {
+#pragma unroll
+    for (int n = 0; n < SPL; n++) st[n] = h[n];
+  }
+  if (q == 0) {
+    if (p.D) acc = fmaf(p.D[d], uu, acc);
+    if (zg) acc *= silu(to_f32(zg[ic]));
+    static_cast<T*>(p.y)[ic] = from_f32<T>(acc);
+  }
 }
 
 template <int N, typename T>
 static cudaError_t launch_t(const DecodeParams& p, cudaStream_t s) {
-  const int64_t total = p.batch * p.d_inner;
-  const int64_t blocks = (total + kDecodeThreads - 1) / kDecodeThreads;
-  state_update_kernel<N, T><<<(unsigned)blocks, kDecodeThreads, 0, s>>>(p);
+  // Lanes per channel: a power of two (the shuffles pair lanes by xor) with 8 states
+  // each where d_state allows (measured fastest at d_state 16: enough bytes in flight per
+  // thread, 16-byte pieces, and twice the threads of one lane per channel).
+  constexpr int LPC = (N % 8 == 0) ? N / 8 : 1;
+  const int64_t threads = p.batch * p.d_inner * LPC;
+  const int64_t blocks = (threads + kDecodeThreads - 1) / kDecodeThreads;
+  state_update_kernel<N, T, LPC><<<(unsigned)blocks, kDecodeThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 

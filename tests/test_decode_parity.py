@@ -12,7 +12,7 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("bf16", [False, True])
-@pytest.mark.parametrize("d_state", [1, 4, 6, 16])
+@pytest.mark.parametrize("d_state", [1, 4, 6, 8, 12, 16])
 def test_decode_steps_small(d_state, bf16):
     w = W.Workload("dec", "decode edge case", 5, 6, 24, d_state, bf16, 21 + d_state, 0.5,
                    decode=True, state_sd=0.1)
