@@ -97,6 +97,25 @@ SSM_API ssm_status_t ssm_scan_fwd(const void* u, const void* delta, const float*
                           size_t workspace_bytes, void* stream);
 
 /*
+ * ssm_scan_fwd continuing from a given state instead of zero: h_{-1} = initial_state
+ * ([batch][d_inner][d_state] fp32, device; NULL = zero, i.e. exactly ssm_scan_fwd).
+ * Loading a state saved from an earlier sequence and continuing from it is the "state
+ * swapping" of d9bl.com, "Mamba 深度解读", section "状态交换作为一种新的提示范式"; it also
+ * chains a long sequence processed in segments: running L1 steps, then the rest from the
+ * returned last_state, gives the same y and last_state as one call.  initial_state must not
+ * overlap last_state (except that with L == 0 the two may be the same buffer); workspace
+ * as for ssm_scan_fwd.  With L == 0, last_state receives initial_state.
+ */
+SSM_API ssm_status_t ssm_scan_fwd_from_state(const void* u, const void* delta, const float* A,
+                                             const void* B, const void* C, const float* D,
+                                             const void* z, const float* delta_bias,
+                                             int softplus_flag, const float* initial_state,
+                                             void* y, float* last_state, int64_t batch, int64_t L,
+                                             int64_t d_inner, int d_state, ssm_dtype_t io,
+                                             void* workspace, size_t workspace_bytes,
+                                             void* stream);
+
+/*
  * One decode step on a carried state, in place:
  *   state [batch][d_inner][d_state] fp32 (read, then overwritten with h_t);
  *   u, delta, z, y [batch][d_inner] (io dtype); B, C [batch][d_state] (io dtype);

@@ -42,6 +42,9 @@ def _load():
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_scan_fwd.argtypes = [dp] * 8 + [ctypes.c_int, dp, dp, i64, i64, i64, i64, ctypes.c_int]
         lib.oracle_scan_fwd.restype = ctypes.c_int
+        lib.oracle_scan_fwd_from_state.argtypes = ([dp] * 8 + [ctypes.c_int, dp, dp, dp, i64, i64,
+                                                               i64, i64, ctypes.c_int])
+        lib.oracle_scan_fwd_from_state.restype = ctypes.c_int
         lib.oracle_state_update.argtypes = [dp] * 10 + [ctypes.c_int, i64, i64, i64, ctypes.c_int]
         lib.oracle_state_update.restype = ctypes.c_int
         _lib = lib
@@ -69,13 +72,15 @@ def softplus(x: float) -> float:
 
 
 def scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus_flag=True,
-             nthreads: int | None = None):
+             nthreads: int | None = None, initial_state=None):
     """y [batch, L, d_inner] and last_state [batch, d_inner, d_state], both float64.
 
     u, delta, z: [batch, L, d_inner]; B, C: [batch, L, d_state];
-    A: [d_inner, d_state]; D, delta_bias: [d_inner] (None = absent).
+    A: [d_inner, d_state]; D, delta_bias: [d_inner] (None = absent);
+    initial_state: [batch, d_inner, d_state] (None = start from zero).
     """
     u, delta, A, B, C, D, z, delta_bias = map(_f64, (u, delta, A, B, C, D, z, delta_bias))
+    initial_state = _f64(initial_state)
     batch, L, d_inner = u.shape
     d_state = A.shape[1]
     assert A.shape == (d_inner, d_state)
@@ -83,11 +88,20 @@ def scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus_flag=T
     assert delta.shape == u.shape and (z is None or z.shape == u.shape)
     for t in (u, delta, A, B, C, D, z, delta_bias):
         assert t is None or np.all(np.isfinite(t)), "oracle inputs must be finite"
+    assert initial_state is None or initial_state.shape == (batch, d_inner, d_state)
     y = np.zeros((batch, L, d_inner), dtype=np.float64)
     last = np.zeros((batch, d_inner, d_state), dtype=np.float64)
-    rc = _load().oracle_scan_fwd(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
-                                 _ptr(delta_bias), int(bool(softplus_flag)), _ptr(y), _ptr(last),
-                                 batch, L, d_inner, d_state, int(nthreads or max_threads()))
+    if initial_state is None:
+        rc = _load().oracle_scan_fwd(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                     _ptr(z), _ptr(delta_bias), int(bool(softplus_flag)), _ptr(y),
+                                     _ptr(last), batch, L, d_inner, d_state,
+                                     int(nthreads or max_threads()))
+    else:
+        rc = _load().oracle_scan_fwd_from_state(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
+                                                _ptr(D), _ptr(z), _ptr(delta_bias),
+                                                int(bool(softplus_flag)), _ptr(initial_state),
+                                                _ptr(y), _ptr(last), batch, L, d_inner, d_state,
+                                                int(nthreads or max_threads()))
     if rc != 0:
         raise RuntimeError(f"oracle_scan_fwd failed ({rc})")
     return y, last

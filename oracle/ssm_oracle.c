@@ -26,9 +26,13 @@
  *      softplus reading is the workload's statement of the problem.
  *  - Decode: one step of the same recurrence on a carried state (ai-lab.club,
  *      "核心优势": constant work per generated token).
+ *  - Starting from a saved state instead of zero: d9bl.com, section
+ *      "状态交换作为一种新的提示范式" (a state computed on one text is loaded
+ *      into the model and the sequence continues from it).
  * Readings where the pages are silent: D and the gate act on the output only
  * (last_state is the pre-readout h); B and C are per (batch, time) and shared
- * by every channel (concept code B.unsqueeze(2)); the state starts at zero.
+ * by every channel (concept code B.unsqueeze(2)); the state starts at zero
+ * unless an initial state is given.
  */
 #include <math.h>
 #include <stdint.h>
@@ -61,16 +65,20 @@ static double step_size(double delta_raw, const double* delta_bias, int64_t d, i
 }
 
 /*
- * Full-sequence forward.
+ * Full-sequence forward from a given state.
  * u, delta, z, y: [batch][L][d_inner]; B, C: [batch][L][d_state];
- * A: [d_inner][d_state]; D, delta_bias: [d_inner]; last_state: [batch][d_inner][d_state].
- * D, z, delta_bias, last_state may be NULL (no skip term, no gate, zero bias, not returned).
+ * A: [d_inner][d_state]; D, delta_bias: [d_inner];
+ * initial_state, last_state: [batch][d_inner][d_state].
+ * D, z, delta_bias, last_state may be NULL (no skip term, no gate, zero bias, not returned);
+ * initial_state NULL means h starts at zero.
  * Returns 0, or -1 for a bad argument.
  */
-int oracle_scan_fwd(const double* u, const double* delta, const double* A, const double* B,
-                    const double* C, const double* D, const double* z,
-                    const double* delta_bias, int softplus_flag, double* y, double* last_state,
-                    int64_t batch, int64_t L, int64_t d_inner, int64_t d_state, int nthreads) {
+int oracle_scan_fwd_from_state(const double* u, const double* delta, const double* A,
+                               const double* B, const double* C, const double* D,
+                               const double* z, const double* delta_bias, int softplus_flag,
+                               const double* initial_state, double* y, double* last_state,
+                               int64_t batch, int64_t L, int64_t d_inner, int64_t d_state,
+                               int nthreads) {
   if (batch < 0 || L < 0 || d_inner < 0 || d_state < 1) return -1;
   if ((L > 0 && (!u || !delta || !B || !C || !y)) || !A) return -1;
   if (nthreads < 1) nthreads = 1;
@@ -87,7 +95,8 @@ int oracle_scan_fwd(const double* u, const double* delta, const double* A, const
     for (int64_t ch = 0; ch < channels; ch++) {
       if (!h) continue;
       int64_t b = ch / d_inner, d = ch % d_inner;
-      for (int64_t n = 0; n < d_state; n++) h[n] = 0.0;
+      for (int64_t n = 0; n < d_state; n++)
+        h[n] = initial_state ? initial_state[(b * d_inner + d) * d_state + n] : 0.0;
       for (int64_t t = 0; t < L; t++) {
         int64_t e = (b * L + t) * d_inner + d;        /* element (b, t, d) */
         const double* Bt = B + (b * L + t) * d_state;  /* row B[b, t, :] */
@@ -110,6 +119,15 @@ int oracle_scan_fwd(const double* u, const double* delta, const double* A, const
     free(h);
   }
   return bad ? -1 : 0;
+}
+
+/* Full-sequence forward from zero: the state before the first step is 0. */
+int oracle_scan_fwd(const double* u, const double* delta, const double* A, const double* B,
+                    const double* C, const double* D, const double* z,
+                    const double* delta_bias, int softplus_flag, double* y, double* last_state,
+                    int64_t batch, int64_t L, int64_t d_inner, int64_t d_state, int nthreads) {
+  return oracle_scan_fwd_from_state(u, delta, A, B, C, D, z, delta_bias, softplus_flag, NULL, y,
+                                    last_state, batch, L, d_inner, d_state, nthreads);
 }
 
 /*

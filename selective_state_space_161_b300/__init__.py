@@ -19,14 +19,16 @@ import torch
 
 from .build import LIB_PATH, build
 
-__all__ = ["SsmError", "ssm_scan_fwd", "ssm_scan_fwd_noalloc", "ssm_state_update",
+__all__ = ["SsmError", "ssm_scan_fwd", "ssm_scan_fwd_from_state", "ssm_scan_fwd_noalloc",
+           "ssm_state_update",
            "ssm_scan_fwd_workspace_size",
            "ssm_status_string", "ssm_version", "selective_scan", "selective_state_update",
            "load_library", "build", "SSM_F32", "SSM_BF16", "EXPORTED_SYMBOLS"]
 
 SSM_F32, SSM_BF16 = 0, 1
-EXPORTED_SYMBOLS = ("ssm_scan_fwd_workspace_size", "ssm_scan_fwd", "ssm_scan_fwd_noalloc",
-                    "ssm_state_update", "ssm_status_string", "ssm_version")
+EXPORTED_SYMBOLS = ("ssm_scan_fwd_workspace_size", "ssm_scan_fwd", "ssm_scan_fwd_from_state",
+                    "ssm_scan_fwd_noalloc", "ssm_state_update", "ssm_status_string",
+                    "ssm_version")
 SSM_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 _lib = None
@@ -52,6 +54,9 @@ def load_library() -> ctypes.CDLL:
         lib.ssm_scan_fwd.argtypes = [vp] * 8 + [c_int, vp, vp, i64, i64, i64, c_int, c_int, vp,
                                               ctypes.c_size_t, vp]
         lib.ssm_scan_fwd.restype = c_int
+        lib.ssm_scan_fwd_from_state.argtypes = [vp] * 8 + [c_int, vp, vp, vp, i64, i64, i64, c_int,
+                                                          c_int, vp, ctypes.c_size_t, vp]
+        lib.ssm_scan_fwd_from_state.restype = c_int
         lib.ssm_scan_fwd_noalloc.argtypes = [vp] * 8 + [c_int, vp, vp, i64, i64, i64, c_int, c_int,
                                                        vp]
         lib.ssm_scan_fwd_noalloc.restype = c_int
@@ -112,6 +117,19 @@ def ssm_scan_fwd_workspace_size(batch: int, L: int, d_inner: int, d_state: int, 
 def ssm_scan_fwd(u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, last_state,
                  workspace=None, stream=None) -> None:
     """C-ABI ``ssm_scan_fwd`` on CUDA tensors (shapes as documented in include/ssm.h)."""
+    _scan_call("ssm_scan_fwd", u, delta, A, B, C, D, z, delta_bias, softplus_flag, None, y,
+               last_state, workspace, stream)
+
+
+def ssm_scan_fwd_from_state(u, delta, A, B, C, D, z, delta_bias, softplus_flag, initial_state, y,
+                            last_state, workspace=None, stream=None) -> None:
+    """C-ABI ``ssm_scan_fwd_from_state``: the scan continuing from ``initial_state``."""
+    _scan_call("ssm_scan_fwd_from_state", u, delta, A, B, C, D, z, delta_bias, softplus_flag,
+               initial_state, y, last_state, workspace, stream)
+
+
+def _scan_call(func, u, delta, A, B, C, D, z, delta_bias, softplus_flag, initial_state, y,
+               last_state, workspace, stream):
     batch, L, d_inner = u.shape
     d_state = A.shape[1]
     io = _io_code(u)
@@ -124,14 +142,20 @@ def ssm_scan_fwd(u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, last_sta
     _check_dev("D", D, torch.float32, (d_inner,))
     _check_dev("delta_bias", delta_bias, torch.float32, (d_inner,))
     _check_dev("last_state", last_state, torch.float32, (batch, d_inner, d_state))
+    _check_dev("initial_state", initial_state, torch.float32, (batch, d_inner, d_state))
     _check_dev("workspace", workspace)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = load_library().ssm_scan_fwd(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
-                                     _ptr(z), _ptr(delta_bias), int(bool(softplus_flag)), _ptr(y),
-                                     _ptr(last_state), batch, L, d_inner, d_state, io,
-                                     _ptr(workspace), ws_bytes, _stream_handle(stream))
+    lib = load_library()
+    head = (_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
+            int(bool(softplus_flag)))
+    tail = (_ptr(y), _ptr(last_state), batch, L, d_inner, d_state, io, _ptr(workspace), ws_bytes,
+            _stream_handle(stream))
+    if func == "ssm_scan_fwd":
+        rc = lib.ssm_scan_fwd(*head, *tail)
+    else:
+        rc = lib.ssm_scan_fwd_from_state(*head, _ptr(initial_state), *tail)
     if rc != 0:
-        raise SsmError("ssm_scan_fwd", rc)
+        raise SsmError(func, rc)
 
 
 def ssm_scan_fwd_noalloc(u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, last_state,
@@ -190,15 +214,16 @@ def _to_device(t, device):
 
 
 def selective_scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True,
-                   return_last_state=True, stream=None):
+                   return_last_state=True, stream=None, initial_state=None):
     """Selective scan forward.  Returns (y, last_state) on the inputs' device.
 
+    ``initial_state`` [batch, d_inner, d_state] continues from a saved state (None: zero).
     Host tensors (pinned for asynchronous copies) are copied to the current
     CUDA device, processed there, and the results copied back."""
     on_host = not u.is_cuda
     device = torch.device("cuda", torch.cuda.current_device()) if on_host else u.device
-    ins = [_to_device(t, device) for t in (u, delta, A, B, C, D, z, delta_bias)]
-    u_d, delta_d, A_d, B_d, C_d, D_d, z_d, bias_d = ins
+    ins = [_to_device(t, device) for t in (u, delta, A, B, C, D, z, delta_bias, initial_state)]
+    u_d, delta_d, A_d, B_d, C_d, D_d, z_d, bias_d, h0_d = ins
     batch, L, d_inner = u_d.shape
     d_state = A_d.shape[1]
     y = torch.empty_like(u_d)
@@ -206,7 +231,11 @@ def selective_scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=
             if return_last_state else None)
     nbytes = ssm_scan_fwd_workspace_size(batch, L, d_inner, d_state, _io_code(u_d))
     ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device) if nbytes else None
-    ssm_scan_fwd(u_d, delta_d, A_d, B_d, C_d, D_d, z_d, bias_d, softplus, y, last, ws, stream)
+    if h0_d is None:
+        ssm_scan_fwd(u_d, delta_d, A_d, B_d, C_d, D_d, z_d, bias_d, softplus, y, last, ws, stream)
+    else:
+        ssm_scan_fwd_from_state(u_d, delta_d, A_d, B_d, C_d, D_d, z_d, bias_d, softplus, h0_d, y,
+                                last, ws, stream)
     if on_host:
         y = y.to("cpu", non_blocking=False)
         last = last.to("cpu") if last is not None else None

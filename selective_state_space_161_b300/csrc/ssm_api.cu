@@ -61,18 +61,24 @@ size_t ssm_scan_fwd_workspace_size(int64_t batch, int64_t L, int64_t d_inner, in
   return scan_workspace_bytes(batch, L, d_inner, d_state, sms, &plan);
 }
 
-ssm_status_t ssm_scan_fwd(const void* u, const void* delta, const float* A, const void* B,
-                          const void* C, const float* D, const void* z, const float* delta_bias,
-                          int softplus_flag, void* y, float* last_state, int64_t batch, int64_t L,
-                          int64_t d_inner, int d_state, ssm_dtype_t io, void* workspace,
-                          size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+ssm_status_t scan_fwd_impl(const void* u, const void* delta, const float* A, const void* B,
+                           const void* C, const float* D, const void* z, const float* delta_bias,
+                           int softplus_flag, const float* initial_state, void* y,
+                           float* last_state, int64_t batch, int64_t L, int64_t d_inner,
+                           int d_state, ssm_dtype_t io, void* workspace, size_t workspace_bytes,
+                           void* stream) {
   ssm_status_t st = check_common(batch, L, d_inner, d_state, io);
   if (st != SSM_OK) return st;
   const int64_t channels = batch * d_inner;
   if (channels == 0) return SSM_OK;
   if (A == nullptr) return SSM_ERR_NULL;
   if (L > 0 && (!u || !delta || !B || !C || !y)) return SSM_ERR_NULL;
-  const void* ptrs[] = {u, delta, A, B, C, D, z, delta_bias, y, last_state, workspace};
+  const void* ptrs[] = {u, delta, A, B, C, D, z, delta_bias, y, last_state, workspace,
+                        initial_state};
   for (const void* q : ptrs)
     if (!aligned16(q)) return SSM_ERR_ALIGN;
   const int sms = current_sm_count();
@@ -80,9 +86,15 @@ ssm_status_t ssm_scan_fwd(const void* u, const void* delta, const float* A, cons
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   if (L == 0) {
-    if (last_state &&
-        cudaMemsetAsync(last_state, 0, (size_t)channels * d_state * sizeof(float), s) != cudaSuccess)
+    const size_t bytes = (size_t)channels * d_state * sizeof(float);
+    if (last_state && initial_state) {
+      if (last_state != initial_state &&
+          cudaMemcpyAsync(last_state, initial_state, bytes, cudaMemcpyDeviceToDevice, s) !=
+              cudaSuccess)
+        return SSM_ERR_CUDA;
+    } else if (last_state && cudaMemsetAsync(last_state, 0, bytes, s) != cudaSuccess) {
       return SSM_ERR_CUDA;
+    }
     return SSM_OK;
   }
 
@@ -98,12 +110,38 @@ ssm_status_t ssm_scan_fwd(const void* u, const void* delta, const float* A, cons
   if (n_dtiles * p.n_chunks * batch >= ((int64_t)1 << 31)) return SSM_ERR_SHAPE;
   p.u = u; p.delta = delta; p.A = A; p.B = B; p.C = C; p.D = D; p.z = z;
   p.delta_bias = delta_bias; p.softplus = softplus_flag != 0; p.y = y; p.last_state = last_state;
+  p.initial_state = initial_state;
   p.batch = batch; p.L = L; p.d_inner = d_inner; p.d_state = d_state;
   if (p.n_chunks > 1) {
     p.ws_S = static_cast<float*>(workspace);
     p.ws_h = p.ws_S + (size_t)batch * (p.n_chunks - 1) * d_inner;
   }
   return ssm::launch_scan(p, io == SSM_BF16, s) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+ssm_status_t ssm_scan_fwd(const void* u, const void* delta, const float* A, const void* B,
+                          const void* C, const float* D, const void* z, const float* delta_bias,
+                          int softplus_flag, void* y, float* last_state, int64_t batch, int64_t L,
+                          int64_t d_inner, int d_state, ssm_dtype_t io, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  return scan_fwd_impl(u, delta, A, B, C, D, z, delta_bias, softplus_flag, nullptr, y, last_state,
+                       batch, L, d_inner, d_state, io, workspace, workspace_bytes, stream);
+}
+
+ssm_status_t ssm_scan_fwd_from_state(const void* u, const void* delta, const float* A,
+                                     const void* B, const void* C, const float* D, const void* z,
+                                     const float* delta_bias, int softplus_flag,
+                                     const float* initial_state, void* y, float* last_state,
+                                     int64_t batch, int64_t L, int64_t d_inner, int d_state,
+                                     ssm_dtype_t io, void* workspace, size_t workspace_bytes,
+                                     void* stream) {
+  return scan_fwd_impl(u, delta, A, B, C, D, z, delta_bias, softplus_flag, initial_state, y,
+                       last_state, batch, L, d_inner, d_state, io, workspace, workspace_bytes,
+                       stream);
 }
 
 ssm_status_t ssm_state_update(float* state, const void* u, const void* delta, const float* A,

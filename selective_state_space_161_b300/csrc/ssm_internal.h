@@ -18,6 +18,7 @@ struct ScanParams {
   int softplus;
   void* y;
   float* last_state;        // may be null
+  const float* initial_state;  // may be null: the state before the first step is zero
   int64_t batch, L, d_inner;
   int d_state;
   // Time chunking: the sequence is cut into n_chunks chunks of chunk_len steps

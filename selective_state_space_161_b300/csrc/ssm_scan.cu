@@ -28,8 +28,8 @@
 // (a2 a1, a2 b1 + b2), so a chunk is summarised by its decay prod_t dA_t =
 // exp(A * sum_t delta_t) and its end state from zero.  Pass 1 writes those summaries
 // for every chunk but the last; pass 2 folds the summaries of the chunks before its own
-// into its start state, then runs the exact recurrence and writes y.  No block waits on
-// another block.
+// into its start state (the given initial state, or zero, folded with every summary before
+// it), then runs the exact recurrence and writes y.  No block waits on another block.
 
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
@@ -195,6 +195,10 @@ scan_chunk_kernel_1lane(const ScanParams p) {
     const float a1 = (active && 2 * j + 1 < N) ? p.A[d * N + 2 * j + 1] * kLog2e : 0.f;
     A2[j] = make_float2(a0, a1);
     h[j] = make_float2(0.f, 0.f);
+    if (!kSummary && active && p.initial_state) {  // the main pass starts from the given state
+      const float* h0 = p.initial_state + (b * Dn + d) * N;
+      h[j] = make_float2(h0[2 * j], 2 * j + 1 < N ? h0[2 * j + 1] : 0.f);
+    }
   }
   const float Dd = (active && p.D) ? p.D[d] : 0.f;
   const float bias = (active && p.delta_bias) ? p.delta_bias[d] : 0.f;
@@ -430,6 +434,10 @@ scan_chunk_kernel_2lane(const ScanParams p) {
     const float a1 = (active && nb < N) ? p.A[d * N + nb] * kLog2e : 0.f;
     A2[j] = make_float2(a0, a1);
     h[j] = make_float2(0.f, 0.f);
+    if (!kSummary && active && p.initial_state) {  // the main pass starts from the given state
+      const float* h0 = p.initial_state + (b * Dn + d) * N;
+      h[j] = make_float2(na < N ? h0[na] : 0.f, nb < N ? h0[nb] : 0.f);
+    }
   }
   const float Dd = (active && p.D) ? p.D[d] : 0.f;
   const float bias = (active && p.delta_bias) ? p.delta_bias[d] : 0.f;

@@ -29,6 +29,8 @@ MUTATIONS = {
     "last_state_index": ("last_state[(b * d_inner + d) * d_state + n] = h[n];",
                          "last_state[(d * batch + b) * d_state + n] = h[n];"),
     "gate_dropped": ("        if (z) s *= oracle_silu(z[e]);\n        y[e] = s;", "        y[e] = s;"),
+    "initial_state_ignored": ("        h[n] = initial_state ? initial_state[(b * d_inner + d) * d_state + n] : 0.0;",
+                              "        h[n] = 0.0;"),
     "decode_no_decay": ("      double dA = exp(dt * A[d * d_state + n]);\n      double dBu = dt * Bb[n] * u[ch];",
                         "      double dA = 1.0;\n      double dBu = dt * Bb[n] * u[ch];"),
 }

@@ -313,3 +313,45 @@ def test_softplus_identity():
     for x in (-5.0, -0.3, 0.0, 0.7, 8.0):
         assert abs(oracle.softplus(x) - oracle.softplus(-x) - x) < 1e-15 * max(1.0, abs(x))
     assert oracle.softplus(0.0) == math.log(2.0)
+
+
+# ---- starting from a saved state ----------------------------------------------------------
+
+def test_initial_state_split_equivalence():
+    """Running L1 steps, then the rest from the returned state, equals one run (exactly the
+    same double arithmetic), for y and the final state."""
+    p = _rand_problem(batch=2, L=23, d_inner=3, d_state=4, seed=71)
+    y, last = oracle.scan_fwd(**p)
+    L1 = 9
+    seg = lambda a, b: {k: (v[:, a:b] if k in ("u", "delta", "z", "B", "C") else v) for k, v in p.items()}
+    y1, l1 = oracle.scan_fwd(**seg(0, L1))
+    y2, l2 = oracle.scan_fwd(**seg(L1, 23), initial_state=l1)
+    np.testing.assert_array_equal(np.concatenate([y1, y2], axis=1), y)
+    np.testing.assert_array_equal(l2, last)
+
+
+def test_initial_state_brute_force():
+    """y_t gains C_t . (prod_{k<=t} dA_k) h_init (before the gate); the state gains the decayed h_init."""
+    p = _rand_problem(batch=1, L=6, d_inner=2, d_state=3, gate=False, seed=73)
+    h0 = RNG.normal(size=(1, 2, 3))
+    y0, l0 = oracle.scan_fwd(**p)
+    y, last = oracle.scan_fwd(**p, initial_state=h0)
+    _, _, dt = _brute_force(p, True)
+    for t in range(6):
+        for d in range(2):
+            decay = np.exp(np.cumsum(dt[0, :t + 1, d])[-1] * p["A"][d])
+            extra = float(np.sum(p["C"][0, t] * decay * h0[0, d]))
+            assert abs(y[0, t, d] - (y0[0, t, d] + extra)) < 1e-12 * max(1, abs(y[0, t, d]))
+    decay_all = np.exp(np.sum(dt[0], axis=0)[:, None] * p["A"])
+    np.testing.assert_allclose(last[0], l0[0] + decay_all * h0[0], rtol=1e-12, atol=1e-14)
+
+
+def test_initial_state_one_step_is_decode():
+    r = np.random.default_rng(75)
+    p = _rand_problem(batch=2, L=1, d_inner=3, d_state=4, seed=75)
+    h0 = r.normal(scale=0.1, size=(2, 3, 4))
+    y, last = oracle.scan_fwd(**p, initial_state=h0)
+    yd, st = oracle.state_update(h0, p["u"][:, 0], p["delta"][:, 0], p["A"], p["B"][:, 0],
+                                 p["C"][:, 0], D=p["D"], z=p["z"][:, 0], delta_bias=p["delta_bias"])
+    np.testing.assert_array_equal(y[:, 0], yd)
+    np.testing.assert_array_equal(last, st)
