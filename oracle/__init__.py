@@ -45,6 +45,8 @@ def _load():
         lib.oracle_scan_fwd_from_state.argtypes = ([dp] * 8 + [ctypes.c_int, dp, dp, dp, i64, i64,
                                                                i64, i64, ctypes.c_int])
         lib.oracle_scan_fwd_from_state.restype = ctypes.c_int
+        lib.oracle_conv1d_silu.argtypes = [dp] * 5 + [i64, i64, i64, i64]
+        lib.oracle_conv1d_silu.restype = ctypes.c_int
         lib.oracle_state_update.argtypes = [dp] * 10 + [ctypes.c_int, i64, i64, i64, ctypes.c_int]
         lib.oracle_state_update.restype = ctypes.c_int
         _lib = lib
@@ -105,6 +107,24 @@ def scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus_flag=T
     if rc != 0:
         raise RuntimeError(f"oracle_scan_fwd failed ({rc})")
     return y, last
+
+
+def conv1d_silu(x, w, bias=None, x_prev=None):
+    """silu(causal depthwise conv1d(x)) [batch, L, d_inner], float64.
+
+    x: [batch, L, d_inner]; w: [d_inner, d_conv]; bias: [d_inner] or None;
+    x_prev: [batch, d_inner, d_conv - 1], the inputs before t = 0 (None = zeros)."""
+    x, w, bias, x_prev = map(_f64, (x, w, bias, x_prev))
+    batch, L, d_inner = x.shape
+    d_conv = w.shape[1]
+    assert w.shape == (d_inner, d_conv)
+    assert x_prev is None or x_prev.shape == (batch, d_inner, d_conv - 1)
+    u = np.zeros_like(x)
+    rc = _load().oracle_conv1d_silu(_ptr(x), _ptr(w), _ptr(bias), _ptr(x_prev), _ptr(u), batch, L,
+                                    d_inner, d_conv)
+    if rc != 0:
+        raise RuntimeError(f"oracle_conv1d_silu failed ({rc})")
+    return u
 
 
 def state_update(state, u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus_flag=True,

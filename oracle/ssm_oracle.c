@@ -131,6 +131,36 @@ int oracle_scan_fwd(const double* u, const double* delta, const double* A, const
 }
 
 /*
+ * Causal depthwise convolution followed by SiLU, the block's input path before the scan:
+ * youngju.dev, section "Mamba 模块架构" (a Conv1d with groups = d_inner, kernel d_conv and
+ * padding d_conv - 1, truncated to the sequence length, then F.silu).  With the padding on
+ * the left only, output t sees inputs t - (d_conv - 1) .. t:
+ *   u[b,t,d] = silu(bias[d] + sum_{k=0}^{d_conv-1} w[d,k] * x[b, t + k - (d_conv - 1), d]),
+ * x outside the sequence being zero.  x_prev ([batch][d_inner][d_conv-1], may be NULL =
+ * zeros) supplies the inputs before t = 0 (x_prev[.., j] is x at time j - (d_conv - 1)).
+ * x, u: [batch][L][d_inner]; w: [d_inner][d_conv]; bias: [d_inner] or NULL.
+ */
+int oracle_conv1d_silu(const double* x, const double* w, const double* bias,
+                       const double* x_prev, double* u, int64_t batch, int64_t L,
+                       int64_t d_inner, int64_t d_conv) {
+  if (batch < 0 || L < 0 || d_inner < 0 || d_conv < 1) return -1;
+  for (int64_t b = 0; b < batch; b++)
+    for (int64_t t = 0; t < L; t++)
+      for (int64_t d = 0; d < d_inner; d++) {
+        double acc = bias ? bias[d] : 0.0;
+        for (int64_t k = 0; k < d_conv; k++) {
+          const int64_t s = t + k - (d_conv - 1);
+          double xv = 0.0;
+          if (s >= 0) xv = x[(b * L + s) * d_inner + d];
+          else if (x_prev) xv = x_prev[(b * d_inner + d) * (d_conv - 1) + (s + d_conv - 1)];
+          acc += w[d * d_conv + k] * xv;
+        }
+        u[(b * L + t) * d_inner + d] = oracle_silu(acc);
+      }
+  return 0;
+}
+
+/*
  * One decode step on a carried state, updated in place.
  * state: [batch][d_inner][d_state]; u, delta, z, y: [batch][d_inner];
  * B, C: [batch][d_state]; A: [d_inner][d_state]; D, delta_bias: [d_inner].

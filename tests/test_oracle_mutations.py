@@ -31,6 +31,10 @@ MUTATIONS = {
     "gate_dropped": ("        if (z) s *= oracle_silu(z[e]);\n        y[e] = s;", "        y[e] = s;"),
     "initial_state_ignored": ("        h[n] = initial_state ? initial_state[(b * d_inner + d) * d_state + n] : 0.0;",
                               "        h[n] = 0.0;"),
+    "conv_taps_reversed": ("          acc += w[d * d_conv + k] * xv;",
+                           "          acc += w[d * d_conv + (d_conv - 1 - k)] * xv;"),
+    "conv_history_shifted": ("else if (x_prev) xv = x_prev[(b * d_inner + d) * (d_conv - 1) + (s + d_conv - 1)];",
+                             "else if (x_prev) xv = x_prev[(b * d_inner + d) * (d_conv - 1) + (s + d_conv - 2)];"),
     "decode_no_decay": ("      double dA = exp(dt * A[d * d_state + n]);\n      double dBu = dt * Bb[n] * u[ch];",
                         "      double dA = 1.0;\n      double dBu = dt * Bb[n] * u[ch];"),
 }

@@ -355,3 +355,40 @@ def test_initial_state_one_step_is_decode():
                                  p["C"][:, 0], D=p["D"], z=p["z"][:, 0], delta_bias=p["delta_bias"])
     np.testing.assert_array_equal(y[:, 0], yd)
     np.testing.assert_array_equal(last, st)
+
+
+# ---- causal depthwise conv1d + SiLU (the block's input path) --------------------------------
+
+def _silu(v):
+    return v / (1.0 + np.exp(-v))
+
+
+@pytest.mark.parametrize("d_conv", [1, 2, 4])
+def test_conv1d_silu_against_numpy_convolution(d_conv):
+    r = np.random.default_rng(81 + d_conv)
+    batch, L, d_inner = 2, 19, 5
+    x = r.normal(size=(batch, L, d_inner))
+    w = r.normal(size=(d_inner, d_conv))
+    bias = r.normal(size=d_inner)
+    u = oracle.conv1d_silu(x, w, bias)
+    for b in range(batch):
+        for d in range(d_inner):
+            # causal: out_t = sum_k w[k] x[t + k - (K-1)]  ==  full convolution with w reversed
+            full = np.convolve(x[b, :, d], w[d, ::-1])[:L]
+            np.testing.assert_allclose(u[b, :, d], _silu(full + bias[d]), rtol=1e-13, atol=1e-14)
+
+
+def test_conv1d_impulse_response_and_history():
+    d_conv, L = 4, 9
+    w = np.array([[0.5, -1.0, 2.0, 3.0]])
+    x = np.zeros((1, L, 1)); x[0, 2, 0] = 1.0
+    u = oracle.conv1d_silu(x, w)
+    pre = np.zeros(L); pre[2:6] = w[0, ::-1]  # t = 2: w[3], t = 3: w[2], ...
+    np.testing.assert_allclose(u[0, :, 0], _silu(pre), rtol=1e-15)
+    # history: inputs before t = 0 act like a longer sequence's prefix
+    r = np.random.default_rng(85)
+    xl = r.normal(size=(2, 12, 3)); wl = r.normal(size=(3, 4)); bl = r.normal(size=3)
+    full = oracle.conv1d_silu(xl, wl, bl)
+    prev = np.transpose(xl[:, 5:8, :], (0, 2, 1))  # x at t = 5, 6, 7
+    tail = oracle.conv1d_silu(xl[:, 8:, :], wl, bl, x_prev=prev)
+    np.testing.assert_array_equal(tail, full[:, 8:, :])
