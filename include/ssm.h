@@ -116,6 +116,26 @@ SSM_API ssm_status_t ssm_scan_fwd_from_state(const void* u, const void* delta, c
                                              void* stream);
 
 /*
+ * The block's input path fused in front of the scan: u = silu(conv1d(x)), a causal
+ * depthwise convolution of the block input x with d_conv taps and optional bias, then
+ * SiLU (youngju.dev, "Mamba 模块架构": Conv1d with groups = d_inner, padding d_conv - 1,
+ * truncated to the sequence length, then F.silu), followed by ssm_scan_fwd_from_state on u:
+ *   u[b,t,d] = silu(conv_bias[d] + sum_{k<d_conv} conv_weight[d][k] * x[b, t+k-(d_conv-1), d])
+ * with x = 0 before t = 0.  u never goes to HBM unless u_out (nullable, io dtype,
+ * [batch][L][d_inner]) asks for it.  conv_weight [d_inner][d_conv] fp32 (required),
+ * conv_bias [d_inner] fp32 (nullable), 1 <= d_conv <= 4.  Other operands, the workspace and
+ * initial_state as for ssm_scan_fwd_from_state.
+ */
+SSM_API ssm_status_t ssm_scan_fwd_conv(const void* x, const float* conv_weight,
+                                       const float* conv_bias, int d_conv, const void* delta,
+                                       const float* A, const void* B, const void* C,
+                                       const float* D, const void* z, const float* delta_bias,
+                                       int softplus_flag, const float* initial_state, void* y,
+                                       float* last_state, void* u_out, int64_t batch, int64_t L,
+                                       int64_t d_inner, int d_state, ssm_dtype_t io,
+                                       void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * One decode step on a carried state, in place:
  *   state [batch][d_inner][d_state] fp32 (read, then overwritten with h_t);
  *   u, delta, z, y [batch][d_inner] (io dtype); B, C [batch][d_state] (io dtype);
@@ -159,6 +179,22 @@ SSM_API ssm_status_t ssm_scan_fwd_noalloc(const void* u, const void* delta, cons
                                           int softplus_flag, void* y, float* last_state,
                                           int64_t batch, int64_t L, int64_t d_inner,
                                           int d_state, ssm_dtype_t io, void* stream);
+
+/*
+ * One decode step with the block's conv1d + SiLU in front (the single-token form of
+ * ssm_scan_fwd_conv): x [batch][d_inner] is the block input; conv_state
+ * [batch][d_inner][d_conv-1] fp32 holds the previous d_conv-1 inputs (oldest first) and is
+ * shifted in place (x appended); u = silu(conv_bias + conv_weight . (conv_state, x)) feeds
+ * the step exactly as ssm_state_update's u.  conv_state may be NULL only when d_conv == 1.
+ * L calls from zero states reproduce ssm_scan_fwd_conv's y and last_state.
+ */
+SSM_API ssm_status_t ssm_state_update_conv(float* state, float* conv_state, const void* x,
+                                           const float* conv_weight, const float* conv_bias,
+                                           int d_conv, const void* delta, const float* A,
+                                           const void* B, const void* C, const float* D,
+                                           const void* z, void* y, const float* delta_bias,
+                                           int softplus_flag, int64_t batch, int64_t d_inner,
+                                           int d_state, ssm_dtype_t io, void* stream);
 
 /* Human-readable name of a status code (static string). */
 SSM_API const char* ssm_status_string(ssm_status_t status);

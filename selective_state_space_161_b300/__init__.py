@@ -19,16 +19,16 @@ import torch
 
 from .build import LIB_PATH, build
 
-__all__ = ["SsmError", "ssm_scan_fwd", "ssm_scan_fwd_from_state", "ssm_scan_fwd_noalloc",
-           "ssm_state_update",
+__all__ = ["SsmError", "ssm_scan_fwd", "ssm_scan_fwd_from_state", "ssm_scan_fwd_conv",
+           "ssm_scan_fwd_noalloc", "ssm_state_update", "ssm_state_update_conv",
            "ssm_scan_fwd_workspace_size",
            "ssm_status_string", "ssm_version", "selective_scan", "selective_state_update",
            "load_library", "build", "SSM_F32", "SSM_BF16", "EXPORTED_SYMBOLS"]
 
 SSM_F32, SSM_BF16 = 0, 1
 EXPORTED_SYMBOLS = ("ssm_scan_fwd_workspace_size", "ssm_scan_fwd", "ssm_scan_fwd_from_state",
-                    "ssm_scan_fwd_noalloc", "ssm_state_update", "ssm_status_string",
-                    "ssm_version")
+                    "ssm_scan_fwd_conv", "ssm_scan_fwd_noalloc", "ssm_state_update",
+                    "ssm_state_update_conv", "ssm_status_string", "ssm_version")
 SSM_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 _lib = None
@@ -57,6 +57,13 @@ def load_library() -> ctypes.CDLL:
         lib.ssm_scan_fwd_from_state.argtypes = [vp] * 8 + [c_int, vp, vp, vp, i64, i64, i64, c_int,
                                                           c_int, vp, ctypes.c_size_t, vp]
         lib.ssm_scan_fwd_from_state.restype = c_int
+        lib.ssm_scan_fwd_conv.argtypes = ([vp, vp, vp, c_int] + [vp] * 7 + [c_int, vp, vp, vp, vp, i64,
+                                                                         i64, i64, c_int, c_int, vp,
+                                                                         ctypes.c_size_t, vp])
+        lib.ssm_scan_fwd_conv.restype = c_int
+        lib.ssm_state_update_conv.argtypes = ([vp] * 5 + [c_int] + [vp] * 8 + [c_int, i64, i64, c_int,
+                                                                              c_int, vp])
+        lib.ssm_state_update_conv.restype = c_int
         lib.ssm_scan_fwd_noalloc.argtypes = [vp] * 8 + [c_int, vp, vp, i64, i64, i64, c_int, c_int,
                                                        vp]
         lib.ssm_scan_fwd_noalloc.restype = c_int
@@ -128,8 +135,18 @@ def ssm_scan_fwd_from_state(u, delta, A, B, C, D, z, delta_bias, softplus_flag, 
                initial_state, y, last_state, workspace, stream)
 
 
+def ssm_scan_fwd_conv(x, conv_weight, conv_bias, delta, A, B, C, D, z, delta_bias,
+                      softplus_flag, initial_state, y, last_state, u_out=None, workspace=None,
+                      stream=None) -> None:
+    """C-ABI ``ssm_scan_fwd_conv``: u = silu(causal depthwise conv1d(x)) fused in front of the
+    scan; ``conv_weight`` is [d_inner, d_conv] (d_conv <= 4), ``u_out`` optionally receives u."""
+    _scan_call("ssm_scan_fwd_conv", x, delta, A, B, C, D, z, delta_bias, softplus_flag,
+               initial_state, y, last_state, workspace, stream,
+               conv=(conv_weight, conv_bias, u_out))
+
+
 def _scan_call(func, u, delta, A, B, C, D, z, delta_bias, softplus_flag, initial_state, y,
-               last_state, workspace, stream):
+               last_state, workspace, stream, conv=None):
     batch, L, d_inner = u.shape
     d_state = A.shape[1]
     io = _io_code(u)
@@ -152,8 +169,18 @@ def _scan_call(func, u, delta, A, B, C, D, z, delta_bias, softplus_flag, initial
             _stream_handle(stream))
     if func == "ssm_scan_fwd":
         rc = lib.ssm_scan_fwd(*head, *tail)
-    else:
+    elif func == "ssm_scan_fwd_from_state":
         rc = lib.ssm_scan_fwd_from_state(*head, _ptr(initial_state), *tail)
+    else:
+        cw, cb, u_out = conv
+        _check_dev("conv_weight", cw, torch.float32)
+        if cw.dim() != 2 or cw.shape[0] != d_inner:
+            raise ValueError("conv_weight must be [d_inner, d_conv]")
+        _check_dev("conv_bias", cb, torch.float32, (d_inner,))
+        _check_dev("u_out", u_out, u.dtype, (batch, L, d_inner))
+        rc = lib.ssm_scan_fwd_conv(_ptr(u), _ptr(cw), _ptr(cb), int(cw.shape[1]), *head[1:],
+                                   _ptr(initial_state), _ptr(y), _ptr(last_state), _ptr(u_out),
+                                   *tail[2:])
     if rc != 0:
         raise SsmError(func, rc)
 
@@ -182,6 +209,34 @@ def ssm_scan_fwd_noalloc(u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, 
                                              _stream_handle(stream))
     if rc != 0:
         raise SsmError("ssm_scan_fwd_noalloc", rc)
+
+
+def ssm_state_update_conv(state, conv_state, x, conv_weight, conv_bias, delta, A, B, C, D, z, y,
+                          delta_bias, softplus_flag, stream=None) -> None:
+    """C-ABI ``ssm_state_update_conv``: one decode step with conv1d + SiLU in front;
+    ``conv_state`` [batch, d_inner, d_conv - 1] fp32 is shifted in place."""
+    batch, d_inner = x.shape
+    d_state = A.shape[1]
+    io = _io_code(x)
+    _check_dev("state", state, torch.float32, (batch, d_inner, d_state))
+    _check_dev("conv_weight", conv_weight, torch.float32)
+    d_conv = int(conv_weight.shape[1])
+    _check_dev("conv_state", conv_state, torch.float32, (batch, d_inner, d_conv - 1))
+    _check_dev("conv_bias", conv_bias, torch.float32, (d_inner,))
+    for name, t, shp in (("x", x, (batch, d_inner)), ("delta", delta, (batch, d_inner)),
+                         ("z", z, (batch, d_inner)), ("y", y, (batch, d_inner)),
+                         ("B", B, (batch, d_state)), ("C", C, (batch, d_state))):
+        _check_dev(name, t, x.dtype, shp)
+    _check_dev("A", A, torch.float32, (d_inner, d_state))
+    _check_dev("D", D, torch.float32, (d_inner,))
+    _check_dev("delta_bias", delta_bias, torch.float32, (d_inner,))
+    rc = load_library().ssm_state_update_conv(
+        _ptr(state), _ptr(conv_state) if d_conv > 1 else None, _ptr(x), _ptr(conv_weight),
+        _ptr(conv_bias), d_conv, _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(y),
+        _ptr(delta_bias), int(bool(softplus_flag)), batch, d_inner, d_state, io,
+        _stream_handle(stream))
+    if rc != 0:
+        raise SsmError("ssm_state_update_conv", rc)
 
 
 def ssm_state_update(state, u, delta, A, B, C, D, z, y, delta_bias, softplus_flag,
@@ -214,16 +269,20 @@ def _to_device(t, device):
 
 
 def selective_scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True,
-                   return_last_state=True, stream=None, initial_state=None):
+                   return_last_state=True, stream=None, initial_state=None, conv_weight=None,
+                   conv_bias=None):
     """Selective scan forward.  Returns (y, last_state) on the inputs' device.
 
     ``initial_state`` [batch, d_inner, d_state] continues from a saved state (None: zero).
+    With ``conv_weight`` [d_inner, d_conv] the first operand is the block input x and
+    u = silu(causal depthwise conv1d(x) + conv_bias) is computed inside the scan.
     Host tensors (pinned for asynchronous copies) are copied to the current
     CUDA device, processed there, and the results copied back."""
     on_host = not u.is_cuda
     device = torch.device("cuda", torch.cuda.current_device()) if on_host else u.device
-    ins = [_to_device(t, device) for t in (u, delta, A, B, C, D, z, delta_bias, initial_state)]
-    u_d, delta_d, A_d, B_d, C_d, D_d, z_d, bias_d, h0_d = ins
+    ins = [_to_device(t, device) for t in (u, delta, A, B, C, D, z, delta_bias, initial_state,
+                                            conv_weight, conv_bias)]
+    u_d, delta_d, A_d, B_d, C_d, D_d, z_d, bias_d, h0_d, cw_d, cb_d = ins
     batch, L, d_inner = u_d.shape
     d_state = A_d.shape[1]
     y = torch.empty_like(u_d)
@@ -231,7 +290,10 @@ def selective_scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=
             if return_last_state else None)
     nbytes = ssm_scan_fwd_workspace_size(batch, L, d_inner, d_state, _io_code(u_d))
     ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device) if nbytes else None
-    if h0_d is None:
+    if cw_d is not None:
+        ssm_scan_fwd_conv(u_d, cw_d, cb_d, delta_d, A_d, B_d, C_d, D_d, z_d, bias_d, softplus, h0_d,
+                          y, last, None, ws, stream)
+    elif h0_d is None:
         ssm_scan_fwd(u_d, delta_d, A_d, B_d, C_d, D_d, z_d, bias_d, softplus, y, last, ws, stream)
     else:
         ssm_scan_fwd_from_state(u_d, delta_d, A_d, B_d, C_d, D_d, z_d, bias_d, softplus, h0_d, y,

@@ -65,20 +65,30 @@ size_t ssm_scan_fwd_workspace_size(int64_t batch, int64_t L, int64_t d_inner, in
 
 namespace {
 
+// Optional parts of a scan call beyond ssm_scan_fwd's operands.
+struct ScanExtras {
+  const float* initial_state = nullptr;
+  const float* conv_w = nullptr;  // non-null: conv1d + SiLU in front, u holds the block input x
+  const float* conv_b = nullptr;
+  int d_conv = 0;
+  void* u_out = nullptr;
+};
+
 ssm_status_t scan_fwd_impl(const void* u, const void* delta, const float* A, const void* B,
                            const void* C, const float* D, const void* z, const float* delta_bias,
-                           int softplus_flag, const float* initial_state, void* y,
-                           float* last_state, int64_t batch, int64_t L, int64_t d_inner,
-                           int d_state, ssm_dtype_t io, void* workspace, size_t workspace_bytes,
-                           void* stream) {
+                           int softplus_flag, const ScanExtras& ex, void* y, float* last_state,
+                           int64_t batch, int64_t L, int64_t d_inner, int d_state, ssm_dtype_t io,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+  const float* initial_state = ex.initial_state;
   ssm_status_t st = check_common(batch, L, d_inner, d_state, io);
   if (st != SSM_OK) return st;
   const int64_t channels = batch * d_inner;
   if (channels == 0) return SSM_OK;
   if (A == nullptr) return SSM_ERR_NULL;
   if (L > 0 && (!u || !delta || !B || !C || !y)) return SSM_ERR_NULL;
+  if (ex.conv_w != nullptr && (ex.d_conv < 1 || ex.d_conv > 4)) return SSM_ERR_SHAPE;
   const void* ptrs[] = {u, delta, A, B, C, D, z, delta_bias, y, last_state, workspace,
-                        initial_state};
+                        initial_state, ex.conv_w, ex.conv_b, ex.u_out};
   for (const void* q : ptrs)
     if (!aligned16(q)) return SSM_ERR_ALIGN;
   const int sms = current_sm_count();
@@ -111,6 +121,8 @@ ssm_status_t scan_fwd_impl(const void* u, const void* delta, const float* A, con
   p.u = u; p.delta = delta; p.A = A; p.B = B; p.C = C; p.D = D; p.z = z;
   p.delta_bias = delta_bias; p.softplus = softplus_flag != 0; p.y = y; p.last_state = last_state;
   p.initial_state = initial_state;
+  p.conv_w = ex.conv_w; p.conv_b = ex.conv_b; p.d_conv = ex.d_conv; p.u_out = ex.u_out;
+  if (p.conv_w != nullptr) p.lanes = 1;  // the conv path exists in the one-lane kernel only
   p.batch = batch; p.L = L; p.d_inner = d_inner; p.d_state = d_state;
   if (p.n_chunks > 1) {
     p.ws_S = static_cast<float*>(workspace);
@@ -128,8 +140,9 @@ ssm_status_t ssm_scan_fwd(const void* u, const void* delta, const float* A, cons
                           int softplus_flag, void* y, float* last_state, int64_t batch, int64_t L,
                           int64_t d_inner, int d_state, ssm_dtype_t io, void* workspace,
                           size_t workspace_bytes, void* stream) {
-  return scan_fwd_impl(u, delta, A, B, C, D, z, delta_bias, softplus_flag, nullptr, y, last_state,
-                       batch, L, d_inner, d_state, io, workspace, workspace_bytes, stream);
+  return scan_fwd_impl(u, delta, A, B, C, D, z, delta_bias, softplus_flag, ScanExtras{}, y,
+                       last_state, batch, L, d_inner, d_state, io, workspace, workspace_bytes,
+                       stream);
 }
 
 ssm_status_t ssm_scan_fwd_from_state(const void* u, const void* delta, const float* A,
@@ -139,21 +152,51 @@ ssm_status_t ssm_scan_fwd_from_state(const void* u, const void* delta, const flo
                                      int64_t batch, int64_t L, int64_t d_inner, int d_state,
                                      ssm_dtype_t io, void* workspace, size_t workspace_bytes,
                                      void* stream) {
-  return scan_fwd_impl(u, delta, A, B, C, D, z, delta_bias, softplus_flag, initial_state, y,
-                       last_state, batch, L, d_inner, d_state, io, workspace, workspace_bytes,
-                       stream);
+  ScanExtras ex;
+  ex.initial_state = initial_state;
+  return scan_fwd_impl(u, delta, A, B, C, D, z, delta_bias, softplus_flag, ex, y, last_state,
+                       batch, L, d_inner, d_state, io, workspace, workspace_bytes, stream);
 }
 
-ssm_status_t ssm_state_update(float* state, const void* u, const void* delta, const float* A,
-                              const void* B, const void* C, const float* D, const void* z,
-                              void* y, const float* delta_bias, int softplus_flag, int64_t batch,
-                              int64_t d_inner, int d_state, ssm_dtype_t io, void* stream) {
+ssm_status_t ssm_scan_fwd_conv(const void* x, const float* conv_weight, const float* conv_bias,
+                               int d_conv, const void* delta, const float* A, const void* B,
+                               const void* C, const float* D, const void* z,
+                               const float* delta_bias, int softplus_flag,
+                               const float* initial_state, void* y, float* last_state,
+                               void* u_out, int64_t batch, int64_t L, int64_t d_inner,
+                               int d_state, ssm_dtype_t io, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  if (conv_weight == nullptr && batch * d_inner > 0) return SSM_ERR_NULL;
+  ScanExtras ex;
+  ex.initial_state = initial_state;
+  ex.conv_w = conv_weight;
+  ex.conv_b = conv_bias;
+  ex.d_conv = d_conv;
+  ex.u_out = u_out;
+  return scan_fwd_impl(x, delta, A, B, C, D, z, delta_bias, softplus_flag, ex, y, last_state,
+                       batch, L, d_inner, d_state, io, workspace, workspace_bytes, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+ssm_status_t state_update_impl(float* state, float* conv_state, const void* u,
+                               const float* conv_w, const float* conv_b, int d_conv,
+                               const void* delta, const float* A, const void* B, const void* C,
+                               const float* D, const void* z, void* y, const float* delta_bias,
+                               int softplus_flag, int64_t batch, int64_t d_inner, int d_state,
+                               ssm_dtype_t io, void* stream) {
   ssm_status_t st = check_common(batch, 1, d_inner, d_state, io);
   if (st != SSM_OK) return st;
   const int64_t channels = batch * d_inner;
   if (channels == 0) return SSM_OK;
   if (!state || !u || !delta || !A || !B || !C || !y) return SSM_ERR_NULL;
-  const void* ptrs[] = {state, u, delta, A, B, C, D, z, y, delta_bias};
+  if (conv_w != nullptr) {
+    if (d_conv < 1 || d_conv > 4) return SSM_ERR_SHAPE;
+    if (d_conv > 1 && conv_state == nullptr) return SSM_ERR_NULL;
+  }
+  const void* ptrs[] = {state, u, delta, A, B, C, D, z, y, delta_bias, conv_state, conv_w, conv_b};
   for (const void* q : ptrs)
     if (!aligned16(q)) return SSM_ERR_ALIGN;
   if (current_sm_count() <= 0) return SSM_ERR_CUDA;
@@ -162,9 +205,34 @@ ssm_status_t ssm_state_update(float* state, const void* u, const void* delta, co
   p.state = state; p.u = u; p.delta = delta; p.A = A; p.B = B; p.C = C; p.D = D; p.z = z; p.y = y;
   p.delta_bias = delta_bias; p.softplus = softplus_flag != 0;
   p.batch = batch; p.d_inner = d_inner; p.d_state = d_state;
+  p.conv_w = conv_w; p.conv_b = conv_b; p.d_conv = d_conv; p.conv_state = conv_state;
   return ssm::launch_state_update(p, io == SSM_BF16, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? SSM_OK
              : SSM_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+ssm_status_t ssm_state_update(float* state, const void* u, const void* delta, const float* A,
+                              const void* B, const void* C, const float* D, const void* z,
+                              void* y, const float* delta_bias, int softplus_flag, int64_t batch,
+                              int64_t d_inner, int d_state, ssm_dtype_t io, void* stream) {
+  return state_update_impl(state, nullptr, u, nullptr, nullptr, 0, delta, A, B, C, D, z, y,
+                           delta_bias, softplus_flag, batch, d_inner, d_state, io, stream);
+}
+
+ssm_status_t ssm_state_update_conv(float* state, float* conv_state, const void* x,
+                                   const float* conv_weight, const float* conv_bias, int d_conv,
+                                   const void* delta, const float* A, const void* B,
+                                   const void* C, const float* D, const void* z, void* y,
+                                   const float* delta_bias, int softplus_flag, int64_t batch,
+                                   int64_t d_inner, int d_state, ssm_dtype_t io, void* stream) {
+  if (conv_weight == nullptr && batch * d_inner > 0) return SSM_ERR_NULL;
+  return state_update_impl(state, conv_state, x, conv_weight, conv_bias, d_conv, delta, A, B, C,
+                           D, z, y, delta_bias, softplus_flag, batch, d_inner, d_state, io,
+                           stream);
 }
 
 const char* ssm_status_string(ssm_status_t status) {

@@ -50,7 +50,7 @@ __device__ __forceinline__ void load_vals(const __nv_bfloat16* g, float* v) {
 // LPC lanes per (batch, channel), each owning SPL = N / LPC consecutive states, so that
 // the state row, A row and B/C rows move as coalesced 16-byte (or 8-byte) pieces; the
 // readout sum over states is finished with log2(LPC) shuffles.
-template <int N, typename T, int LPC>
+template <int N, typename T, int LPC, bool kConv>
 __global__ void __launch_bounds__(kDecodeThreads) state_update_kernel(const DecodeParams p) {
   constexpr int SPL = N / LPC;
   const int64_t gid = (int64_t)blockIdx.x * kDecodeThreads + threadIdx.x;
@@ -65,7 +65,18 @@ __global__ void __launch_bounds__(kDecodeThreads) state_update_kernel(const Deco
 
   const float x = to_f32(dl[ic]) + (p.delta_bias ? p.delta_bias[d] : 0.f);
   const float dt = p.softplus ? softplus(x) : x;
-  const float uu = to_f32(u[ic]);
+  float uu = to_f32(u[ic]);
+  float x_new = 0.f;
+  if constexpr (kConv) {
+    // u = silu(conv_b + sum_{j<K-1} w[j] * x_{t-(K-1)+j} + w[K-1] * x_t), the earlier inputs
+    // coming from conv_state (both lanes of the channel compute it; lane 0 shifts it below)
+    const int K = p.d_conv;
+    const float* cs = p.conv_state + ic * (K - 1);
+    float c = p.conv_b ? p.conv_b[d] : 0.f;
+    for (int j = 0; j < K - 1; j++) c = fmaf(p.conv_w[d * K + j], cs[j], c);
+    x_new = uu;
+    uu = silu(fmaf(p.conv_w[d * K + K - 1], x_new, c));
+  }
   const float w = dt * uu;
 
   float h[SPL], A[SPL], Bv[SPL], Cv[SPL];
@@ -92,6 +103,13 @@ __global__ void __launch_bounds__(kDecodeThreads) state_update_kernel(const Deco
 #pragma unroll
     for (int n = 0; n < SPL; n++) st[n] = h[n];
   }
+  if constexpr (kConv) {
+    if (q == 0 && p.d_conv > 1) {  // after the shuffle: every lane has read conv_state
+      float* cs = p.conv_state + ic * (p.d_conv - 1);
+      for (int j = 0; j < p.d_conv - 2; j++) cs[j] = cs[j + 1];
+      cs[p.d_conv - 2] = x_new;
+    }
+  }
   if (q == 0) {
     if (p.D) acc = fmaf(p.D[d], uu, acc);
     if (zg) acc *= silu(to_f32(zg[ic]));
@@ -107,7 +125,10 @@ static cudaError_t launch_t(const DecodeParams& p, cudaStream_t s) {
   constexpr int LPC = (N % 8 == 0) ? N / 8 : 1;
   const int64_t threads = p.batch * p.d_inner * LPC;
   const int64_t blocks = (threads + kDecodeThreads - 1) / kDecodeThreads;
-  state_update_kernel<N, T, LPC><<<(unsigned)blocks, kDecodeThreads, 0, s>>>(p);
+  if (p.conv_w != nullptr)
+    state_update_kernel<N, T, LPC, true><<<(unsigned)blocks, kDecodeThreads, 0, s>>>(p);
+  else
+    state_update_kernel<N, T, LPC, false><<<(unsigned)blocks, kDecodeThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -19,6 +19,12 @@ struct ScanParams {
   void* y;
   float* last_state;        // may be null
   const float* initial_state;  // may be null: the state before the first step is zero
+  // Optional causal depthwise conv1d + SiLU in front of the scan (conv_w non-null): the
+  // u operand then holds the block input x, and u = silu(conv_b + sum_k conv_w[d,k] x[t+k-(K-1)]).
+  const float* conv_w;      // [d_inner][d_conv]
+  const float* conv_b;      // [d_inner], may be null
+  int d_conv;               // 1..4
+  void* u_out;              // may be null: the conv output u, I/O dtype
   int64_t batch, L, d_inner;
   int d_state;
   // Time chunking: the sequence is cut into n_chunks chunks of chunk_len steps
@@ -46,6 +52,12 @@ struct DecodeParams {
   int softplus;
   int64_t batch, d_inner;
   int d_state;
+  // Optional conv1d + SiLU on the step's input (conv_w non-null): u holds the block input x,
+  // conv_state [batch][d_inner][d_conv-1] fp32 the previous inputs, shifted in place.
+  const float* conv_w;
+  const float* conv_b;
+  int d_conv;
+  float* conv_state;
 };
 
 // Channels handled by one CTA of the scan kernels.

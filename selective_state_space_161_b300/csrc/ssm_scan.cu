@@ -80,7 +80,7 @@ __device__ __forceinline__ float shfl_pair(float v) { return __shfl_xor_sync(0xF
 
 // One lane per channel: a 32-thread CTA covers kScanCh channels of one batch row over one
 // time chunk; each thread keeps all of its channel's states (as fp32 pairs) in registers.
-template <int N, typename T, bool kSummary>
+template <int N, typename T, bool kSummary, bool kConv>
 __global__ void __launch_bounds__(kScanCh)
 scan_chunk_kernel_1lane(const ScanParams p) {
   constexpr int kS = sizeof(T);
@@ -220,10 +220,33 @@ scan_chunk_kernel_1lane(const ScanParams p) {
   }
   float S = 0.f, S_comp = 0.f;
   T* __restrict__ yg = static_cast<T*>(p.y);
+  // Causal conv1d window (kConv): x at t-1, t-2, t-3 and the 4-tap weights, tap j
+  // multiplying x[t-3+j] (kernels shorter than 4 get leading zero taps).
+  float cw[4] = {0.f, 0.f, 0.f, 0.f}, cb = 0.f, xw1 = 0.f, xw2 = 0.f, xw3 = 0.f;
+  if constexpr (kConv) {
+    if (active) {
+      const int K = p.d_conv;
+#pragma unroll
+      for (int j = 0; j < 4; j++)
+        if (j >= 4 - K) cw[j] = p.conv_w[d * K + j - (4 - K)];
+      cb = p.conv_b ? p.conv_b[d] : 0.f;
+      const T* xg = static_cast<const T*>(p.u);
+      if (t0 >= 1) xw1 = to_f32(xg[(b * L + t0 - 1) * Dn + d]);
+      if (t0 >= 2) xw2 = to_f32(xg[(b * L + t0 - 2) * Dn + d]);
+      if (t0 >= 3) xw3 = to_f32(xg[(b * L + t0 - 3) * Dn + d]);
+    }
+  }
   auto step = [&](int stage, int k, T* yrow) {
     const float x = to_f32(sX[stage][0][k][tid]) + bias;
     const float dt = sp ? softplus(x) : x;
-    const float uu = to_f32(sX[stage][1][k][tid]);
+    float uu = to_f32(sX[stage][1][k][tid]);
+    if constexpr (kConv) {
+      const float xt = uu;
+      uu = silu(fmaf(cw[3], xt, fmaf(cw[2], xw1, fmaf(cw[1], xw2, fmaf(cw[0], xw3, cb)))));
+      xw3 = xw2; xw2 = xw1; xw1 = xt;
+      // u_out has y's layout: the same flat element index as this step's y
+      if (!kSummary && p.u_out) static_cast<T*>(p.u_out)[yrow - static_cast<T*>(p.y)] = from_f32<T>(uu);
+    }
     const float w = dt * uu;
     if (kSummary) { const float yk = dt - S_comp; const float tk = S + yk; S_comp = (tk - S) - yk; S = tk; }
     const float2 dt2 = make_float2(dt, dt), w2 = make_float2(w, w);
@@ -637,14 +660,18 @@ static cudaError_t launch_scan_t(const ScanParams& p, cudaStream_t stream) {
   const int64_t n_dtiles = (p.d_inner + kScanCh - 1) / kScanCh;
   const int64_t sblocks = n_dtiles * (p.n_chunks - 1) * p.batch;
   const int64_t mblocks = n_dtiles * p.n_chunks * p.batch;
-  if (p.lanes == 2) {
+  if (p.conv_w != nullptr) {  // conv1d + SiLU in front: one-lane kernel only
+    if (p.n_chunks > 1)
+      scan_chunk_kernel_1lane<N, T, true, true><<<(unsigned)sblocks, kScanCh, 0, stream>>>(p);
+    scan_chunk_kernel_1lane<N, T, false, true><<<(unsigned)mblocks, kScanCh, 0, stream>>>(p);
+  } else if (p.lanes == 2) {
     if (p.n_chunks > 1)
       scan_chunk_kernel_2lane<N, T, true><<<(unsigned)sblocks, kScanThreads, 0, stream>>>(p);
     scan_chunk_kernel_2lane<N, T, false><<<(unsigned)mblocks, kScanThreads, 0, stream>>>(p);
   } else {
     if (p.n_chunks > 1)
-      scan_chunk_kernel_1lane<N, T, true><<<(unsigned)sblocks, kScanCh, 0, stream>>>(p);
-    scan_chunk_kernel_1lane<N, T, false><<<(unsigned)mblocks, kScanCh, 0, stream>>>(p);
+      scan_chunk_kernel_1lane<N, T, true, false><<<(unsigned)sblocks, kScanCh, 0, stream>>>(p);
+    scan_chunk_kernel_1lane<N, T, false, false><<<(unsigned)mblocks, kScanCh, 0, stream>>>(p);
   }
   return cudaGetLastError();
 }
