@@ -78,6 +78,14 @@ __device__ __forceinline__ void store_bc_chunk(float* dst, uint4 v, __nv_bfloat1
 
 __device__ __forceinline__ float shfl_pair(float v) { return __shfl_xor_sync(0xFFFFFFFFu, v, 1); }
 
+// Programmatic dependent launch: the main pass is launched while the summary pass is still
+// running; a main-pass CTA that needs summaries waits here until the summary grid has
+// completed and its writes are visible (a hardware wait; returns at once without a
+// prerequisite grid).  The summary pass lets the main grid launch once each of its CTAs
+// has stored its summary.
+__device__ __forceinline__ void wait_for_summaries() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_main_pass() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // One lane per channel: a 32-thread CTA covers kScanCh channels of one batch row over one
 // time chunk; each thread keeps all of its channel's states (as fp32 pairs) in registers.
 template <int N, typename T, bool kSummary, bool kConv>
@@ -204,6 +212,7 @@ scan_chunk_kernel_1lane(const ScanParams p) {
   const float bias = (active && p.delta_bias) ? p.delta_bias[d] : 0.f;
   const bool sp = p.softplus != 0;
   if (ntiles > 0) { issue_x(0, 0); cp_async_commit(); load_bc(0); store_bc(0); }
+  if (!kSummary && c > 0) wait_for_summaries();
   if (!kSummary && c > 0 && active) {
     const int64_t base = b * (p.n_chunks - 1);
     for (int j = 0; j < c; j++) {
@@ -302,6 +311,7 @@ scan_chunk_kernel_1lane(const ScanParams p) {
     p.ws_S[slot] = S;
 #pragma unroll
     for (int j = 0; j < NP; j++) { p.ws_h[slot * N + 2 * j] = h[j].x; if (2 * j + 1 < N) p.ws_h[slot * N + 2 * j + 1] = h[j].y; }
+    allow_main_pass();
   } else if (c == p.n_chunks - 1 && p.last_state) {
     float* ls = p.last_state + (b * Dn + d) * N;
 #pragma unroll
@@ -473,6 +483,7 @@ scan_chunk_kernel_2lane(const ScanParams p) {
     store_bc(0);
   }
 
+  if (!kSummary && c > 0) wait_for_summaries();
   if (!kSummary && c > 0 && active) {
     // Start state of chunk c: fold the summaries of chunks 0 .. c-1 in order.
     const int64_t base = b * (p.n_chunks - 1);
@@ -612,6 +623,7 @@ scan_chunk_kernel_2lane(const ScanParams p) {
       if (na < N) p.ws_h[slot * N + na] = h[j].x;
       if (nb < N) p.ws_h[slot * N + nb] = h[j].y;
     }
+    allow_main_pass();
   } else if (c == p.n_chunks - 1 && p.last_state) {
     float* ls = p.last_state + (b * Dn + d) * N;
 #pragma unroll
@@ -655,25 +667,46 @@ void plan_scan(int64_t batch, int64_t L, int64_t d_inner, int sms, ScanPlan* pla
   plan->n_chunks = L > 0 ? (int)((L + len - 1) / len) : 1;
 }
 
+// Summary pass (if there are several chunks), then the main pass; the main pass is a
+// programmatic dependent launch so that it can start while the summary pass drains.
+static cudaError_t launch_passes(void (*summary)(const ScanParams), void (*main_pass)(const ScanParams),
+                                 const ScanParams& p, int threads, int64_t sblocks, int64_t mblocks,
+                                 cudaStream_t stream) {
+  if (p.n_chunks <= 1) {
+    main_pass<<<(unsigned)mblocks, threads, 0, stream>>>(p);
+    return cudaGetLastError();
+  }
+  summary<<<(unsigned)sblocks, threads, 0, stream>>>(p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)mblocks);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, main_pass, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 template <int N, typename T>
 static cudaError_t launch_scan_t(const ScanParams& p, cudaStream_t stream) {
   const int64_t n_dtiles = (p.d_inner + kScanCh - 1) / kScanCh;
   const int64_t sblocks = n_dtiles * (p.n_chunks - 1) * p.batch;
   const int64_t mblocks = n_dtiles * p.n_chunks * p.batch;
   if (p.conv_w != nullptr) {  // conv1d + SiLU in front: one-lane kernel only
-    if (p.n_chunks > 1)
-      scan_chunk_kernel_1lane<N, T, true, true><<<(unsigned)sblocks, kScanCh, 0, stream>>>(p);
-    scan_chunk_kernel_1lane<N, T, false, true><<<(unsigned)mblocks, kScanCh, 0, stream>>>(p);
+    return launch_passes(scan_chunk_kernel_1lane<N, T, true, true>,
+                         scan_chunk_kernel_1lane<N, T, false, true>, p, kScanCh, sblocks, mblocks,
+                         stream);
   } else if (p.lanes == 2) {
-    if (p.n_chunks > 1)
-      scan_chunk_kernel_2lane<N, T, true><<<(unsigned)sblocks, kScanThreads, 0, stream>>>(p);
-    scan_chunk_kernel_2lane<N, T, false><<<(unsigned)mblocks, kScanThreads, 0, stream>>>(p);
-  } else {
-    if (p.n_chunks > 1)
-      scan_chunk_kernel_1lane<N, T, true, false><<<(unsigned)sblocks, kScanCh, 0, stream>>>(p);
-    scan_chunk_kernel_1lane<N, T, false, false><<<(unsigned)mblocks, kScanCh, 0, stream>>>(p);
+    return launch_passes(scan_chunk_kernel_2lane<N, T, true>, scan_chunk_kernel_2lane<N, T, false>,
+                         p, kScanThreads, sblocks, mblocks, stream);
   }
-  return cudaGetLastError();
+  return launch_passes(scan_chunk_kernel_1lane<N, T, true, false>,
+                       scan_chunk_kernel_1lane<N, T, false, false>, p, kScanCh, sblocks, mblocks,
+                       stream);
 }
 
 template <typename T>
