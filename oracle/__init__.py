@@ -45,6 +45,8 @@ def _load():
         lib.oracle_scan_fwd_from_state.argtypes = ([dp] * 8 + [ctypes.c_int, dp, dp, dp, i64, i64,
                                                                i64, i64, ctypes.c_int])
         lib.oracle_scan_fwd_from_state.restype = ctypes.c_int
+        lib.oracle_scan_bwd.argtypes = [dp] * 8 + [ctypes.c_int] + [dp] * 12 + [i64, i64, i64, i64]
+        lib.oracle_scan_bwd.restype = ctypes.c_int
         lib.oracle_conv1d_silu.argtypes = [dp] * 5 + [i64, i64, i64, i64]
         lib.oracle_conv1d_silu.restype = ctypes.c_int
         lib.oracle_state_update.argtypes = [dp] * 10 + [ctypes.c_int, i64, i64, i64, ctypes.c_int]
@@ -107,6 +109,32 @@ def scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus_flag=T
     if rc != 0:
         raise RuntimeError(f"oracle_scan_fwd failed ({rc})")
     return y, last
+
+
+def scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, softplus_flag=True,
+             initial_state=None, dlast=None):
+    """Gradients of scan_fwd for given dL/dy (and dL/dlast_state).  Returns a dict with
+    du, ddelta, dA, dB, dC, and dD / dz / ddelta_bias / dinitial_state where those operands
+    exist, all float64."""
+    u, delta, A, B, C, D, z, delta_bias, initial_state, dy, dlast = map(
+        _f64, (u, delta, A, B, C, D, z, delta_bias, initial_state, dy, dlast))
+    batch, L, d_inner = u.shape
+    d_state = A.shape[1]
+    out = dict(du=np.zeros_like(u), ddelta=np.zeros_like(u), dA=np.zeros_like(A),
+               dB=np.zeros_like(B), dC=np.zeros_like(C))
+    out["dD"] = np.zeros(d_inner) if D is not None else None
+    out["dz"] = np.zeros_like(u) if z is not None else None
+    out["ddelta_bias"] = np.zeros(d_inner) if delta_bias is not None else None
+    out["dinitial_state"] = np.zeros((batch, d_inner, d_state))
+    rc = _load().oracle_scan_bwd(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                                 _ptr(delta_bias), int(bool(softplus_flag)), _ptr(initial_state),
+                                 _ptr(dy), _ptr(dlast), _ptr(out["du"]), _ptr(out["ddelta"]),
+                                 _ptr(out["dA"]), _ptr(out["dB"]), _ptr(out["dC"]), _ptr(out["dD"]),
+                                 _ptr(out["dz"]), _ptr(out["ddelta_bias"]),
+                                 _ptr(out["dinitial_state"]), batch, L, d_inner, d_state)
+    if rc != 0:
+        raise RuntimeError(f"oracle_scan_bwd failed ({rc})")
+    return {k: v for k, v in out.items() if v is not None}
 
 
 def conv1d_silu(x, w, bias=None, x_prev=None):

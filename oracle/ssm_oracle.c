@@ -160,6 +160,103 @@ int oracle_conv1d_silu(const double* x, const double* w, const double* bias,
   return 0;
 }
 
+/* sigmoid(x) = 1 / (1 + e^-x): the derivative of softplus. */
+static double oracle_sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+
+/*
+ * Gradients of the forward scan (reverse mode), for a loss L whose gradients with respect
+ * to y (dy, [batch][L][d_inner]) and, optionally, to last_state (dlast,
+ * [batch][d_inner][d_state], NULL = 0) are given.  The pages prescribe this pass only as
+ * "recompute the intermediate states in the backward pass" (youngju.dev, section
+ * "解决方案：Kernel Fusion + Recomputation"); the arithmetic is the chain rule through the
+ * forward of oracle_scan_fwd_from_state, written out step by step:
+ *   s_t = sum_n C_t,n h_t,n + D u_t,   y_t = s_t g_t,  g_t = silu(z_t)
+ *   ds_t = dy_t g_t,  dz_t = dy_t s_t silu'(z_t),  silu'(z) = sig(z) (1 + z (1 - sig(z)))
+ *   lambda_t = ds_t C_t + dA_{t+1} lambda_{t+1}   (lambda_{L-1} gets dlast added)
+ *   dC_t,n = ds_t h_t,n;  dD += ds_t u_t;  du_t = ds_t D + delta_t sum_n lambda_t,n B_t,n
+ *   ddelta_t = sum_n lambda_t,n (h_{t-1},n dA_t,n A_n + B_t,n u_t)
+ *   dA_n += lambda_t,n h_{t-1},n dA_t,n delta_t;  dB_t,n = lambda_t,n delta_t u_t
+ *   ddelta_raw_t = ddelta_t softplus'(x_t) (= sigmoid(x_t)), or ddelta_t without softplus;
+ *   dbias += ddelta_raw_t;  dinitial_state = dA_0 lambda_0.
+ * Outputs (all required unless noted): du, ddelta, dz (NULL iff z is NULL): [batch][L][d_inner];
+ * dB, dC: [batch][L][d_state]; dA: [d_inner][d_state]; dD, dbias: [d_inner] (dD NULL iff D is
+ * NULL, dbias may be NULL); dinit: [batch][d_inner][d_state] or NULL.  Accumulated outputs
+ * are overwritten, not added to.  Serial over channels (dB, dC sum over channels).
+ */
+int oracle_scan_bwd(const double* u, const double* delta, const double* A, const double* B,
+                    const double* C, const double* D, const double* z, const double* delta_bias,
+                    int softplus_flag, const double* initial_state, const double* dy,
+                    const double* dlast, double* du, double* ddelta, double* dA, double* dB,
+                    double* dC, double* dD, double* dz, double* dbias, double* dinit,
+                    int64_t batch, int64_t L, int64_t d_inner, int64_t d_state) {
+  if (batch < 0 || L < 0 || d_inner < 0 || d_state < 1) return -1;
+  const int64_t N = d_state;
+  for (int64_t i = 0; i < d_inner * N; i++) dA[i] = 0.0;
+  for (int64_t i = 0; i < batch * L * N; i++) { dB[i] = 0.0; dC[i] = 0.0; }
+  for (int64_t d = 0; d < d_inner; d++) {
+    if (dD) dD[d] = 0.0;
+    if (dbias) dbias[d] = 0.0;
+  }
+  double* hs = (double*)malloc(sizeof(double) * (size_t)((L + 1) * N));  /* h_{-1} .. h_{L-1} */
+  double* lam = (double*)malloc(sizeof(double) * (size_t)N);
+  if (!hs || !lam) { free(hs); free(lam); return -1; }
+  for (int64_t b = 0; b < batch; b++)
+    for (int64_t d = 0; d < d_inner; d++) {
+      /* forward, keeping every state (this is the oracle, not the fast path) */
+      for (int64_t n = 0; n < N; n++)
+        hs[n] = initial_state ? initial_state[(b * d_inner + d) * N + n] : 0.0;
+      for (int64_t t = 0; t < L; t++) {
+        const int64_t e = (b * L + t) * d_inner + d;
+        const double dt = step_size(delta[e], delta_bias, d, softplus_flag);
+        for (int64_t n = 0; n < N; n++)
+          hs[(t + 1) * N + n] = exp(dt * A[d * N + n]) * hs[t * N + n] +
+                                dt * B[(b * L + t) * N + n] * u[e];
+      }
+      /* reverse */
+      for (int64_t n = 0; n < N; n++) lam[n] = dlast ? dlast[(b * d_inner + d) * N + n] : 0.0;
+      for (int64_t t = L - 1; t >= 0; t--) {
+        const int64_t e = (b * L + t) * d_inner + d;
+        const double x = delta[e] + (delta_bias ? delta_bias[d] : 0.0);
+        const double dt = softplus_flag ? oracle_softplus(x) : x;
+        const double* Bt = B + (b * L + t) * N;
+        const double* Ct = C + (b * L + t) * N;
+        const double* h = hs + (t + 1) * N;      /* h_t */
+        const double* hp = hs + t * N;           /* h_{t-1} */
+        double s = 0.0;
+        for (int64_t n = 0; n < N; n++) s += Ct[n] * h[n];
+        if (D) s += D[d] * u[e];
+        double g = 1.0;
+        if (z) {
+          g = oracle_silu(z[e]);
+          const double sg = oracle_sigmoid(z[e]);
+          dz[e] = dy[e] * s * sg * (1.0 + z[e] * (1.0 - sg));
+        }
+        const double ds = dy[e] * g;
+        double ddt = 0.0, du_e = D ? ds * D[d] : 0.0;
+        if (D) dD[d] += ds * u[e];
+        for (int64_t n = 0; n < N; n++) {
+          lam[n] += ds * Ct[n];                  /* lambda_t */
+          const double dAn = exp(dt * A[d * N + n]);
+          dC[(b * L + t) * N + n] += ds * h[n];
+          dB[(b * L + t) * N + n] += lam[n] * dt * u[e];
+          du_e += lam[n] * dt * Bt[n];
+          ddt += lam[n] * (hp[n] * dAn * A[d * N + n] + Bt[n] * u[e]);
+          dA[d * N + n] += lam[n] * hp[n] * dAn * dt;
+          lam[n] *= dAn;                         /* carry dA_t lambda_t to step t-1 */
+        }
+        du[e] = du_e;
+        const double dx = softplus_flag ? ddt * oracle_sigmoid(x) : ddt;
+        ddelta[e] = dx;
+        if (dbias) dbias[d] += dx;
+      }
+      if (dinit)
+        for (int64_t n = 0; n < N; n++) dinit[(b * d_inner + d) * N + n] = lam[n];
+    }
+  free(hs);
+  free(lam);
+  return 0;
+}
+
 /*
  * One decode step on a carried state, updated in place.
  * state: [batch][d_inner][d_state]; u, delta, z, y: [batch][d_inner];

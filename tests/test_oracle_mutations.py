@@ -35,6 +35,13 @@ MUTATIONS = {
                            "          acc += w[d * d_conv + (d_conv - 1 - k)] * xv;"),
     "conv_history_shifted": ("else if (x_prev) xv = x_prev[(b * d_inner + d) * (d_conv - 1) + (s + d_conv - 1)];",
                              "else if (x_prev) xv = x_prev[(b * d_inner + d) * (d_conv - 1) + (s + d_conv - 2)];"),
+    "bwd_carry_without_decay": ("          lam[n] *= dAn;                         /* carry dA_t lambda_t to step t-1 */",
+                                "          lam[n] *= 1.0;"),
+    "bwd_dB_without_step": ("dB[(b * L + t) * N + n] += lam[n] * dt * u[e];",
+                            "dB[(b * L + t) * N + n] += lam[n] * u[e];"),
+    "bwd_dC_previous_state": ("dC[(b * L + t) * N + n] += ds * h[n];", "dC[(b * L + t) * N + n] += ds * hp[n];"),
+    "bwd_softplus_derivative": ("const double dx = softplus_flag ? ddt * oracle_sigmoid(x) : ddt;",
+                                "const double dx = softplus_flag ? ddt * oracle_sigmoid(-x) : ddt;"),
     "decode_no_decay": ("      double dA = exp(dt * A[d * d_state + n]);\n      double dBu = dt * Bb[n] * u[ch];",
                         "      double dA = 1.0;\n      double dBu = dt * Bb[n] * u[ch];"),
 }

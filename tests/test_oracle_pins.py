@@ -392,3 +392,61 @@ def test_conv1d_impulse_response_and_history():
     prev = np.transpose(xl[:, 5:8, :], (0, 2, 1))  # x at t = 5, 6, 7
     tail = oracle.conv1d_silu(xl[:, 8:, :], wl, bl, x_prev=prev)
     np.testing.assert_array_equal(tail, full[:, 8:, :])
+
+
+# ---- backward (reverse mode) -------------------------------------------------------------------
+
+def _loss_grad_fd(p, dy, dlast, key, eps=1e-6, softplus_flag=True):
+    """Central finite differences of <dy, y> + <dlast, last_state> w.r.t. every entry of p[key]."""
+    base = p[key]
+    g = np.zeros_like(base)
+    it = np.nditer(base, flags=["multi_index"])
+    for _ in it:
+        idx = it.multi_index
+        vals = []
+        for sgn in (1.0, -1.0):
+            q = dict(p)
+            arr = base.copy()
+            arr[idx] += sgn * eps
+            q[key] = arr
+            y, last = oracle.scan_fwd(**q, softplus_flag=softplus_flag)
+            vals.append(np.sum(dy * y) + np.sum(dlast * last))
+        g[idx] = (vals[0] - vals[1]) / (2 * eps)
+    return g
+
+
+@pytest.mark.parametrize("softplus_flag", [True, False])
+def test_backward_against_finite_differences(softplus_flag):
+    p = _rand_problem(batch=2, L=7, d_inner=3, d_state=3, seed=91)
+    if not softplus_flag:
+        p["delta"] = np.abs(p["delta"]) * 0.5
+        p["delta_bias"] = np.abs(p["delta_bias"]) * 0.2
+    r = np.random.default_rng(92)
+    dy = r.normal(size=p["u"].shape)
+    dlast = r.normal(size=(2, 3, 3))
+    h0 = r.normal(scale=0.3, size=(2, 3, 3))
+    g = oracle.scan_bwd(**p, dy=dy, dlast=dlast, initial_state=h0, softplus_flag=softplus_flag)
+    p0 = dict(p, initial_state=h0)
+    names = {"u": "du", "delta": "ddelta", "A": "dA", "B": "dB", "C": "dC", "D": "dD", "z": "dz",
+             "delta_bias": "ddelta_bias", "initial_state": "dinitial_state"}
+    for key, gname in names.items():
+        fd = _loss_grad_fd(p0, dy, dlast, key, softplus_flag=softplus_flag)
+        np.testing.assert_allclose(g[gname], fd, rtol=2e-6, atol=2e-7, err_msg=gname)
+
+
+def test_backward_adjoint_identity():
+    """<dy, J v> = <J^T dy, v> for a random joint direction v over every input."""
+    p = _rand_problem(batch=2, L=12, d_inner=4, d_state=5, seed=95)
+    r = np.random.default_rng(96)
+    dy = r.normal(size=p["u"].shape)
+    g = oracle.scan_bwd(**p, dy=dy)
+    v = {k: r.normal(size=np.shape(val)) for k, val in p.items()}
+    eps = 1e-6
+    plus = {k: p[k] + eps * v[k] for k in p}
+    minus = {k: p[k] - eps * v[k] for k in p}
+    jv = (oracle.scan_fwd(**plus)[0] - oracle.scan_fwd(**minus)[0]) / (2 * eps)
+    lhs = float(np.sum(dy * jv))
+    names = {"u": "du", "delta": "ddelta", "A": "dA", "B": "dB", "C": "dC", "D": "dD", "z": "dz",
+             "delta_bias": "ddelta_bias"}
+    rhs = sum(float(np.sum(g[gn] * v[k])) for k, gn in names.items())
+    assert abs(lhs - rhs) <= 1e-7 * max(1.0, abs(lhs))
