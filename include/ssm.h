@@ -196,6 +196,35 @@ SSM_API ssm_status_t ssm_state_update_conv(float* state, float* conv_state, cons
                                            int softplus_flag, int64_t batch, int64_t d_inner,
                                            int d_state, ssm_dtype_t io, void* stream);
 
+/*
+ * Backward pass of ssm_scan_fwd_from_state (gradients for training).  Given dy = dL/dy
+ * ([batch][L][d_inner], io dtype) and optionally dlast_state = dL/dlast_state
+ * ([batch][d_inner][d_state] fp32, NULL = 0), writes
+ *   du, ddelta (gradient w.r.t. delta_raw), dz (NULL iff z is NULL): io dtype, like u;
+ *   dA [d_inner][d_state], dB, dC [batch][L][d_state], dD (NULL iff D is NULL),
+ *   ddelta_bias (NULL: not computed), dinitial_state (NULL: not computed): fp32.
+ * dA, dB, dC, dD, ddelta_bias are sums over batch/time/channels; they are overwritten.
+ * The forward inputs (u, delta, A, B, C, D, z, delta_bias, softplus_flag, initial_state)
+ * are the ones the forward call used; no forward output is needed.  The intermediate
+ * states are recomputed, not stored by the forward (youngju.dev, "Mamba: Linear-Time
+ * Sequence Modeling with Selective State Spaces 论文分析", section "解决方案：Kernel
+ * Fusion + Recomputation"): the pass keeps one state per 16 steps and per channel in the
+ * workspace (ssm_scan_bwd_workspace_size bytes, about 2 * batch * L * d_inner * d_state / 4
+ * bytes; not initialised by the caller).  dB and dC are accumulated with atomic additions, so
+ * their last bits may vary from run to run.
+ */
+SSM_API size_t ssm_scan_bwd_workspace_size(int64_t batch, int64_t L, int64_t d_inner,
+                                           int d_state, ssm_dtype_t io);
+SSM_API ssm_status_t ssm_scan_bwd(const void* u, const void* delta, const float* A, const void* B,
+                                  const void* C, const float* D, const void* z,
+                                  const float* delta_bias, int softplus_flag,
+                                  const float* initial_state, const void* dy,
+                                  const float* dlast_state, void* du, void* ddelta, float* dA,
+                                  float* dB, float* dC, float* dD, void* dz, float* ddelta_bias,
+                                  float* dinitial_state, int64_t batch, int64_t L,
+                                  int64_t d_inner, int d_state, ssm_dtype_t io, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
 /* Human-readable name of a status code (static string). */
 SSM_API const char* ssm_status_string(ssm_status_t status);
 

@@ -20,7 +20,8 @@ import torch
 from .build import LIB_PATH, build
 
 __all__ = ["SsmError", "ssm_scan_fwd", "ssm_scan_fwd_from_state", "ssm_scan_fwd_conv",
-           "ssm_scan_fwd_noalloc", "ssm_state_update", "ssm_state_update_conv",
+           "ssm_scan_fwd_noalloc", "ssm_state_update", "ssm_state_update_conv", "ssm_scan_bwd",
+           "ssm_scan_bwd_workspace_size", "selective_scan_backward",
            "ssm_scan_fwd_workspace_size",
            "ssm_status_string", "ssm_version", "selective_scan", "selective_state_update",
            "load_library", "build", "SSM_F32", "SSM_BF16", "EXPORTED_SYMBOLS"]
@@ -28,7 +29,8 @@ __all__ = ["SsmError", "ssm_scan_fwd", "ssm_scan_fwd_from_state", "ssm_scan_fwd_
 SSM_F32, SSM_BF16 = 0, 1
 EXPORTED_SYMBOLS = ("ssm_scan_fwd_workspace_size", "ssm_scan_fwd", "ssm_scan_fwd_from_state",
                     "ssm_scan_fwd_conv", "ssm_scan_fwd_noalloc", "ssm_state_update",
-                    "ssm_state_update_conv", "ssm_status_string", "ssm_version")
+                    "ssm_state_update_conv", "ssm_scan_bwd", "ssm_scan_bwd_workspace_size",
+                    "ssm_status_string", "ssm_version")
 SSM_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 _lib = None
@@ -64,6 +66,11 @@ def load_library() -> ctypes.CDLL:
         lib.ssm_state_update_conv.argtypes = ([vp] * 5 + [c_int] + [vp] * 8 + [c_int, i64, i64, c_int,
                                                                               c_int, vp])
         lib.ssm_state_update_conv.restype = c_int
+        lib.ssm_scan_bwd_workspace_size.argtypes = [i64, i64, i64, c_int, c_int]
+        lib.ssm_scan_bwd_workspace_size.restype = ctypes.c_size_t
+        lib.ssm_scan_bwd.argtypes = [vp] * 8 + [c_int] + [vp] * 12 + [i64, i64, i64, c_int, c_int, vp,
+                                                                   ctypes.c_size_t, vp]
+        lib.ssm_scan_bwd.restype = c_int
         lib.ssm_scan_fwd_noalloc.argtypes = [vp] * 8 + [c_int, vp, vp, i64, i64, i64, c_int, c_int,
                                                        vp]
         lib.ssm_scan_fwd_noalloc.restype = c_int
@@ -209,6 +216,68 @@ def ssm_scan_fwd_noalloc(u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, 
                                              _stream_handle(stream))
     if rc != 0:
         raise SsmError("ssm_scan_fwd_noalloc", rc)
+
+
+def ssm_scan_bwd_workspace_size(batch: int, L: int, d_inner: int, d_state: int, io: int) -> int:
+    return int(load_library().ssm_scan_bwd_workspace_size(batch, L, d_inner, d_state, io))
+
+
+def ssm_scan_bwd(u, delta, A, B, C, D, z, delta_bias, softplus_flag, initial_state, dy,
+                 dlast_state, du, ddelta, dA, dB, dC, dD, dz, ddelta_bias, dinitial_state,
+                 workspace, stream=None) -> None:
+    """C-ABI ``ssm_scan_bwd`` on CUDA tensors (shapes as documented in include/ssm.h)."""
+    batch, L, d_inner = u.shape
+    d_state = A.shape[1]
+    io = _io_code(u)
+    dt = u.dtype
+    for name, t, shp, ty in (("u", u, (batch, L, d_inner), dt), ("delta", delta, (batch, L, d_inner), dt),
+                             ("z", z, (batch, L, d_inner), dt), ("dy", dy, (batch, L, d_inner), dt),
+                             ("du", du, (batch, L, d_inner), dt), ("ddelta", ddelta, (batch, L, d_inner), dt),
+                             ("dz", dz, (batch, L, d_inner), dt), ("B", B, (batch, L, d_state), dt),
+                             ("C", C, (batch, L, d_state), dt),
+                             ("dB", dB, (batch, L, d_state), torch.float32),
+                             ("dC", dC, (batch, L, d_state), torch.float32),
+                             ("A", A, (d_inner, d_state), torch.float32),
+                             ("dA", dA, (d_inner, d_state), torch.float32),
+                             ("D", D, (d_inner,), torch.float32), ("dD", dD, (d_inner,), torch.float32),
+                             ("delta_bias", delta_bias, (d_inner,), torch.float32),
+                             ("ddelta_bias", ddelta_bias, (d_inner,), torch.float32),
+                             ("initial_state", initial_state, (batch, d_inner, d_state), torch.float32),
+                             ("dlast_state", dlast_state, (batch, d_inner, d_state), torch.float32),
+                             ("dinitial_state", dinitial_state, (batch, d_inner, d_state), torch.float32)):
+        _check_dev(name, t, ty, shp)
+    _check_dev("workspace", workspace)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load_library().ssm_scan_bwd(
+        _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
+        int(bool(softplus_flag)), _ptr(initial_state), _ptr(dy), _ptr(dlast_state), _ptr(du),
+        _ptr(ddelta), _ptr(dA), _ptr(dB), _ptr(dC), _ptr(dD), _ptr(dz), _ptr(ddelta_bias),
+        _ptr(dinitial_state), batch, L, d_inner, d_state, io, _ptr(workspace), ws_bytes,
+        _stream_handle(stream))
+    if rc != 0:
+        raise SsmError("ssm_scan_bwd", rc)
+
+
+def selective_scan_backward(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, softplus=True,
+                            initial_state=None, dlast_state=None, stream=None):
+    """Gradients of ``selective_scan`` (CUDA tensors).  Returns a dict with du, ddelta, dA, dB,
+    dC and, where those inputs were given, dD, dz, ddelta_bias, dinitial_state."""
+    batch, L, d_inner = u.shape
+    d_state = A.shape[1]
+    dev = u.device
+    f32 = dict(dtype=torch.float32, device=dev)
+    g = dict(du=torch.empty_like(u), ddelta=torch.empty_like(u), dA=torch.empty((d_inner, d_state), **f32),
+             dB=torch.empty((batch, L, d_state), **f32), dC=torch.empty((batch, L, d_state), **f32))
+    g["dD"] = torch.empty(d_inner, **f32) if D is not None else None
+    g["dz"] = torch.empty_like(u) if z is not None else None
+    g["ddelta_bias"] = torch.empty(d_inner, **f32) if delta_bias is not None else None
+    g["dinitial_state"] = torch.empty((batch, d_inner, d_state), **f32)
+    nbytes = ssm_scan_bwd_workspace_size(batch, L, d_inner, d_state, _io_code(u))
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+    ssm_scan_bwd(u, delta, A, B, C, D, z, delta_bias, softplus, initial_state, dy, dlast_state,
+                 g["du"], g["ddelta"], g["dA"], g["dB"], g["dC"], g["dD"], g["dz"], g["ddelta_bias"],
+                 g["dinitial_state"], ws, stream)
+    return {k: v for k, v in g.items() if v is not None}
 
 
 def ssm_state_update_conv(state, conv_state, x, conv_weight, conv_bias, delta, A, B, C, D, z, y,

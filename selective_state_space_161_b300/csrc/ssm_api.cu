@@ -235,6 +235,109 @@ ssm_status_t ssm_state_update_conv(float* state, float* conv_state, const void* 
                            stream);
 }
 
+}  // extern "C"
+
+namespace {
+
+// Time chunking of the backward pass: the forward plan's chunks, rounded to whole tiles.
+void bwd_plan(int64_t batch, int64_t L, int64_t d_inner, int sms, ssm::ScanPlan* plan) {
+  ssm::plan_scan(batch, L, d_inner, sms, plan);
+  plan->lanes = 1;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ssm_scan_bwd_workspace_size(int64_t batch, int64_t L, int64_t d_inner, int d_state,
+                                   ssm_dtype_t io) {
+  if (check_common(batch, L, d_inner, d_state, io) != SSM_OK) return 0;
+  const int sms = current_sm_count();
+  if (sms <= 0 || batch * d_inner * L == 0) return 0;
+  ssm::ScanPlan plan;
+  bwd_plan(batch, L, d_inner, sms, &plan);
+  return ssm::bwd_workspace_floats(batch, L, d_inner, d_state, plan.n_chunks) * sizeof(float);
+}
+
+ssm_status_t ssm_scan_bwd(const void* u, const void* delta, const float* A, const void* B,
+                          const void* C, const float* D, const void* z, const float* delta_bias,
+                          int softplus_flag, const float* initial_state, const void* dy,
+                          const float* dlast_state, void* du, void* ddelta, float* dA, float* dB,
+                          float* dC, float* dD, void* dz, float* ddelta_bias,
+                          float* dinitial_state, int64_t batch, int64_t L, int64_t d_inner,
+                          int d_state, ssm_dtype_t io, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+  ssm_status_t st = check_common(batch, L, d_inner, d_state, io);
+  if (st != SSM_OK) return st;
+  const int64_t channels = batch * d_inner;
+  if (channels == 0) return SSM_OK;
+  if (!A || !dA) return SSM_ERR_NULL;
+  if (L > 0 && (!u || !delta || !B || !C || !dy || !du || !ddelta || !dB || !dC)) return SSM_ERR_NULL;
+  if ((D != nullptr) != (dD != nullptr) || (z != nullptr) != (dz != nullptr)) return SSM_ERR_NULL;
+  const void* ptrs[] = {u, delta, A, B, C, D, z, delta_bias, initial_state, dy, dlast_state, du,
+                        ddelta, dA, dB, dC, dD, dz, ddelta_bias, dinitial_state, workspace};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return SSM_ERR_ALIGN;
+  const int sms = current_sm_count();
+  if (sms <= 0) return SSM_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // accumulated outputs start at zero
+  if (cudaMemsetAsync(dA, 0, (size_t)d_inner * d_state * sizeof(float), s) != cudaSuccess)
+    return SSM_ERR_CUDA;
+  if (dD && cudaMemsetAsync(dD, 0, (size_t)d_inner * sizeof(float), s) != cudaSuccess)
+    return SSM_ERR_CUDA;
+  if (ddelta_bias && cudaMemsetAsync(ddelta_bias, 0, (size_t)d_inner * sizeof(float), s) != cudaSuccess)
+    return SSM_ERR_CUDA;
+  if (L == 0) {  // nothing flows: dinit = dlast
+    const size_t bytes = (size_t)channels * d_state * sizeof(float);
+    if (dinitial_state) {
+      const cudaError_t e = dlast_state ? cudaMemcpyAsync(dinitial_state, dlast_state, bytes,
+                                                          cudaMemcpyDeviceToDevice, s)
+                                        : cudaMemsetAsync(dinitial_state, 0, bytes, s);
+      if (e != cudaSuccess) return SSM_ERR_CUDA;
+    }
+    return SSM_OK;
+  }
+  const size_t bc_bytes = (size_t)batch * L * d_state * sizeof(float);
+  if (cudaMemsetAsync(dB, 0, bc_bytes, s) != cudaSuccess || cudaMemsetAsync(dC, 0, bc_bytes, s) != cudaSuccess)
+    return SSM_ERR_CUDA;
+
+  ssm::ScanPlan plan;
+  bwd_plan(batch, L, d_inner, sms, &plan);
+  const size_t need = ssm::bwd_workspace_floats(batch, L, d_inner, d_state, plan.n_chunks) * sizeof(float);
+  if (workspace == nullptr || workspace_bytes < need) return SSM_ERR_WORKSPACE;
+  const int64_t tiles = (L + 15) / 16;
+  if ((d_inner + 31) / 32 * tiles * batch >= ((int64_t)1 << 31)) return SSM_ERR_SHAPE;
+
+  float* ws = static_cast<float*>(workspace);
+  const int64_t ck = batch * tiles * d_inner * d_state;
+  const int64_t fws = batch * (int64_t)(plan.n_chunks - 1) * d_inner;
+  const int64_t rws = batch * (int64_t)plan.n_chunks * d_inner;
+  ssm::BwdArgs a{};
+  a.u = u; a.delta = delta; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z; a.delta_bias = delta_bias;
+  a.softplus = softplus_flag != 0; a.initial_state = initial_state; a.dy = dy; a.dlast = dlast_state;
+  a.du = du; a.ddelta = ddelta; a.dz = dz; a.dA = dA; a.dB = dB; a.dC = dC; a.dD = dD;
+  a.dbias = ddelta_bias; a.dinit = dinitial_state;
+  a.batch = batch; a.L = L; a.d_inner = d_inner; a.d_state = d_state;
+  a.chunk_len = plan.chunk_len; a.n_chunks = plan.n_chunks;
+  a.ckpt_h = ws;
+  a.ckpt_m = ws + ck;
+  float* fS = ws + 2 * ck;
+  a.fws_S = fS;
+  a.fws_h = fS + fws;
+  float* rS = fS + fws * (d_state + 1);
+  a.rws_S = rS;
+  a.rws_m = rS + rws;
+
+  ssm::ScanParams f{};
+  f.u = u; f.delta = delta; f.A = A; f.B = B; f.C = C; f.delta_bias = delta_bias;
+  f.softplus = softplus_flag != 0; f.batch = batch; f.L = L; f.d_inner = d_inner;
+  f.d_state = d_state; f.chunk_len = plan.chunk_len; f.n_chunks = plan.n_chunks; f.lanes = 1;
+  f.ws_S = fS;
+  f.ws_h = fS + fws;
+  return ssm::launch_scan_bwd(a, f, io == SSM_BF16, s) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
 const char* ssm_status_string(ssm_status_t status) {
   switch (status) {
     case SSM_OK: return "ok";

@@ -60,6 +60,42 @@ struct DecodeParams {
   float* conv_state;
 };
 
+// Arguments of the backward pass (see ssm_scan_bwd.cu and include/ssm.h).
+struct BwdArgs {
+  const void* u;
+  const void* delta;
+  const float* A;
+  const void* B;
+  const void* C;
+  const float* D;
+  const void* z;
+  const float* delta_bias;
+  int softplus;
+  const float* initial_state;
+  const void* dy;
+  const float* dlast;
+  void* du;
+  void* ddelta;
+  void* dz;
+  float* dA;
+  float* dB;
+  float* dC;
+  float* dD;
+  float* dbias;
+  float* dinit;
+  int64_t batch, L, d_inner;
+  int d_state;
+  int64_t chunk_len;
+  int n_chunks;
+  const float* fws_S;  // forward chunk summaries (written by the forward summary kernel)
+  const float* fws_h;
+  float* rws_S;        // reverse chunk summaries [batch][n_chunks][d_inner] (+ [.][d_state])
+  float* rws_m;
+  float* ckpt_h;       // [batch][tiles][d_inner][d_state]: state before each tile
+  float* ckpt_m;       // [batch][tiles][d_inner][d_state]: carry entering each tile's last step
+};
+
+
 // Channels handled by one CTA of the scan kernels.
 int scan_channels_per_cta();
 
@@ -73,6 +109,11 @@ struct ScanPlan {
 void plan_scan(int64_t batch, int64_t L, int64_t d_inner, int sms, ScanPlan* plan);
 
 cudaError_t launch_scan(const ScanParams& p, bool bf16, cudaStream_t stream);
+// Only the forward summary pass (one lane per channel) of a chunked scan plan.
+cudaError_t launch_scan_summary(const ScanParams& p, bool bf16, cudaStream_t stream);
+// Floats of scratch the backward pass needs for n_chunks time chunks.
+size_t bwd_workspace_floats(int64_t batch, int64_t L, int64_t d_inner, int d_state, int n_chunks);
+cudaError_t launch_scan_bwd(const BwdArgs& a, const ScanParams& fwd, bool bf16, cudaStream_t s);
 cudaError_t launch_state_update(const DecodeParams& p, bool bf16, cudaStream_t stream);
 
 }  // namespace ssm

@@ -732,6 +732,27 @@ static cudaError_t dispatch_n(const ScanParams& p, cudaStream_t s) {
   }
 }
 
+template <typename T>
+static cudaError_t summary_only(const ScanParams& p, cudaStream_t s) {
+  const int64_t blocks = (p.d_inner + kScanCh - 1) / kScanCh * (p.n_chunks - 1) * p.batch;
+  switch (p.d_state) {
+#define SSM_SUMMARY_CASE(NN) \
+    case NN: scan_chunk_kernel_1lane<NN, T, true, false><<<(unsigned)blocks, kScanCh, 0, s>>>(p); break;
+    SSM_SUMMARY_CASE(1) SSM_SUMMARY_CASE(2) SSM_SUMMARY_CASE(3) SSM_SUMMARY_CASE(4)
+    SSM_SUMMARY_CASE(5) SSM_SUMMARY_CASE(6) SSM_SUMMARY_CASE(7) SSM_SUMMARY_CASE(8)
+    SSM_SUMMARY_CASE(9) SSM_SUMMARY_CASE(10) SSM_SUMMARY_CASE(11) SSM_SUMMARY_CASE(12)
+    SSM_SUMMARY_CASE(13) SSM_SUMMARY_CASE(14) SSM_SUMMARY_CASE(15) SSM_SUMMARY_CASE(16)
+#undef SSM_SUMMARY_CASE
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scan_summary(const ScanParams& p, bool bf16, cudaStream_t stream) {
+  if (p.n_chunks <= 1) return cudaSuccess;
+  return bf16 ? summary_only<__nv_bfloat16>(p, stream) : summary_only<float>(p, stream);
+}
+
 cudaError_t launch_scan(const ScanParams& p, bool bf16, cudaStream_t stream) {
   return bf16 ? dispatch_n<__nv_bfloat16>(p, stream) : dispatch_n<float>(p, stream);
 }

@@ -1,0 +1,359 @@
+// Backward pass of the selective scan: gradients with respect to u, delta_raw, A, B, C, D, z,
+// delta_bias and the initial state, given dL/dy and (optionally) dL/dlast_state.
+//
+// The pages describe the backward only as "recompute the intermediate states in the backward
+// pass instead of storing them" (youngju.dev, "Mamba: Linear-Time Sequence Modeling with
+// Selective State Spaces 论文分析", section "解决方案：Kernel Fusion + Recomputation").  Here:
+//  1. forward checkpoints: the forward recurrence (time-chunked exactly like the forward
+//     scan: the forward summary kernel, then the checkpoint kernel below) stores the state
+//     before every 16-step tile — one state per 16 steps, never the per-step states;
+//  2. reverse checkpoints: the adjoint lambda_t = ds_t C_t + dA_{t+1} lambda_{t+1} runs
+//     backwards in time with the same chunk decomposition (a reverse summary per chunk: its
+//     carry-out from a zero carry-in and its decay exp(A sum delta)), storing the carry that
+//     enters each tile from the right;
+//  3. gradients: one CTA per (batch row, tile, 32 channels) recomputes the tile's 16 states
+//     into shared memory from its checkpoint, then walks the tile backwards.  dB and dC sum
+//     over channels: the 32 lanes reduce them by a shuffle reduce-scatter and add one value
+//     per lane atomically.
+// All arithmetic is fp32; one thread per (batch, channel), all d_state states in registers.
+
+#include "ssm_device.cuh"
+#include "ssm_internal.h"
+
+#include <algorithm>
+
+namespace ssm {
+
+constexpr int kBwdCh = 32;    // channels per CTA (one warp)
+constexpr int kBwdTile = 16;  // time steps per tile
+
+template <typename T>
+__device__ __forceinline__ float ldf(const void* p, int64_t i) {
+  return to_f32(static_cast<const T*>(p)[i]);
+}
+
+// ---------------------------------------------------------------------------------------
+// 1. Forward checkpoints: chunk c folds the forward summaries of chunks < c into its start
+//    state (from the initial state), then runs the recurrence over its tiles, storing the
+//    state before each tile.
+template <int N, typename T>
+__global__ void __launch_bounds__(kBwdCh) bwd_fwd_ckpt_kernel(const BwdArgs p) {
+  const int64_t n_dtiles = (p.d_inner + kBwdCh - 1) / kBwdCh;
+  int64_t blk = blockIdx.x;
+  const int64_t dtile = blk % n_dtiles;
+  blk /= n_dtiles;
+  const int c = (int)(blk % p.n_chunks);
+  const int64_t b = blk / p.n_chunks;
+  const int lane = threadIdx.x;
+  const int64_t Dn = p.d_inner, L = p.L, d = dtile * kBwdCh + lane;
+  const bool active = d < Dn;
+  const int64_t dc = active ? d : 0;
+  const int64_t t0 = (int64_t)c * p.chunk_len, t1 = min(t0 + p.chunk_len, L);
+  const int64_t tiles = (L + kBwdTile - 1) / kBwdTile;
+  __shared__ float sB[kBwdTile][N];
+
+  float A2[N], h[N];
+#pragma unroll
+  for (int n = 0; n < N; n++) {
+    A2[n] = p.A[dc * N + n] * kLog2e;
+    h[n] = p.initial_state ? p.initial_state[(b * Dn + dc) * N + n] : 0.f;
+  }
+  const float bias = p.delta_bias ? p.delta_bias[dc] : 0.f;
+  for (int j = 0; j < c; j++) {
+    const int64_t slot = (b * (p.n_chunks - 1) + j) * Dn + dc;
+    const float S = p.fws_S[slot];
+#pragma unroll
+    for (int n = 0; n < N; n++) h[n] = fmaf(ex2(A2[n] * S), h[n], p.fws_h[slot * N + n]);
+  }
+  for (int64_t ts = t0; ts < t1; ts += kBwdTile) {
+    const int steps = (int)min((int64_t)kBwdTile, t1 - ts);
+    if (active) {
+      float* ck = p.ckpt_h + ((b * tiles + ts / kBwdTile) * Dn + d) * N;
+#pragma unroll
+      for (int n = 0; n < N; n++) ck[n] = h[n];
+    }
+    __syncwarp();
+    for (int i = lane; i < steps * N; i += kBwdCh) sB[i / N][i % N] = ldf<T>(p.B, (b * L + ts) * N + i);
+    __syncwarp();
+    for (int k = 0; k < steps; k++) {
+      const int64_t e = (b * L + ts + k) * Dn + dc;
+      const float x = ldf<T>(p.delta, e) + bias;
+      const float dt = p.softplus ? softplus(x) : x;
+      const float w = dt * ldf<T>(p.u, e);
+#pragma unroll
+      for (int n = 0; n < N; n++) h[n] = fmaf(ex2(dt * A2[n]), h[n], w * sB[k][n]);
+    }
+    __syncwarp();
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// 2. Reverse pass.  Walking a chunk backwards from carry m (entering its last step):
+//      lambda_t = m + ds_t C_t,   m <- dA_t lambda_t   (carry to step t - 1),
+//    with ds_t = dy_t silu(z_t).  kSummary: from m = 0, store (sum delta, m after the chunk's
+//    first step) for chunks >= 1.  Otherwise: fold the summaries of the chunks after c into
+//    the carry (from dlast), then store the carry entering each tile, walking right to left.
+template <int N, typename T, bool kSummary>
+__global__ void __launch_bounds__(kBwdCh) bwd_reverse_kernel(const BwdArgs p) {
+  const int64_t n_dtiles = (p.d_inner + kBwdCh - 1) / kBwdCh;
+  const int chunks = kSummary ? p.n_chunks - 1 : p.n_chunks;
+  int64_t blk = blockIdx.x;
+  const int64_t dtile = blk % n_dtiles;
+  blk /= n_dtiles;
+  const int c = (int)(blk % chunks) + (kSummary ? 1 : 0);
+  const int64_t b = blk / chunks;
+  const int lane = threadIdx.x;
+  const int64_t Dn = p.d_inner, L = p.L, d = dtile * kBwdCh + lane;
+  const bool active = d < Dn;
+  const int64_t dc = active ? d : 0;
+  const int64_t t0 = (int64_t)c * p.chunk_len, t1 = min(t0 + p.chunk_len, L);
+  const int64_t tiles = (L + kBwdTile - 1) / kBwdTile;
+  __shared__ float sC[kBwdTile][N];
+
+  float A2[N], m[N];
+#pragma unroll
+  for (int n = 0; n < N; n++) {
+    A2[n] = p.A[dc * N + n] * kLog2e;
+    m[n] = 0.f;
+  }
+  const float bias = p.delta_bias ? p.delta_bias[dc] : 0.f;
+  if (!kSummary) {
+#pragma unroll
+    for (int n = 0; n < N; n++) m[n] = p.dlast ? p.dlast[(b * Dn + dc) * N + n] : 0.f;
+    for (int j = p.n_chunks - 1; j > c; j--) {
+      const int64_t slot = (b * p.n_chunks + j) * Dn + dc;
+      const float S = p.rws_S[slot];
+#pragma unroll
+      for (int n = 0; n < N; n++) m[n] = fmaf(ex2(A2[n] * S), m[n], p.rws_m[slot * N + n]);
+    }
+  }
+  float S = 0.f, S_comp = 0.f;
+  const int64_t first_tile = t0 / kBwdTile, last_tile = (t1 - 1) / kBwdTile;
+  for (int64_t tl = last_tile; tl >= first_tile; tl--) {
+    const int64_t ts = tl * kBwdTile;
+    const int steps = (int)min((int64_t)kBwdTile, t1 - ts);
+    if (!kSummary && active) {
+      float* ck = p.ckpt_m + ((b * tiles + tl) * Dn + d) * N;
+#pragma unroll
+      for (int n = 0; n < N; n++) ck[n] = m[n];
+    }
+    __syncwarp();
+    for (int i = lane; i < steps * N; i += kBwdCh) sC[i / N][i % N] = ldf<T>(p.C, (b * L + ts) * N + i);
+    __syncwarp();
+    for (int k = steps - 1; k >= 0; k--) {
+      const int64_t e = (b * L + ts + k) * Dn + dc;
+      const float x = ldf<T>(p.delta, e) + bias;
+      const float dt = p.softplus ? softplus(x) : x;
+      if (kSummary) {
+        const float yk = dt - S_comp;
+        const float tk = S + yk;
+        S_comp = (tk - S) - yk;
+        S = tk;
+      }
+      float ds = ldf<T>(p.dy, e);
+      if (p.z) ds *= silu(ldf<T>(p.z, e));
+#pragma unroll
+      for (int n = 0; n < N; n++) m[n] = ex2(dt * A2[n]) * fmaf(ds, sC[k][n], m[n]);
+    }
+    __syncwarp();
+  }
+  if (kSummary && active) {
+    const int64_t slot = (b * p.n_chunks + c) * Dn + d;
+    p.rws_S[slot] = S;
+#pragma unroll
+    for (int n = 0; n < N; n++) p.rws_m[slot * N + n] = m[n];
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// 3. Gradients for one tile.  Lane = channel; the 2N per-step partials of dB (lambda dt u) and
+//    dC (ds h) are summed over the 32 channels by a reduce-scatter: after five halving
+//    exchanges lane j holds the warp's total of value j, and adds it to global memory.
+template <int N>
+__device__ __forceinline__ void warp_reduce_scatter_add(float (&v)[32], int lane, float* dB_row,
+                                                        float* dC_row) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int j = 0; j < o; j++) {
+      const float send = upper ? v[j] : v[j + o];
+      const float keep = upper ? v[j + o] : v[j];
+      v[j] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, o);
+    }
+  }
+  if (lane < N) atomicAdd(dB_row + lane, v[0]);
+  else if (lane < 2 * N) atomicAdd(dC_row + lane - N, v[0]);
+}
+
+template <int N, typename T>
+__global__ void __launch_bounds__(kBwdCh) bwd_grad_kernel(const BwdArgs p) {
+  static_assert(2 * N <= 32, "dB/dC partials must fit one value per lane");
+  const int64_t n_dtiles = (p.d_inner + kBwdCh - 1) / kBwdCh;
+  const int64_t tiles = (p.L + kBwdTile - 1) / kBwdTile;
+  int64_t blk = blockIdx.x;
+  const int64_t dtile = blk % n_dtiles;
+  blk /= n_dtiles;
+  const int64_t tl = blk % tiles;
+  const int64_t b = blk / tiles;
+  const int lane = threadIdx.x;
+  const int64_t Dn = p.d_inner, L = p.L, d = dtile * kBwdCh + lane;
+  const bool active = d < Dn;
+  const int64_t dc = active ? d : 0;
+  const int64_t ts = tl * kBwdTile;
+  const int steps = (int)min((int64_t)kBwdTile, L - ts);
+  __shared__ float sB[kBwdTile][N], sC[kBwdTile][N];
+  __shared__ float sH[kBwdTile][N][kBwdCh];  // state after each step of the tile
+
+  for (int i = lane; i < steps * N; i += kBwdCh) {
+    sB[i / N][i % N] = ldf<T>(p.B, (b * L + ts) * N + i);
+    sC[i / N][i % N] = ldf<T>(p.C, (b * L + ts) * N + i);
+  }
+  float A2[N], Af[N], h0[N], m[N], dAacc[N];
+#pragma unroll
+  for (int n = 0; n < N; n++) {
+    Af[n] = p.A[dc * N + n];
+    A2[n] = Af[n] * kLog2e;
+    h0[n] = active ? p.ckpt_h[((b * tiles + tl) * Dn + d) * N + n] : 0.f;
+    m[n] = active ? p.ckpt_m[((b * tiles + tl) * Dn + d) * N + n] : 0.f;
+    dAacc[n] = 0.f;
+  }
+  const float bias = p.delta_bias ? p.delta_bias[dc] : 0.f;
+  const float Dd = p.D ? p.D[dc] : 0.f;
+  float xs[kBwdTile], dts[kBwdTile], us[kBwdTile];
+#pragma unroll
+  for (int k = 0; k < kBwdTile; k++) {
+    const int64_t e = (b * L + ts + min(k, steps - 1)) * Dn + dc;
+    xs[k] = ldf<T>(p.delta, e) + bias;
+    dts[k] = p.softplus ? softplus(xs[k]) : xs[k];
+    us[k] = ldf<T>(p.u, e);
+  }
+  __syncwarp();
+
+  // forward recompute of the tile's states
+  {
+    float h[N];
+#pragma unroll
+    for (int n = 0; n < N; n++) h[n] = h0[n];
+#pragma unroll
+    for (int k = 0; k < kBwdTile; k++) {
+      if (k < steps) {
+        const float w = dts[k] * us[k];
+#pragma unroll
+        for (int n = 0; n < N; n++) {
+          h[n] = fmaf(ex2(dts[k] * A2[n]), h[n], w * sB[k][n]);
+          sH[k][n][lane] = h[n];
+        }
+      }
+    }
+  }
+  __syncwarp();
+
+  float dDacc = 0.f, dbacc = 0.f;
+#pragma unroll
+  for (int k = kBwdTile - 1; k >= 0; k--) {
+    if (k >= steps) continue;
+    const int64_t e = (b * L + ts + k) * Dn + dc;
+    const float dyk = ldf<T>(p.dy, e);
+    float s = Dd * us[k];
+#pragma unroll
+    for (int n = 0; n < N; n++) s = fmaf(sC[k][n], sH[k][n][lane], s);
+    float g = 1.f;
+    if (p.z) {
+      const float zk = ldf<T>(p.z, e);
+      const float sg = rcp(1.f + ex2(-zk * kLog2e));
+      g = zk * sg;
+      if (active) static_cast<T*>(p.dz)[e] = from_f32<T>(dyk * s * sg * fmaf(zk, 1.f - sg, 1.f));
+    }
+    const float ds = dyk * g;
+    dDacc = fmaf(ds, us[k], dDacc);
+    float ddt = 0.f, sumlB = 0.f;
+    float v[32];
+#pragma unroll
+    for (int n = 0; n < N; n++) {
+      const float lam = fmaf(ds, sC[k][n], m[n]);
+      const float hp = k > 0 ? sH[k - 1][n][lane] : h0[n];
+      const float dA = ex2(dts[k] * A2[n]);
+      const float t1 = lam * hp * dA;
+      ddt = fmaf(t1, Af[n], fmaf(lam * sB[k][n], us[k], ddt));
+      dAacc[n] = fmaf(t1, dts[k], dAacc[n]);
+      sumlB = fmaf(lam, sB[k][n], sumlB);
+      v[n] = active ? lam * dts[k] * us[k] : 0.f;       // dB partial
+      v[N + n] = active ? ds * sH[k][n][lane] : 0.f;     // dC partial
+      m[n] = dA * lam;
+    }
+#pragma unroll
+    for (int j = 2 * N; j < 32; j++) v[j] = 0.f;
+    const float dx = p.softplus ? ddt * rcp(1.f + ex2(-xs[k] * kLog2e)) : ddt;
+    dbacc += dx;
+    if (active) {
+      static_cast<T*>(p.du)[e] = from_f32<T>(fmaf(ds, Dd, dts[k] * sumlB));
+      static_cast<T*>(p.ddelta)[e] = from_f32<T>(dx);
+    }
+    warp_reduce_scatter_add<N>(v, lane, p.dB + (b * L + ts + k) * N, p.dC + (b * L + ts + k) * N);
+  }
+  if (!active) return;
+#pragma unroll
+  for (int n = 0; n < N; n++) atomicAdd(p.dA + d * N + n, dAacc[n]);
+  if (p.dD) atomicAdd(p.dD + d, dDacc);
+  if (p.dbias) atomicAdd(p.dbias + d, dbacc);
+  if (p.dinit && tl == 0) {
+#pragma unroll
+    for (int n = 0; n < N; n++) p.dinit[(b * Dn + d) * N + n] = m[n];
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+
+size_t bwd_workspace_floats(int64_t batch, int64_t L, int64_t d_inner, int d_state, int n_chunks) {
+  const int64_t tiles = (L + kBwdTile - 1) / kBwdTile;
+  const int64_t ck = batch * tiles * d_inner * d_state;                 // each checkpoint array
+  const int64_t fws = batch * (int64_t)std::max(n_chunks - 1, 0) * d_inner * (d_state + 1);
+  const int64_t rws = batch * (int64_t)n_chunks * d_inner * (d_state + 1);
+  return (size_t)(2 * ck + fws + rws);
+}
+
+template <int N, typename T>
+static cudaError_t launch_bwd_t(const BwdArgs& a, const ScanParams& fwd, cudaStream_t s) {
+  const int64_t n_dtiles = (a.d_inner + kBwdCh - 1) / kBwdCh;
+  const int64_t tiles = (a.L + kBwdTile - 1) / kBwdTile;
+  if (a.n_chunks > 1) {
+    // forward chunk summaries: the forward scan's own summary pass
+    cudaError_t e = launch_scan_summary(fwd, sizeof(T) == 2, s);
+    if (e != cudaSuccess) return e;
+    bwd_reverse_kernel<N, T, true><<<(unsigned)(n_dtiles * (a.n_chunks - 1) * a.batch), kBwdCh, 0, s>>>(a);
+  }
+  bwd_fwd_ckpt_kernel<N, T><<<(unsigned)(n_dtiles * a.n_chunks * a.batch), kBwdCh, 0, s>>>(a);
+  bwd_reverse_kernel<N, T, false><<<(unsigned)(n_dtiles * a.n_chunks * a.batch), kBwdCh, 0, s>>>(a);
+  bwd_grad_kernel<N, T><<<(unsigned)(n_dtiles * tiles * a.batch), kBwdCh, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t dispatch_bwd(const BwdArgs& a, const ScanParams& fwd, cudaStream_t s) {
+  switch (a.d_state) {
+    case 1: return launch_bwd_t<1, T>(a, fwd, s);
+    case 2: return launch_bwd_t<2, T>(a, fwd, s);
+    case 3: return launch_bwd_t<3, T>(a, fwd, s);
+    case 4: return launch_bwd_t<4, T>(a, fwd, s);
+    case 5: return launch_bwd_t<5, T>(a, fwd, s);
+    case 6: return launch_bwd_t<6, T>(a, fwd, s);
+    case 7: return launch_bwd_t<7, T>(a, fwd, s);
+    case 8: return launch_bwd_t<8, T>(a, fwd, s);
+    case 9: return launch_bwd_t<9, T>(a, fwd, s);
+    case 10: return launch_bwd_t<10, T>(a, fwd, s);
+    case 11: return launch_bwd_t<11, T>(a, fwd, s);
+    case 12: return launch_bwd_t<12, T>(a, fwd, s);
+    case 13: return launch_bwd_t<13, T>(a, fwd, s);
+    case 14: return launch_bwd_t<14, T>(a, fwd, s);
+    case 15: return launch_bwd_t<15, T>(a, fwd, s);
+    case 16: return launch_bwd_t<16, T>(a, fwd, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_scan_bwd(const BwdArgs& a, const ScanParams& fwd, bool bf16, cudaStream_t s) {
+  return bf16 ? dispatch_bwd<__nv_bfloat16>(a, fwd, s) : dispatch_bwd<float>(a, fwd, s);
+}
+
+}  // namespace ssm
