@@ -52,6 +52,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--pass", dest="which", default="forward", choices=["forward", "backward", "conv"],
+                    help="forward: ssm_scan_fwd (default); backward: ssm_scan_bwd (gradients); "
+                         "conv: ssm_scan_fwd_conv (causal conv1d + SiLU fused in front)")
     ap.add_argument("--decode-steps", type=int, default=None,
                     help="decode steps per bench step (default: the workload's 1024); "
                          "only for small profiling captures")
@@ -74,6 +77,28 @@ def algorithmic_bytes(w: W.Workload) -> float:
     bc = w.batch * w.L * 2 * N * s                       # B, C rows
     last = w.batch * w.d_inner * N * 4                   # last_state write
     return float(acts + bc + params + last)
+
+
+def bwd_algorithmic_bytes(w: W.Workload) -> float:
+    """Backward: read u, delta, z, dy, B, C (io dtype), write du, ddelta, dz (io dtype) and
+    dB, dC (fp32); A, D, bias and their gradients once."""
+    s = 2 if w.bf16 else 4
+    N = w.d_state
+    acts = w.batch * w.L * w.d_inner * 7 * s
+    bc = w.batch * w.L * N * (2 * s + 2 * 4)
+    params = w.d_inner * (N + 2) * 4 * 2
+    return float(acts + bc + params)
+
+
+def bwd_alu_clocks_per_element(N: int) -> float:
+    """Backward lower bound per element: recomputing the state (4 FP32 + 1 ex2 per state) and
+    the reverse step (per state: the adjoint FMA, dA's product and ex2, the two terms of the
+    step-size gradient, the A-gradient FMA, the u-gradient FMA, the B and C partials and the
+    carry: 11 FP32 + 1 ex2), plus ~16 FP32, 4 ex2, 4 slow SFU ops per element."""
+    fp32 = 15 * N + 16
+    ex2 = 2 * N + 4
+    slow = 4
+    return max(fp32 / FP32_PER_CLK, ex2 / EX2_PER_CLK, slow / MUFU_SLOW_PER_CLK)
 
 
 def alu_clocks_per_element(N: int) -> float:
@@ -235,6 +260,54 @@ class ScanStep:
                               d["delta_bias"], True, self.y, self.last, self.ws, stream)
 
 
+class ConvScanStep(ScanStep):
+    """One step = one ssm_scan_fwd_conv call: u = silu(conv1d(x)) fused in front of the scan
+    (x: the workload's u tensor; d_conv = 4 taps ~ N(0, 0.5), bias ~ N(0, 0.2), seeded)."""
+
+    def __init__(self, w, dev, ssm, torch):
+        super().__init__(w, dev, ssm, torch)
+        import inputgen
+        self.cw = torch.from_numpy(inputgen.normal(w.seed, 10, 0.0, 0.5, 0, w.d_inner * 4, False)
+                                   .reshape(w.d_inner, 4)).cuda()
+        self.cb = torch.from_numpy(inputgen.normal(w.seed, 11, 0.0, 0.2, 0, w.d_inner, False)).cuda()
+
+    def __call__(self, stream=None):
+        d = self.dev
+        self.ssm.ssm_scan_fwd_conv(d["u"], self.cw, self.cb, d["delta"], d["A"], d["B"], d["C"], d["D"],
+                                   d["z"], d["delta_bias"], True, None, self.y, self.last, None,
+                                   self.ws, stream)
+
+
+class BackwardStep:
+    """One step = one ssm_scan_bwd call (all gradients) for dy ~ N(0, 1) (seeded)."""
+
+    def __init__(self, w, dev, ssm, torch):
+        import inputgen
+        self.dev, self.ssm = dev, ssm
+        self.dy = torch.empty_like(dev["u"])
+        inputgen.dev_fill_normal(w.seed, 9, 0.0, 1.0, 0, self.dy.numel(), w.bf16, self.dy.data_ptr(),
+                                 torch.cuda.current_stream().cuda_stream)
+        f32 = dict(dtype=torch.float32, device="cuda")
+        N = w.d_state
+        self.g = dict(du=torch.empty_like(dev["u"]), ddelta=torch.empty_like(dev["u"]),
+                      dz=torch.empty_like(dev["u"]), dA=torch.empty((w.d_inner, N), **f32),
+                      dB=torch.empty((w.batch, w.L, N), **f32), dC=torch.empty((w.batch, w.L, N), **f32),
+                      dD=torch.empty(w.d_inner, **f32), ddelta_bias=torch.empty(w.d_inner, **f32))
+        io = ssm.SSM_BF16 if w.bf16 else ssm.SSM_F32
+        nbytes = ssm.ssm_scan_bwd_workspace_size(w.batch, w.L, w.d_inner, N, io)
+        self.ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        nf = ssm.ssm_scan_fwd_workspace_size(w.batch, w.L, w.d_inner, N, io)
+        # summary + reverse summary when chunked, checkpoints, reverse checkpoints, gradients
+        self.launches = 5 if nf else 3
+
+    def __call__(self, stream=None):
+        d, g = self.dev, self.g
+        self.ssm.ssm_scan_bwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"],
+                              d["delta_bias"], True, None, self.dy, None, g["du"], g["ddelta"],
+                              g["dA"], g["dB"], g["dC"], g["dD"], g["dz"], g["ddelta_bias"], None,
+                              self.ws, stream)
+
+
 class DecodeStep:
     """One step = the workload's sequential single-token decode steps."""
 
@@ -344,12 +417,17 @@ def whole_job_rate(elements_per_rank: int, world: int, ms_max: float) -> float:
     return world * elements_per_rank / (ms_max * 1e-3)
 
 
-def roofline(w, ms_per_step, hbm_gbs, sm_mhz, sms, peak_src, traffic=None):
+def roofline(w, ms_per_step, hbm_gbs, sm_mhz, sms, peak_src, traffic=None, which="forward"):
     el_rate = w.elements / (ms_per_step * 1e-3)
-    t_hbm = algorithmic_bytes(w) / (hbm_gbs * 1e9)
-    t_alu = w.elements * alu_clocks_per_element(w.d_state) / (sms * sm_mhz * 1e6)
+    nbytes = bwd_algorithmic_bytes(w) if which == "backward" else algorithmic_bytes(w)
+    clocks = (bwd_alu_clocks_per_element if which == "backward" else alu_clocks_per_element)(w.d_state)
+    if which == "conv":  # conv1d (4 FMA) + SiLU (3 FP32, 1 ex2, 1 rcp) more per element
+        clocks = max(clocks, (4 * w.d_state + 13) / FP32_PER_CLK, (w.d_state + 3) / EX2_PER_CLK,
+                     3 / MUFU_SLOW_PER_CLK)
+    t_hbm = nbytes / (hbm_gbs * 1e9)
+    t_alu = w.elements * clocks / (sms * sm_mhz * 1e6)
     if t_hbm >= t_alu:
-        achieved = algorithmic_bytes(w) / (ms_per_step * 1e-3) / 1e9
+        achieved = nbytes / (ms_per_step * 1e-3) / 1e9
         return {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
                 "frac": achieved / hbm_gbs, "traffic": traffic,
                 "algorithmic_bytes": algorithmic_bytes(w),
@@ -374,7 +452,14 @@ def main_ours(args, rank, world, local_rank):
         import dataclasses
         w = dataclasses.replace(w, L=args.decode_steps)
     dev = W.device_inputs(w)
-    step = DecodeStep(w, dev, ssm, torch) if w.decode else ScanStep(w, dev, ssm, torch)
+    if w.decode:
+        step = DecodeStep(w, dev, ssm, torch)
+    elif args.which == "backward":
+        step = BackwardStep(w, dev, ssm, torch)
+    elif args.which == "conv":
+        step = ConvScanStep(w, dev, ssm, torch)
+    else:
+        step = ScanStep(w, dev, ssm, torch)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
     sms = torch.cuda.get_device_properties(local_rank).multi_processor_count
@@ -400,7 +485,7 @@ def main_ours(args, rank, world, local_rank):
     ms = max_over_ranks(float(np.mean([e0.elapsed_time(e1) for e0, e1 in events])), world, "cuda")
 
     e2e = None
-    if not args.no_e2e and not w.decode:
+    if not args.no_e2e and not w.decode and args.which == "forward":
         e2e = run_e2e(w, dev, ssm, torch, args.e2e_steps)
         if e2e is not None and world > 1:
             e2e["ms_per_step"] = max_over_ranks(e2e["ms_per_step"], world, "cuda")
@@ -412,8 +497,9 @@ def main_ours(args, rank, world, local_rank):
     clk = clocks.summary()
     sm_mhz_peak = float(clk["sm_max_mhz"] or SM_MAX_MHZ_NOMINAL)
     out = {
-        "metric": "scan elements/s (B*L*d_inner)" if not w.decode
-        else "decode elements/s (B*d_inner*steps)",
+        "metric": ("decode elements/s (B*d_inner*steps)" if w.decode else
+                   "scan backward elements/s (B*L*d_inner)" if args.which == "backward" else
+                   "scan elements/s (B*L*d_inner)"),
         "value": whole_job_rate(w.elements, world, ms),
         "unit": "elements/s",
         "n_gpus": world,
@@ -428,10 +514,12 @@ def main_ours(args, rank, world, local_rank):
         "config": {"workload": w.desc, "batch": w.batch,
                    ("steps" if w.decode else "seq_len"): w.L, "d_inner": w.d_inner,
                    "d_state": w.d_state, "io_dtype": "bf16" if w.bf16 else "f32",
+                   "pass": args.which,
                    "parallelism": f"replica per GPU x{world}" if world > 1 else "single GPU",
                    "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write)"},
         "roofline": roofline(w, ms, hbm_gbs, sm_mhz_peak, sms, peak_src,
-                             measured_traffic(w.key)),
+                             measured_traffic(w.key) if args.which == "forward" else None,
+                             args.which),
         "gpu_launches": step.launches * args.steps,
         "clocks": clk,
     }

@@ -65,8 +65,24 @@ __global__ void __launch_bounds__(kBwdCh) bwd_fwd_ckpt_kernel(const BwdArgs p) {
 #pragma unroll
     for (int n = 0; n < N; n++) h[n] = fmaf(ex2(A2[n] * S), h[n], p.fws_h[slot * N + n]);
   }
+  // A tile's activations are loaded into registers all at once (16 independent loads per
+  // tensor), and the next tile's are requested before the current one is computed.
+  float xr[kBwdTile], ur[kBwdTile];
+  auto load_tile = [&](int64_t ts, float* xa, float* ua) {
+    const int steps = (int)min((int64_t)kBwdTile, t1 - ts);
+#pragma unroll
+    for (int k = 0; k < kBwdTile; k++) {
+      const int64_t e = (b * L + ts + min(k, steps - 1)) * Dn + dc;
+      xa[k] = ldf<T>(p.delta, e);
+      ua[k] = ldf<T>(p.u, e);
+    }
+  };
+  if (t0 < t1) load_tile(t0, xr, ur);
   for (int64_t ts = t0; ts < t1; ts += kBwdTile) {
     const int steps = (int)min((int64_t)kBwdTile, t1 - ts);
+    float xn[kBwdTile], un[kBwdTile];
+    const bool more = ts + kBwdTile < t1;
+    if (more) load_tile(ts + kBwdTile, xn, un);
     if (active) {
       float* ck = p.ckpt_h + ((b * tiles + ts / kBwdTile) * Dn + d) * N;
 #pragma unroll
@@ -75,15 +91,21 @@ __global__ void __launch_bounds__(kBwdCh) bwd_fwd_ckpt_kernel(const BwdArgs p) {
     __syncwarp();
     for (int i = lane; i < steps * N; i += kBwdCh) sB[i / N][i % N] = ldf<T>(p.B, (b * L + ts) * N + i);
     __syncwarp();
-    for (int k = 0; k < steps; k++) {
-      const int64_t e = (b * L + ts + k) * Dn + dc;
-      const float x = ldf<T>(p.delta, e) + bias;
-      const float dt = p.softplus ? softplus(x) : x;
-      const float w = dt * ldf<T>(p.u, e);
 #pragma unroll
-      for (int n = 0; n < N; n++) h[n] = fmaf(ex2(dt * A2[n]), h[n], w * sB[k][n]);
+    for (int k = 0; k < kBwdTile; k++) {
+      if (k < steps) {
+        const float x = xr[k] + bias;
+        const float dt = p.softplus ? softplus(x) : x;
+        const float w = dt * ur[k];
+#pragma unroll
+        for (int n = 0; n < N; n++) h[n] = fmaf(ex2(dt * A2[n]), h[n], w * sB[k][n]);
+      }
     }
     __syncwarp();
+    if (more) {
+#pragma unroll
+      for (int k = 0; k < kBwdTile; k++) { xr[k] = xn[k]; ur[k] = un[k]; }
+    }
   }
 }
 
@@ -129,9 +151,26 @@ __global__ void __launch_bounds__(kBwdCh) bwd_reverse_kernel(const BwdArgs p) {
   }
   float S = 0.f, S_comp = 0.f;
   const int64_t first_tile = t0 / kBwdTile, last_tile = (t1 - 1) / kBwdTile;
+  // per tile: delta_raw, dy (times silu(z)) in registers, loaded at once, next tile prefetched
+  float xr[kBwdTile], dr[kBwdTile], zr[kBwdTile];
+  auto load_tile = [&](int64_t tl, float* xa, float* da, float* za) {
+    const int64_t ts = tl * kBwdTile;
+    const int steps = (int)min((int64_t)kBwdTile, t1 - ts);
+#pragma unroll
+    for (int k = 0; k < kBwdTile; k++) {
+      const int64_t e = (b * L + ts + min(k, steps - 1)) * Dn + dc;
+      xa[k] = ldf<T>(p.delta, e);
+      da[k] = ldf<T>(p.dy, e);
+      za[k] = p.z ? ldf<T>(p.z, e) : 0.f;
+    }
+  };
+  if (t0 < t1) load_tile(last_tile, xr, dr, zr);
   for (int64_t tl = last_tile; tl >= first_tile; tl--) {
     const int64_t ts = tl * kBwdTile;
     const int steps = (int)min((int64_t)kBwdTile, t1 - ts);
+    float xn[kBwdTile], dn[kBwdTile], zn[kBwdTile];
+    const bool more = tl > first_tile;
+    if (more) load_tile(tl - 1, xn, dn, zn);
     if (!kSummary && active) {
       float* ck = p.ckpt_m + ((b * tiles + tl) * Dn + d) * N;
 #pragma unroll
@@ -140,22 +179,27 @@ __global__ void __launch_bounds__(kBwdCh) bwd_reverse_kernel(const BwdArgs p) {
     __syncwarp();
     for (int i = lane; i < steps * N; i += kBwdCh) sC[i / N][i % N] = ldf<T>(p.C, (b * L + ts) * N + i);
     __syncwarp();
-    for (int k = steps - 1; k >= 0; k--) {
-      const int64_t e = (b * L + ts + k) * Dn + dc;
-      const float x = ldf<T>(p.delta, e) + bias;
-      const float dt = p.softplus ? softplus(x) : x;
-      if (kSummary) {
-        const float yk = dt - S_comp;
-        const float tk = S + yk;
-        S_comp = (tk - S) - yk;
-        S = tk;
-      }
-      float ds = ldf<T>(p.dy, e);
-      if (p.z) ds *= silu(ldf<T>(p.z, e));
 #pragma unroll
-      for (int n = 0; n < N; n++) m[n] = ex2(dt * A2[n]) * fmaf(ds, sC[k][n], m[n]);
+    for (int k = kBwdTile - 1; k >= 0; k--) {
+      if (k < steps) {
+        const float x = xr[k] + bias;
+        const float dt = p.softplus ? softplus(x) : x;
+        if (kSummary) {
+          const float yk = dt - S_comp;
+          const float tk = S + yk;
+          S_comp = (tk - S) - yk;
+          S = tk;
+        }
+        const float ds = p.z ? dr[k] * silu(zr[k]) : dr[k];
+#pragma unroll
+        for (int n = 0; n < N; n++) m[n] = ex2(dt * A2[n]) * fmaf(ds, sC[k][n], m[n]);
+      }
     }
     __syncwarp();
+    if (more) {
+#pragma unroll
+      for (int k = 0; k < kBwdTile; k++) { xr[k] = xn[k]; dr[k] = dn[k]; zr[k] = zn[k]; }
+    }
   }
   if (kSummary && active) {
     const int64_t slot = (b * p.n_chunks + c) * Dn + d;
@@ -220,14 +264,17 @@ __global__ void __launch_bounds__(kBwdCh) bwd_grad_kernel(const BwdArgs p) {
   }
   const float bias = p.delta_bias ? p.delta_bias[dc] : 0.f;
   const float Dd = p.D ? p.D[dc] : 0.f;
-  float xs[kBwdTile], dts[kBwdTile], us[kBwdTile];
+  float xs[kBwdTile], dts[kBwdTile], us[kBwdTile], dys[kBwdTile], zs[kBwdTile];
 #pragma unroll
   for (int k = 0; k < kBwdTile; k++) {
     const int64_t e = (b * L + ts + min(k, steps - 1)) * Dn + dc;
     xs[k] = ldf<T>(p.delta, e) + bias;
-    dts[k] = p.softplus ? softplus(xs[k]) : xs[k];
     us[k] = ldf<T>(p.u, e);
+    dys[k] = ldf<T>(p.dy, e);
+    zs[k] = p.z ? ldf<T>(p.z, e) : 0.f;
   }
+#pragma unroll
+  for (int k = 0; k < kBwdTile; k++) dts[k] = p.softplus ? softplus(xs[k]) : xs[k];
   __syncwarp();
 
   // forward recompute of the tile's states
@@ -254,13 +301,13 @@ __global__ void __launch_bounds__(kBwdCh) bwd_grad_kernel(const BwdArgs p) {
   for (int k = kBwdTile - 1; k >= 0; k--) {
     if (k >= steps) continue;
     const int64_t e = (b * L + ts + k) * Dn + dc;
-    const float dyk = ldf<T>(p.dy, e);
+    const float dyk = dys[k];
     float s = Dd * us[k];
 #pragma unroll
     for (int n = 0; n < N; n++) s = fmaf(sC[k][n], sH[k][n][lane], s);
     float g = 1.f;
     if (p.z) {
-      const float zk = ldf<T>(p.z, e);
+      const float zk = zs[k];
       const float sg = rcp(1.f + ex2(-zk * kLog2e));
       g = zk * sg;
       if (active) static_cast<T*>(p.dz)[e] = from_f32<T>(dyk * s * sg * fmaf(zk, 1.f - sg, 1.f));
