@@ -38,6 +38,7 @@ __device__ __forceinline__ float ldf(const void* p, int64_t i) {
 //    state before each tile.
 template <int N, typename T>
 __global__ void __launch_bounds__(kBwdCh) bwd_fwd_ckpt_kernel(const BwdArgs p) {
+  constexpr int NP = (N + 1) / 2;  // state pairs (packed fp32x2 arithmetic)
   const int64_t n_dtiles = (p.d_inner + kBwdCh - 1) / kBwdCh;
   int64_t blk = blockIdx.x;
   const int64_t dtile = blk % n_dtiles;
@@ -50,20 +51,28 @@ __global__ void __launch_bounds__(kBwdCh) bwd_fwd_ckpt_kernel(const BwdArgs p) {
   const int64_t dc = active ? d : 0;
   const int64_t t0 = (int64_t)c * p.chunk_len, t1 = min(t0 + p.chunk_len, L);
   const int64_t tiles = (L + kBwdTile - 1) / kBwdTile;
-  __shared__ float sB[kBwdTile][N];
+  __shared__ __align__(16) float sB[kBwdTile][2 * NP];
 
-  float A2[N], h[N];
+  float2 A2[NP], h[NP];
 #pragma unroll
-  for (int n = 0; n < N; n++) {
-    A2[n] = p.A[dc * N + n] * kLog2e;
-    h[n] = p.initial_state ? p.initial_state[(b * Dn + dc) * N + n] : 0.f;
+  for (int j = 0; j < NP; j++) {
+    const int n0 = 2 * j, n1 = n0 + 1;
+    A2[j] = make_float2(p.A[dc * N + n0] * kLog2e, n1 < N ? p.A[dc * N + n1] * kLog2e : 0.f);
+    const float* h0 = p.initial_state ? p.initial_state + (b * Dn + dc) * N : nullptr;
+    h[j] = h0 ? make_float2(h0[n0], n1 < N ? h0[n1] : 0.f) : make_float2(0.f, 0.f);
   }
+  if (2 * NP != N)
+    for (int i = lane; i < kBwdTile; i += kBwdCh) sB[i][N] = 0.f;
   const float bias = p.delta_bias ? p.delta_bias[dc] : 0.f;
   for (int j = 0; j < c; j++) {
     const int64_t slot = (b * (p.n_chunks - 1) + j) * Dn + dc;
     const float S = p.fws_S[slot];
+    const float* hs = p.fws_h + slot * N;
 #pragma unroll
-    for (int n = 0; n < N; n++) h[n] = fmaf(ex2(A2[n] * S), h[n], p.fws_h[slot * N + n]);
+    for (int q = 0; q < NP; q++) {
+      h[q].x = fmaf(ex2(A2[q].x * S), h[q].x, hs[2 * q]);
+      h[q].y = fmaf(ex2(A2[q].y * S), h[q].y, 2 * q + 1 < N ? hs[2 * q + 1] : 0.f);
+    }
   }
   // A tile's activations are loaded into registers all at once (16 independent loads per
   // tensor), and the next tile's are requested before the current one is computed.
@@ -86,7 +95,10 @@ __global__ void __launch_bounds__(kBwdCh) bwd_fwd_ckpt_kernel(const BwdArgs p) {
     if (active) {
       float* ck = p.ckpt_h + ((b * tiles + ts / kBwdTile) * Dn + d) * N;
 #pragma unroll
-      for (int n = 0; n < N; n++) ck[n] = h[n];
+      for (int j = 0; j < NP; j++) {
+        ck[2 * j] = h[j].x;
+        if (2 * j + 1 < N) ck[2 * j + 1] = h[j].y;
+      }
     }
     __syncwarp();
     for (int i = lane; i < steps * N; i += kBwdCh) sB[i / N][i % N] = ldf<T>(p.B, (b * L + ts) * N + i);
@@ -97,8 +109,13 @@ __global__ void __launch_bounds__(kBwdCh) bwd_fwd_ckpt_kernel(const BwdArgs p) {
         const float x = xr[k] + bias;
         const float dt = p.softplus ? softplus(x) : x;
         const float w = dt * ur[k];
+        const float2 dt2 = make_float2(dt, dt), w2 = make_float2(w, w);
 #pragma unroll
-        for (int n = 0; n < N; n++) h[n] = fmaf(ex2(dt * A2[n]), h[n], w * sB[k][n]);
+        for (int j = 0; j < NP; j++) {
+          const float2 xa = __fmul2_rn(dt2, A2[j]);
+          h[j] = __ffma2_rn(make_float2(ex2(xa.x), ex2(xa.y)), h[j],
+                            __fmul2_rn(w2, *reinterpret_cast<const float2*>(&sB[k][2 * j])));
+        }
       }
     }
     __syncwarp();
@@ -117,6 +134,7 @@ __global__ void __launch_bounds__(kBwdCh) bwd_fwd_ckpt_kernel(const BwdArgs p) {
 //    the carry (from dlast), then store the carry entering each tile, walking right to left.
 template <int N, typename T, bool kSummary>
 __global__ void __launch_bounds__(kBwdCh) bwd_reverse_kernel(const BwdArgs p) {
+  constexpr int NP = (N + 1) / 2;
   const int64_t n_dtiles = (p.d_inner + kBwdCh - 1) / kBwdCh;
   const int chunks = kSummary ? p.n_chunks - 1 : p.n_chunks;
   int64_t blk = blockIdx.x;
@@ -130,28 +148,38 @@ __global__ void __launch_bounds__(kBwdCh) bwd_reverse_kernel(const BwdArgs p) {
   const int64_t dc = active ? d : 0;
   const int64_t t0 = (int64_t)c * p.chunk_len, t1 = min(t0 + p.chunk_len, L);
   const int64_t tiles = (L + kBwdTile - 1) / kBwdTile;
-  __shared__ float sC[kBwdTile][N];
+  __shared__ __align__(16) float sC[kBwdTile][2 * NP];
 
-  float A2[N], m[N];
+  float2 A2[NP], m[NP];
 #pragma unroll
-  for (int n = 0; n < N; n++) {
-    A2[n] = p.A[dc * N + n] * kLog2e;
-    m[n] = 0.f;
+  for (int j = 0; j < NP; j++) {
+    const int n0 = 2 * j, n1 = n0 + 1;
+    A2[j] = make_float2(p.A[dc * N + n0] * kLog2e, n1 < N ? p.A[dc * N + n1] * kLog2e : 0.f);
+    m[j] = make_float2(0.f, 0.f);
   }
+  if (2 * NP != N)
+    for (int i = lane; i < kBwdTile; i += kBwdCh) sC[i][N] = 0.f;
   const float bias = p.delta_bias ? p.delta_bias[dc] : 0.f;
   if (!kSummary) {
+    if (p.dlast) {
+      const float* dl = p.dlast + (b * Dn + dc) * N;
 #pragma unroll
-    for (int n = 0; n < N; n++) m[n] = p.dlast ? p.dlast[(b * Dn + dc) * N + n] : 0.f;
+      for (int j = 0; j < NP; j++) m[j] = make_float2(dl[2 * j], 2 * j + 1 < N ? dl[2 * j + 1] : 0.f);
+    }
     for (int j = p.n_chunks - 1; j > c; j--) {
       const int64_t slot = (b * p.n_chunks + j) * Dn + dc;
       const float S = p.rws_S[slot];
+      const float* ms = p.rws_m + slot * N;
 #pragma unroll
-      for (int n = 0; n < N; n++) m[n] = fmaf(ex2(A2[n] * S), m[n], p.rws_m[slot * N + n]);
+      for (int q = 0; q < NP; q++) {
+        m[q].x = fmaf(ex2(A2[q].x * S), m[q].x, ms[2 * q]);
+        m[q].y = fmaf(ex2(A2[q].y * S), m[q].y, 2 * q + 1 < N ? ms[2 * q + 1] : 0.f);
+      }
     }
   }
   float S = 0.f, S_comp = 0.f;
   const int64_t first_tile = t0 / kBwdTile, last_tile = (t1 - 1) / kBwdTile;
-  // per tile: delta_raw, dy (times silu(z)) in registers, loaded at once, next tile prefetched
+  // per tile: delta_raw, dy, z in registers, loaded at once, next tile prefetched
   float xr[kBwdTile], dr[kBwdTile], zr[kBwdTile];
   auto load_tile = [&](int64_t tl, float* xa, float* da, float* za) {
     const int64_t ts = tl * kBwdTile;
@@ -174,7 +202,10 @@ __global__ void __launch_bounds__(kBwdCh) bwd_reverse_kernel(const BwdArgs p) {
     if (!kSummary && active) {
       float* ck = p.ckpt_m + ((b * tiles + tl) * Dn + d) * N;
 #pragma unroll
-      for (int n = 0; n < N; n++) ck[n] = m[n];
+      for (int j = 0; j < NP; j++) {
+        ck[2 * j] = m[j].x;
+        if (2 * j + 1 < N) ck[2 * j + 1] = m[j].y;
+      }
     }
     __syncwarp();
     for (int i = lane; i < steps * N; i += kBwdCh) sC[i / N][i % N] = ldf<T>(p.C, (b * L + ts) * N + i);
@@ -191,8 +222,13 @@ __global__ void __launch_bounds__(kBwdCh) bwd_reverse_kernel(const BwdArgs p) {
           S = tk;
         }
         const float ds = p.z ? dr[k] * silu(zr[k]) : dr[k];
+        const float2 dt2 = make_float2(dt, dt), ds2 = make_float2(ds, ds);
 #pragma unroll
-        for (int n = 0; n < N; n++) m[n] = ex2(dt * A2[n]) * fmaf(ds, sC[k][n], m[n]);
+        for (int j = 0; j < NP; j++) {
+          const float2 xa = __fmul2_rn(dt2, A2[j]);
+          m[j] = __fmul2_rn(make_float2(ex2(xa.x), ex2(xa.y)),
+                            __ffma2_rn(ds2, *reinterpret_cast<const float2*>(&sC[k][2 * j]), m[j]));
+        }
       }
     }
     __syncwarp();
@@ -205,7 +241,10 @@ __global__ void __launch_bounds__(kBwdCh) bwd_reverse_kernel(const BwdArgs p) {
     const int64_t slot = (b * p.n_chunks + c) * Dn + d;
     p.rws_S[slot] = S;
 #pragma unroll
-    for (int n = 0; n < N; n++) p.rws_m[slot * N + n] = m[n];
+    for (int j = 0; j < NP; j++) {
+      p.rws_m[slot * N + 2 * j] = m[j].x;
+      if (2 * j + 1 < N) p.rws_m[slot * N + 2 * j + 1] = m[j].y;
+    }
   }
 }
 
@@ -230,123 +269,190 @@ __device__ __forceinline__ void warp_reduce_scatter_add(float (&v)[32], int lane
   else if (lane < 2 * N) atomicAdd(dC_row + lane - N, v[0]);
 }
 
+constexpr int kGradTiles = 4;  // tiles per gradient CTA, walked backwards
+
 template <int N, typename T>
 __global__ void __launch_bounds__(kBwdCh) bwd_grad_kernel(const BwdArgs p) {
   static_assert(2 * N <= 32, "dB/dC partials must fit one value per lane");
+  constexpr int NP = (N + 1) / 2;          // state pairs (packed fp32x2 arithmetic)
+  constexpr int NQ = (2 * NP + 3) / 4;     // groups of 4 states in the shared state rows
   const int64_t n_dtiles = (p.d_inner + kBwdCh - 1) / kBwdCh;
   const int64_t tiles = (p.L + kBwdTile - 1) / kBwdTile;
+  const int64_t ranges = (tiles + kGradTiles - 1) / kGradTiles;
   int64_t blk = blockIdx.x;
   const int64_t dtile = blk % n_dtiles;
   blk /= n_dtiles;
-  const int64_t tl = blk % tiles;
-  const int64_t b = blk / tiles;
+  const int64_t r = blk % ranges;
+  const int64_t b = blk / ranges;
   const int lane = threadIdx.x;
   const int64_t Dn = p.d_inner, L = p.L, d = dtile * kBwdCh + lane;
   const bool active = d < Dn;
   const int64_t dc = active ? d : 0;
-  const int64_t ts = tl * kBwdTile;
-  const int steps = (int)min((int64_t)kBwdTile, L - ts);
-  __shared__ float sB[kBwdTile][N], sC[kBwdTile][N];
-  __shared__ float sH[kBwdTile][N][kBwdCh];  // state after each step of the tile
+  const int64_t tl_lo = r * kGradTiles, tl_hi = min(tl_lo + kGradTiles, tiles) - 1;
+  __shared__ __align__(16) float sB[kBwdTile][4 * NQ], sC[kBwdTile][4 * NQ];
+  // states after each step of the tile: [step][group of 4 states][lane][4] (16-byte rows)
+  __shared__ __align__(16) float4 sH[kBwdTile][NQ][kBwdCh];
 
-  for (int i = lane; i < steps * N; i += kBwdCh) {
-    sB[i / N][i % N] = ldf<T>(p.B, (b * L + ts) * N + i);
-    sC[i / N][i % N] = ldf<T>(p.C, (b * L + ts) * N + i);
-  }
-  float A2[N], Af[N], h0[N], m[N], dAacc[N];
+  float2 A2[NP], Af[NP], m[NP], dAacc[NP];
 #pragma unroll
-  for (int n = 0; n < N; n++) {
-    Af[n] = p.A[dc * N + n];
-    A2[n] = Af[n] * kLog2e;
-    h0[n] = active ? p.ckpt_h[((b * tiles + tl) * Dn + d) * N + n] : 0.f;
-    m[n] = active ? p.ckpt_m[((b * tiles + tl) * Dn + d) * N + n] : 0.f;
-    dAacc[n] = 0.f;
+  for (int j = 0; j < NP; j++) {
+    const int n0 = 2 * j, n1 = 2 * j + 1;
+    const float a0 = p.A[dc * N + n0], a1 = n1 < N ? p.A[dc * N + n1] : 0.f;
+    Af[j] = make_float2(a0, a1);
+    A2[j] = make_float2(a0 * kLog2e, a1 * kLog2e);
+    const float* mk = p.ckpt_m + ((b * tiles + tl_hi) * Dn + dc) * N;
+    m[j] = active ? make_float2(mk[n0], n1 < N ? mk[n1] : 0.f) : make_float2(0.f, 0.f);
+    dAacc[j] = make_float2(0.f, 0.f);
+  }
+  if (2 * NP != 4 * NQ || 2 * NP != N) {  // zero the padding columns of the B/C rows
+    for (int i = lane; i < kBwdTile * 4 * NQ; i += kBwdCh) { sB[i / (4 * NQ)][i % (4 * NQ)] = 0.f; sC[i / (4 * NQ)][i % (4 * NQ)] = 0.f; }
   }
   const float bias = p.delta_bias ? p.delta_bias[dc] : 0.f;
   const float Dd = p.D ? p.D[dc] : 0.f;
-  float xs[kBwdTile], dts[kBwdTile], us[kBwdTile], dys[kBwdTile], zs[kBwdTile];
-#pragma unroll
-  for (int k = 0; k < kBwdTile; k++) {
-    const int64_t e = (b * L + ts + min(k, steps - 1)) * Dn + dc;
-    xs[k] = ldf<T>(p.delta, e) + bias;
-    us[k] = ldf<T>(p.u, e);
-    dys[k] = ldf<T>(p.dy, e);
-    zs[k] = p.z ? ldf<T>(p.z, e) : 0.f;
-  }
-#pragma unroll
-  for (int k = 0; k < kBwdTile; k++) dts[k] = p.softplus ? softplus(xs[k]) : xs[k];
-  __syncwarp();
+  float dDacc = 0.f, dbacc = 0.f;
+  auto hrow = [&](int k, int j) -> float2 {
+    const float4 q = sH[k][j / 2][lane];
+    return (j & 1) ? make_float2(q.z, q.w) : make_float2(q.x, q.y);
+  };
+  auto pair_of = [&](const float* row, int j) -> float2 {
+    return *reinterpret_cast<const float2*>(row + 2 * j);
+  };
 
-  // forward recompute of the tile's states
-  {
-    float h[N];
-#pragma unroll
-    for (int n = 0; n < N; n++) h[n] = h0[n];
+  for (int64_t tl = tl_hi; tl >= tl_lo; tl--) {
+    const int64_t ts = tl * kBwdTile;
+    const int steps = (int)min((int64_t)kBwdTile, L - ts);
+    float xs[kBwdTile], us[kBwdTile], dys[kBwdTile], zs[kBwdTile];
 #pragma unroll
     for (int k = 0; k < kBwdTile; k++) {
-      if (k < steps) {
-        const float w = dts[k] * us[k];
+      const int64_t e = (b * L + ts + min(k, steps - 1)) * Dn + dc;
+      xs[k] = ldf<T>(p.delta, e) + bias;
+      us[k] = ldf<T>(p.u, e);
+      dys[k] = ldf<T>(p.dy, e);
+      zs[k] = p.z ? ldf<T>(p.z, e) : 0.f;
+    }
+    __syncwarp();
+    for (int i = lane; i < steps * N; i += kBwdCh) {
+      sB[i / N][i % N] = ldf<T>(p.B, (b * L + ts) * N + i);
+      sC[i / N][i % N] = ldf<T>(p.C, (b * L + ts) * N + i);
+    }
+    float2 h0[NP];
+    {
+      const float* hk = p.ckpt_h + ((b * tiles + tl) * Dn + dc) * N;
 #pragma unroll
-        for (int n = 0; n < N; n++) {
-          h[n] = fmaf(ex2(dts[k] * A2[n]), h[n], w * sB[k][n]);
-          sH[k][n][lane] = h[n];
+      for (int j = 0; j < NP; j++)
+        h0[j] = active ? make_float2(hk[2 * j], 2 * j + 1 < N ? hk[2 * j + 1] : 0.f) : make_float2(0.f, 0.f);
+    }
+    __syncwarp();
+    float dts[kBwdTile];
+#pragma unroll
+    for (int k = 0; k < kBwdTile; k++) dts[k] = p.softplus ? softplus(xs[k]) : xs[k];
+
+    // forward recompute of the tile's states into shared memory
+    {
+      float2 h[NP];
+#pragma unroll
+      for (int j = 0; j < NP; j++) h[j] = h0[j];
+#pragma unroll
+      for (int k = 0; k < kBwdTile; k++) {
+        if (k < steps) {
+          const float2 dt2 = make_float2(dts[k], dts[k]);
+          const float w = dts[k] * us[k];
+          const float2 w2 = make_float2(w, w);
+#pragma unroll
+          for (int j = 0; j < NP; j++) {
+            const float2 xa = __fmul2_rn(dt2, A2[j]);
+            h[j] = __ffma2_rn(make_float2(ex2(xa.x), ex2(xa.y)), h[j], __fmul2_rn(w2, pair_of(sB[k], j)));
+          }
+#pragma unroll
+          for (int q = 0; q < NQ; q++)
+            sH[k][q][lane] = make_float4(h[2 * q].x, h[2 * q].y, 2 * q + 1 < NP ? h[2 * q + 1].x : 0.f,
+                                         2 * q + 1 < NP ? h[2 * q + 1].y : 0.f);
         }
       }
     }
-  }
-  __syncwarp();
+    __syncwarp();
 
-  float dDacc = 0.f, dbacc = 0.f;
+    // reverse over the tile; hk holds the state after step k, loaded one step ahead
+    float2 hk[NP];
 #pragma unroll
-  for (int k = kBwdTile - 1; k >= 0; k--) {
-    if (k >= steps) continue;
-    const int64_t e = (b * L + ts + k) * Dn + dc;
-    const float dyk = dys[k];
-    float s = Dd * us[k];
+    for (int j = 0; j < NP; j++) hk[j] = hrow(kBwdTile - 1 < steps ? kBwdTile - 1 : 0, j);
 #pragma unroll
-    for (int n = 0; n < N; n++) s = fmaf(sC[k][n], sH[k][n][lane], s);
-    float g = 1.f;
-    if (p.z) {
-      const float zk = zs[k];
-      const float sg = rcp(1.f + ex2(-zk * kLog2e));
-      g = zk * sg;
-      if (active) static_cast<T*>(p.dz)[e] = from_f32<T>(dyk * s * sg * fmaf(zk, 1.f - sg, 1.f));
+    for (int k = kBwdTile - 1; k >= 0; k--) {
+      if (k >= steps) {
+        if (k - 1 >= 0 && k - 1 < steps) {
+#pragma unroll
+          for (int j = 0; j < NP; j++) hk[j] = hrow(k - 1, j);
+        }
+        continue;
+      }
+      const int64_t e = (b * L + ts + k) * Dn + dc;
+      float2 hp[NP];
+#pragma unroll
+      for (int j = 0; j < NP; j++) hp[j] = k > 0 ? hrow(k - 1, j) : h0[j];
+      float2 s2 = make_float2(Dd * us[k], 0.f);
+#pragma unroll
+      for (int j = 0; j < NP; j++) s2 = __ffma2_rn(pair_of(sC[k], j), hk[j], s2);
+      const float s = s2.x + s2.y;
+      float g = 1.f;
+      if (p.z) {
+        const float sg = rcp(1.f + ex2(-zs[k] * kLog2e));
+        g = zs[k] * sg;
+        if (active) static_cast<T*>(p.dz)[e] = from_f32<T>(dys[k] * s * sg * fmaf(zs[k], 1.f - sg, 1.f));
+      }
+      const float ds = dys[k] * g;
+      dDacc = fmaf(ds, us[k], dDacc);
+      const float dt = dts[k];
+      const float2 dt2 = make_float2(dt, dt), ds2 = make_float2(ds, ds), u2 = make_float2(us[k], us[k]);
+      const float dtu = dt * us[k];
+      const float2 dtu2 = make_float2(active ? dtu : 0.f, active ? dtu : 0.f);
+      const float2 dsa = make_float2(active ? ds : 0.f, active ? ds : 0.f);
+      float2 ddt2 = make_float2(0.f, 0.f), slb2 = make_float2(0.f, 0.f);
+      float v[32];
+#pragma unroll
+      for (int j = 0; j < NP; j++) {
+        const float2 Bv = pair_of(sB[k], j);
+        const float2 lam = __ffma2_rn(ds2, pair_of(sC[k], j), m[j]);
+        const float2 xa = __fmul2_rn(dt2, A2[j]);
+        const float2 dA = make_float2(ex2(xa.x), ex2(xa.y));
+        const float2 t1 = __fmul2_rn(__fmul2_rn(lam, hp[j]), dA);
+        ddt2 = __ffma2_rn(t1, Af[j], __ffma2_rn(lam, __fmul2_rn(Bv, u2), ddt2));
+        dAacc[j] = __ffma2_rn(t1, dt2, dAacc[j]);
+        slb2 = __ffma2_rn(lam, Bv, slb2);
+        const float2 pb = __fmul2_rn(lam, dtu2), pc = __fmul2_rn(dsa, hk[j]);
+        v[2 * j] = pb.x;
+        if (2 * j + 1 < N) v[2 * j + 1] = pb.y;
+        v[N + 2 * j] = pc.x;
+        if (2 * j + 1 < N) v[N + 2 * j + 1] = pc.y;
+        m[j] = __fmul2_rn(dA, lam);
+        hk[j] = hp[j];
+      }
+#pragma unroll
+      for (int j = 2 * N; j < 32; j++) v[j] = 0.f;
+      const float ddt = ddt2.x + ddt2.y;
+      const float dx = p.softplus ? ddt * rcp(1.f + ex2(-xs[k] * kLog2e)) : ddt;
+      dbacc += dx;
+      if (active) {
+        static_cast<T*>(p.du)[e] = from_f32<T>(fmaf(ds, Dd, dt * (slb2.x + slb2.y)));
+        static_cast<T*>(p.ddelta)[e] = from_f32<T>(dx);
+      }
+      warp_reduce_scatter_add<N>(v, lane, p.dB + (b * L + ts + k) * N, p.dC + (b * L + ts + k) * N);
     }
-    const float ds = dyk * g;
-    dDacc = fmaf(ds, us[k], dDacc);
-    float ddt = 0.f, sumlB = 0.f;
-    float v[32];
-#pragma unroll
-    for (int n = 0; n < N; n++) {
-      const float lam = fmaf(ds, sC[k][n], m[n]);
-      const float hp = k > 0 ? sH[k - 1][n][lane] : h0[n];
-      const float dA = ex2(dts[k] * A2[n]);
-      const float t1 = lam * hp * dA;
-      ddt = fmaf(t1, Af[n], fmaf(lam * sB[k][n], us[k], ddt));
-      dAacc[n] = fmaf(t1, dts[k], dAacc[n]);
-      sumlB = fmaf(lam, sB[k][n], sumlB);
-      v[n] = active ? lam * dts[k] * us[k] : 0.f;       // dB partial
-      v[N + n] = active ? ds * sH[k][n][lane] : 0.f;     // dC partial
-      m[n] = dA * lam;
-    }
-#pragma unroll
-    for (int j = 2 * N; j < 32; j++) v[j] = 0.f;
-    const float dx = p.softplus ? ddt * rcp(1.f + ex2(-xs[k] * kLog2e)) : ddt;
-    dbacc += dx;
-    if (active) {
-      static_cast<T*>(p.du)[e] = from_f32<T>(fmaf(ds, Dd, dts[k] * sumlB));
-      static_cast<T*>(p.ddelta)[e] = from_f32<T>(dx);
-    }
-    warp_reduce_scatter_add<N>(v, lane, p.dB + (b * L + ts + k) * N, p.dC + (b * L + ts + k) * N);
+    __syncwarp();
   }
   if (!active) return;
 #pragma unroll
-  for (int n = 0; n < N; n++) atomicAdd(p.dA + d * N + n, dAacc[n]);
+  for (int j = 0; j < NP; j++) {
+    atomicAdd(p.dA + d * N + 2 * j, dAacc[j].x);
+    if (2 * j + 1 < N) atomicAdd(p.dA + d * N + 2 * j + 1, dAacc[j].y);
+  }
   if (p.dD) atomicAdd(p.dD + d, dDacc);
   if (p.dbias) atomicAdd(p.dbias + d, dbacc);
-  if (p.dinit && tl == 0) {
+  if (p.dinit && tl_lo == 0) {
 #pragma unroll
-    for (int n = 0; n < N; n++) p.dinit[(b * Dn + d) * N + n] = m[n];
+    for (int j = 0; j < NP; j++) {
+      p.dinit[(b * Dn + d) * N + 2 * j] = m[j].x;
+      if (2 * j + 1 < N) p.dinit[(b * Dn + d) * N + 2 * j + 1] = m[j].y;
+    }
   }
 }
 
@@ -372,7 +478,8 @@ static cudaError_t launch_bwd_t(const BwdArgs& a, const ScanParams& fwd, cudaStr
   }
   bwd_fwd_ckpt_kernel<N, T><<<(unsigned)(n_dtiles * a.n_chunks * a.batch), kBwdCh, 0, s>>>(a);
   bwd_reverse_kernel<N, T, false><<<(unsigned)(n_dtiles * a.n_chunks * a.batch), kBwdCh, 0, s>>>(a);
-  bwd_grad_kernel<N, T><<<(unsigned)(n_dtiles * tiles * a.batch), kBwdCh, 0, s>>>(a);
+  const int64_t ranges = (tiles + kGradTiles - 1) / kGradTiles;
+  bwd_grad_kernel<N, T><<<(unsigned)(n_dtiles * ranges * a.batch), kBwdCh, 0, s>>>(a);
   return cudaGetLastError();
 }
 
