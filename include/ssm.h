@@ -225,6 +225,30 @@ SSM_API ssm_status_t ssm_scan_bwd(const void* u, const void* delta, const float*
                                   int64_t d_inner, int d_state, ssm_dtype_t io, void* workspace,
                                   size_t workspace_bytes, void* stream);
 
+/*
+ * The chunked tensor-core ("state space duality", Mamba-2) form, for the case of one scalar
+ * A and one step size per head: youngju.dev, section "后续研究：Mamba-2 与混合架构" names
+ * State Space Duality (the recurrence as attention-like matrix products) without equations.
+ * It computes exactly ssm_scan_fwd with A[d][n] = A_head[h] and delta[b][t][d] = dt[b][t][h]
+ * for the head's channels d = h * 64 .. h * 64 + 63, every state n (and delta_bias per head):
+ * per chunk of 64 steps, the products C B^T (masked by the decays), (.) x, x^T B and C H^T
+ * run on the tensor cores (bf16 operands, fp32 accumulation); the states entering chunks are
+ * an fp32 scan across chunks.
+ *   x, z, y [batch][L][d_inner]; dt [batch][L][n_heads]; B, C [batch][L][d_state]: bf16;
+ *   A_head, dt_bias [n_heads], D [d_inner], last_state [batch][d_inner][d_state]: fp32.
+ * Requirements: io == SSM_BF16; d_inner == 64 * n_heads (head dimension 64); d_state in
+ * {16, 32, 64, 128}; D, z, dt_bias, last_state nullable; workspace of
+ * ssm_ssd_fwd_workspace_size bytes (batch * n_heads * ceil(L/64) * (64 * d_state + 1) floats).
+ */
+SSM_API size_t ssm_ssd_fwd_workspace_size(int64_t batch, int64_t L, int64_t d_inner, int n_heads,
+                                          int d_state);
+SSM_API ssm_status_t ssm_ssd_fwd(const void* x, const void* dt, const float* A_head,
+                                 const void* B, const void* C, const float* D, const void* z,
+                                 const float* dt_bias, int softplus_flag, void* y,
+                                 float* last_state, int64_t batch, int64_t L, int64_t d_inner,
+                                 int n_heads, int d_state, ssm_dtype_t io, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
 /* Human-readable name of a status code (static string). */
 SSM_API const char* ssm_status_string(ssm_status_t status);
 

@@ -37,6 +37,7 @@ class Workload:
     delta_sd: float
     decode: bool = False
     state_sd: float = 0.0
+    heads: int = 0    # > 0: chunked-SSD workload (one A and one step size per head of 64 channels)
 
     @property
     def elements(self) -> int:
@@ -53,7 +54,65 @@ WORKLOADS = {
                      1, 1 << 20, 2048, 16, True, 3, 0.5),
     "decode": Workload("decode", "selective_state_update, 1024 sequential steps, bf16 I/O",
                        256, 1024, 5120, 16, True, 4, 0.5, decode=True, state_sd=0.1),
+    "ssd2p7b": Workload("ssd2p7b", "Mamba-2-2.7B-layer-shaped chunked SSD scan (80 heads of 64, "
+                        "d_state 128), bf16 I/O", 8, 2048, 5120, 128, True, 5, 0.5, heads=80),
 }
+
+
+def ssd_A_head(w: Workload) -> np.ndarray:
+    """One decay rate per head: A_h = -(1 + h mod 16)."""
+    return -(1.0 + (np.arange(w.heads) % 16)).astype(np.float32)
+
+
+def ssd_dt_bias(w: Workload) -> np.ndarray:
+    return delta_bias(w.seed, TID_BIAS, DT_MIN, DT_MAX, w.heads)
+
+
+def host_ssd_inputs(w: Workload, b_sel=None, d_sel=None):
+    """SSD workload inputs for batches b_sel and channels d_sel (whole heads or not), as the
+    equivalent per-channel scan operands in float64 for the oracle: delta and delta_bias
+    broadcast from the head, A[d, n] = A_head[h]."""
+    assert w.heads > 0
+    b_sel = np.arange(w.batch) if b_sel is None else np.asarray(b_sel, dtype=np.int64)
+    d_sel = np.arange(w.d_inner) if d_sel is None else np.asarray(d_sel, dtype=np.int64)
+    P = w.d_inner // w.heads
+    h_sel = d_sel // P
+    t = np.arange(w.L, dtype=np.int64)
+    out = {}
+    for name, tid in (("u", TID_U), ("z", TID_Z)):
+        idx = ((b_sel[:, None, None] * w.L + t[None, :, None]) * w.d_inner + d_sel[None, None, :]).ravel()
+        out[name] = _as_f64(normal_at(w.seed, tid, 0.0, 1.0, idx, True), True).reshape(len(b_sel), w.L, len(d_sel))
+    idx = ((b_sel[:, None, None] * w.L + t[None, :, None]) * w.heads + h_sel[None, None, :]).ravel()
+    out["delta"] = _as_f64(normal_at(w.seed, TID_DELTA, 0.0, w.delta_sd, idx, True), True).reshape(
+        len(b_sel), w.L, len(d_sel))
+    for name, tid in (("B", TID_B), ("C", TID_C)):
+        parts = [normal(w.seed, tid, 0.0, 1.0, int(b) * w.L * w.d_state, w.L * w.d_state, True) for b in b_sel]
+        out[name] = _as_f64(np.concatenate(parts), True).reshape(len(b_sel), w.L, w.d_state)
+    out["A"] = np.repeat(ssd_A_head(w)[h_sel][:, None], w.d_state, axis=1).astype(np.float64)
+    out["D"] = D_vector(w)[d_sel].astype(np.float64)
+    out["delta_bias"] = ssd_dt_bias(w)[h_sel].astype(np.float64)
+    return out
+
+
+def device_ssd_inputs(w: Workload, device="cuda"):
+    """Full-size SSD inputs on the GPU: x, z [batch, L, d_inner], dt [batch, L, heads],
+    B, C [batch, L, d_state] (bf16), A_head, dt_bias [heads], D [d_inner] (fp32)."""
+    import torch
+    assert w.heads > 0
+    stream = torch.cuda.current_stream(device).cuda_stream
+    out = {}
+    for name, tid, shape, sd in (("x", TID_U, (w.batch, w.L, w.d_inner), 1.0),
+                                 ("z", TID_Z, (w.batch, w.L, w.d_inner), 1.0),
+                                 ("dt", TID_DELTA, (w.batch, w.L, w.heads), w.delta_sd),
+                                 ("B", TID_B, (w.batch, w.L, w.d_state), 1.0),
+                                 ("C", TID_C, (w.batch, w.L, w.d_state), 1.0)):
+        t = torch.empty(shape, dtype=torch.bfloat16, device=device)
+        dev_fill_normal(w.seed, tid, 0.0, sd, 0, t.numel(), True, t.data_ptr(), stream)
+        out[name] = t
+    out["A_head"] = torch.from_numpy(ssd_A_head(w)).to(device)
+    out["dt_bias"] = torch.from_numpy(ssd_dt_bias(w)).to(device)
+    out["D"] = torch.from_numpy(D_vector(w)).to(device)
+    return out
 
 
 def A_matrix(w: Workload) -> np.ndarray:

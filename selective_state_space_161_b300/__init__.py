@@ -21,7 +21,8 @@ from .build import LIB_PATH, build
 
 __all__ = ["SsmError", "ssm_scan_fwd", "ssm_scan_fwd_from_state", "ssm_scan_fwd_conv",
            "ssm_scan_fwd_noalloc", "ssm_state_update", "ssm_state_update_conv", "ssm_scan_bwd",
-           "ssm_scan_bwd_workspace_size", "selective_scan_backward",
+           "ssm_scan_bwd_workspace_size", "selective_scan_backward", "ssm_ssd_fwd",
+           "ssm_ssd_fwd_workspace_size", "selective_scan_ssd",
            "ssm_scan_fwd_workspace_size",
            "ssm_status_string", "ssm_version", "selective_scan", "selective_state_update",
            "load_library", "build", "SSM_F32", "SSM_BF16", "EXPORTED_SYMBOLS"]
@@ -30,6 +31,7 @@ SSM_F32, SSM_BF16 = 0, 1
 EXPORTED_SYMBOLS = ("ssm_scan_fwd_workspace_size", "ssm_scan_fwd", "ssm_scan_fwd_from_state",
                     "ssm_scan_fwd_conv", "ssm_scan_fwd_noalloc", "ssm_state_update",
                     "ssm_state_update_conv", "ssm_scan_bwd", "ssm_scan_bwd_workspace_size",
+                    "ssm_ssd_fwd", "ssm_ssd_fwd_workspace_size",
                     "ssm_status_string", "ssm_version")
 SSM_NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -71,6 +73,11 @@ def load_library() -> ctypes.CDLL:
         lib.ssm_scan_bwd.argtypes = [vp] * 8 + [c_int] + [vp] * 12 + [i64, i64, i64, c_int, c_int, vp,
                                                                    ctypes.c_size_t, vp]
         lib.ssm_scan_bwd.restype = c_int
+        lib.ssm_ssd_fwd_workspace_size.argtypes = [i64, i64, i64, c_int, c_int]
+        lib.ssm_ssd_fwd_workspace_size.restype = ctypes.c_size_t
+        lib.ssm_ssd_fwd.argtypes = [vp] * 8 + [c_int, vp, vp, i64, i64, i64, c_int, c_int, c_int, vp,
+                                              ctypes.c_size_t, vp]
+        lib.ssm_ssd_fwd.restype = c_int
         lib.ssm_scan_fwd_noalloc.argtypes = [vp] * 8 + [c_int, vp, vp, i64, i64, i64, c_int, c_int,
                                                        vp]
         lib.ssm_scan_fwd_noalloc.restype = c_int
@@ -278,6 +285,49 @@ def selective_scan_backward(u, delta, A, B, C, dy, D=None, z=None, delta_bias=No
                  g["du"], g["ddelta"], g["dA"], g["dB"], g["dC"], g["dD"], g["dz"], g["ddelta_bias"],
                  g["dinitial_state"], ws, stream)
     return {k: v for k, v in g.items() if v is not None}
+
+
+def ssm_ssd_fwd_workspace_size(batch: int, L: int, d_inner: int, n_heads: int, d_state: int) -> int:
+    return int(load_library().ssm_ssd_fwd_workspace_size(batch, L, d_inner, n_heads, d_state))
+
+
+def ssm_ssd_fwd(x, dt, A_head, B, C, D, z, dt_bias, softplus_flag, y, last_state, workspace,
+                stream=None) -> None:
+    """C-ABI ``ssm_ssd_fwd``: the chunked tensor-core form for one A and one step size per head
+    (bf16 I/O, heads of 64 channels; see include/ssm.h)."""
+    batch, L, d_inner = x.shape
+    n_heads = dt.shape[2]
+    d_state = B.shape[2]
+    bf = torch.bfloat16
+    for name, t, shp, ty in (("x", x, (batch, L, d_inner), bf), ("z", z, (batch, L, d_inner), bf),
+                             ("y", y, (batch, L, d_inner), bf), ("dt", dt, (batch, L, n_heads), bf),
+                             ("B", B, (batch, L, d_state), bf), ("C", C, (batch, L, d_state), bf),
+                             ("A_head", A_head, (n_heads,), torch.float32),
+                             ("dt_bias", dt_bias, (n_heads,), torch.float32),
+                             ("D", D, (d_inner,), torch.float32),
+                             ("last_state", last_state, (batch, d_inner, d_state), torch.float32)):
+        _check_dev(name, t, ty, shp)
+    _check_dev("workspace", workspace)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load_library().ssm_ssd_fwd(_ptr(x), _ptr(dt), _ptr(A_head), _ptr(B), _ptr(C), _ptr(D),
+                                    _ptr(z), _ptr(dt_bias), int(bool(softplus_flag)), _ptr(y),
+                                    _ptr(last_state), batch, L, d_inner, n_heads, d_state, SSM_BF16,
+                                    _ptr(workspace), ws_bytes, _stream_handle(stream))
+    if rc != 0:
+        raise SsmError("ssm_ssd_fwd", rc)
+
+
+def selective_scan_ssd(x, dt, A_head, B, C, D=None, z=None, dt_bias=None, softplus=True,
+                       stream=None):
+    """Chunked SSD scan on CUDA bf16 tensors; returns (y, last_state)."""
+    batch, L, d_inner = x.shape
+    d_state = B.shape[2]
+    y = torch.empty_like(x)
+    last = torch.empty((batch, d_inner, d_state), dtype=torch.float32, device=x.device)
+    nbytes = ssm_ssd_fwd_workspace_size(batch, L, d_inner, dt.shape[2], d_state)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=x.device)
+    ssm_ssd_fwd(x, dt, A_head, B, C, D, z, dt_bias, softplus, y, last, ws, stream)
+    return y, last
 
 
 def ssm_state_update_conv(state, conv_state, x, conv_weight, conv_bias, delta, A, B, C, D, z, y,

@@ -338,6 +338,58 @@ ssm_status_t ssm_scan_bwd(const void* u, const void* delta, const float* A, cons
   return ssm::launch_scan_bwd(a, f, io == SSM_BF16, s) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
+size_t ssm_ssd_fwd_workspace_size(int64_t batch, int64_t L, int64_t d_inner, int n_heads,
+                                  int d_state) {
+  if (batch < 0 || L < 0 || n_heads < 1 || d_state < 1) return 0;
+  return ssm::ssd_workspace_floats(batch, L, n_heads, d_state) * sizeof(float);
+}
+
+ssm_status_t ssm_ssd_fwd(const void* x, const void* dt, const float* A, const void* B,
+                         const void* C, const float* D, const void* z, const float* dt_bias,
+                         int softplus_flag, void* y, float* last_state, int64_t batch, int64_t L,
+                         int64_t d_inner, int n_heads, int d_state, ssm_dtype_t io,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  if (io != SSM_BF16) return SSM_ERR_DTYPE;
+  if (batch < 0 || L < 0 || d_inner < 0 || n_heads < 1) return SSM_ERR_SHAPE;
+  if (d_state != 16 && d_state != 32 && d_state != 64 && d_state != 128) return SSM_ERR_SHAPE;
+  if (d_inner != (int64_t)n_heads * ssm::ssd_head_dim()) return SSM_ERR_SHAPE;
+  if (batch == 0) return SSM_OK;
+  if (!A) return SSM_ERR_NULL;
+  if (L > 0 && (!x || !dt || !B || !C || !y)) return SSM_ERR_NULL;
+  const void* ptrs[] = {x, dt, A, B, C, D, z, dt_bias, y, last_state, workspace};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return SSM_ERR_ALIGN;
+  if (current_sm_count() <= 0) return SSM_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (L == 0) {
+    if (last_state &&
+        cudaMemsetAsync(last_state, 0, (size_t)batch * d_inner * d_state * sizeof(float), s) != cudaSuccess)
+      return SSM_ERR_CUDA;
+    return SSM_OK;
+  }
+  const size_t need = ssm::ssd_workspace_floats(batch, L, n_heads, d_state) * sizeof(float);
+  if (workspace == nullptr || workspace_bytes < need) return SSM_ERR_WORKSPACE;
+  ssm::SsdParams p{};
+  p.x = static_cast<const __nv_bfloat16*>(x);
+  p.dt = static_cast<const __nv_bfloat16*>(dt);
+  p.A = A;
+  p.B = static_cast<const __nv_bfloat16*>(B);
+  p.C = static_cast<const __nv_bfloat16*>(C);
+  p.D = D;
+  p.z = static_cast<const __nv_bfloat16*>(z);
+  p.dt_bias = dt_bias;
+  p.softplus = softplus_flag != 0;
+  p.y = static_cast<__nv_bfloat16*>(y);
+  p.last_state = last_state;
+  p.batch = batch; p.L = L; p.d_inner = d_inner; p.heads = n_heads; p.N = d_state;
+  p.nchunks = (int)((L + 63) / 64);
+  const int64_t hs = batch * n_heads * (int64_t)p.nchunks * ssm::ssd_head_dim() * d_state;
+  p.Hs = static_cast<float*>(workspace);
+  p.Sc = p.Hs + hs;
+  if (batch * n_heads * (int64_t)p.nchunks >= ((int64_t)1 << 31)) return SSM_ERR_SHAPE;
+  return ssm::launch_ssd(p, s) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
 const char* ssm_status_string(ssm_status_t status) {
   switch (status) {
     case SSM_OK: return "ok";

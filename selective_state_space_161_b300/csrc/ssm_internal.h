@@ -1,6 +1,7 @@
 // Internal launch interface between the C ABI layer (ssm_api.cu) and the kernels.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -95,6 +96,29 @@ struct BwdArgs {
   float* ckpt_m;       // [batch][tiles][d_inner][d_state]: carry entering each tile's last step
 };
 
+
+// The chunked tensor-core form for one scalar A and one step size per head (ssm_ssd.cu).
+struct SsdParams {
+  const __nv_bfloat16* x;   // [batch][L][d_inner]
+  const __nv_bfloat16* dt;  // [batch][L][heads] (raw step size)
+  const float* A;           // [heads]
+  const __nv_bfloat16* B;   // [batch][L][N]
+  const __nv_bfloat16* C;
+  const float* D;           // [d_inner], may be null
+  const __nv_bfloat16* z;   // may be null
+  const float* dt_bias;     // [heads], may be null
+  int softplus;
+  __nv_bfloat16* y;
+  float* last_state;        // [batch][d_inner][N], may be null
+  int64_t batch, L, d_inner;
+  int heads, N;
+  int nchunks;
+  float* Hs;  // [batch][heads][nchunks][P][N]: chunk end states, then the states entering chunks
+  float* Sc;  // [batch][heads][nchunks]: log2 decay over each chunk
+};
+size_t ssd_workspace_floats(int64_t batch, int64_t L, int heads, int N);
+int ssd_head_dim();
+cudaError_t launch_ssd(const SsdParams& p, cudaStream_t s);
 
 // Channels handled by one CTA of the scan kernels.
 int scan_channels_per_cta();

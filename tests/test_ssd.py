@@ -1,0 +1,52 @@
+"""ssm_ssd_fwd (chunked tensor-core form for one A and one step size per head) against the
+oracle's scan run on the equivalent per-channel operands."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import selective_state_space_161_b300 as ssm
+from inputgen import workloads as W
+from tests.helpers import BF16_TOL, rel_err, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(w, use_D=True, use_z=True, use_bias=True, d_sel=None):
+    dev = W.device_ssd_inputs(w)
+    y, last = ssm.selective_scan_ssd(dev["x"], dev["dt"], dev["A_head"], dev["B"], dev["C"],
+                                     D=dev["D"] if use_D else None, z=dev["z"] if use_z else None,
+                                     dt_bias=dev["dt_bias"] if use_bias else None)
+    torch.cuda.synchronize()
+    x = W.host_ssd_inputs(w, d_sel=d_sel)
+    y_ref, last_ref = oracle.scan_fwd(x["u"], x["delta"], x["A"], x["B"], x["C"],
+                                      D=x["D"] if use_D else None, z=x["z"] if use_z else None,
+                                      delta_bias=x["delta_bias"] if use_bias else None)
+    if d_sel is not None:
+        ds = torch.from_numpy(np.asarray(d_sel)).cuda()
+        y, last = y.index_select(2, ds), last.index_select(1, ds)
+    ey, el = rel_err(to_f64(y), y_ref), rel_err(to_f64(last), last_ref)
+    assert ey <= BF16_TOL and el <= BF16_TOL, f"y err {ey:.3g}, last_state err {el:.3g}"
+
+
+@pytest.mark.parametrize("N", [16, 32, 64, 128])
+def test_ssd_small_ragged(N):
+    # 200 steps: three full chunks of 64 and a ragged one
+    _run(W.Workload("ssd", "ssd case", 2, 200, 128, N, True, 40 + N, 0.5, heads=2))
+
+
+@pytest.mark.parametrize("flags", [dict(use_D=False), dict(use_z=False), dict(use_bias=False)])
+def test_ssd_optional_operands(flags):
+    _run(W.Workload("ssd", "ssd case", 1, 130, 192, 64, True, 7, 0.5, heads=3), **flags)
+
+
+def test_ssd_single_step_and_one_chunk():
+    _run(W.Workload("ssd", "ssd case", 3, 1, 64, 16, True, 8, 0.5, heads=1))
+    _run(W.Workload("ssd", "ssd case", 1, 64, 64, 128, True, 9, 0.5, heads=1))
+
+
+def test_ssd_full_size_sampled():
+    """Mamba-2-2.7B-shaped layer on the GPU; the oracle follows sampled channels of three heads."""
+    w = W.WORKLOADS["ssd2p7b"]
+    d_sel = np.concatenate([np.arange(0, 4), np.arange(64 * 37 + 30, 64 * 37 + 34), np.arange(5116, 5120)])
+    _run(w, d_sel=d_sel)
