@@ -33,7 +33,11 @@ from inputgen import workloads as W  # noqa: E402
 
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
-KERNEL_SOURCES = ("ssm_scan.cu", "ssm_decode.cu", "ssm_device.cuh")
+# The kernel sources each workload kind runs; DRAM counters taken under another version of them
+# are stale.
+KERNEL_SOURCES = {"scan": ("ssm_scan.cu", "ssm_device.cuh"),
+                  "decode": ("ssm_decode.cu", "ssm_device.cuh"),
+                  "ssd": ("ssm_ssd.cu", "ssm_device.cuh")}
 FALLBACK_HBM_GBS = 6400.0
 SM_MAX_MHZ_NOMINAL = 2032.0
 # Per-SM issue rates of the pipes the scan uses (operations per clock), measured on B300
@@ -79,6 +83,30 @@ def algorithmic_bytes(w: W.Workload) -> float:
     return float(acts + bc + params + last)
 
 
+def ssd_algorithmic_bytes(w: W.Workload) -> float:
+    """Chunked SSD: read x, z (bf16, per channel), dt (bf16, per head), B, C (bf16, shared by
+    the heads); write y (bf16) and the last state (fp32); A_head, dt_bias, D once."""
+    acts = w.batch * w.L * w.d_inner * 3 * 2
+    dt = w.batch * w.L * w.heads * 2
+    bc = w.batch * w.L * 2 * w.d_state * 2
+    last = w.batch * w.d_inner * w.d_state * 4
+    return float(acts + dt + bc + last + (2 * w.heads + w.d_inner) * 4)
+
+
+SSD_Q = 64  # chunk length of the tensor-core form
+
+
+def ssd_flops(w: W.Workload) -> float:
+    """Tensor-core FLOPs of the chunked form, each product counted once (Q = 64, P = 64):
+    per (batch, head, chunk) the local state X^T (w B) (2 Q P N), the intra-chunk scores
+    C B^T (2 Q^2 N), the carried-state readout C H^T (2 Q N P) and the masked mix M X
+    (2 Q^2 P)."""
+    P, N, Q = w.d_inner // w.heads, w.d_state, SSD_Q
+    chunks = -(-w.L // Q)
+    per = 2 * Q * P * N + 2 * Q * Q * N + 2 * Q * N * P + 2 * Q * Q * P
+    return float(w.batch * w.heads * chunks * per)
+
+
 def bwd_algorithmic_bytes(w: W.Workload) -> float:
     """Backward: read u, delta, z, dy, B, C (io dtype), write du, ddelta, dz (io dtype) and
     dB, dC (fp32); A, D, bias and their gradients once."""
@@ -113,25 +141,29 @@ def alu_clocks_per_element(N: int) -> float:
     return max(fp32 / FP32_PER_CLK, ex2 / EX2_PER_CLK, slow / MUFU_SLOW_PER_CLK)
 
 
-def kernel_source_hash() -> str:
-    """Hash of the kernel sources; DRAM counters recorded for another hash are stale."""
+def workload_kind(w: W.Workload) -> str:
+    return "ssd" if w.heads else "decode" if w.decode else "scan"
+
+
+def kernel_source_hash(kind: str) -> str:
+    """Hash of the kernel sources of one workload kind."""
     import hashlib
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in KERNEL_SOURCES[kind]:
         with open(os.path.join(ROOT, "selective_state_space_161_b300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def measured_traffic(workload_key: str):
+def measured_traffic(w: W.Workload):
     """DRAM bytes (read + write) per step from the committed ncu capture of this workload,
     or None if there is none or the kernels changed since it was taken."""
     try:
         with open(TRAFFIC_FILE) as f:
-            rec = json.load(f).get(workload_key)
+            rec = json.load(f).get(w.key)
     except (OSError, ValueError):
         return None
-    if not rec or rec.get("kernel_hash") != kernel_source_hash():
+    if not rec or rec.get("kernel_hash") != kernel_source_hash(workload_kind(w)):
         return None
     return float(rec["dram_bytes_per_step"])
 
@@ -245,6 +277,8 @@ class ClockSampler:
 class ScanStep:
     """One step = one ssm_scan_fwd call over the whole workload."""
 
+    input_names = ("u", "delta", "z", "B", "C", "A", "D", "delta_bias")
+
     def __init__(self, w, dev, ssm, torch):
         self.w, self.dev, self.ssm, self.torch = w, dev, ssm, torch
         self.y = torch.empty_like(dev["u"])
@@ -254,10 +288,31 @@ class ScanStep:
         self.ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda") if nbytes else None
         self.launches = 2 if nbytes else 1  # summary pass + main pass when time is chunked
 
-    def __call__(self, stream=None):
-        d = self.dev
+    def call(self, d, stream=None):
         self.ssm.ssm_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"],
                               d["delta_bias"], True, self.y, self.last, self.ws, stream)
+
+    def __call__(self, stream=None):
+        self.call(self.dev, stream)
+
+
+class SsdStep(ScanStep):
+    """One step = one ssm_ssd_fwd call: the chunked tensor-core form over the whole workload
+    (one A and one step size per head of 64 channels)."""
+
+    input_names = ("x", "z", "dt", "B", "C", "A_head", "dt_bias", "D")
+
+    def __init__(self, w, dev, ssm, torch):
+        self.w, self.dev, self.ssm = w, dev, ssm
+        self.y = torch.empty_like(dev["x"])
+        self.last = torch.empty((w.batch, w.d_inner, w.d_state), dtype=torch.float32, device="cuda")
+        nbytes = ssm.ssm_ssd_fwd_workspace_size(w.batch, w.L, w.d_inner, w.heads, w.d_state)
+        self.ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        self.launches = 3  # chunk states, state pass over chunks, output
+
+    def call(self, d, stream=None):
+        self.ssm.ssm_ssd_fwd(d["x"], d["dt"], d["A_head"], d["B"], d["C"], d["D"], d["z"],
+                             d["dt_bias"], True, self.y, self.last, self.ws, stream)
 
 
 class ConvScanStep(ScanStep):
@@ -326,29 +381,24 @@ class DecodeStep:
                                       stream)
 
 
-def run_e2e(w, dev, ssm, torch, steps):
+def run_e2e(w, step, torch, steps):
     """Same metric through the public call with pinned host buffers: every step copies the
-    inputs host->device, runs the scan, and copies y and last_state back."""
+    inputs host->device, runs the step's entry point, and copies y and last_state back."""
     if w.decode:
         return None
-    names = ["u", "delta", "z", "B", "C", "A", "D", "delta_bias"]
-    host = {k: dev[k].cpu().pin_memory() for k in names}
-    dbuf = {k: torch.empty_like(dev[k]) for k in names}
-    y = torch.empty_like(dev["u"])
-    last = torch.empty((w.batch, w.d_inner, w.d_state), dtype=torch.float32, device="cuda")
+    names = step.input_names
+    host = {k: step.dev[k].cpu().pin_memory() for k in names}
+    dbuf = {k: torch.empty_like(step.dev[k]) for k in names}
+    y, last = step.y, step.last
     y_h = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
     last_h = torch.empty(last.shape, dtype=last.dtype, pin_memory=True)
-    io = ssm.SSM_BF16 if w.bf16 else ssm.SSM_F32
-    nbytes = ssm.ssm_scan_fwd_workspace_size(w.batch, w.L, w.d_inner, w.d_state, io)
-    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda") if nbytes else None
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = y.numel() * y.element_size() + last.numel() * 4
 
     def one():
         for k in names:
             dbuf[k].copy_(host[k], non_blocking=True)
-        ssm.ssm_scan_fwd(dbuf["u"], dbuf["delta"], dbuf["A"], dbuf["B"], dbuf["C"], dbuf["D"],
-                         dbuf["z"], dbuf["delta_bias"], True, y, last, ws)
+        step.call(dbuf)
         y_h.copy_(y, non_blocking=True)
         last_h.copy_(last, non_blocking=True)
 
@@ -385,13 +435,19 @@ def oracle_sample_rate(w, budget_s: float, threads: int | None = None):
             f"{steps} decode steps x {w.batch} batch x 64 of {w.d_inner} channels"
     T = min(w.L, 1 << 16)
     d_try = max(1, min(w.d_inner, threads))
-    x = W.host_scan_inputs(w, d_sel=np.arange(d_try), t_count=T)
+    if w.heads:  # the chunked form's oracle is the per-channel scan with head-broadcast operands
+        def inputs(d_cnt):
+            return W.host_ssd_inputs(w, d_sel=np.arange(d_cnt))
+    else:
+        def inputs(d_cnt):
+            return W.host_scan_inputs(w, d_sel=np.arange(d_cnt), t_count=T)
+    x = inputs(d_try)
     t0 = time.perf_counter()
     oracle.scan_fwd(x["u"], x["delta"], x["A"], x["B"], x["C"], D=x["D"], z=x["z"],
                     delta_bias=x["delta_bias"], nthreads=threads)
     rate = w.batch * T * d_try / (time.perf_counter() - t0)
     d_cnt = int(min(w.d_inner, max(d_try, rate * budget_s / (w.batch * T))))
-    x = W.host_scan_inputs(w, d_sel=np.arange(d_cnt), t_count=T)
+    x = inputs(d_cnt)
     t0 = time.perf_counter()
     oracle.scan_fwd(x["u"], x["delta"], x["A"], x["B"], x["C"], D=x["D"], z=x["z"],
                     delta_bias=x["delta_bias"], nthreads=threads)
@@ -424,6 +480,13 @@ def roofline(w, ms_per_step, hbm_gbs, sm_mhz, sms, peak_src, traffic=None, which
     if which == "conv":  # conv1d (4 FMA) + SiLU (3 FP32, 1 ex2, 1 rcp) more per element
         clocks = max(clocks, (4 * w.d_state + 13) / FP32_PER_CLK, (w.d_state + 3) / EX2_PER_CLK,
                      3 / MUFU_SLOW_PER_CLK)
+    if which == "ssd":
+        nbytes = ssd_algorithmic_bytes(w)
+        achieved = nbytes / (ms_per_step * 1e-3) / 1e9
+        return {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                "frac": achieved / hbm_gbs, "traffic": traffic, "algorithmic_bytes": nbytes,
+                "peak_source": f"{peak_src} copy bandwidth",
+                "tensor_tflops": ssd_flops(w) / (ms_per_step * 1e-3) / 1e12}
     t_hbm = nbytes / (hbm_gbs * 1e9)
     t_alu = w.elements * clocks / (sms * sm_mhz * 1e6)
     if t_hbm >= t_alu:
@@ -451,8 +514,14 @@ def main_ours(args, rank, world, local_rank):
     if w.decode and args.decode_steps:
         import dataclasses
         w = dataclasses.replace(w, L=args.decode_steps)
-    dev = W.device_inputs(w)
-    if w.decode:
+    if w.heads:
+        args.which = "ssd"
+        dev = W.device_ssd_inputs(w)
+    else:
+        dev = W.device_inputs(w)
+    if w.heads:
+        step = SsdStep(w, dev, ssm, torch)
+    elif w.decode:
         step = DecodeStep(w, dev, ssm, torch)
     elif args.which == "backward":
         step = BackwardStep(w, dev, ssm, torch)
@@ -485,8 +554,8 @@ def main_ours(args, rank, world, local_rank):
     ms = max_over_ranks(float(np.mean([e0.elapsed_time(e1) for e0, e1 in events])), world, "cuda")
 
     e2e = None
-    if not args.no_e2e and not w.decode and args.which == "forward":
-        e2e = run_e2e(w, dev, ssm, torch, args.e2e_steps)
+    if not args.no_e2e and not w.decode and args.which in ("forward", "ssd"):
+        e2e = run_e2e(w, step, torch, args.e2e_steps)
         if e2e is not None and world > 1:
             e2e["ms_per_step"] = max_over_ranks(e2e["ms_per_step"], world, "cuda")
             e2e["value"] = whole_job_rate(w.elements, world, e2e["ms_per_step"])
@@ -497,9 +566,7 @@ def main_ours(args, rank, world, local_rank):
     clk = clocks.summary()
     sm_mhz_peak = float(clk["sm_max_mhz"] or SM_MAX_MHZ_NOMINAL)
     out = {
-        "metric": ("decode elements/s (B*d_inner*steps)" if w.decode else
-                   "scan backward elements/s (B*L*d_inner)" if args.which == "backward" else
-                   "scan elements/s (B*L*d_inner)"),
+        "metric": metric_name(w, args.which),
         "value": whole_job_rate(w.elements, world, ms),
         "unit": "elements/s",
         "n_gpus": world,
@@ -509,16 +576,18 @@ def main_ours(args, rank, world, local_rank):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16 I/O, f32 state and arithmetic" if w.bf16 else "f32",
+        "dtype": ("bf16 tensor-core products (hi+lo split operands), f32 accumulation"
+                  if w.heads else "bf16 I/O, f32 state and arithmetic" if w.bf16 else "f32"),
         "data": "synthetic (seeded; recipe in inputgen/workloads.py)",
         "config": {"workload": w.desc, "batch": w.batch,
                    ("steps" if w.decode else "seq_len"): w.L, "d_inner": w.d_inner,
                    "d_state": w.d_state, "io_dtype": "bf16" if w.bf16 else "f32",
+                   **({"heads": w.heads, "chunk": SSD_Q} if w.heads else {}),
                    "pass": args.which,
                    "parallelism": f"replica per GPU x{world}" if world > 1 else "single GPU",
                    "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write)"},
         "roofline": roofline(w, ms, hbm_gbs, sm_mhz_peak, sms, peak_src,
-                             measured_traffic(w.key) if args.which == "forward" else None,
+                             measured_traffic(w) if args.which in ("forward", "ssd") else None,
                              args.which),
         "gpu_launches": step.launches * args.steps,
         "clocks": clk,
@@ -530,6 +599,16 @@ def main_ours(args, rank, world, local_rank):
         out["cpu_baseline"] = {"value": rate, "unit": "elements/s", "cores": cores,
                                "kind": "oracle", "sample": sample}
     print(json.dumps(out), flush=True)
+
+
+def metric_name(w, which):
+    if w.decode:
+        return "decode elements/s (B*d_inner*steps)"
+    if which == "backward":
+        return "scan backward elements/s (B*L*d_inner)"
+    if w.heads:
+        return "chunked SSD scan elements/s (B*L*d_inner)"
+    return "scan elements/s (B*L*d_inner)"
 
 
 def main_reference(args, rank, world):
@@ -547,8 +626,7 @@ def main_reference(args, rank, world):
     value = float(np.median(rates))
     out = {
         "impl": "reference",
-        "metric": "scan elements/s (B*L*d_inner)" if not w.decode
-        else "decode elements/s (B*d_inner*steps)",
+        "metric": metric_name(w, "ssd" if w.heads else "forward"),
         "value": value, "unit": "elements/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": w.elements / value * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64",

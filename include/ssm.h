@@ -232,13 +232,13 @@ SSM_API ssm_status_t ssm_scan_bwd(const void* u, const void* delta, const float*
  * It computes exactly ssm_scan_fwd with A[d][n] = A_head[h] and delta[b][t][d] = dt[b][t][h]
  * for the head's channels d = h * 64 .. h * 64 + 63, every state n (and delta_bias per head):
  * per chunk of 64 steps, the products C B^T (masked by the decays), (.) x, x^T B and C H^T
- * run on the tensor cores (bf16 operands, fp32 accumulation); the states entering chunks are
- * an fp32 scan across chunks.
+ * run on the tensor cores (bf16 operands, computed operands split into bf16 hi + lo parts,
+ * fp32 accumulation); the fp32 state is carried from chunk to chunk on chip.
  *   x, z, y [batch][L][d_inner]; dt [batch][L][n_heads]; B, C [batch][L][d_state]: bf16;
  *   A_head, dt_bias [n_heads], D [d_inner], last_state [batch][d_inner][d_state]: fp32.
  * Requirements: io == SSM_BF16; d_inner == 64 * n_heads (head dimension 64); d_state in
- * {16, 32, 64, 128}; D, z, dt_bias, last_state nullable; workspace of
- * ssm_ssd_fwd_workspace_size bytes (batch * n_heads * ceil(L/64) * (64 * d_state + 1) floats).
+ * {16, 32, 64, 128}; D, z, dt_bias, last_state nullable.  ssm_ssd_fwd_workspace_size
+ * returns 0 (the form needs no workspace); workspace may be null and is not touched.
  */
 SSM_API size_t ssm_ssd_fwd_workspace_size(int64_t batch, int64_t L, int64_t d_inner, int n_heads,
                                           int d_state);

@@ -112,11 +112,7 @@ struct SsdParams {
   float* last_state;        // [batch][d_inner][N], may be null
   int64_t batch, L, d_inner;
   int heads, N;
-  int nchunks;
-  float* Hs;  // [batch][heads][nchunks][P][N]: chunk end states, then the states entering chunks
-  float* Sc;  // [batch][heads][nchunks]: log2 decay over each chunk
 };
-size_t ssd_workspace_floats(int64_t batch, int64_t L, int heads, int N);
 int ssd_head_dim();
 cudaError_t launch_ssd(const SsdParams& p, cudaStream_t s);
 

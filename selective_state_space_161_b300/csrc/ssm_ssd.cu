@@ -12,14 +12,19 @@
 // followed by y = (y + D x) silu(z), exactly the recurrence h_t = exp(delta a) h + delta B x,
 // y = C h + D x of the scan (the oracle checks it through that equivalence).
 //
-// Three launches: (A) each chunk's local end state X^T (w * B) on the tensor cores;
-// (B) the states entering every chunk, an elementwise scan over chunks; (C) the outputs:
-// C B^T masked with the decays, times X, plus C H_in^T scaled by exp(S_i), on the tensor
-// cores.  Tensor-core tiles: mma.sync m16n8k16, bf16 operands, fp32 accumulation, fed from
-// padded shared-memory tiles by ldmatrix.  The inputs x, B, C are bf16 already; the computed
-// operands (the masked decay matrix, w * B, the carried-in state) go in as a bf16 hi part
-// plus a bf16 lo part (the rounding remainder), two products each, so their rounding error
-// is ~2^-16 rather than bf16's 2^-8.
+// One launch, one CTA of 4 warps per (batch, head), walking the head's chunks in order with
+// the P x N state in registers: it never leaves the SM until the last state is written, so
+// HBM sees only x, z, dt, B, C in and y out.  Per chunk:
+//   G = C B^T (only the 16 x 8 tiles on or below the diagonal), masked and decayed into
+//   M = G delta_j 2^(S_i - S_j), staged in shared memory;  Y = 2^(S_i) C H_in^T + M X;
+//   y = (Y + D x) silu(z);  H = 2^(S_last) H + X^T (w B), w_j = delta_j 2^(S_last - S_j).
+// Warp w owns channels p in [16 w, 16 w + 16) of H, Y and y.  The accumulator layout of the
+// mma.sync tile holding H (rows p, columns n) is exactly the B-operand layout that C H^T needs
+// (k = n, column = p), so the state feeds the next chunk's readout straight from registers.
+// Tensor-core tiles: mma.sync m16n8k16, bf16 operands, fp32 accumulation, fed from padded
+// shared-memory tiles by ldmatrix.  The inputs x, B, C are bf16 already; the computed operands
+// (M, w B, the carried state) go in as a bf16 hi part plus a bf16 lo part (the rounding
+// remainder), two products each, so their rounding error is ~2^-16 rather than bf16's 2^-8.
 
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
@@ -44,8 +49,9 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void* p) {
 }
 // D += A (16x16, row) * B (16x8, col), bf16 in, fp32 accumulate.
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+  // not volatile: a pure function of its registers, so the compiler may interleave
+  // independent products (back-to-back dependent ones would wait on the pipe's latency)
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
@@ -55,292 +61,332 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-// Per chunk: step sizes, and the running decay S_i in log2 units (sum of delta a log2 e),
-// both into shared memory; steps past the sequence end get delta = 0.
-__device__ __forceinline__ void chunk_decays(const SsdParams& p, int64_t b, int h, int64_t t0,
+// Raw step sizes of steps t0 + 2 lane and t0 + 2 lane + 1 (warp 0 holds a whole chunk; steps
+// at or past the sequence end read as 0 and are masked below).
+__device__ __forceinline__ float2 load_dt_pair(const SsdParams& p, int64_t b, int h, int64_t t0, int lane) {
+  float2 v = make_float2(0.f, 0.f);
+  const int64_t t = t0 + 2 * lane;
+  if (t < p.L) v.x = __bfloat162float(p.dt[(b * p.L + t) * p.heads + h]);
+  if (t + 1 < p.L) v.y = __bfloat162float(p.dt[(b * p.L + t + 1) * p.heads + h]);
+  return v;
+}
+
+// Warp 0: step sizes delta_t and the running decay S_i in log2 units (inclusive prefix sum of
+// delta a log2 e) of one chunk, from the raw pair loaded above, into shared memory.
+__device__ __forceinline__ void chunk_decays(const SsdParams& p, int h, int64_t t0, float2 raw, int lane,
                                              float* sDt, float* sS) {
-  const int tid = threadIdx.x;
-  if (tid < kQ) {
-    const int64_t t = t0 + tid;
-    float dt = 0.f;
-    if (t < p.L) {
-      const float x = __bfloat162float(p.dt[(b * p.L + t) * p.heads + h]) + (p.dt_bias ? p.dt_bias[h] : 0.f);
-      dt = p.softplus ? softplus(x) : x;
-    }
-    sDt[tid] = dt;
-    sS[tid] = dt * p.A[h] * kLog2e;
-  }
-  __syncthreads();
-  if (tid < 32) {  // inclusive prefix sum of 64 values: 2 per lane, then a warp scan
-    const float a = sS[2 * tid], c = sS[2 * tid + 1];
-    float run = a + c;
+  const float bias = p.dt_bias ? p.dt_bias[h] : 0.f;
+  const int64_t t = t0 + 2 * lane;
+  float d0 = raw.x + bias, d1 = raw.y + bias;
+  if (p.softplus) { d0 = softplus(d0); d1 = softplus(d1); }
+  if (t >= p.L) d0 = 0.f;
+  if (t + 1 >= p.L) d1 = 0.f;
+  const float a = p.A[h] * kLog2e;
+  const float e0 = d0 * a, e1 = d1 * a;
+  float run = e0 + e1;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float v = __shfl_up_sync(0xFFFFFFFFu, run, o);
-      if (tid >= o) run += v;
-    }
-    const float before = run - (a + c);
-    sS[2 * tid] = before + a;
-    sS[2 * tid + 1] = run;
+  for (int o = 1; o < 32; o <<= 1) {
+    const float v = __shfl_up_sync(0xFFFFFFFFu, run, o);
+    if (lane >= o) run += v;
   }
-  __syncthreads();
+  sDt[2 * lane] = d0;
+  sDt[2 * lane + 1] = d1;
+  sS[2 * lane] = run - e1;
+  sS[2 * lane + 1] = run;
+}
+
+__device__ __forceinline__ void ldsm_x2(uint32_t (&r)[2], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];\n"
+               : "=r"(r[0]), "=r"(r[1]) : "r"(smem_u32(p)));
+}
+// 16-byte global -> shared copy; src_bytes 0 fills the destination with zeros.
+__device__ __forceinline__ void ssd_cp_async16(void* dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n"
+               :: "r"(smem_u32(dst)), "l"(src), "r"(src_bytes));
+}
+__device__ __forceinline__ void ssd_cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int kPending>
+__device__ __forceinline__ void ssd_cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" :: "n"(kPending) : "memory");
+}
+// bf16 hi part of a pair, and the bf16 of what it leaves over.
+__device__ __forceinline__ void split_pair(float v0, float v1, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(v0, v1);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = pack_bf16(v0 - __bfloat162float(h.x), v1 - __bfloat162float(h.y));
 }
 
 // Rows [0, 64) x cols [0, W) of a bf16 matrix with row stride ld (elements) into shared memory
-// (row stride W + kRowPad); rows at or past `rows` are zero.
+// (row stride W + kRowPad) by 16-byte asynchronous copies; rows at or past `rows` are zero.
 template <int W>
-__device__ __forceinline__ void load_tile(__nv_bfloat16* s, const __nv_bfloat16* g, int64_t ld, int rows) {
-  constexpr int kPerRow = W / 8;  // 16-byte pieces per row
+__device__ __forceinline__ void load_tile_async(__nv_bfloat16* s, const __nv_bfloat16* g, int64_t ld,
+                                                int rows) {
+  constexpr int kPerRow = W / 8;
   for (int i = threadIdx.x; i < kQ * kPerRow; i += kSsdThreads) {
     const int r = i / kPerRow, c = (i % kPerRow) * 8;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < rows) v = *reinterpret_cast<const uint4*>(g + r * ld + c);
-    *reinterpret_cast<uint4*>(s + r * (W + kRowPad) + c) = v;
+    const bool in = r < rows;
+    ssd_cp_async16(s + r * (W + kRowPad) + c, in ? g + r * ld + c : g, in ? 16 : 0);
   }
 }
 
-// (A) local end state of a chunk: H_loc[p][n] = sum_j X[j][p] w_j B[j][n], w_j = delta_j 2^(S_last - S_j).
 template <int N>
-__global__ void __launch_bounds__(kSsdThreads) ssd_chunk_state_kernel(const SsdParams p) {
-  const int c = blockIdx.x % p.nchunks;
-  const int h = (blockIdx.x / p.nchunks) % p.heads;
-  const int64_t b = blockIdx.x / ((int64_t)p.nchunks * p.heads);
-  const int64_t t0 = (int64_t)c * kQ;
-  const int rows = (int)min((int64_t)kQ, p.L - t0);
-  __shared__ float sDt[kQ], sS[kQ];
-  __shared__ __align__(16) __nv_bfloat16 sX[kQ][kP + kRowPad];
-  __shared__ __align__(16) __nv_bfloat16 sB[kQ][N + kRowPad], sBlo[kQ][N + kRowPad];
-  chunk_decays(p, b, h, t0, sDt, sS);
-  load_tile<kP>(&sX[0][0], p.x + (b * p.L + t0) * p.d_inner + h * kP, p.d_inner, rows);
-  const float s_last = sS[kQ - 1];
-  for (int i = threadIdx.x; i < kQ * N; i += kSsdThreads) {  // B scaled by w_j, as bf16 hi + lo
-    const int r = i / N, n = i % N;
-    float v = 0.f;
-    if (r < rows) v = __bfloat162float(p.B[(b * p.L + t0 + r) * N + n]) * sDt[r] * ex2(s_last - sS[r]);
-    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-    sB[r][n] = hi;
-    sBlo[r][n] = __float2bfloat16_rn(v - __bfloat162float(hi));
-  }
-  __syncthreads();
+struct SsdSmem {
+  float dt[kQ], S[kQ];                          // step sizes; running log2 decay
+  __nv_bfloat16 X[kQ][kP + kRowPad];            // x tile [step][channel]
+  __nv_bfloat16 Z[kQ][kP + kRowPad];            // z tile [step][channel]
+  __nv_bfloat16 B[kQ][N + kRowPad];             // B tile, then (w B) hi
+  __nv_bfloat16 C[kQ][N + kRowPad];             // C tile, then (w B) lo
+  __nv_bfloat16 M[kQ][kQ + kRowPad], Mlo[kQ][kQ + kRowPad];  // masked decayed C B^T, hi / lo
+};
 
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int g = lane / 4, tq = lane % 4;
-  float acc[N / 8][4];
-#pragma unroll
-  for (int nt = 0; nt < N / 8; nt++) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-#pragma unroll
-  for (int kk = 0; kk < kQ / 16; kk++) {
-    // A = X^T (rows p, cols j): transposed 8x8 blocks of sX[j][p]
-    uint32_t a[4];
-    ldsm_x4_t(a, &sX[kk * 16 + (lane % 8) + 8 * (lane / 16)][16 * warp + 8 * ((lane / 8) % 2)]);
-#pragma unroll
-    for (int nt = 0; nt < N / 8; nt += 2) {
-      // B = sB[j][n] (j = k, n contiguous): transposed loads give the K-major fragments
-      uint32_t bb[4], bl[4];
-      ldsm_x4_t(bb, &sB[kk * 16 + (lane % 8) + 8 * ((lane / 8) % 2)][8 * nt + 8 * (lane / 16)]);
-      ldsm_x4_t(bl, &sBlo[kk * 16 + (lane % 8) + 8 * ((lane / 8) % 2)][8 * nt + 8 * (lane / 16)]);
-      mma16816(acc[nt], a, bb[0], bb[1]);
-      mma16816(acc[nt + 1], a, bb[2], bb[3]);
-      mma16816(acc[nt], a, bl[0], bl[1]);
-      mma16816(acc[nt + 1], a, bl[2], bl[3]);
-    }
-  }
-  float* Ho = p.Hs + (((b * p.heads + h) * p.nchunks + c) * kP) * N;
-#pragma unroll
-  for (int nt = 0; nt < N / 8; nt++) {
-    const int row = 16 * warp + g, col = 8 * nt + 2 * tq;
-    *reinterpret_cast<float2*>(Ho + row * N + col) = make_float2(acc[nt][0], acc[nt][1]);
-    *reinterpret_cast<float2*>(Ho + (row + 8) * N + col) = make_float2(acc[nt][2], acc[nt][3]);
-  }
-  if (threadIdx.x == 0) p.Sc[(b * p.heads + h) * p.nchunks + c] = s_last;
+// The lower-triangular 16 x 8 tiles (r, jt) of G (jt <= 2 r + 1: 20 tiles), five per warp,
+// grouped so that a warp's tiles share as few row blocks r as possible.
+__device__ __forceinline__ void g_tile(int warp, int s, int& r, int& jt) {
+  // warp 0: r3 j0-4 | warp 1: r3 j5-7, r0 j0-1 | warp 2: r2 j0-4 | warp 3: r2 j5, r1 j0-3
+  // (one hex digit per tile, tile 0 lowest; s is a compile-time index, warp is uniform)
+  const uint32_t rc = warp == 0 ? 0x33333u : warp == 1 ? 0x00333u : warp == 2 ? 0x22222u : 0x11112u;
+  const uint32_t jc = warp == 0 ? 0x43210u : warp == 1 ? 0x10765u : warp == 2 ? 0x43210u : 0x32105u;
+  r = (int)((rc >> (4 * s)) & 0xFu);
+  jt = (int)((jc >> (4 * s)) & 0xFu);
 }
 
-// (B) states entering each chunk: H_in(0) = 0, H_in(c+1) = 2^(S_last(c)) H_in(c) + H_loc(c),
-// written over H_loc; the state after the last chunk is last_state.
-__global__ void __launch_bounds__(256) ssd_state_scan_kernel(const SsdParams p) {
-  const int64_t per_head = (int64_t)kP * p.N;
-  const int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x;  // over batch * heads * P * N
-  if (i >= p.batch * p.heads * per_head) return;
-  const int64_t bh = i / per_head, e = i % per_head;
-  float H = 0.f;
-  for (int c = 0; c < p.nchunks; c++) {
-    float* slot = p.Hs + (bh * p.nchunks + c) * per_head + e;
-    const float loc = *slot;
-    *slot = H;
-    H = fmaf(ex2(p.Sc[bh * p.nchunks + c]), H, loc);
-  }
-  if (p.last_state) {
-    const int64_t b = bh / p.heads, h = bh % p.heads, pp = e / p.N, n = e % p.N;
-    p.last_state[(b * p.d_inner + h * kP + pp) * p.N + n] = H;
-  }
-}
-
-// (C) outputs of a chunk.
 template <int N>
-__global__ void __launch_bounds__(kSsdThreads) ssd_output_kernel(const SsdParams p) {
-  const int c = blockIdx.x % p.nchunks;
-  const int h = (blockIdx.x / p.nchunks) % p.heads;
-  const int64_t b = blockIdx.x / ((int64_t)p.nchunks * p.heads);
-  const int64_t t0 = (int64_t)c * kQ;
-  const int rows = (int)min((int64_t)kQ, p.L - t0);
-  // shared memory (dynamic: 61 KB at N = 128): step sizes, decays, X, B, C and H_in tiles
+__global__ void __launch_bounds__(kSsdThreads, 3) ssd_fused_kernel(const SsdParams p) {
   extern __shared__ __align__(16) unsigned char ssd_smem[];
-  float* sDt = reinterpret_cast<float*>(ssd_smem);
-  float* sS = sDt + kQ;
-  auto* sX = reinterpret_cast<__nv_bfloat16(*)[kP + kRowPad]>(sS + kQ);
-  auto* sB = reinterpret_cast<__nv_bfloat16(*)[N + kRowPad]>(&sX[kQ][0]);
-  auto* sC = reinterpret_cast<__nv_bfloat16(*)[N + kRowPad]>(&sB[kQ][0]);
-  auto* sH = reinterpret_cast<__nv_bfloat16(*)[N + kRowPad]>(&sC[kQ][0]);
-  auto* sHlo = reinterpret_cast<__nv_bfloat16(*)[N + kRowPad]>(&sH[kP][0]);
-  chunk_decays(p, b, h, t0, sDt, sS);
-  load_tile<kP>(&sX[0][0], p.x + (b * p.L + t0) * p.d_inner + h * kP, p.d_inner, rows);
-  load_tile<N>(&sB[0][0], p.B + (b * p.L + t0) * N, N, rows);
-  load_tile<N>(&sC[0][0], p.C + (b * p.L + t0) * N, N, rows);
-  const float* Hin = p.Hs + (((b * p.heads + h) * p.nchunks + c) * kP) * N;
-  for (int i = threadIdx.x; i < kP * N / 2; i += kSsdThreads) {
-    const float2 v = reinterpret_cast<const float2*>(Hin)[i];
-    const int r = (2 * i) / N, n = (2 * i) % N;
-    const __nv_bfloat162 hi = __floats2bfloat162_rn(v.x, v.y);  // H_in as bf16 hi + lo
-    *reinterpret_cast<__nv_bfloat162*>(&sH[r][n]) = hi;
-    *reinterpret_cast<__nv_bfloat162*>(&sHlo[r][n]) =
-        __floats2bfloat162_rn(v.x - __bfloat162float(hi.x), v.y - __bfloat162float(hi.y));
-  }
-  __syncthreads();
-
+  SsdSmem<N>& sm = *reinterpret_cast<SsdSmem<N>*>(ssd_smem);
+  const int h = blockIdx.x % p.heads;
+  const int64_t b = blockIdx.x / p.heads;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int g = lane / 4, tq = lane % 4;
-  const int i0 = 16 * warp + g, i1 = i0 + 8;  // this lane's two output rows (steps)
+  const int p0 = 16 * warp;  // this warp's channels within the head
+  const __nv_bfloat16* xh = p.x + b * p.L * p.d_inner + h * kP;
+  const __nv_bfloat16* zh = p.z ? p.z + b * p.L * p.d_inner + h * kP : nullptr;
+  const __nv_bfloat16* Bb = p.B + b * p.L * N;
+  const __nv_bfloat16* Cb = p.C + b * p.L * N;
 
-  // G = C B^T (rows i, cols j), K = N
-  float G[kQ / 8][4];
+  float Dv[2][2];  // D of this lane's output channels p0 + 8 pt + 2 tq (+1)
 #pragma unroll
-  for (int jt = 0; jt < kQ / 8; jt++) G[jt][0] = G[jt][1] = G[jt][2] = G[jt][3] = 0.f;
-  // Yi = C H_in^T (rows i, cols p), K = N
-  float Yi[kP / 8][4];
+  for (int pt = 0; pt < 2; pt++)
 #pragma unroll
-  for (int pt = 0; pt < kP / 8; pt++) Yi[pt][0] = Yi[pt][1] = Yi[pt][2] = Yi[pt][3] = 0.f;
-#pragma unroll
-  for (int kk = 0; kk < N / 16; kk++) {
-    uint32_t a[4];
-    ldsm_x4(a, &sC[16 * warp + (lane % 16)][kk * 16 + 8 * (lane / 16)]);
-#pragma unroll
-    for (int jt = 0; jt < kQ / 8; jt += 2) {  // B operand (n, j) = sB[j][n]: n contiguous
-      uint32_t bb[4];
-      ldsm_x4(bb, &sB[8 * jt + (lane % 8) + 8 * (lane / 16)][kk * 16 + 8 * ((lane / 8) % 2)]);
-      mma16816(G[jt], a, bb[0], bb[1]);
-      mma16816(G[jt + 1], a, bb[2], bb[3]);
-    }
-#pragma unroll
-    for (int pt = 0; pt < kP / 8; pt += 2) {  // B operand (n, p) = sH[p][n] (+ the lo part)
-      uint32_t bb[4], bl[4];
-      ldsm_x4(bb, &sH[8 * pt + (lane % 8) + 8 * (lane / 16)][kk * 16 + 8 * ((lane / 8) % 2)]);
-      ldsm_x4(bl, &sHlo[8 * pt + (lane % 8) + 8 * (lane / 16)][kk * 16 + 8 * ((lane / 8) % 2)]);
-      mma16816(Yi[pt], a, bb[0], bb[1]);
-      mma16816(Yi[pt + 1], a, bb[2], bb[3]);
-      mma16816(Yi[pt], a, bl[0], bl[1]);
-      mma16816(Yi[pt + 1], a, bl[2], bl[3]);
-    }
-  }
-  // causal mask and decays: M[i][j] = G[i][j] delta_j 2^(S_i - S_j) for j <= i
-  const float s_i0 = sS[i0], s_i1 = sS[i1];
-#pragma unroll
-  for (int jt = 0; jt < kQ / 8; jt++) {
-#pragma unroll
-    for (int q = 0; q < 2; q++) {
-      const int j = 8 * jt + 2 * tq + q;
-      const float dj = sDt[j], sj = sS[j];
-      G[jt][q] = j <= i0 ? G[jt][q] * dj * ex2(s_i0 - sj) : 0.f;
-      G[jt][2 + q] = j <= i1 ? G[jt][2 + q] * dj * ex2(s_i1 - sj) : 0.f;
-    }
-  }
-  // Y = M X (rows i, cols p), K = j; the M fragments come straight from G's accumulators
-  float Y[kP / 8][4];
-#pragma unroll
-  for (int pt = 0; pt < kP / 8; pt++) {
-    const float e0 = ex2(s_i0), e1 = ex2(s_i1);
-    Y[pt][0] = Yi[pt][0] * e0; Y[pt][1] = Yi[pt][1] * e0;
-    Y[pt][2] = Yi[pt][2] * e1; Y[pt][3] = Yi[pt][3] * e1;
-  }
-#pragma unroll
-  for (int kk = 0; kk < kQ / 16; kk++) {
-    // M as bf16 hi + lo fragments (the products are exact in fp32 accumulation)
-    const float* g0 = G[2 * kk];
-    const float* g1 = G[2 * kk + 1];
-    uint32_t a[4], al[4];
-    a[0] = pack_bf16(g0[0], g0[1]);
-    a[1] = pack_bf16(g0[2], g0[3]);
-    a[2] = pack_bf16(g1[0], g1[1]);
-    a[3] = pack_bf16(g1[2], g1[3]);
-    auto lo_of = [](float v0, float v1, uint32_t hi) {
-      const __nv_bfloat162 h2 = *reinterpret_cast<const __nv_bfloat162*>(&hi);
-      return pack_bf16(v0 - __bfloat162float(h2.x), v1 - __bfloat162float(h2.y));
-    };
-    al[0] = lo_of(g0[0], g0[1], a[0]);
-    al[1] = lo_of(g0[2], g0[3], a[1]);
-    al[2] = lo_of(g1[0], g1[1], a[2]);
-    al[3] = lo_of(g1[2], g1[3], a[3]);
-#pragma unroll
-    for (int pt = 0; pt < kP / 8; pt += 2) {  // B operand (j, p) = sX[j][p]: p contiguous
-      uint32_t bb[4];
-      ldsm_x4_t(bb, &sX[kk * 16 + (lane % 8) + 8 * ((lane / 8) % 2)][8 * pt + 8 * (lane / 16)]);
-      mma16816(Y[pt], a, bb[0], bb[1]);
-      mma16816(Y[pt + 1], a, bb[2], bb[3]);
-      mma16816(Y[pt], al, bb[0], bb[1]);
-      mma16816(Y[pt + 1], al, bb[2], bb[3]);
-    }
-  }
-  // y = (Y + D x) silu(z)
-#pragma unroll
-  for (int pt = 0; pt < kP / 8; pt++) {
-#pragma unroll
-    for (int half = 0; half < 2; half++) {
-      const int i = half ? i1 : i0;
-      if (i >= rows) continue;
-      const int pp = 8 * pt + 2 * tq;
-      const int64_t d0 = (int64_t)h * kP + pp;
-      const int64_t e = (b * p.L + t0 + i) * p.d_inner + d0;
-      float v0 = Y[pt][2 * half], v1 = Y[pt][2 * half + 1];
-      if (p.D) {
-        v0 = fmaf(p.D[d0], __bfloat162float(sX[i][pp]), v0);
-        v1 = fmaf(p.D[d0 + 1], __bfloat162float(sX[i][pp + 1]), v1);
-      }
-      if (p.z) {
-        const __nv_bfloat162 zz = *reinterpret_cast<const __nv_bfloat162*>(p.z + e);
-        v0 *= silu(__bfloat162float(zz.x));
-        v1 *= silu(__bfloat162float(zz.y));
-      }
-      *reinterpret_cast<__nv_bfloat162*>(p.y + e) = __floats2bfloat162_rn(v0, v1);
-    }
-  }
-}
+    for (int q = 0; q < 2; q++) Dv[pt][q] = p.D ? p.D[h * kP + p0 + 8 * pt + 2 * tq + q] : 0.f;
 
-template <int N>
-static size_t ssd_output_smem() {
-  return 2 * kQ * sizeof(float) + (size_t)kQ * (kP + kRowPad) * 2 + 4 * (size_t)kQ * (N + kRowPad) * 2;
+  float H[N / 8][4];  // state: rows p0 + g (+8), columns n = 8 nt + 2 tq (+1)
+#pragma unroll
+  for (int nt = 0; nt < N / 8; nt++) H[nt][0] = H[nt][1] = H[nt][2] = H[nt][3] = 0.f;
+
+  // Pipeline: B, C of a chunk are requested while the previous chunk finishes (M X and the
+  // outputs), x, z at the chunk's start, the raw step sizes one chunk ahead.
+  load_tile_async<N>(&sm.B[0][0], Bb, N, (int)min((int64_t)kQ, p.L));
+  load_tile_async<N>(&sm.C[0][0], Cb, N, (int)min((int64_t)kQ, p.L));
+  ssd_cp_async_commit();
+  float2 dt_raw = warp == 0 ? load_dt_pair(p, b, h, 0, lane) : make_float2(0.f, 0.f);
+
+  for (int64_t t0 = 0; t0 < p.L; t0 += kQ) {
+    const int rows = (int)min((int64_t)kQ, p.L - t0);
+    load_tile_async<kP>(&sm.X[0][0], xh + t0 * p.d_inner, p.d_inner, rows);
+    if (zh) load_tile_async<kP>(&sm.Z[0][0], zh + t0 * p.d_inner, p.d_inner, rows);
+    ssd_cp_async_commit();
+    if (warp == 0) {
+      chunk_decays(p, h, t0, dt_raw, lane, sm.dt, sm.S);
+      if (t0 + kQ < p.L) dt_raw = load_dt_pair(p, b, h, t0 + kQ, lane);
+    }
+    ssd_cp_async_wait<1>();  // this chunk's B, C have landed (x, z may still be in flight)
+    __syncthreads();
+
+    // ---- G = C B^T on this warp's five tiles, then M (hi, lo) into shared memory
+    {
+      float G[5][4];
+#pragma unroll
+      for (int s = 0; s < 5; s++) G[s][0] = G[s][1] = G[s][2] = G[s][3] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < N / 16; kk++) {
+        uint32_t a[4];
+        int r_prev = -1;
+#pragma unroll
+        for (int s = 0; s < 5; s++) {
+          int r, jt;
+          g_tile(warp, s, r, jt);
+          if (r != r_prev) {  // warp-uniform
+            ldsm_x4(a, &sm.C[16 * r + (lane % 16)][kk * 16 + 8 * (lane / 16)]);
+            r_prev = r;
+          }
+          uint32_t bb[2];  // B operand (k = n, column = j) = B[j][n]
+          ldsm_x2(bb, &sm.B[8 * jt + (lane % 8)][kk * 16 + 8 * ((lane / 8) % 2)]);
+          mma16816(G[s], a, bb[0], bb[1]);
+        }
+      }
+#pragma unroll
+      for (int s = 0; s < 5; s++) {
+        int r, jt;
+        g_tile(warp, s, r, jt);
+#pragma unroll
+        for (int half = 0; half < 2; half++) {
+          const int i = 16 * r + g + 8 * half;
+          const int j = 8 * jt + 2 * tq;
+          const float si = sm.S[i];
+          const float m0 = j <= i ? G[s][2 * half] * sm.dt[j] * ex2(si - sm.S[j]) : 0.f;
+          const float m1 = j + 1 <= i ? G[s][2 * half + 1] * sm.dt[j + 1] * ex2(si - sm.S[j + 1]) : 0.f;
+          uint32_t hi, lo;
+          split_pair(m0, m1, hi, lo);
+          *reinterpret_cast<uint32_t*>(&sm.M[i][j]) = hi;
+          *reinterpret_cast<uint32_t*>(&sm.Mlo[i][j]) = lo;
+        }
+      }
+    }
+
+    // ---- Y = 2^(S_i) C H_in^T: rows i (four 16-row blocks) x this warp's 16 channels
+    float Y[4][2][4];
+#pragma unroll
+    for (int r = 0; r < 4; r++)
+#pragma unroll
+      for (int pt = 0; pt < 2; pt++) Y[r][pt][0] = Y[r][pt][1] = Y[r][pt][2] = Y[r][pt][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < N / 16; kk++) {
+      // B operand (k = n, column = p) straight from the state's accumulator tiles 2 kk, 2 kk + 1
+      uint32_t bh[2][2], bl[2][2];
+#pragma unroll
+      for (int pt = 0; pt < 2; pt++) {
+        split_pair(H[2 * kk][2 * pt], H[2 * kk][2 * pt + 1], bh[pt][0], bl[pt][0]);
+        split_pair(H[2 * kk + 1][2 * pt], H[2 * kk + 1][2 * pt + 1], bh[pt][1], bl[pt][1]);
+      }
+#pragma unroll
+      for (int r = 0; r < 4; r++) {
+        uint32_t a[4];
+        ldsm_x4(a, &sm.C[16 * r + (lane % 16)][kk * 16 + 8 * (lane / 16)]);
+#pragma unroll
+        for (int pt = 0; pt < 2; pt++) mma16816(Y[r][pt], a, bh[pt][0], bh[pt][1]);
+#pragma unroll
+        for (int pt = 0; pt < 2; pt++) mma16816(Y[r][pt], a, bl[pt][0], bl[pt][1]);
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; r++) {
+      const float e0 = ex2(sm.S[16 * r + g]), e1 = ex2(sm.S[16 * r + g + 8]);
+#pragma unroll
+      for (int pt = 0; pt < 2; pt++) {
+        Y[r][pt][0] *= e0; Y[r][pt][1] *= e0;
+        Y[r][pt][2] *= e1; Y[r][pt][3] *= e1;
+      }
+    }
+    __syncthreads();  // M complete; every warp is done reading the B and C tiles
+
+    // ---- w B (hi, lo) over the B and C tiles, for the state update
+    {
+      const float s_last = sm.S[kQ - 1];
+      for (int e = threadIdx.x; e < kQ * N / 8; e += kSsdThreads) {
+        const int j = e / (N / 8), n = (e % (N / 8)) * 8;
+        const float wj = sm.dt[j] * ex2(s_last - sm.S[j]);
+        const uint4 raw = *reinterpret_cast<const uint4*>(&sm.B[j][n]);
+        const uint32_t in[4] = {raw.x, raw.y, raw.z, raw.w};
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+          const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&in[k]);
+          split_pair(__bfloat162float(v.x) * wj, __bfloat162float(v.y) * wj, hi[k], lo[k]);
+        }
+        *reinterpret_cast<uint4*>(&sm.B[j][n]) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(&sm.C[j][n]) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
+    }
+    ssd_cp_async_wait<0>();  // x, z have landed
+    __syncthreads();         // w B and x visible to every warp
+
+    // ---- H = 2^(S_last) H + X^T (w B): rows p (this warp's 16), columns n
+    {
+      const float decay = ex2(sm.S[kQ - 1]);
+#pragma unroll
+      for (int nt = 0; nt < N / 8; nt++) {
+        H[nt][0] *= decay; H[nt][1] *= decay; H[nt][2] *= decay; H[nt][3] *= decay;
+      }
+#pragma unroll
+      for (int kk = 0; kk < kQ / 16; kk++) {
+        uint32_t a[4];  // A = X^T (rows p, k = j): transposed 8 x 8 blocks of X[j][p]
+        ldsm_x4_t(a, &sm.X[kk * 16 + (lane % 8) + 8 * (lane / 16)][p0 + 8 * ((lane / 8) % 2)]);
+#pragma unroll
+        for (int nt = 0; nt < N / 8; nt += 2) {
+          uint32_t bh[4], bl[4];  // B operand (k = j, column = n) = (w B)[j][n]
+          ldsm_x4_t(bh, &sm.B[kk * 16 + (lane % 8) + 8 * ((lane / 8) % 2)][8 * nt + 8 * (lane / 16)]);
+          ldsm_x4_t(bl, &sm.C[kk * 16 + (lane % 8) + 8 * ((lane / 8) % 2)][8 * nt + 8 * (lane / 16)]);
+          mma16816(H[nt], a, bh[0], bh[1]);
+          mma16816(H[nt + 1], a, bh[2], bh[3]);
+          mma16816(H[nt], a, bl[0], bl[1]);
+          mma16816(H[nt + 1], a, bl[2], bl[3]);
+        }
+      }
+    }
+    __syncthreads();  // every warp is done with the B and C tiles: request the next chunk's
+    if (t0 + kQ < p.L) {
+      const int next_rows = (int)min((int64_t)kQ, p.L - t0 - kQ);
+      load_tile_async<N>(&sm.B[0][0], Bb + (t0 + kQ) * N, N, next_rows);
+      load_tile_async<N>(&sm.C[0][0], Cb + (t0 + kQ) * N, N, next_rows);
+    }
+    ssd_cp_async_commit();
+
+    // ---- Y += M X over the blocks on or below the diagonal
+#pragma unroll
+    for (int kk = 0; kk < kQ / 16; kk++) {
+      uint32_t bx[4];  // B operand (k = j, column = p) = X[j][p], two 8-channel tiles
+      ldsm_x4_t(bx, &sm.X[kk * 16 + (lane % 8) + 8 * ((lane / 8) % 2)][p0 + 8 * (lane / 16)]);
+#pragma unroll
+      for (int r = kk; r < 4; r++) {
+        uint32_t a[4], al[4];
+        ldsm_x4(a, &sm.M[16 * r + (lane % 16)][kk * 16 + 8 * (lane / 16)]);
+        ldsm_x4(al, &sm.Mlo[16 * r + (lane % 16)][kk * 16 + 8 * (lane / 16)]);
+#pragma unroll
+        for (int pt = 0; pt < 2; pt++) mma16816(Y[r][pt], a, bx[2 * pt], bx[2 * pt + 1]);
+#pragma unroll
+        for (int pt = 0; pt < 2; pt++) mma16816(Y[r][pt], al, bx[2 * pt], bx[2 * pt + 1]);
+      }
+    }
+
+    // ---- y = (Y + D x) silu(z)
+#pragma unroll
+    for (int r = 0; r < 4; r++) {
+#pragma unroll
+      for (int pt = 0; pt < 2; pt++) {
+#pragma unroll
+        for (int half = 0; half < 2; half++) {
+          const int i = 16 * r + g + 8 * half;
+          if (i >= rows) continue;
+          const int pp = p0 + 8 * pt + 2 * tq;
+          const __nv_bfloat162 xx = *reinterpret_cast<const __nv_bfloat162*>(&sm.X[i][pp]);
+          float v0 = fmaf(Dv[pt][0], __bfloat162float(xx.x), Y[r][pt][2 * half]);
+          float v1 = fmaf(Dv[pt][1], __bfloat162float(xx.y), Y[r][pt][2 * half + 1]);
+          if (zh) {
+            const __nv_bfloat162 zz = *reinterpret_cast<const __nv_bfloat162*>(&sm.Z[i][pp]);
+            v0 *= silu(__bfloat162float(zz.x));
+            v1 *= silu(__bfloat162float(zz.y));
+          }
+          *reinterpret_cast<__nv_bfloat162*>(p.y + (b * p.L + t0 + i) * p.d_inner + h * kP + pp) =
+              __floats2bfloat162_rn(v0, v1);
+        }
+      }
+    }
+    __syncthreads();  // x, z, M free for the next chunk
+  }
+  ssd_cp_async_wait<0>();  // nothing left in flight (the last commit is an empty group)
+
+  if (p.last_state) {
+    float* out = p.last_state + (b * p.d_inner + (int64_t)h * kP + p0) * N;
+#pragma unroll
+    for (int nt = 0; nt < N / 8; nt++) {
+      const int col = 8 * nt + 2 * tq;
+      *reinterpret_cast<float2*>(out + g * N + col) = make_float2(H[nt][0], H[nt][1]);
+      *reinterpret_cast<float2*>(out + (g + 8) * N + col) = make_float2(H[nt][2], H[nt][3]);
+    }
+  }
 }
 
 template <int N>
 static cudaError_t launch_ssd_n(const SsdParams& p, cudaStream_t s) {
-  static_assert(kP == kQ, "the H_in tile reuses the chunk-row layout");
-  static bool attr_set = false;  // opt in to > 48 KB of dynamic shared memory once
-  if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(ssd_output_kernel<N>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)ssd_output_smem<N>());
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  const int64_t blocks = p.batch * p.heads * p.nchunks;
-  ssd_chunk_state_kernel<N><<<(unsigned)blocks, kSsdThreads, 0, s>>>(p);
-  const int64_t elems = p.batch * p.heads * (int64_t)kP * N;
-  ssd_state_scan_kernel<<<(unsigned)((elems + 255) / 256), 256, 0, s>>>(p);
-  ssd_output_kernel<N><<<(unsigned)blocks, kSsdThreads, ssd_output_smem<N>(), s>>>(p);
+  const int smem = (int)sizeof(SsdSmem<N>);
+  cudaError_t e = cudaFuncSetAttribute(ssd_fused_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(ssd_fused_kernel<N>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
+  ssd_fused_kernel<N><<<(unsigned)(p.batch * p.heads), kSsdThreads, smem, s>>>(p);
   return cudaGetLastError();
-}
-
-size_t ssd_workspace_floats(int64_t batch, int64_t L, int heads, int N) {
-  const int64_t chunks = (L + kQ - 1) / kQ;
-  return (size_t)(batch * heads * chunks * ((int64_t)kP * N + 1));
 }
 
 int ssd_head_dim() { return kP; }
