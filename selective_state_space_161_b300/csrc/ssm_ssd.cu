@@ -17,13 +17,13 @@
 // HBM sees only x, z, dt, B, C in and y out.  Per chunk:
 //   G = C B^T (only the 16 x 8 tiles on or below the diagonal), masked and decayed into
 //   M = G delta_j 2^(S_i - S_j), staged in shared memory;  Y = 2^(S_i) C H_in^T + M X;
-//   y = (Y + D x) silu(z);  H = 2^(S_last) H + X^T (w B), w_j = delta_j 2^(S_last - S_j).
+//   y = (Y + D x) silu(z);  H = 2^(S_last) H + (w X)^T B, w_j = delta_j 2^(S_last - S_j).
 // Warp w owns channels p in [16 w, 16 w + 16) of H, Y and y.  The accumulator layout of the
 // mma.sync tile holding H (rows p, columns n) is exactly the B-operand layout that C H^T needs
 // (k = n, column = p), so the state feeds the next chunk's readout straight from registers.
 // Tensor-core tiles: mma.sync m16n8k16, bf16 operands, fp32 accumulation, fed from padded
 // shared-memory tiles by ldmatrix.  The inputs x, B, C are bf16 already; the computed operands
-// (M, w B, the carried state) go in as a bf16 hi part plus a bf16 lo part (the rounding
+// (M, w x, the carried state) go in as a bf16 hi part plus a bf16 lo part (the rounding
 // remainder), two products each, so their rounding error is ~2^-16 rather than bf16's 2^-8.
 
 #include "ssm_device.cuh"
@@ -71,10 +71,11 @@ __device__ __forceinline__ float2 load_dt_pair(const SsdParams& p, int64_t b, in
   return v;
 }
 
-// Warp 0: step sizes delta_t and the running decay S_i in log2 units (inclusive prefix sum of
-// delta a log2 e) of one chunk, from the raw pair loaded above, into shared memory.
+// Warp 0: step sizes delta_t, the running decay S_i in log2 units (inclusive prefix sum of
+// delta a log2 e) and the state-update weights w_j of one chunk, from the raw pair loaded
+// above, into shared memory.
 __device__ __forceinline__ void chunk_decays(const SsdParams& p, int h, int64_t t0, float2 raw, int lane,
-                                             float* sDt, float* sS) {
+                                             float* sDt, float* sS, float* sW) {
   const float bias = p.dt_bias ? p.dt_bias[h] : 0.f;
   const int64_t t = t0 + 2 * lane;
   float d0 = raw.x + bias, d1 = raw.y + bias;
@@ -89,10 +90,13 @@ __device__ __forceinline__ void chunk_decays(const SsdParams& p, int h, int64_t 
     const float v = __shfl_up_sync(0xFFFFFFFFu, run, o);
     if (lane >= o) run += v;
   }
+  const float s_last = __shfl_sync(0xFFFFFFFFu, run, 31);
   sDt[2 * lane] = d0;
   sDt[2 * lane + 1] = d1;
   sS[2 * lane] = run - e1;
   sS[2 * lane + 1] = run;
+  sW[2 * lane] = d0 * ex2(s_last - (run - e1));  // w_j = delta_j 2^(S_last - S_j)
+  sW[2 * lane + 1] = d1 * ex2(s_last - run);
 }
 
 __device__ __forceinline__ void ldsm_x2(uint32_t (&r)[2], const void* p) {
@@ -121,9 +125,13 @@ __device__ __forceinline__ void split_pair(float v0, float v1, uint32_t& hi, uin
 template <int W>
 __device__ __forceinline__ void load_tile_async(__nv_bfloat16* s, const __nv_bfloat16* g, int64_t ld,
                                                 int rows) {
-  constexpr int kPerRow = W / 8;
-  for (int i = threadIdx.x; i < kQ * kPerRow; i += kSsdThreads) {
-    const int r = i / kPerRow, c = (i % kPerRow) * 8;
+  constexpr int kPerRow = W / 8;  // 16-byte pieces per row
+  static_assert((kQ * kPerRow) % kSsdThreads == 0, "whole pieces per thread");
+  const int r0 = threadIdx.x / kPerRow, c = (threadIdx.x % kPerRow) * 8;
+  constexpr int kRowStep = kSsdThreads / kPerRow;
+#pragma unroll
+  for (int k = 0; k < kQ * kPerRow / kSsdThreads; k++) {
+    const int r = r0 + k * kRowStep;
     const bool in = r < rows;
     ssd_cp_async16(s + r * (W + kRowPad) + c, in ? g + r * ld + c : g, in ? 16 : 0);
   }
@@ -131,11 +139,12 @@ __device__ __forceinline__ void load_tile_async(__nv_bfloat16* s, const __nv_bfl
 
 template <int N>
 struct SsdSmem {
-  float dt[kQ], S[kQ];                          // step sizes; running log2 decay
+  float dt[kQ], S[kQ], W[kQ];                   // step sizes; running log2 decay; w_j
+  float D[kP];                                  // D of the head's channels (0 if absent)
   __nv_bfloat16 X[kQ][kP + kRowPad];            // x tile [step][channel]
   __nv_bfloat16 Z[kQ][kP + kRowPad];            // z tile [step][channel]
-  __nv_bfloat16 B[kQ][N + kRowPad];             // B tile, then (w B) hi
-  __nv_bfloat16 C[kQ][N + kRowPad];             // C tile, then (w B) lo
+  __nv_bfloat16 B[kQ][N + kRowPad];             // B tile [step][state]
+  __nv_bfloat16 C[kQ][N + kRowPad];             // C tile [step][state]
   __nv_bfloat16 M[kQ][kQ + kRowPad], Mlo[kQ][kQ + kRowPad];  // masked decayed C B^T, hi / lo
 };
 
@@ -164,11 +173,7 @@ __global__ void __launch_bounds__(kSsdThreads, 3) ssd_fused_kernel(const SsdPara
   const __nv_bfloat16* Bb = p.B + b * p.L * N;
   const __nv_bfloat16* Cb = p.C + b * p.L * N;
 
-  float Dv[2][2];  // D of this lane's output channels p0 + 8 pt + 2 tq (+1)
-#pragma unroll
-  for (int pt = 0; pt < 2; pt++)
-#pragma unroll
-    for (int q = 0; q < 2; q++) Dv[pt][q] = p.D ? p.D[h * kP + p0 + 8 * pt + 2 * tq + q] : 0.f;
+  if (threadIdx.x < kP) sm.D[threadIdx.x] = p.D ? p.D[h * kP + threadIdx.x] : 0.f;  // read after the first barrier
 
   float H[N / 8][4];  // state: rows p0 + g (+8), columns n = 8 nt + 2 tq (+1)
 #pragma unroll
@@ -187,7 +192,7 @@ __global__ void __launch_bounds__(kSsdThreads, 3) ssd_fused_kernel(const SsdPara
     if (zh) load_tile_async<kP>(&sm.Z[0][0], zh + t0 * p.d_inner, p.d_inner, rows);
     ssd_cp_async_commit();
     if (warp == 0) {
-      chunk_decays(p, h, t0, dt_raw, lane, sm.dt, sm.S);
+      chunk_decays(p, h, t0, dt_raw, lane, sm.dt, sm.S, sm.W);
       if (t0 + kQ < p.L) dt_raw = load_dt_pair(p, b, h, t0 + kQ, lane);
     }
     ssd_cp_async_wait<1>();  // this chunk's B, C have landed (x, z may still be in flight)
@@ -268,30 +273,11 @@ __global__ void __launch_bounds__(kSsdThreads, 3) ssd_fused_kernel(const SsdPara
         Y[r][pt][2] *= e1; Y[r][pt][3] *= e1;
       }
     }
-    __syncthreads();  // M complete; every warp is done reading the B and C tiles
-
-    // ---- w B (hi, lo) over the B and C tiles, for the state update
-    {
-      const float s_last = sm.S[kQ - 1];
-      for (int e = threadIdx.x; e < kQ * N / 8; e += kSsdThreads) {
-        const int j = e / (N / 8), n = (e % (N / 8)) * 8;
-        const float wj = sm.dt[j] * ex2(s_last - sm.S[j]);
-        const uint4 raw = *reinterpret_cast<const uint4*>(&sm.B[j][n]);
-        const uint32_t in[4] = {raw.x, raw.y, raw.z, raw.w};
-        uint32_t hi[4], lo[4];
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-          const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&in[k]);
-          split_pair(__bfloat162float(v.x) * wj, __bfloat162float(v.y) * wj, hi[k], lo[k]);
-        }
-        *reinterpret_cast<uint4*>(&sm.B[j][n]) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(&sm.C[j][n]) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-      }
-    }
     ssd_cp_async_wait<0>();  // x, z have landed
-    __syncthreads();         // w B and x visible to every warp
+    __syncthreads();         // M and x visible to every warp
 
-    // ---- H = 2^(S_last) H + X^T (w B): rows p (this warp's 16), columns n
+    // ---- H = 2^(S_last) H + (w X)^T B: rows p (this warp's 16), columns n.  The weights w_j
+    // scale the A fragments in registers (w X as bf16 hi + lo); B goes in as loaded.
     {
       const float decay = ex2(sm.S[kQ - 1]);
 #pragma unroll
@@ -302,15 +288,24 @@ __global__ void __launch_bounds__(kSsdThreads, 3) ssd_fused_kernel(const SsdPara
       for (int kk = 0; kk < kQ / 16; kk++) {
         uint32_t a[4];  // A = X^T (rows p, k = j): transposed 8 x 8 blocks of X[j][p]
         ldsm_x4_t(a, &sm.X[kk * 16 + (lane % 8) + 8 * (lane / 16)][p0 + 8 * ((lane / 8) % 2)]);
+        // a0, a1 hold k = j = 16 kk + 2 tq (+1); a2, a3 hold j + 8 (+1)
+        const float2 w0 = *reinterpret_cast<const float2*>(&sm.W[kk * 16 + 2 * tq]);
+        const float2 w1 = *reinterpret_cast<const float2*>(&sm.W[kk * 16 + 8 + 2 * tq]);
+        uint32_t ah[4], al[4];
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+          const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&a[q]);
+          const float2 w = q < 2 ? w0 : w1;
+          split_pair(__bfloat162float(v.x) * w.x, __bfloat162float(v.y) * w.y, ah[q], al[q]);
+        }
 #pragma unroll
         for (int nt = 0; nt < N / 8; nt += 2) {
-          uint32_t bh[4], bl[4];  // B operand (k = j, column = n) = (w B)[j][n]
-          ldsm_x4_t(bh, &sm.B[kk * 16 + (lane % 8) + 8 * ((lane / 8) % 2)][8 * nt + 8 * (lane / 16)]);
-          ldsm_x4_t(bl, &sm.C[kk * 16 + (lane % 8) + 8 * ((lane / 8) % 2)][8 * nt + 8 * (lane / 16)]);
-          mma16816(H[nt], a, bh[0], bh[1]);
-          mma16816(H[nt + 1], a, bh[2], bh[3]);
-          mma16816(H[nt], a, bl[0], bl[1]);
-          mma16816(H[nt + 1], a, bl[2], bl[3]);
+          uint32_t bb[4];  // B operand (k = j, column = n) = B[j][n]
+          ldsm_x4_t(bb, &sm.B[kk * 16 + (lane % 8) + 8 * ((lane / 8) % 2)][8 * nt + 8 * (lane / 16)]);
+          mma16816(H[nt], ah, bb[0], bb[1]);
+          mma16816(H[nt + 1], ah, bb[2], bb[3]);
+          mma16816(H[nt], al, bb[0], bb[1]);
+          mma16816(H[nt + 1], al, bb[2], bb[3]);
         }
       }
     }
@@ -350,8 +345,9 @@ __global__ void __launch_bounds__(kSsdThreads, 3) ssd_fused_kernel(const SsdPara
           if (i >= rows) continue;
           const int pp = p0 + 8 * pt + 2 * tq;
           const __nv_bfloat162 xx = *reinterpret_cast<const __nv_bfloat162*>(&sm.X[i][pp]);
-          float v0 = fmaf(Dv[pt][0], __bfloat162float(xx.x), Y[r][pt][2 * half]);
-          float v1 = fmaf(Dv[pt][1], __bfloat162float(xx.y), Y[r][pt][2 * half + 1]);
+          const float2 dd = *reinterpret_cast<const float2*>(&sm.D[pp]);
+          float v0 = fmaf(dd.x, __bfloat162float(xx.x), Y[r][pt][2 * half]);
+          float v1 = fmaf(dd.y, __bfloat162float(xx.y), Y[r][pt][2 * half + 1]);
           if (zh) {
             const __nv_bfloat162 zz = *reinterpret_cast<const __nv_bfloat162*>(&sm.Z[i][pp]);
             v0 *= silu(__bfloat162float(zz.x));
