@@ -139,7 +139,7 @@ __device__ __forceinline__ void load_tile_async(__nv_bfloat16* s, const __nv_bfl
 
 template <int N>
 struct SsdSmem {
-  float dt[kQ], S[kQ], W[kQ];                   // step sizes; running log2 decay; w_j
+  float dt[2][kQ], S[2][kQ], W[2][kQ];          // per chunk parity: step sizes, running log2 decay, w_j
   float D[kP];                                  // D of the head's channels (0 if absent)
   __nv_bfloat16 X[kQ][kP + kRowPad];            // x tile [step][channel]
   __nv_bfloat16 Z[kQ][kP + kRowPad];            // z tile [step][channel]
@@ -180,23 +180,33 @@ __global__ void __launch_bounds__(kSsdThreads, 3) ssd_fused_kernel(const SsdPara
   for (int nt = 0; nt < N / 8; nt++) H[nt][0] = H[nt][1] = H[nt][2] = H[nt][3] = 0.f;
 
   // Pipeline: B, C of a chunk are requested while the previous chunk finishes (M X and the
-  // outputs), x, z at the chunk's start, the raw step sizes one chunk ahead.
+  // outputs), x, z at the chunk's start; warp 0 computes the next chunk's step sizes and decays
+  // (into the other parity's arrays) while the current chunk runs, from raw step sizes loaded
+  // a chunk earlier still.
   load_tile_async<N>(&sm.B[0][0], Bb, N, (int)min((int64_t)kQ, p.L));
   load_tile_async<N>(&sm.C[0][0], Cb, N, (int)min((int64_t)kQ, p.L));
   ssd_cp_async_commit();
-  float2 dt_raw = warp == 0 ? load_dt_pair(p, b, h, 0, lane) : make_float2(0.f, 0.f);
+  float2 dt_raw = make_float2(0.f, 0.f);
+  if (warp == 0) {
+    chunk_decays(p, h, 0, load_dt_pair(p, b, h, 0, lane), lane, sm.dt[0], sm.S[0], sm.W[0]);
+    if (kQ < p.L) dt_raw = load_dt_pair(p, b, h, kQ, lane);
+  }
 
-  for (int64_t t0 = 0; t0 < p.L; t0 += kQ) {
+  int par = 0;  // parity of the current chunk's decay arrays
+  for (int64_t t0 = 0; t0 < p.L; t0 += kQ, par ^= 1) {
     const int rows = (int)min((int64_t)kQ, p.L - t0);
+    const float* sDt = sm.dt[par];
+    const float* sS = sm.S[par];
+    const float* sW = sm.W[par];
     load_tile_async<kP>(&sm.X[0][0], xh + t0 * p.d_inner, p.d_inner, rows);
     if (zh) load_tile_async<kP>(&sm.Z[0][0], zh + t0 * p.d_inner, p.d_inner, rows);
     ssd_cp_async_commit();
-    if (warp == 0) {
-      chunk_decays(p, h, t0, dt_raw, lane, sm.dt, sm.S, sm.W);
-      if (t0 + kQ < p.L) dt_raw = load_dt_pair(p, b, h, t0 + kQ, lane);
-    }
     ssd_cp_async_wait<1>();  // this chunk's B, C have landed (x, z may still be in flight)
-    __syncthreads();
+    __syncthreads();         // ... and this chunk's decays (written during the previous chunk)
+    if (warp == 0 && t0 + kQ < p.L) {
+      chunk_decays(p, h, t0 + kQ, dt_raw, lane, sm.dt[par ^ 1], sm.S[par ^ 1], sm.W[par ^ 1]);
+      if (t0 + 2 * kQ < p.L) dt_raw = load_dt_pair(p, b, h, t0 + 2 * kQ, lane);
+    }
 
     // ---- G = C B^T on this warp's five tiles, then M (hi, lo) into shared memory
     {
@@ -228,9 +238,11 @@ __global__ void __launch_bounds__(kSsdThreads, 3) ssd_fused_kernel(const SsdPara
         for (int half = 0; half < 2; half++) {
           const int i = 16 * r + g + 8 * half;
           const int j = 8 * jt + 2 * tq;
-          const float si = sm.S[i];
-          const float m0 = j <= i ? G[s][2 * half] * sm.dt[j] * ex2(si - sm.S[j]) : 0.f;
-          const float m1 = j + 1 <= i ? G[s][2 * half + 1] * sm.dt[j + 1] * ex2(si - sm.S[j + 1]) : 0.f;
+          const float si = sS[i];
+          const float2 sj = *reinterpret_cast<const float2*>(&sS[j]);
+          const float2 dj = *reinterpret_cast<const float2*>(&sDt[j]);
+          const float m0 = j <= i ? G[s][2 * half] * dj.x * ex2(si - sj.x) : 0.f;
+          const float m1 = j + 1 <= i ? G[s][2 * half + 1] * dj.y * ex2(si - sj.y) : 0.f;
           uint32_t hi, lo;
           split_pair(m0, m1, hi, lo);
           *reinterpret_cast<uint32_t*>(&sm.M[i][j]) = hi;
@@ -266,7 +278,7 @@ __global__ void __launch_bounds__(kSsdThreads, 3) ssd_fused_kernel(const SsdPara
     }
 #pragma unroll
     for (int r = 0; r < 4; r++) {
-      const float e0 = ex2(sm.S[16 * r + g]), e1 = ex2(sm.S[16 * r + g + 8]);
+      const float e0 = ex2(sS[16 * r + g]), e1 = ex2(sS[16 * r + g + 8]);
 #pragma unroll
       for (int pt = 0; pt < 2; pt++) {
         Y[r][pt][0] *= e0; Y[r][pt][1] *= e0;
@@ -279,7 +291,7 @@ __global__ void __launch_bounds__(kSsdThreads, 3) ssd_fused_kernel(const SsdPara
     // ---- H = 2^(S_last) H + (w X)^T B: rows p (this warp's 16), columns n.  The weights w_j
     // scale the A fragments in registers (w X as bf16 hi + lo); B goes in as loaded.
     {
-      const float decay = ex2(sm.S[kQ - 1]);
+      const float decay = ex2(sS[kQ - 1]);
 #pragma unroll
       for (int nt = 0; nt < N / 8; nt++) {
         H[nt][0] *= decay; H[nt][1] *= decay; H[nt][2] *= decay; H[nt][3] *= decay;
@@ -289,8 +301,8 @@ __global__ void __launch_bounds__(kSsdThreads, 3) ssd_fused_kernel(const SsdPara
         uint32_t a[4];  // A = X^T (rows p, k = j): transposed 8 x 8 blocks of X[j][p]
         ldsm_x4_t(a, &sm.X[kk * 16 + (lane % 8) + 8 * (lane / 16)][p0 + 8 * ((lane / 8) % 2)]);
         // a0, a1 hold k = j = 16 kk + 2 tq (+1); a2, a3 hold j + 8 (+1)
-        const float2 w0 = *reinterpret_cast<const float2*>(&sm.W[kk * 16 + 2 * tq]);
-        const float2 w1 = *reinterpret_cast<const float2*>(&sm.W[kk * 16 + 8 + 2 * tq]);
+        const float2 w0 = *reinterpret_cast<const float2*>(&sW[kk * 16 + 2 * tq]);
+        const float2 w1 = *reinterpret_cast<const float2*>(&sW[kk * 16 + 8 + 2 * tq]);
         uint32_t ah[4], al[4];
 #pragma unroll
         for (int q = 0; q < 4; q++) {
@@ -334,7 +346,8 @@ __global__ void __launch_bounds__(kSsdThreads, 3) ssd_fused_kernel(const SsdPara
       }
     }
 
-    // ---- y = (Y + D x) silu(z)
+    // ---- y = (Y + D x) silu(z), staged in this warp's own columns of the z tile (each value
+    // over the z it was gated by), then written as 16-byte pieces: whole 32-byte sectors
 #pragma unroll
     for (int r = 0; r < 4; r++) {
 #pragma unroll
@@ -342,20 +355,30 @@ __global__ void __launch_bounds__(kSsdThreads, 3) ssd_fused_kernel(const SsdPara
 #pragma unroll
         for (int half = 0; half < 2; half++) {
           const int i = 16 * r + g + 8 * half;
-          if (i >= rows) continue;
           const int pp = p0 + 8 * pt + 2 * tq;
           const __nv_bfloat162 xx = *reinterpret_cast<const __nv_bfloat162*>(&sm.X[i][pp]);
           const float2 dd = *reinterpret_cast<const float2*>(&sm.D[pp]);
           float v0 = fmaf(dd.x, __bfloat162float(xx.x), Y[r][pt][2 * half]);
           float v1 = fmaf(dd.y, __bfloat162float(xx.y), Y[r][pt][2 * half + 1]);
+          __nv_bfloat162* zy = reinterpret_cast<__nv_bfloat162*>(&sm.Z[i][pp]);
           if (zh) {
-            const __nv_bfloat162 zz = *reinterpret_cast<const __nv_bfloat162*>(&sm.Z[i][pp]);
+            const __nv_bfloat162 zz = *zy;
             v0 *= silu(__bfloat162float(zz.x));
             v1 *= silu(__bfloat162float(zz.y));
           }
-          *reinterpret_cast<__nv_bfloat162*>(p.y + (b * p.L + t0 + i) * p.d_inner + h * kP + pp) =
-              __floats2bfloat162_rn(v0, v1);
+          *zy = __floats2bfloat162_rn(v0, v1);
         }
+      }
+    }
+    __syncwarp();
+    {
+      __nv_bfloat16* yc = p.y + (b * p.L + t0) * p.d_inner + h * kP + p0 + 8 * (lane % 2);
+#pragma unroll
+      for (int k = 0; k < 4; k++) {
+        const int i = lane / 2 + 16 * k;
+        if (i < rows)
+          *reinterpret_cast<uint4*>(yc + (int64_t)i * p.d_inner) =
+              *reinterpret_cast<const uint4*>(&sm.Z[i][p0 + 8 * (lane % 2)]);
       }
     }
     __syncthreads();  // x, z, M free for the next chunk
