@@ -149,14 +149,59 @@ struct SsdSmem {
 };
 
 // The lower-triangular 16 x 8 tiles (r, jt) of G (jt <= 2 r + 1: 20 tiles), five per warp,
-// grouped so that a warp's tiles share as few row blocks r as possible.
-__device__ __forceinline__ void g_tile(int warp, int s, int& r, int& jt) {
-  // warp 0: r3 j0-4 | warp 1: r3 j5-7, r0 j0-1 | warp 2: r2 j0-4 | warp 3: r2 j5, r1 j0-3
-  // (one hex digit per tile, tile 0 lowest; s is a compile-time index, warp is uniform)
-  const uint32_t rc = warp == 0 ? 0x33333u : warp == 1 ? 0x00333u : warp == 2 ? 0x22222u : 0x11112u;
-  const uint32_t jc = warp == 0 ? 0x43210u : warp == 1 ? 0x10765u : warp == 2 ? 0x43210u : 0x32105u;
-  r = (int)((rc >> (4 * s)) & 0xFu);
-  jt = (int)((jc >> (4 * s)) & 0xFu);
+// grouped so that a warp's tiles share as few row blocks r as possible:
+//   warp 0: r3 j0-4 | warp 1: r3 j5-7, r0 j0-1 | warp 2: r2 j0-4 | warp 3: r2 j5, r1 j0-3
+// Compile-time per warp, so that every shared-memory address and mask below folds.
+__host__ __device__ constexpr int g_tile_r(int w, int s) {
+  return w == 0 ? 3 : w == 1 ? (s < 3 ? 3 : 0) : w == 2 ? 2 : (s == 0 ? 2 : 1);
+}
+__host__ __device__ constexpr int g_tile_j(int w, int s) {
+  return w == 0 ? s : w == 1 ? (s < 3 ? 5 + s : s - 3) : w == 2 ? s : (s == 0 ? 5 : s - 1);
+}
+
+// G = C B^T on warp WARP's five tiles, masked (j <= i) and decayed into
+// M[i][j] = G[i][j] delta_j 2^(S_i - S_j), stored as bf16 hi and lo.
+template <int N, int WARP>
+__device__ __forceinline__ void g_phase(SsdSmem<N>& sm, const float* sS, const float* sDt, int lane) {
+  const int g = lane / 4, tq = lane % 4;
+  float G[5][4];
+#pragma unroll
+  for (int s = 0; s < 5; s++) G[s][0] = G[s][1] = G[s][2] = G[s][3] = 0.f;
+#pragma unroll
+  for (int kk = 0; kk < N / 16; kk++) {
+    uint32_t a[4];
+#pragma unroll
+    for (int s = 0; s < 5; s++) {
+      const int r = g_tile_r(WARP, s), jt = g_tile_j(WARP, s);
+      if (s == 0 || r != g_tile_r(WARP, s - 1))
+        ldsm_x4(a, &sm.C[16 * r + (lane % 16)][kk * 16 + 8 * (lane / 16)]);
+      uint32_t bb[2];  // B operand (k = n, column = j) = B[j][n]
+      ldsm_x2(bb, &sm.B[8 * jt + (lane % 8)][kk * 16 + 8 * ((lane / 8) % 2)]);
+      mma16816(G[s], a, bb[0], bb[1]);
+    }
+  }
+#pragma unroll
+  for (int s = 0; s < 5; s++) {
+    const int r = g_tile_r(WARP, s), jt = g_tile_j(WARP, s);
+    const int j = 8 * jt + 2 * tq;
+    const float2 sj = *reinterpret_cast<const float2*>(&sS[j]);
+    const float2 dj = *reinterpret_cast<const float2*>(&sDt[j]);
+#pragma unroll
+    for (int half = 0; half < 2; half++) {
+      const int i = 16 * r + g + 8 * half;
+      const float si = sS[i];
+      float m0 = G[s][2 * half] * dj.x * ex2(si - sj.x);
+      float m1 = G[s][2 * half + 1] * dj.y * ex2(si - sj.y);
+      if (jt >= 2 * r) {  // tiles on the diagonal: the causal mask
+        if (j > i) m0 = 0.f;
+        if (j + 1 > i) m1 = 0.f;
+      }
+      uint32_t hi, lo;
+      split_pair(m0, m1, hi, lo);
+      *reinterpret_cast<uint32_t*>(&sm.M[i][j]) = hi;
+      *reinterpret_cast<uint32_t*>(&sm.Mlo[i][j]) = lo;
+    }
+  }
 }
 
 template <int N>
@@ -168,10 +213,7 @@ __global__ void __launch_bounds__(kSsdThreads, 3) ssd_fused_kernel(const SsdPara
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int g = lane / 4, tq = lane % 4;
   const int p0 = 16 * warp;  // this warp's channels within the head
-  const __nv_bfloat16* xh = p.x + b * p.L * p.d_inner + h * kP;
-  const __nv_bfloat16* zh = p.z ? p.z + b * p.L * p.d_inner + h * kP : nullptr;
-  const __nv_bfloat16* Bb = p.B + b * p.L * N;
-  const __nv_bfloat16* Cb = p.C + b * p.L * N;
+  // (tile addresses are rebuilt from the kernel parameters where used: fewer live registers)
 
   if (threadIdx.x < kP) sm.D[threadIdx.x] = p.D ? p.D[h * kP + threadIdx.x] : 0.f;  // read after the first barrier
 
@@ -183,8 +225,8 @@ __global__ void __launch_bounds__(kSsdThreads, 3) ssd_fused_kernel(const SsdPara
   // outputs), x, z at the chunk's start; warp 0 computes the next chunk's step sizes and decays
   // (into the other parity's arrays) while the current chunk runs, from raw step sizes loaded
   // a chunk earlier still.
-  load_tile_async<N>(&sm.B[0][0], Bb, N, (int)min((int64_t)kQ, p.L));
-  load_tile_async<N>(&sm.C[0][0], Cb, N, (int)min((int64_t)kQ, p.L));
+  load_tile_async<N>(&sm.B[0][0], p.B + b * p.L * N, N, (int)min((int64_t)kQ, p.L));
+  load_tile_async<N>(&sm.C[0][0], p.C + b * p.L * N, N, (int)min((int64_t)kQ, p.L));
   ssd_cp_async_commit();
   float2 dt_raw = make_float2(0.f, 0.f);
   if (warp == 0) {
@@ -198,8 +240,9 @@ __global__ void __launch_bounds__(kSsdThreads, 3) ssd_fused_kernel(const SsdPara
     const float* sDt = sm.dt[par];
     const float* sS = sm.S[par];
     const float* sW = sm.W[par];
-    load_tile_async<kP>(&sm.X[0][0], xh + t0 * p.d_inner, p.d_inner, rows);
-    if (zh) load_tile_async<kP>(&sm.Z[0][0], zh + t0 * p.d_inner, p.d_inner, rows);
+    const int64_t act0 = (b * p.L + t0) * p.d_inner + h * kP;  // this chunk's x / z / y tile
+    load_tile_async<kP>(&sm.X[0][0], p.x + act0, p.d_inner, rows);
+    if (p.z) load_tile_async<kP>(&sm.Z[0][0], p.z + act0, p.d_inner, rows);
     ssd_cp_async_commit();
     ssd_cp_async_wait<1>();  // this chunk's B, C have landed (x, z may still be in flight)
     __syncthreads();         // ... and this chunk's decays (written during the previous chunk)
@@ -209,46 +252,11 @@ __global__ void __launch_bounds__(kSsdThreads, 3) ssd_fused_kernel(const SsdPara
     }
 
     // ---- G = C B^T on this warp's five tiles, then M (hi, lo) into shared memory
-    {
-      float G[5][4];
-#pragma unroll
-      for (int s = 0; s < 5; s++) G[s][0] = G[s][1] = G[s][2] = G[s][3] = 0.f;
-#pragma unroll
-      for (int kk = 0; kk < N / 16; kk++) {
-        uint32_t a[4];
-        int r_prev = -1;
-#pragma unroll
-        for (int s = 0; s < 5; s++) {
-          int r, jt;
-          g_tile(warp, s, r, jt);
-          if (r != r_prev) {  // warp-uniform
-            ldsm_x4(a, &sm.C[16 * r + (lane % 16)][kk * 16 + 8 * (lane / 16)]);
-            r_prev = r;
-          }
-          uint32_t bb[2];  // B operand (k = n, column = j) = B[j][n]
-          ldsm_x2(bb, &sm.B[8 * jt + (lane % 8)][kk * 16 + 8 * ((lane / 8) % 2)]);
-          mma16816(G[s], a, bb[0], bb[1]);
-        }
-      }
-#pragma unroll
-      for (int s = 0; s < 5; s++) {
-        int r, jt;
-        g_tile(warp, s, r, jt);
-#pragma unroll
-        for (int half = 0; half < 2; half++) {
-          const int i = 16 * r + g + 8 * half;
-          const int j = 8 * jt + 2 * tq;
-          const float si = sS[i];
-          const float2 sj = *reinterpret_cast<const float2*>(&sS[j]);
-          const float2 dj = *reinterpret_cast<const float2*>(&sDt[j]);
-          const float m0 = j <= i ? G[s][2 * half] * dj.x * ex2(si - sj.x) : 0.f;
-          const float m1 = j + 1 <= i ? G[s][2 * half + 1] * dj.y * ex2(si - sj.y) : 0.f;
-          uint32_t hi, lo;
-          split_pair(m0, m1, hi, lo);
-          *reinterpret_cast<uint32_t*>(&sm.M[i][j]) = hi;
-          *reinterpret_cast<uint32_t*>(&sm.Mlo[i][j]) = lo;
-        }
-      }
+    switch (warp) {
+      case 0: g_phase<N, 0>(sm, sS, sDt, lane); break;
+      case 1: g_phase<N, 1>(sm, sS, sDt, lane); break;
+      case 2: g_phase<N, 2>(sm, sS, sDt, lane); break;
+      default: g_phase<N, 3>(sm, sS, sDt, lane); break;
     }
 
     // ---- Y = 2^(S_i) C H_in^T: rows i (four 16-row blocks) x this warp's 16 channels
@@ -324,8 +332,8 @@ __global__ void __launch_bounds__(kSsdThreads, 3) ssd_fused_kernel(const SsdPara
     __syncthreads();  // every warp is done with the B and C tiles: request the next chunk's
     if (t0 + kQ < p.L) {
       const int next_rows = (int)min((int64_t)kQ, p.L - t0 - kQ);
-      load_tile_async<N>(&sm.B[0][0], Bb + (t0 + kQ) * N, N, next_rows);
-      load_tile_async<N>(&sm.C[0][0], Cb + (t0 + kQ) * N, N, next_rows);
+      load_tile_async<N>(&sm.B[0][0], p.B + (b * p.L + t0 + kQ) * N, N, next_rows);
+      load_tile_async<N>(&sm.C[0][0], p.C + (b * p.L + t0 + kQ) * N, N, next_rows);
     }
     ssd_cp_async_commit();
 
@@ -361,7 +369,7 @@ __global__ void __launch_bounds__(kSsdThreads, 3) ssd_fused_kernel(const SsdPara
           float v0 = fmaf(dd.x, __bfloat162float(xx.x), Y[r][pt][2 * half]);
           float v1 = fmaf(dd.y, __bfloat162float(xx.y), Y[r][pt][2 * half + 1]);
           __nv_bfloat162* zy = reinterpret_cast<__nv_bfloat162*>(&sm.Z[i][pp]);
-          if (zh) {
+          if (p.z) {
             const __nv_bfloat162 zz = *zy;
             v0 *= silu(__bfloat162float(zz.x));
             v1 *= silu(__bfloat162float(zz.y));
@@ -372,7 +380,7 @@ __global__ void __launch_bounds__(kSsdThreads, 3) ssd_fused_kernel(const SsdPara
     }
     __syncwarp();
     {
-      __nv_bfloat16* yc = p.y + (b * p.L + t0) * p.d_inner + h * kP + p0 + 8 * (lane % 2);
+      __nv_bfloat16* yc = p.y + act0 + p0 + 8 * (lane % 2);
 #pragma unroll
       for (int k = 0; k < 4; k++) {
         const int i = lane / 2 + 16 * k;
