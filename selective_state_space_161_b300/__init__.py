@@ -325,7 +325,7 @@ def selective_scan_ssd(x, dt, A_head, B, C, D=None, z=None, dt_bias=None, softpl
     y = torch.empty_like(x)
     last = torch.empty((batch, d_inner, d_state), dtype=torch.float32, device=x.device)
     nbytes = ssm_ssd_fwd_workspace_size(batch, L, d_inner, dt.shape[2], d_state)
-    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=x.device)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=x.device) if nbytes else None
     ssm_ssd_fwd(x, dt, A_head, B, C, D, z, dt_bias, softplus, y, last, ws, stream)
     return y, last
 

@@ -66,3 +66,24 @@ def test_product_path_does_not_import_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
                 assert "liboracle" not in text, f
+
+
+def _ssd_rc(**kw):
+    lib = ssm.load_library()
+    args = dict(x=None, dt=None, A=None, B=None, C=None, D=None, z=None, bias=None, sp=1, y=None,
+                last=None, batch=1, L=64, d_inner=128, heads=2, d_state=64, io=1, ws=None, ws_bytes=0,
+                stream=None)
+    args.update(kw)
+    return lib.ssm_ssd_fwd(*args.values())
+
+
+def test_ssd_host_validation_before_any_device_call():
+    assert _ssd_rc(io=0) == 3                      # the chunked form is bf16 only
+    assert _ssd_rc(d_state=48) == 2                # d_state in {16, 32, 64, 128}
+    assert _ssd_rc(d_state=256) == 2
+    assert _ssd_rc(d_inner=96) == 2                # head dimension is 64
+    assert _ssd_rc(heads=0) == 2
+    assert _ssd_rc(L=-1) == 2
+    assert _ssd_rc(batch=0) == 0                   # empty problem
+    assert _ssd_rc() == 1                          # A (and the tensors) missing
+    assert ssm.ssm_ssd_fwd_workspace_size(8, 2048, 5120, 80, 128) == 0  # state kept on chip

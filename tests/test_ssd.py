@@ -50,3 +50,30 @@ def test_ssd_full_size_sampled():
     w = W.WORKLOADS["ssd2p7b"]
     d_sel = np.concatenate([np.arange(0, 4), np.arange(64 * 37 + 30, 64 * 37 + 34), np.arange(5116, 5120)])
     _run(w, d_sel=d_sel)
+
+
+def test_ssd_without_softplus():
+    """softplus_flag = 0: the step size is dt (+ bias) as given; here dt = |raw| / 8, which is
+    exact in bf16 on either side, and no bias, so every step size is positive."""
+    w = W.Workload("ssd", "ssd case", 2, 150, 128, 32, True, 77, 0.5, heads=2)
+    dev = W.device_ssd_inputs(w)
+    dt = dev["dt"].abs() / 8
+    y, last = ssm.selective_scan_ssd(dev["x"], dt, dev["A_head"], dev["B"], dev["C"], D=dev["D"],
+                                     z=dev["z"], dt_bias=None, softplus=False)
+    torch.cuda.synchronize()
+    x = W.host_ssd_inputs(w)
+    y_ref, last_ref = oracle.scan_fwd(x["u"], np.abs(x["delta"]) / 8, x["A"], x["B"], x["C"], D=x["D"],
+                                      z=x["z"], delta_bias=None, softplus_flag=False)
+    ey, el = rel_err(to_f64(y), y_ref), rel_err(to_f64(last), last_ref)
+    assert ey <= BF16_TOL and el <= BF16_TOL, f"y err {ey:.3g}, last_state err {el:.3g}"
+
+
+def test_ssd_empty_sequence_gives_zero_state():
+    w = W.Workload("ssd", "ssd case", 2, 0, 128, 64, True, 3, 0.5, heads=2)
+    x = torch.empty((2, 0, 128), dtype=torch.bfloat16, device="cuda")
+    dt = torch.empty((2, 0, 2), dtype=torch.bfloat16, device="cuda")
+    bc = torch.empty((2, 0, 64), dtype=torch.bfloat16, device="cuda")
+    A = torch.from_numpy(W.ssd_A_head(w)).cuda()
+    y, last = ssm.selective_scan_ssd(x, dt, A, bc, bc)
+    torch.cuda.synchronize()
+    assert y.shape == (2, 0, 128) and torch.count_nonzero(last).item() == 0
