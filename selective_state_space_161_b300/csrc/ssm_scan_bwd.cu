@@ -457,6 +457,216 @@ __global__ void __launch_bounds__(kBwdCh) bwd_grad_kernel(const BwdArgs p) {
 }
 
 // ---------------------------------------------------------------------------------------
+// 3b. Gradients with two lanes per channel (d_state a multiple of 8): lane 2c + q of the warp
+//     holds states [q N/2, (q + 1) N/2) of channel c, so a CTA covers 16 channels with half
+//     the per-lane registers and half the shared state tile of the one-lane kernel per warp
+//     (about twice the warps per SM).  The per-step readout and the step-size and u gradients
+//     add the two halves with one shfl.xor each; dB and dC are summed over the 16 channels
+//     through a transpose in shared memory (each lane stores its N partials as one row, then
+//     sums one column over the 16 lanes of its parity) and added atomically, one value per
+//     lane.
+constexpr int kBwdCh2 = 16;  // channels per CTA of the two-lane gradient kernel
+
+template <int N, typename T>
+__global__ void __launch_bounds__(32) bwd_grad_kernel2(const BwdArgs p) {
+  static_assert(N % 8 == 0 && N <= 16, "two lanes of whole float4 state groups");
+  constexpr int NL = N / 2;        // states per lane
+  constexpr int NP = NL / 2;       // state pairs per lane (packed fp32x2 arithmetic)
+  constexpr int NQ = NL / 4;       // float4 groups per lane in the shared state rows
+  constexpr int kPitch = N + 4;    // reduction rows: N partials + padding (16-byte aligned)
+  const int64_t n_dtiles = (p.d_inner + kBwdCh2 - 1) / kBwdCh2;
+  const int64_t tiles = (p.L + kBwdTile - 1) / kBwdTile;
+  const int64_t ranges = (tiles + kGradTiles - 1) / kGradTiles;
+  int64_t blk = blockIdx.x;
+  const int64_t dtile = blk % n_dtiles;
+  blk /= n_dtiles;
+  const int64_t r = blk % ranges;
+  const int64_t b = blk / ranges;
+  const int lane = threadIdx.x, q = lane & 1;
+  const int64_t Dn = p.d_inner, L = p.L, d = dtile * kBwdCh2 + (lane >> 1);
+  const bool active = d < Dn;
+  const int64_t dc = active ? d : 0;
+  const int nb = q * NL;  // first state of this lane
+  const int64_t tl_lo = r * kGradTiles, tl_hi = min(tl_lo + kGradTiles, tiles) - 1;
+  __shared__ __align__(16) float sB[kBwdTile][N], sC[kBwdTile][N];
+  __shared__ __align__(16) float4 sH[kBwdTile][NQ][32];  // this lane's states after each step
+  __shared__ __align__(16) float sR[32][kPitch];          // dB/dC partials, one row per lane
+  // the reduced value this lane adds: output o = lane (o < N: dB[o], else dC[o - N]), the sum
+  // over channels of column (o < N ? 0 : NL) + o mod NL of the rows of parity (o mod N) / NL
+  const int o_col = (lane < N ? 0 : NL) + (lane % N) % NL, o_par = (lane % N) / NL;
+
+  float2 A2[NP], Af[NP], m[NP], dAacc[NP];
+#pragma unroll
+  for (int j = 0; j < NP; j++) {
+    const float a0 = p.A[dc * N + nb + 2 * j], a1 = p.A[dc * N + nb + 2 * j + 1];
+    Af[j] = make_float2(a0, a1);
+    A2[j] = make_float2(a0 * kLog2e, a1 * kLog2e);
+    const float* mk = p.ckpt_m + ((b * tiles + tl_hi) * Dn + dc) * N + nb;
+    m[j] = active ? make_float2(mk[2 * j], mk[2 * j + 1]) : make_float2(0.f, 0.f);
+    dAacc[j] = make_float2(0.f, 0.f);
+  }
+  const float bias = p.delta_bias ? p.delta_bias[dc] : 0.f;
+  const float Dd = p.D ? p.D[dc] : 0.f;
+  float dDacc = 0.f, dbacc = 0.f;
+  auto hrow = [&](int k, int j) -> float2 {
+    const float4 v = sH[k][j / 2][lane];
+    return (j & 1) ? make_float2(v.z, v.w) : make_float2(v.x, v.y);
+  };
+  auto pair_of = [&](const float* row, int j) -> float2 {
+    return *reinterpret_cast<const float2*>(row + nb + 2 * j);
+  };
+
+  for (int64_t tl = tl_hi; tl >= tl_lo; tl--) {
+    const int64_t ts = tl * kBwdTile;
+    const int steps = (int)min((int64_t)kBwdTile, L - ts);
+    float xs[kBwdTile], us[kBwdTile], dys[kBwdTile], zs[kBwdTile];
+#pragma unroll
+    for (int k = 0; k < kBwdTile; k++) {
+      const int64_t e = (b * L + ts + min(k, steps - 1)) * Dn + dc;
+      xs[k] = ldf<T>(p.delta, e) + bias;
+      us[k] = ldf<T>(p.u, e);
+      dys[k] = ldf<T>(p.dy, e);
+      zs[k] = p.z ? ldf<T>(p.z, e) : 0.f;
+    }
+    __syncwarp();
+    for (int i = lane; i < steps * N; i += 32) {
+      sB[i / N][i % N] = ldf<T>(p.B, (b * L + ts) * N + i);
+      sC[i / N][i % N] = ldf<T>(p.C, (b * L + ts) * N + i);
+    }
+    float2 h0[NP];
+    {
+      const float* hk = p.ckpt_h + ((b * tiles + tl) * Dn + dc) * N + nb;
+#pragma unroll
+      for (int j = 0; j < NP; j++) h0[j] = active ? make_float2(hk[2 * j], hk[2 * j + 1]) : make_float2(0.f, 0.f);
+    }
+    __syncwarp();
+    float dts[kBwdTile];
+#pragma unroll
+    for (int k = 0; k < kBwdTile; k++) dts[k] = p.softplus ? softplus(xs[k]) : xs[k];
+
+    // forward recompute of this lane's states over the tile into shared memory
+    {
+      float2 h[NP];
+#pragma unroll
+      for (int j = 0; j < NP; j++) h[j] = h0[j];
+#pragma unroll
+      for (int k = 0; k < kBwdTile; k++) {
+        if (k < steps) {
+          const float2 dt2 = make_float2(dts[k], dts[k]);
+          const float w = dts[k] * us[k];
+          const float2 w2 = make_float2(w, w);
+#pragma unroll
+          for (int j = 0; j < NP; j++) {
+            const float2 xa = __fmul2_rn(dt2, A2[j]);
+            h[j] = __ffma2_rn(make_float2(ex2(xa.x), ex2(xa.y)), h[j], __fmul2_rn(w2, pair_of(sB[k], j)));
+          }
+#pragma unroll
+          for (int g = 0; g < NQ; g++) sH[k][g][lane] = make_float4(h[2 * g].x, h[2 * g].y, h[2 * g + 1].x, h[2 * g + 1].y);
+        }
+      }
+    }
+    __syncwarp();
+
+    // reverse over the tile; hk holds the state after step k
+    float2 hk[NP];
+#pragma unroll
+    for (int j = 0; j < NP; j++) hk[j] = hrow(kBwdTile - 1 < steps ? kBwdTile - 1 : 0, j);
+#pragma unroll
+    for (int k = kBwdTile - 1; k >= 0; k--) {
+      if (k >= steps) {
+        if (k - 1 >= 0 && k - 1 < steps) {
+#pragma unroll
+          for (int j = 0; j < NP; j++) hk[j] = hrow(k - 1, j);
+        }
+        continue;
+      }
+      const int64_t e = (b * L + ts + k) * Dn + dc;
+      float2 hp[NP];
+#pragma unroll
+      for (int j = 0; j < NP; j++) hp[j] = k > 0 ? hrow(k - 1, j) : h0[j];
+      float2 s2 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < NP; j++) s2 = __ffma2_rn(pair_of(sC[k], j), hk[j], s2);
+      const float s_half = s2.x + s2.y;
+      const float s = s_half + __shfl_xor_sync(0xFFFFFFFFu, s_half, 1) + Dd * us[k];
+      float g = 1.f;
+      if (p.z) {
+        const float sg = rcp(1.f + ex2(-zs[k] * kLog2e));
+        g = zs[k] * sg;
+        if (active && q == 0) static_cast<T*>(p.dz)[e] = from_f32<T>(dys[k] * s * sg * fmaf(zs[k], 1.f - sg, 1.f));
+      }
+      const float ds = dys[k] * g;
+      dDacc = fmaf(ds, us[k], dDacc);
+      const float dt = dts[k];
+      const float2 dt2 = make_float2(dt, dt), ds2 = make_float2(ds, ds), u2 = make_float2(us[k], us[k]);
+      const float dtu = dt * us[k];
+      const float2 dtu2 = make_float2(active ? dtu : 0.f, active ? dtu : 0.f);
+      const float2 dsa = make_float2(active ? ds : 0.f, active ? ds : 0.f);
+      float2 ddt2 = make_float2(0.f, 0.f), slb2 = make_float2(0.f, 0.f);
+      float v[N];  // dB partials of this lane's states, then dC partials
+#pragma unroll
+      for (int j = 0; j < NP; j++) {
+        const float2 Bv = pair_of(sB[k], j);
+        const float2 lam = __ffma2_rn(ds2, pair_of(sC[k], j), m[j]);
+        const float2 xa = __fmul2_rn(dt2, A2[j]);
+        const float2 dA = make_float2(ex2(xa.x), ex2(xa.y));
+        const float2 t1 = __fmul2_rn(__fmul2_rn(lam, hp[j]), dA);
+        ddt2 = __ffma2_rn(t1, Af[j], __ffma2_rn(lam, __fmul2_rn(Bv, u2), ddt2));
+        dAacc[j] = __ffma2_rn(t1, dt2, dAacc[j]);
+        slb2 = __ffma2_rn(lam, Bv, slb2);
+        const float2 pb = __fmul2_rn(lam, dtu2), pc = __fmul2_rn(dsa, hk[j]);
+        v[2 * j] = pb.x;
+        v[2 * j + 1] = pb.y;
+        v[NL + 2 * j] = pc.x;
+        v[NL + 2 * j + 1] = pc.y;
+        m[j] = __fmul2_rn(dA, lam);
+        hk[j] = hp[j];
+      }
+      const float ddt_half = ddt2.x + ddt2.y, slb_half = slb2.x + slb2.y;
+      const float ddt = ddt_half + __shfl_xor_sync(0xFFFFFFFFu, ddt_half, 1);
+      const float slb = slb_half + __shfl_xor_sync(0xFFFFFFFFu, slb_half, 1);
+      const float dx = p.softplus ? ddt * rcp(1.f + ex2(-xs[k] * kLog2e)) : ddt;
+      dbacc += dx;
+      if (active) {
+        if (q == 0) static_cast<T*>(p.du)[e] = from_f32<T>(fmaf(ds, Dd, dt * slb));
+        else static_cast<T*>(p.ddelta)[e] = from_f32<T>(dx);
+      }
+      // dB / dC: sum the partials over the 16 channels through shared memory
+#pragma unroll
+      for (int c4 = 0; c4 < N / 4; c4++)
+        *reinterpret_cast<float4*>(&sR[lane][4 * c4]) = make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
+      __syncwarp();
+      if (lane < 2 * N) {
+        float acc = 0.f;
+#pragma unroll
+        for (int c = 0; c < kBwdCh2; c++) acc += sR[2 * c + o_par][o_col];
+        float* row = (lane < N ? p.dB : p.dC) + (b * L + ts + k) * N;
+        atomicAdd(row + lane % N, acc);
+      }
+      __syncwarp();
+    }
+    __syncwarp();
+  }
+  if (!active) return;
+#pragma unroll
+  for (int j = 0; j < NP; j++) {
+    atomicAdd(p.dA + d * N + nb + 2 * j, dAacc[j].x);
+    atomicAdd(p.dA + d * N + nb + 2 * j + 1, dAacc[j].y);
+  }
+  if (q == 0) {  // per-channel sums: both lanes hold them
+    if (p.dD) atomicAdd(p.dD + d, dDacc);
+    if (p.dbias) atomicAdd(p.dbias + d, dbacc);
+  }
+  if (p.dinit && tl_lo == 0) {
+#pragma unroll
+    for (int j = 0; j < NP; j++) {
+      p.dinit[(b * Dn + d) * N + nb + 2 * j] = m[j].x;
+      p.dinit[(b * Dn + d) * N + nb + 2 * j + 1] = m[j].y;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------------
 
 size_t bwd_workspace_floats(int64_t batch, int64_t L, int64_t d_inner, int d_state, int n_chunks) {
   const int64_t tiles = (L + kBwdTile - 1) / kBwdTile;
@@ -479,7 +689,12 @@ static cudaError_t launch_bwd_t(const BwdArgs& a, const ScanParams& fwd, cudaStr
   bwd_fwd_ckpt_kernel<N, T><<<(unsigned)(n_dtiles * a.n_chunks * a.batch), kBwdCh, 0, s>>>(a);
   bwd_reverse_kernel<N, T, false><<<(unsigned)(n_dtiles * a.n_chunks * a.batch), kBwdCh, 0, s>>>(a);
   const int64_t ranges = (tiles + kGradTiles - 1) / kGradTiles;
-  bwd_grad_kernel<N, T><<<(unsigned)(n_dtiles * ranges * a.batch), kBwdCh, 0, s>>>(a);
+  if constexpr (N % 8 == 0) {  // two lanes per channel
+    const int64_t n_dtiles2 = (a.d_inner + kBwdCh2 - 1) / kBwdCh2;
+    bwd_grad_kernel2<N, T><<<(unsigned)(n_dtiles2 * ranges * a.batch), 32, 0, s>>>(a);
+  } else {
+    bwd_grad_kernel<N, T><<<(unsigned)(n_dtiles * ranges * a.batch), kBwdCh, 0, s>>>(a);
+  }
   return cudaGetLastError();
 }
 
