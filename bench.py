@@ -358,8 +358,8 @@ class BackwardStep:
         nbytes = ssm.ssm_scan_bwd_workspace_size(w.batch, w.L, w.d_inner, N, io)
         self.ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
         nf = ssm.ssm_scan_fwd_workspace_size(w.batch, w.L, w.d_inner, N, io)
-        # summary + reverse summary when chunked, checkpoints, reverse checkpoints, gradients
-        self.launches = 5 if nf else 3
+        # forward and reverse chunk summaries when chunked, checkpoints, gradients
+        self.launches = 4 if nf else 2
 
     def __call__(self, stream=None):
         d, g = self.dev, self.g

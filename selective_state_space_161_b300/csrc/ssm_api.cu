@@ -321,8 +321,7 @@ ssm_status_t ssm_scan_bwd(const void* u, const void* delta, const float* A, cons
   a.batch = batch; a.L = L; a.d_inner = d_inner; a.d_state = d_state;
   a.chunk_len = plan.chunk_len; a.n_chunks = plan.n_chunks;
   a.ckpt_h = ws;
-  a.ckpt_m = ws + ck;
-  float* fS = ws + 2 * ck;
+  float* fS = ws + ck;
   a.fws_S = fS;
   a.fws_h = fS + fws;
   float* rS = fS + fws * (d_state + 1);

@@ -93,7 +93,6 @@ struct BwdArgs {
   float* rws_S;        // reverse chunk summaries [batch][n_chunks][d_inner] (+ [.][d_state])
   float* rws_m;
   float* ckpt_h;       // [batch][tiles][d_inner][d_state]: state before each tile
-  float* ckpt_m;       // [batch][tiles][d_inner][d_state]: carry entering each tile's last step
 };
 
 

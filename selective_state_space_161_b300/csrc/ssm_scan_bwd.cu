@@ -7,14 +7,15 @@
 //  1. forward checkpoints: the forward recurrence (time-chunked exactly like the forward
 //     scan: the forward summary kernel, then the checkpoint kernel below) stores the state
 //     before every 16-step tile — one state per 16 steps, never the per-step states;
-//  2. reverse checkpoints: the adjoint lambda_t = ds_t C_t + dA_{t+1} lambda_{t+1} runs
-//     backwards in time with the same chunk decomposition (a reverse summary per chunk: its
-//     carry-out from a zero carry-in and its decay exp(A sum delta)), storing the carry that
-//     enters each tile from the right;
-//  3. gradients: one CTA per (batch row, tile, 32 channels) recomputes the tile's 16 states
-//     into shared memory from its checkpoint, then walks the tile backwards.  dB and dC sum
-//     over channels: the 32 lanes reduce them by a shuffle reduce-scatter and add one value
-//     per lane atomically.
+//  2. reverse summaries: the adjoint lambda_t = ds_t C_t + dA_{t+1} lambda_{t+1} runs
+//     backwards in time with the same chunk decomposition; per chunk, its carry-out from a
+//     zero carry-in and its decay exp(A sum delta);
+//  3. gradients: one CTA per (batch row, time chunk, 32 or 16 channels) starts from the
+//     adjoint carry entering its chunk from the right (dL/dlast_state folded with the
+//     summaries of the later chunks) and walks the chunk's tiles backwards: per tile it
+//     recomputes the 16 states into shared memory from the tile's checkpoint, then carries
+//     the adjoint through the tile while forming every gradient.  dB and dC sum over
+//     channels (a warp reduction, then one atomic add per lane).
 // All arithmetic is fp32; one thread per (batch, channel), all d_state states in registers.
 
 #include "ssm_device.cuh"
@@ -127,13 +128,13 @@ __global__ void __launch_bounds__(kBwdCh) bwd_fwd_ckpt_kernel(const BwdArgs p) {
 }
 
 // ---------------------------------------------------------------------------------------
-// 2. Reverse pass.  Walking a chunk backwards from carry m (entering its last step):
+// 2. Reverse summaries.  Walking a chunk backwards from carry m (entering its last step):
 //      lambda_t = m + ds_t C_t,   m <- dA_t lambda_t   (carry to step t - 1),
-//    with ds_t = dy_t silu(z_t).  kSummary: from m = 0, store (sum delta, m after the chunk's
-//    first step) for chunks >= 1.  Otherwise: fold the summaries of the chunks after c into
-//    the carry (from dlast), then store the carry entering each tile, walking right to left.
-template <int N, typename T, bool kSummary>
-__global__ void __launch_bounds__(kBwdCh) bwd_reverse_kernel(const BwdArgs p) {
+//    with ds_t = dy_t silu(z_t): from m = 0, store (sum delta, m after the chunk's first
+//    step) for chunks >= 1.
+template <int N, typename T>
+__global__ void __launch_bounds__(kBwdCh) bwd_reverse_summary_kernel(const BwdArgs p) {
+  constexpr bool kSummary = true;
   constexpr int NP = (N + 1) / 2;
   const int64_t n_dtiles = (p.d_inner + kBwdCh - 1) / kBwdCh;
   const int chunks = kSummary ? p.n_chunks - 1 : p.n_chunks;
@@ -147,7 +148,6 @@ __global__ void __launch_bounds__(kBwdCh) bwd_reverse_kernel(const BwdArgs p) {
   const bool active = d < Dn;
   const int64_t dc = active ? d : 0;
   const int64_t t0 = (int64_t)c * p.chunk_len, t1 = min(t0 + p.chunk_len, L);
-  const int64_t tiles = (L + kBwdTile - 1) / kBwdTile;
   __shared__ __align__(16) float sC[kBwdTile][2 * NP];
 
   float2 A2[NP], m[NP];
@@ -160,23 +160,6 @@ __global__ void __launch_bounds__(kBwdCh) bwd_reverse_kernel(const BwdArgs p) {
   if (2 * NP != N)
     for (int i = lane; i < kBwdTile; i += kBwdCh) sC[i][N] = 0.f;
   const float bias = p.delta_bias ? p.delta_bias[dc] : 0.f;
-  if (!kSummary) {
-    if (p.dlast) {
-      const float* dl = p.dlast + (b * Dn + dc) * N;
-#pragma unroll
-      for (int j = 0; j < NP; j++) m[j] = make_float2(dl[2 * j], 2 * j + 1 < N ? dl[2 * j + 1] : 0.f);
-    }
-    for (int j = p.n_chunks - 1; j > c; j--) {
-      const int64_t slot = (b * p.n_chunks + j) * Dn + dc;
-      const float S = p.rws_S[slot];
-      const float* ms = p.rws_m + slot * N;
-#pragma unroll
-      for (int q = 0; q < NP; q++) {
-        m[q].x = fmaf(ex2(A2[q].x * S), m[q].x, ms[2 * q]);
-        m[q].y = fmaf(ex2(A2[q].y * S), m[q].y, 2 * q + 1 < N ? ms[2 * q + 1] : 0.f);
-      }
-    }
-  }
   float S = 0.f, S_comp = 0.f;
   const int64_t first_tile = t0 / kBwdTile, last_tile = (t1 - 1) / kBwdTile;
   // per tile: delta_raw, dy, z in registers, loaded at once, next tile prefetched
@@ -199,14 +182,6 @@ __global__ void __launch_bounds__(kBwdCh) bwd_reverse_kernel(const BwdArgs p) {
     float xn[kBwdTile], dn[kBwdTile], zn[kBwdTile];
     const bool more = tl > first_tile;
     if (more) load_tile(tl - 1, xn, dn, zn);
-    if (!kSummary && active) {
-      float* ck = p.ckpt_m + ((b * tiles + tl) * Dn + d) * N;
-#pragma unroll
-      for (int j = 0; j < NP; j++) {
-        ck[2 * j] = m[j].x;
-        if (2 * j + 1 < N) ck[2 * j + 1] = m[j].y;
-      }
-    }
     __syncwarp();
     for (int i = lane; i < steps * N; i += kBwdCh) sC[i / N][i % N] = ldf<T>(p.C, (b * L + ts) * N + i);
     __syncwarp();
@@ -269,7 +244,30 @@ __device__ __forceinline__ void warp_reduce_scatter_add(float (&v)[32], int lane
   else if (lane < 2 * N) atomicAdd(dC_row + lane - N, v[0]);
 }
 
-constexpr int kGradTiles = 4;  // tiles per gradient CTA, walked backwards
+// The adjoint carry entering chunk c from the right for states nb + 2j, nb + 2j + 1 (j < NP):
+// dL/dlast_state (or zero) folded with the reverse summaries of chunks n_chunks - 1 .. c + 1.
+template <int N, int NP>
+__device__ __forceinline__ void chunk_carry_in(const BwdArgs& p, int64_t b, int64_t dc, int c, int nb,
+                                               const float2 (&A2)[NP], float2 (&m)[NP]) {
+  const int64_t Dn = p.d_inner;
+#pragma unroll
+  for (int j = 0; j < NP; j++) m[j] = make_float2(0.f, 0.f);
+  if (p.dlast) {
+    const float* dl = p.dlast + (b * Dn + dc) * N + nb;
+#pragma unroll
+    for (int j = 0; j < NP; j++) m[j] = make_float2(dl[2 * j], nb + 2 * j + 1 < N ? dl[2 * j + 1] : 0.f);
+  }
+  for (int jc = p.n_chunks - 1; jc > c; jc--) {
+    const int64_t slot = (b * p.n_chunks + jc) * Dn + dc;
+    const float S = p.rws_S[slot];
+    const float* ms = p.rws_m + slot * N + nb;
+#pragma unroll
+    for (int j = 0; j < NP; j++) {
+      m[j].x = fmaf(ex2(A2[j].x * S), m[j].x, ms[2 * j]);
+      m[j].y = fmaf(ex2(A2[j].y * S), m[j].y, nb + 2 * j + 1 < N ? ms[2 * j + 1] : 0.f);
+    }
+  }
+}
 
 template <int N, typename T>
 __global__ void __launch_bounds__(kBwdCh) bwd_grad_kernel(const BwdArgs p) {
@@ -278,17 +276,17 @@ __global__ void __launch_bounds__(kBwdCh) bwd_grad_kernel(const BwdArgs p) {
   constexpr int NQ = (2 * NP + 3) / 4;     // groups of 4 states in the shared state rows
   const int64_t n_dtiles = (p.d_inner + kBwdCh - 1) / kBwdCh;
   const int64_t tiles = (p.L + kBwdTile - 1) / kBwdTile;
-  const int64_t ranges = (tiles + kGradTiles - 1) / kGradTiles;
   int64_t blk = blockIdx.x;
   const int64_t dtile = blk % n_dtiles;
   blk /= n_dtiles;
-  const int64_t r = blk % ranges;
-  const int64_t b = blk / ranges;
+  const int c = (int)(blk % p.n_chunks);
+  const int64_t b = blk / p.n_chunks;
   const int lane = threadIdx.x;
   const int64_t Dn = p.d_inner, L = p.L, d = dtile * kBwdCh + lane;
   const bool active = d < Dn;
   const int64_t dc = active ? d : 0;
-  const int64_t tl_lo = r * kGradTiles, tl_hi = min(tl_lo + kGradTiles, tiles) - 1;
+  const int64_t t0 = (int64_t)c * p.chunk_len, t1 = min(t0 + p.chunk_len, L);
+  const int64_t tl_lo = t0 / kBwdTile, tl_hi = (t1 - 1) / kBwdTile;  // chunks hold whole tiles
   __shared__ __align__(16) float sB[kBwdTile][4 * NQ], sC[kBwdTile][4 * NQ];
   // states after each step of the tile: [step][group of 4 states][lane][4] (16-byte rows)
   __shared__ __align__(16) float4 sH[kBwdTile][NQ][kBwdCh];
@@ -300,10 +298,9 @@ __global__ void __launch_bounds__(kBwdCh) bwd_grad_kernel(const BwdArgs p) {
     const float a0 = p.A[dc * N + n0], a1 = n1 < N ? p.A[dc * N + n1] : 0.f;
     Af[j] = make_float2(a0, a1);
     A2[j] = make_float2(a0 * kLog2e, a1 * kLog2e);
-    const float* mk = p.ckpt_m + ((b * tiles + tl_hi) * Dn + dc) * N;
-    m[j] = active ? make_float2(mk[n0], n1 < N ? mk[n1] : 0.f) : make_float2(0.f, 0.f);
     dAacc[j] = make_float2(0.f, 0.f);
   }
+  chunk_carry_in<N, NP>(p, b, dc, c, 0, A2, m);
   if (2 * NP != 4 * NQ || 2 * NP != N) {  // zero the padding columns of the B/C rows
     for (int i = lane; i < kBwdTile * 4 * NQ; i += kBwdCh) { sB[i / (4 * NQ)][i % (4 * NQ)] = 0.f; sC[i / (4 * NQ)][i % (4 * NQ)] = 0.f; }
   }
@@ -476,18 +473,18 @@ __global__ void __launch_bounds__(32) bwd_grad_kernel2(const BwdArgs p) {
   constexpr int kPitch = N + 4;    // reduction rows: N partials + padding (16-byte aligned)
   const int64_t n_dtiles = (p.d_inner + kBwdCh2 - 1) / kBwdCh2;
   const int64_t tiles = (p.L + kBwdTile - 1) / kBwdTile;
-  const int64_t ranges = (tiles + kGradTiles - 1) / kGradTiles;
   int64_t blk = blockIdx.x;
   const int64_t dtile = blk % n_dtiles;
   blk /= n_dtiles;
-  const int64_t r = blk % ranges;
-  const int64_t b = blk / ranges;
+  const int c = (int)(blk % p.n_chunks);
+  const int64_t b = blk / p.n_chunks;
   const int lane = threadIdx.x, q = lane & 1;
   const int64_t Dn = p.d_inner, L = p.L, d = dtile * kBwdCh2 + (lane >> 1);
   const bool active = d < Dn;
   const int64_t dc = active ? d : 0;
   const int nb = q * NL;  // first state of this lane
-  const int64_t tl_lo = r * kGradTiles, tl_hi = min(tl_lo + kGradTiles, tiles) - 1;
+  const int64_t t0 = (int64_t)c * p.chunk_len, t1 = min(t0 + p.chunk_len, L);
+  const int64_t tl_lo = t0 / kBwdTile, tl_hi = (t1 - 1) / kBwdTile;  // chunks hold whole tiles
   __shared__ __align__(16) float sB[kBwdTile][N], sC[kBwdTile][N];
   __shared__ __align__(16) float4 sH[kBwdTile][NQ][32];  // this lane's states after each step
   __shared__ __align__(16) float sR[32][kPitch];          // dB/dC partials, one row per lane
@@ -501,10 +498,9 @@ __global__ void __launch_bounds__(32) bwd_grad_kernel2(const BwdArgs p) {
     const float a0 = p.A[dc * N + nb + 2 * j], a1 = p.A[dc * N + nb + 2 * j + 1];
     Af[j] = make_float2(a0, a1);
     A2[j] = make_float2(a0 * kLog2e, a1 * kLog2e);
-    const float* mk = p.ckpt_m + ((b * tiles + tl_hi) * Dn + dc) * N + nb;
-    m[j] = active ? make_float2(mk[2 * j], mk[2 * j + 1]) : make_float2(0.f, 0.f);
     dAacc[j] = make_float2(0.f, 0.f);
   }
+  chunk_carry_in<N, NP>(p, b, dc, c, nb, A2, m);
   const float bias = p.delta_bias ? p.delta_bias[dc] : 0.f;
   const float Dd = p.D ? p.D[dc] : 0.f;
   float dDacc = 0.f, dbacc = 0.f;
@@ -670,30 +666,27 @@ __global__ void __launch_bounds__(32) bwd_grad_kernel2(const BwdArgs p) {
 
 size_t bwd_workspace_floats(int64_t batch, int64_t L, int64_t d_inner, int d_state, int n_chunks) {
   const int64_t tiles = (L + kBwdTile - 1) / kBwdTile;
-  const int64_t ck = batch * tiles * d_inner * d_state;                 // each checkpoint array
+  const int64_t ck = batch * tiles * d_inner * d_state;                 // forward checkpoints
   const int64_t fws = batch * (int64_t)std::max(n_chunks - 1, 0) * d_inner * (d_state + 1);
   const int64_t rws = batch * (int64_t)n_chunks * d_inner * (d_state + 1);
-  return (size_t)(2 * ck + fws + rws);
+  return (size_t)(ck + fws + rws);
 }
 
 template <int N, typename T>
 static cudaError_t launch_bwd_t(const BwdArgs& a, const ScanParams& fwd, cudaStream_t s) {
   const int64_t n_dtiles = (a.d_inner + kBwdCh - 1) / kBwdCh;
-  const int64_t tiles = (a.L + kBwdTile - 1) / kBwdTile;
   if (a.n_chunks > 1) {
     // forward chunk summaries: the forward scan's own summary pass
     cudaError_t e = launch_scan_summary(fwd, sizeof(T) == 2, s);
     if (e != cudaSuccess) return e;
-    bwd_reverse_kernel<N, T, true><<<(unsigned)(n_dtiles * (a.n_chunks - 1) * a.batch), kBwdCh, 0, s>>>(a);
+    bwd_reverse_summary_kernel<N, T><<<(unsigned)(n_dtiles * (a.n_chunks - 1) * a.batch), kBwdCh, 0, s>>>(a);
   }
   bwd_fwd_ckpt_kernel<N, T><<<(unsigned)(n_dtiles * a.n_chunks * a.batch), kBwdCh, 0, s>>>(a);
-  bwd_reverse_kernel<N, T, false><<<(unsigned)(n_dtiles * a.n_chunks * a.batch), kBwdCh, 0, s>>>(a);
-  const int64_t ranges = (tiles + kGradTiles - 1) / kGradTiles;
   if constexpr (N % 8 == 0) {  // two lanes per channel
     const int64_t n_dtiles2 = (a.d_inner + kBwdCh2 - 1) / kBwdCh2;
-    bwd_grad_kernel2<N, T><<<(unsigned)(n_dtiles2 * ranges * a.batch), 32, 0, s>>>(a);
+    bwd_grad_kernel2<N, T><<<(unsigned)(n_dtiles2 * a.n_chunks * a.batch), 32, 0, s>>>(a);
   } else {
-    bwd_grad_kernel<N, T><<<(unsigned)(n_dtiles * ranges * a.batch), kBwdCh, 0, s>>>(a);
+    bwd_grad_kernel<N, T><<<(unsigned)(n_dtiles * a.n_chunks * a.batch), kBwdCh, 0, s>>>(a);
   }
   return cudaGetLastError();
 }
