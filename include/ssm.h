@@ -209,9 +209,9 @@ SSM_API ssm_status_t ssm_state_update_conv(float* state, float* conv_state, cons
  * states are recomputed, not stored by the forward (youngju.dev, "Mamba: Linear-Time
  * Sequence Modeling with Selective State Spaces 论文分析", section "解决方案：Kernel
  * Fusion + Recomputation"): the pass keeps one state per 16 steps and per channel in the
- * workspace (ssm_scan_bwd_workspace_size bytes, about 2 * batch * L * d_inner * d_state / 4
- * bytes; not initialised by the caller).  dB and dC are accumulated with atomic additions, so
- * their last bits may vary from run to run.
+ * workspace (ssm_scan_bwd_workspace_size bytes, about batch * L * d_inner * d_state / 4
+ * bytes plus per-chunk summaries; not initialised by the caller).  dB and dC are
+ * accumulated with atomic additions, so their last bits may vary from run to run.
  */
 SSM_API size_t ssm_scan_bwd_workspace_size(int64_t batch, int64_t L, int64_t d_inner,
                                            int d_state, ssm_dtype_t io);
