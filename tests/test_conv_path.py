@@ -85,3 +85,38 @@ def test_decode_conv_reproduces_scan_conv(bf16, d_conv):
     if d_conv > 1:  # the window holds the last d_conv - 1 inputs, oldest first
         xin = to_f64(t["u"])
         np.testing.assert_array_equal(to_f64(conv_state), np.transpose(xin[:, -(d_conv - 1):, :], (0, 2, 1)))
+
+
+@pytest.mark.parametrize("key", ["mamba130m", "mamba2p8b"])
+def test_scan_conv_full_size_sampled(key):
+    """ssm_scan_fwd_conv at the bench's full sizes (the u tensor is the block input x; 4-tap
+    weights); the conv is per channel, so the oracle checks u and y on sampled channels over
+    every batch row and step, and their final states."""
+    w = W.WORKLOADS[key]
+    dev = W.device_inputs(w)
+    r = np.random.default_rng(w.seed)
+    cw = r.normal(scale=0.5, size=(w.d_inner, 4)).astype(np.float32)
+    cb = r.normal(scale=0.2, size=w.d_inner).astype(np.float32)
+    y = torch.empty_like(dev["u"])
+    u_out = torch.empty_like(dev["u"])
+    last = torch.empty((w.batch, w.d_inner, w.d_state), device="cuda")
+    io = ssm.SSM_BF16 if w.bf16 else ssm.SSM_F32
+    nb = ssm.ssm_scan_fwd_workspace_size(w.batch, w.L, w.d_inner, w.d_state, io)
+    ws = torch.empty(max(nb, 16), dtype=torch.uint8, device="cuda")
+    ssm.ssm_scan_fwd_conv(dev["u"], torch.from_numpy(cw).cuda(), torch.from_numpy(cb).cuda(), dev["delta"],
+                          dev["A"], dev["B"], dev["C"], dev["D"], dev["z"], dev["delta_bias"], True, None,
+                          y, last, u_out, ws)
+    torch.cuda.synchronize()
+    d_sel = np.unique(np.concatenate([[0, 1, 31, 32, w.d_inner - 1],
+                                      np.random.default_rng(w.seed + 1).choice(w.d_inner, 7, replace=False)]))
+    ds = torch.from_numpy(d_sel).cuda()
+    got_u, got_y = to_f64(u_out.index_select(2, ds)), to_f64(y.index_select(2, ds))
+    got_last = to_f64(last.index_select(1, ds))
+    del dev, y, u_out
+    x = W.host_scan_inputs(w, d_sel=d_sel)
+    u_ref = oracle.conv1d_silu(x["u"], cw[d_sel], cb[d_sel])
+    y_ref, last_ref = oracle.scan_fwd(u_ref, x["delta"], x["A"], x["B"], x["C"], D=x["D"], z=x["z"],
+                                      delta_bias=x["delta_bias"])
+    tol = BF16_TOL if w.bf16 else FP32_TOL
+    eu, ey, el = rel_err(got_u, u_ref), rel_err(got_y, y_ref), rel_err(got_last, last_ref)
+    assert eu <= tol and ey <= tol and el <= tol, f"u err {eu:.3g}, y err {ey:.3g}, last err {el:.3g}"
