@@ -285,6 +285,63 @@ scan_chunk_kernel_1lane(const ScanParams p) {
       *yrow = from_f32<T>(yv);
     }
   };
+  // Two steps at once for full tiles: the per-step work that does not touch the state
+  // (step size, input, skip term, gate) in packed fp32x2 arithmetic, then the recurrence for
+  // step k and step k + 1 in order.
+  auto step_pair = [&](int stage, int k, T* yrow) {
+    const float2 x = __fadd2_rn(make_float2(to_f32(sX[stage][0][k][tid]), to_f32(sX[stage][0][k + 1][tid])),
+                                make_float2(bias, bias));
+    const float2 dt = sp ? softplus2(x) : x;
+    float2 uu = make_float2(to_f32(sX[stage][1][k][tid]), to_f32(sX[stage][1][k + 1][tid]));
+    if constexpr (kConv) {
+      const float x0 = uu.x, x1 = uu.y;
+      const float2 pre = make_float2(fmaf(cw[3], x0, fmaf(cw[2], xw1, fmaf(cw[1], xw2, fmaf(cw[0], xw3, cb)))),
+                                     fmaf(cw[3], x1, fmaf(cw[2], x0, fmaf(cw[1], xw1, fmaf(cw[0], xw2, cb)))));
+      uu = silu2(pre);
+      xw3 = xw1; xw2 = x0; xw1 = x1;
+      if (!kSummary && p.u_out) {
+        T* uo = static_cast<T*>(p.u_out) + (yrow - static_cast<T*>(p.y));
+        uo[0] = from_f32<T>(uu.x);
+        uo[Dn] = from_f32<T>(uu.y);
+      }
+    }
+    const float2 w = __fmul2_rn(dt, uu);
+    float2 g = make_float2(1.f, 1.f), du = make_float2(0.f, 0.f);
+    if (!kSummary) {
+      du = __fmul2_rn(make_float2(Dd, Dd), uu);
+      if (has_z) g = silu2(make_float2(to_f32(sX[stage][kNX - 1][k][tid]), to_f32(sX[stage][kNX - 1][k + 1][tid])));
+    }
+#pragma unroll
+    for (int e = 0; e < 2; e++) {
+      const float dte = e ? dt.y : dt.x, we = e ? w.y : w.x;
+      if (kSummary) { const float yk = dte - S_comp; const float tk = S + yk; S_comp = (tk - S) - yk; S = tk; }
+      const float2 dt2 = make_float2(dte, dte), w2 = make_float2(we, we);
+      const float* Bk = sBC[stage][0][k + e];
+      const float* Ck = sBC[stage][kNBC - 1][k + e];
+      float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < NP; j++) {
+        float2 Bv, Cv;
+        if constexpr (NPAD % 4 == 0) {
+          const float4 b4 = *reinterpret_cast<const float4*>(Bk + 4 * (j / 2));
+          Bv = (j & 1) ? make_float2(b4.z, b4.w) : make_float2(b4.x, b4.y);
+          if (!kSummary) { const float4 c4 = *reinterpret_cast<const float4*>(Ck + 4 * (j / 2)); Cv = (j & 1) ? make_float2(c4.z, c4.w) : make_float2(c4.x, c4.y); }
+        } else {
+          Bv = *reinterpret_cast<const float2*>(Bk + 2 * j);
+          if (!kSummary) Cv = *reinterpret_cast<const float2*>(Ck + 2 * j);
+        }
+        const float2 xa = __fmul2_rn(dt2, A2[j]);
+        const float2 dA = make_float2(ex2(xa.x), ex2(xa.y));
+        h[j] = __ffma2_rn(dA, h[j], __fmul2_rn(w2, Bv));
+        if (!kSummary) { if (j & 1) acc1 = __ffma2_rn(Cv, h[j], acc1); else acc0 = __ffma2_rn(Cv, h[j], acc0); }
+      }
+      if (!kSummary) {
+        const float2 a = __fadd2_rn(acc0, acc1);
+        const float yv = ((e ? du.y : du.x) + (a.x + a.y)) * (e ? g.y : g.x);
+        yrow[e * Dn] = from_f32<T>(yv);
+      }
+    }
+  };
   for (int tile = 0; tile < ntiles; tile++) {
     const int stage = tile & 1;
     if (tile + 1 < ntiles) { issue_x(tile + 1, stage ^ 1); load_bc(tile + 1); }
@@ -296,7 +353,7 @@ scan_chunk_kernel_1lane(const ScanParams p) {
     if (active) {
       if (ts + kScanTile <= t1) {
 #pragma unroll
-        for (int k = 0; k < kScanTile; k++) step(stage, k, yrow + k * Dn);
+        for (int k = 0; k < kScanTile; k += 2) step_pair(stage, k, yrow + k * Dn);
       } else {
         const int steps = (int)(t1 - ts);
         for (int k = 0; k < steps; k++) step(stage, k, yrow + k * Dn);
@@ -658,6 +715,7 @@ void plan_scan(int64_t batch, int64_t L, int64_t d_inner, int sms, ScanPlan* pla
   const int64_t full = (int64_t)sms * env_int("SSM_SCAN_THREADS_PER_SM", 1024);
   int64_t G = 1;
   if (threads > 0 && threads < (int64_t)sms * 256) G = (full + threads - 1) / threads;
+  G = env_int("SSM_SCAN_CHUNKS", G);  // tuning override
   G = std::min<int64_t>(G, std::max<int64_t>(1, L / 64));
   G = std::min<int64_t>(G, 4096);
   int64_t len = L > 0 ? (L + G - 1) / G : 1;
