@@ -33,6 +33,19 @@ __device__ __forceinline__ float ldf(const void* p, int64_t i) {
   return to_f32(static_cast<const T*>(p)[i]);
 }
 
+// Step sizes of a tile, two at a time in packed fp32x2: dt_k = softplus(x_k + bias) (or
+// x_k + bias without softplus).
+__device__ __forceinline__ void tile_step_sizes(const float (&x)[kBwdTile], float bias, bool sp,
+                                                float (&dt)[kBwdTile]) {
+#pragma unroll
+  for (int k = 0; k < kBwdTile; k += 2) {
+    const float2 v = __fadd2_rn(make_float2(x[k], x[k + 1]), make_float2(bias, bias));
+    const float2 d = sp ? softplus2(v) : v;
+    dt[k] = d.x;
+    dt[k + 1] = d.y;
+  }
+}
+
 // ---------------------------------------------------------------------------------------
 // 1. Forward checkpoints: chunk c folds the forward summaries of chunks < c into its start
 //    state (from the initial state), then runs the recurrence over its tiles, storing the
@@ -104,11 +117,12 @@ __global__ void __launch_bounds__(kBwdCh) bwd_fwd_ckpt_kernel(const BwdArgs p) {
     __syncwarp();
     for (int i = lane; i < steps * N; i += kBwdCh) sB[i / N][i % N] = ldf<T>(p.B, (b * L + ts) * N + i);
     __syncwarp();
+    float dts[kBwdTile];
+    tile_step_sizes(xr, bias, p.softplus != 0, dts);
 #pragma unroll
     for (int k = 0; k < kBwdTile; k++) {
       if (k < steps) {
-        const float x = xr[k] + bias;
-        const float dt = p.softplus ? softplus(x) : x;
+        const float dt = dts[k];
         const float w = dt * ur[k];
         const float2 dt2 = make_float2(dt, dt), w2 = make_float2(w, w);
 #pragma unroll
@@ -185,11 +199,12 @@ __global__ void __launch_bounds__(kBwdCh) bwd_reverse_summary_kernel(const BwdAr
     __syncwarp();
     for (int i = lane; i < steps * N; i += kBwdCh) sC[i / N][i % N] = ldf<T>(p.C, (b * L + ts) * N + i);
     __syncwarp();
+    float dts[kBwdTile];
+    tile_step_sizes(xr, bias, p.softplus != 0, dts);
 #pragma unroll
     for (int k = kBwdTile - 1; k >= 0; k--) {
       if (k < steps) {
-        const float x = xr[k] + bias;
-        const float dt = p.softplus ? softplus(x) : x;
+        const float dt = dts[k];
         if (kSummary) {
           const float yk = dt - S_comp;
           const float tk = S + yk;
@@ -341,8 +356,7 @@ __global__ void __launch_bounds__(kBwdCh) bwd_grad_kernel(const BwdArgs p) {
     }
     __syncwarp();
     float dts[kBwdTile];
-#pragma unroll
-    for (int k = 0; k < kBwdTile; k++) dts[k] = p.softplus ? softplus(xs[k]) : xs[k];
+    tile_step_sizes(xs, 0.f, p.softplus != 0, dts);  // xs hold delta_raw + bias
 
     // forward recompute of the tile's states into shared memory
     {
@@ -537,8 +551,7 @@ __global__ void __launch_bounds__(32) bwd_grad_kernel2(const BwdArgs p) {
     }
     __syncwarp();
     float dts[kBwdTile];
-#pragma unroll
-    for (int k = 0; k < kBwdTile; k++) dts[k] = p.softplus ? softplus(xs[k]) : xs[k];
+    tile_step_sizes(xs, 0.f, p.softplus != 0, dts);  // xs hold delta_raw + bias
 
     // forward recompute of this lane's states over the tile into shared memory
     {
