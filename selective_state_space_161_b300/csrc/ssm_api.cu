@@ -122,7 +122,6 @@ ssm_status_t scan_fwd_impl(const void* u, const void* delta, const float* A, con
   p.delta_bias = delta_bias; p.softplus = softplus_flag != 0; p.y = y; p.last_state = last_state;
   p.initial_state = initial_state;
   p.conv_w = ex.conv_w; p.conv_b = ex.conv_b; p.d_conv = ex.d_conv; p.u_out = ex.u_out;
-  if (p.conv_w != nullptr) p.lanes = 1;  // the conv path exists in the one-lane kernel only
   p.batch = batch; p.L = L; p.d_inner = d_inner; p.d_state = d_state;
   if (p.n_chunks > 1) {
     p.ws_S = static_cast<float*>(workspace);

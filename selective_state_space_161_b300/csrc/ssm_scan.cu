@@ -389,7 +389,7 @@ scan_chunk_kernel_1lane(const ScanParams p) {
 // of use; the next tile's B/C rows are fetched into registers while the current
 // tile is computed and converted to fp32 in shared memory.  So no step waits on
 // HBM latency.  State pairs are updated with packed fp32x2 instructions.
-template <int N, typename T, bool kSummary>
+template <int N, typename T, bool kSummary, bool kConv>
 __global__ void __launch_bounds__(kScanThreads)
 scan_chunk_kernel_2lane(const ScanParams p) {
   using SS = StateSplit<N>;
@@ -532,6 +532,22 @@ scan_chunk_kernel_2lane(const ScanParams p) {
   const float Dd = (active && p.D) ? p.D[d] : 0.f;
   const float bias = (active && p.delta_bias) ? p.delta_bias[d] : 0.f;
   const bool sp = p.softplus != 0;
+  // Causal conv1d window (kConv): the 4-tap weights (tap j multiplies x[t-3+j]; shorter
+  // kernels get leading zero taps) and x at the three steps before the current tile.
+  float cw[4] = {0.f, 0.f, 0.f, 0.f}, cb = 0.f, xh1 = 0.f, xh2 = 0.f, xh3 = 0.f;
+  if constexpr (kConv) {
+    if (active) {
+      const int K = p.d_conv;
+#pragma unroll
+      for (int j = 0; j < 4; j++)
+        if (j >= 4 - K) cw[j] = p.conv_w[d * K + j - (4 - K)];
+      cb = p.conv_b ? p.conv_b[d] : 0.f;
+      const T* xg = static_cast<const T*>(p.u);
+      if (t0 >= 1) xh1 = to_f32(xg[(b * L + t0 - 1) * Dn + d]);
+      if (t0 >= 2) xh2 = to_f32(xg[(b * L + t0 - 2) * Dn + d]);
+      if (t0 >= 3) xh3 = to_f32(xg[(b * L + t0 - 3) * Dn + d]);
+    }
+  }
 
   if (ntiles > 0) {
     issue_x(0, 0);
@@ -579,7 +595,22 @@ scan_chunk_kernel_2lane(const ScanParams p) {
       const float2 x = __fadd2_rn(make_float2(to_f32(sX[stage][0][k0][cl]), to_f32(sX[stage][0][k1][cl])),
                                   make_float2(bias, bias));
       const float2 dt = sp ? softplus2(x) : x;
-      const float2 uu = make_float2(to_f32(sX[stage][1][k0][cl]), to_f32(sX[stage][1][k1][cl]));
+      float2 uu = make_float2(to_f32(sX[stage][1][k0][cl]), to_f32(sX[stage][1][k1][cl]));
+      if constexpr (kConv) {
+        // x before the tile comes from the window carried in registers
+        auto xv = [&](int k) -> float {
+          return k >= 0 ? to_f32(sX[stage][1][k][cl]) : (k == -1 ? xh1 : (k == -2 ? xh2 : xh3));
+        };
+        const float2 pre = make_float2(
+            fmaf(cw[3], uu.x, fmaf(cw[2], xv(k0 - 1), fmaf(cw[1], xv(k0 - 2), fmaf(cw[0], xv(k0 - 3), cb)))),
+            fmaf(cw[3], uu.y, fmaf(cw[2], xv(k1 - 1), fmaf(cw[1], xv(k1 - 2), fmaf(cw[0], xv(k1 - 3), cb)))));
+        uu = silu2(pre);
+        if (!kSummary && p.u_out && active) {
+          T* uo = static_cast<T*>(p.u_out) + (b * L + ts) * Dn + d;
+          if (k0 < steps) uo[(int64_t)k0 * Dn] = from_f32<T>(uu.x);
+          if (k1 < steps) uo[(int64_t)k1 * Dn] = from_f32<T>(uu.y);
+        }
+      }
       const float2 w = __fmul2_rn(dt, uu);
       odt[i] = dt.x; odt[i + 1] = dt.y;
       ow[i] = w.x; ow[i + 1] = w.y;
@@ -665,6 +696,11 @@ scan_chunk_kernel_2lane(const ScanParams p) {
         if (has_z) v *= og[i];
         if (active && 2 * i + par < steps) yrow[(int64_t)2 * i * Dn] = from_f32<T>(v);
       }
+    }
+    if constexpr (kConv) {  // the window for the next tile: this tile's last three inputs
+      xh1 = to_f32(sX[stage][1][kScanTile - 1][cl]);
+      xh2 = to_f32(sX[stage][1][kScanTile - 2][cl]);
+      xh3 = to_f32(sX[stage][1][kScanTile - 3][cl]);
     }
     __syncthreads();  // stage is free for the tile after next
     if (tile + 1 < ntiles) store_bc(stage ^ 1);
@@ -754,13 +790,18 @@ static cudaError_t launch_scan_t(const ScanParams& p, cudaStream_t stream) {
   const int64_t n_dtiles = (p.d_inner + kScanCh - 1) / kScanCh;
   const int64_t sblocks = n_dtiles * (p.n_chunks - 1) * p.batch;
   const int64_t mblocks = n_dtiles * p.n_chunks * p.batch;
-  if (p.conv_w != nullptr) {  // conv1d + SiLU in front: one-lane kernel only
+  if (p.conv_w != nullptr) {  // conv1d + SiLU in front
+    if (p.lanes == 2)
+      return launch_passes(scan_chunk_kernel_2lane<N, T, true, true>,
+                           scan_chunk_kernel_2lane<N, T, false, true>, p, kScanThreads, sblocks,
+                           mblocks, stream);
     return launch_passes(scan_chunk_kernel_1lane<N, T, true, true>,
                          scan_chunk_kernel_1lane<N, T, false, true>, p, kScanCh, sblocks, mblocks,
                          stream);
   } else if (p.lanes == 2) {
-    return launch_passes(scan_chunk_kernel_2lane<N, T, true>, scan_chunk_kernel_2lane<N, T, false>,
-                         p, kScanThreads, sblocks, mblocks, stream);
+    return launch_passes(scan_chunk_kernel_2lane<N, T, true, false>,
+                         scan_chunk_kernel_2lane<N, T, false, false>, p, kScanThreads, sblocks,
+                         mblocks, stream);
   }
   return launch_passes(scan_chunk_kernel_1lane<N, T, true, false>,
                        scan_chunk_kernel_1lane<N, T, false, false>, p, kScanCh, sblocks, mblocks,
