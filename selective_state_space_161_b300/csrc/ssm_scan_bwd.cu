@@ -479,7 +479,7 @@ __global__ void __launch_bounds__(kBwdCh) bwd_grad_kernel(const BwdArgs p) {
 constexpr int kBwdCh2 = 16;  // channels per CTA of the two-lane gradient kernel
 
 template <int N, typename T>
-__global__ void __launch_bounds__(32) bwd_grad_kernel2(const BwdArgs p) {
+__global__ void __launch_bounds__(32, 10) bwd_grad_kernel2(const BwdArgs p) {
   static_assert(N % 8 == 0 && N <= 16, "two lanes of whole float4 state groups");
   constexpr int NL = N / 2;        // states per lane
   constexpr int NP = NL / 2;       // state pairs per lane (packed fp32x2 arithmetic)
