@@ -88,10 +88,11 @@ __global__ void __launch_bounds__(kBwdCh) bwd_fwd_ckpt_kernel(const BwdArgs p) {
       h[q].y = fmaf(ex2(A2[q].y * S), h[q].y, 2 * q + 1 < N ? hs[2 * q + 1] : 0.f);
     }
   }
-  // A tile's activations are loaded into registers all at once (16 independent loads per
-  // tensor), and the next tile's are requested before the current one is computed.
-  float xr[kBwdTile], ur[kBwdTile];
-  auto load_tile = [&](int64_t ts, float* xa, float* ua) {
+  // A tile's activations and B rows are loaded into registers all at once (independent
+  // loads), and the next tile's are requested before the current one is computed.
+  constexpr int kBPL = (kBwdTile * N + kBwdCh - 1) / kBwdCh;  // B values per lane per tile
+  float xr[kBwdTile], ur[kBwdTile], br[kBPL];
+  auto load_tile = [&](int64_t ts, float* xa, float* ua, float* ba) {
     const int steps = (int)min((int64_t)kBwdTile, t1 - ts);
 #pragma unroll
     for (int k = 0; k < kBwdTile; k++) {
@@ -99,13 +100,18 @@ __global__ void __launch_bounds__(kBwdCh) bwd_fwd_ckpt_kernel(const BwdArgs p) {
       xa[k] = ldf<T>(p.delta, e);
       ua[k] = ldf<T>(p.u, e);
     }
+#pragma unroll
+    for (int r = 0; r < kBPL; r++) {
+      const int i = lane + r * kBwdCh;
+      ba[r] = i < steps * N ? ldf<T>(p.B, (b * L + ts) * N + i) : 0.f;
+    }
   };
-  if (t0 < t1) load_tile(t0, xr, ur);
+  if (t0 < t1) load_tile(t0, xr, ur, br);
   for (int64_t ts = t0; ts < t1; ts += kBwdTile) {
     const int steps = (int)min((int64_t)kBwdTile, t1 - ts);
-    float xn[kBwdTile], un[kBwdTile];
+    float xn[kBwdTile], un[kBwdTile], bn[kBPL];
     const bool more = ts + kBwdTile < t1;
-    if (more) load_tile(ts + kBwdTile, xn, un);
+    if (more) load_tile(ts + kBwdTile, xn, un, bn);
     if (active) {
       float* ck = p.ckpt_h + ((b * tiles + ts / kBwdTile) * Dn + d) * N;
 #pragma unroll
@@ -115,7 +121,11 @@ __global__ void __launch_bounds__(kBwdCh) bwd_fwd_ckpt_kernel(const BwdArgs p) {
       }
     }
     __syncwarp();
-    for (int i = lane; i < steps * N; i += kBwdCh) sB[i / N][i % N] = ldf<T>(p.B, (b * L + ts) * N + i);
+#pragma unroll
+    for (int r = 0; r < kBPL; r++) {
+      const int i = lane + r * kBwdCh;
+      if (i < kBwdTile * N) sB[i / N][i % N] = br[r];
+    }
     __syncwarp();
     float dts[kBwdTile];
     tile_step_sizes(xr, bias, p.softplus != 0, dts);
@@ -137,6 +147,8 @@ __global__ void __launch_bounds__(kBwdCh) bwd_fwd_ckpt_kernel(const BwdArgs p) {
     if (more) {
 #pragma unroll
       for (int k = 0; k < kBwdTile; k++) { xr[k] = xn[k]; ur[k] = un[k]; }
+#pragma unroll
+      for (int r = 0; r < kBPL; r++) br[r] = bn[r];
     }
   }
 }
