@@ -120,3 +120,30 @@ def test_scan_conv_full_size_sampled(key):
     tol = BF16_TOL if w.bf16 else FP32_TOL
     eu, ey, el = rel_err(got_u, u_ref), rel_err(got_y, y_ref), rel_err(got_last, last_ref)
     assert eu <= tol and ey <= tol and el <= tol, f"u err {eu:.3g}, y err {ey:.3g}, last err {el:.3g}"
+
+
+@pytest.mark.parametrize("lanes", ["1", "2"])
+@pytest.mark.parametrize("bf16,batch,L,d_inner,d_state,d_conv", [
+    (False, 2, 3000, 96, 16, 4), (True, 1, 4100, 64, 16, 3), (False, 3, 700, 40, 5, 4)])
+def test_scan_conv_both_kernels_from_state(lanes, bf16, batch, L, d_inner, d_state, d_conv, monkeypatch):
+    """The conv path in both kernels (one or two lanes per channel), over many ragged time
+    chunks (each chunk after the first starts its window from the inputs before it), from a
+    given initial state."""
+    monkeypatch.setenv("SSM_SCAN_LANES", lanes)
+    w, raw, cw, cb = _case(batch, L, d_inner, d_state, bf16, d_conv, seed=800 + L + int(lanes))
+    h0 = np.random.default_rng(L).normal(scale=0.3, size=(batch, d_inner, d_state)).astype(np.float32)
+    t = {k: to_torch(v, bf16 and k in ("u", "delta", "z", "B", "C")) for k, v in raw.items()}
+    y = torch.empty_like(t["u"])
+    u_out = torch.empty_like(t["u"])
+    last = torch.empty((batch, d_inner, d_state), device="cuda")
+    io = ssm.SSM_BF16 if bf16 else ssm.SSM_F32
+    nb = ssm.ssm_scan_fwd_workspace_size(batch, L, d_inner, d_state, io)
+    ws = torch.empty(max(nb, 16), dtype=torch.uint8, device="cuda")
+    ssm.ssm_scan_fwd_conv(t["u"], torch.from_numpy(cw).cuda(), torch.from_numpy(cb).cuda(), t["delta"], t["A"],
+                          t["B"], t["C"], t["D"], t["z"], t["delta_bias"], True, torch.from_numpy(h0).cuda(),
+                          y, last, u_out, ws)
+    torch.cuda.synchronize()
+    u_ref, y_ref, last_ref = _oracle(w, raw, cw, cb, h0=h0.astype(np.float64))
+    tol = BF16_TOL if bf16 else FP32_TOL
+    eu, ey, el = rel_err(to_f64(u_out), u_ref), rel_err(to_f64(y), y_ref), rel_err(to_f64(last), last_ref)
+    assert eu <= tol and ey <= tol and el <= tol, f"u err {eu:.3g}, y err {ey:.3g}, last err {el:.3g}"
