@@ -331,6 +331,7 @@ ssm_status_t ssm_scan_bwd(const void* u, const void* delta, const float* A, cons
   f.u = u; f.delta = delta; f.A = A; f.B = B; f.C = C; f.delta_bias = delta_bias;
   f.softplus = softplus_flag != 0; f.batch = batch; f.L = L; f.d_inner = d_inner;
   f.d_state = d_state; f.chunk_len = plan.chunk_len; f.n_chunks = plan.n_chunks; f.lanes = 1;
+  f.initial_state = initial_state;
   f.ws_S = fS;
   f.ws_h = fS + fws;
   return ssm::launch_scan_bwd(a, f, io == SSM_BF16, s) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;

@@ -37,6 +37,7 @@ struct ScanParams {
   int lanes;  // 1 or 2 lanes per channel (which kernel runs)
   float* ws_S;  // [batch][n_chunks-1][d_inner]
   float* ws_h;  // [batch][n_chunks-1][d_inner][d_state]
+  float* ckpt_h = nullptr;  // checkpoint pass only: [batch][ceil(L/16)][d_inner][d_state]
 };
 
 struct DecodeParams {
@@ -130,6 +131,9 @@ void plan_scan(int64_t batch, int64_t L, int64_t d_inner, int sms, ScanPlan* pla
 cudaError_t launch_scan(const ScanParams& p, bool bf16, cudaStream_t stream);
 // Only the forward summary pass (one lane per channel) of a chunked scan plan.
 cudaError_t launch_scan_summary(const ScanParams& p, bool bf16, cudaStream_t stream);
+// The main pass's states from initial_state and the chunk summaries, with no output: the state
+// before every 16-step tile into p.ckpt_h (one lane per channel).
+cudaError_t launch_scan_ckpt(const ScanParams& p, bool bf16, cudaStream_t stream);
 // Floats of scratch the backward pass needs for n_chunks time chunks.
 size_t bwd_workspace_floats(int64_t batch, int64_t L, int64_t d_inner, int d_state, int n_chunks);
 cudaError_t launch_scan_bwd(const BwdArgs& a, const ScanParams& fwd, bool bf16, cudaStream_t s);

@@ -88,16 +88,19 @@ __device__ __forceinline__ void allow_main_pass() { asm volatile("griddepcontrol
 
 // One lane per channel: a 32-thread CTA covers kScanCh channels of one batch row over one
 // time chunk; each thread keeps all of its channel's states (as fp32 pairs) in registers.
-template <int N, typename T, bool kSummary, bool kConv>
+template <int N, typename T, bool kSummary, bool kConv, bool kCkpt>
 __global__ void __launch_bounds__(kScanCh)
 scan_chunk_kernel_1lane(const ScanParams p) {
+  // kCkpt: the main pass's true states without any output, storing the state before every
+  // tile of kScanTile steps into p.ckpt_h (the checkpoints of the training backward).
+  constexpr bool kOut = !kSummary && !kCkpt;
   constexpr int kS = sizeof(T);
   constexpr int kVec = 16 / kS;
   constexpr int kCPR = kScanCh / kVec;
   constexpr int kRowsPerPass = kScanCh / kCPR;
   constexpr int kPasses = kScanTile / kRowsPerPass;
-  constexpr int kNX = kSummary ? 2 : 3;
-  constexpr int kNBC = kSummary ? 1 : 2;
+  constexpr int kNX = kOut ? 3 : 2;
+  constexpr int kNBC = kOut ? 2 : 1;
   constexpr int NP = (N + 1) / 2;
   constexpr int NPAD = 2 * NP;
   constexpr bool kVecBC = (N * kS) % 16 == 0;
@@ -124,8 +127,8 @@ scan_chunk_kernel_1lane(const ScanParams p) {
   const int ntiles = (int)((t1 - t0 + kScanTile - 1) / kScanTile);
   const T* __restrict__ Bg = static_cast<const T*>(p.B);
   const T* __restrict__ Cg = static_cast<const T*>(p.C);
-  const bool has_z = !kSummary && p.z != nullptr;
-  const int nx = kSummary ? 2 : (has_z ? 3 : 2);
+  const bool has_z = kOut && p.z != nullptr;
+  const int nx = kOut ? (has_z ? 3 : 2) : 2;
   const int ci = tid % kCPR, rb = tid / kCPR;
   const bool dvalid = d0 + (int64_t)ci * kVec < Dn;
   const int64_t row_bytes = Dn * kS;
@@ -254,7 +257,7 @@ scan_chunk_kernel_1lane(const ScanParams p) {
       uu = silu(fmaf(cw[3], xt, fmaf(cw[2], xw1, fmaf(cw[1], xw2, fmaf(cw[0], xw3, cb)))));
       xw3 = xw2; xw2 = xw1; xw1 = xt;
       // u_out has y's layout: the same flat element index as this step's y
-      if (!kSummary && p.u_out) static_cast<T*>(p.u_out)[yrow - static_cast<T*>(p.y)] = from_f32<T>(uu);
+      if (kOut && p.u_out) static_cast<T*>(p.u_out)[yrow - static_cast<T*>(p.y)] = from_f32<T>(uu);
     }
     const float w = dt * uu;
     if (kSummary) { const float yk = dt - S_comp; const float tk = S + yk; S_comp = (tk - S) - yk; S = tk; }
@@ -268,17 +271,17 @@ scan_chunk_kernel_1lane(const ScanParams p) {
       if constexpr (NPAD % 4 == 0) {
         const float4 b4 = *reinterpret_cast<const float4*>(Bk + 4 * (j / 2));
         Bv = (j & 1) ? make_float2(b4.z, b4.w) : make_float2(b4.x, b4.y);
-        if (!kSummary) { const float4 c4 = *reinterpret_cast<const float4*>(Ck + 4 * (j / 2)); Cv = (j & 1) ? make_float2(c4.z, c4.w) : make_float2(c4.x, c4.y); }
+        if (kOut) { const float4 c4 = *reinterpret_cast<const float4*>(Ck + 4 * (j / 2)); Cv = (j & 1) ? make_float2(c4.z, c4.w) : make_float2(c4.x, c4.y); }
       } else {
         Bv = *reinterpret_cast<const float2*>(Bk + 2 * j);
-        if (!kSummary) Cv = *reinterpret_cast<const float2*>(Ck + 2 * j);
+        if (kOut) Cv = *reinterpret_cast<const float2*>(Ck + 2 * j);
       }
       const float2 xa = __fmul2_rn(dt2, A2[j]);
       const float2 dA = make_float2(ex2(xa.x), ex2(xa.y));
       h[j] = __ffma2_rn(dA, h[j], __fmul2_rn(w2, Bv));
-      if (!kSummary) { if (j & 1) acc1 = __ffma2_rn(Cv, h[j], acc1); else acc0 = __ffma2_rn(Cv, h[j], acc0); }
+      if (kOut) { if (j & 1) acc1 = __ffma2_rn(Cv, h[j], acc1); else acc0 = __ffma2_rn(Cv, h[j], acc0); }
     }
-    if (!kSummary) {
+    if (kOut) {
       const float2 a = __fadd2_rn(acc0, acc1);
       float yv = fmaf(Dd, uu, a.x + a.y);
       if (has_z) yv *= silu(to_f32(sX[stage][kNX - 1][k][tid]));
@@ -299,7 +302,7 @@ scan_chunk_kernel_1lane(const ScanParams p) {
                                      fmaf(cw[3], x1, fmaf(cw[2], x0, fmaf(cw[1], xw1, fmaf(cw[0], xw2, cb)))));
       uu = silu2(pre);
       xw3 = xw1; xw2 = x0; xw1 = x1;
-      if (!kSummary && p.u_out) {
+      if (kOut && p.u_out) {
         T* uo = static_cast<T*>(p.u_out) + (yrow - static_cast<T*>(p.y));
         uo[0] = from_f32<T>(uu.x);
         uo[Dn] = from_f32<T>(uu.y);
@@ -307,7 +310,7 @@ scan_chunk_kernel_1lane(const ScanParams p) {
     }
     const float2 w = __fmul2_rn(dt, uu);
     float2 g = make_float2(1.f, 1.f), du = make_float2(0.f, 0.f);
-    if (!kSummary) {
+    if (kOut) {
       du = __fmul2_rn(make_float2(Dd, Dd), uu);
       if (has_z) g = silu2(make_float2(to_f32(sX[stage][kNX - 1][k][tid]), to_f32(sX[stage][kNX - 1][k + 1][tid])));
     }
@@ -325,17 +328,17 @@ scan_chunk_kernel_1lane(const ScanParams p) {
         if constexpr (NPAD % 4 == 0) {
           const float4 b4 = *reinterpret_cast<const float4*>(Bk + 4 * (j / 2));
           Bv = (j & 1) ? make_float2(b4.z, b4.w) : make_float2(b4.x, b4.y);
-          if (!kSummary) { const float4 c4 = *reinterpret_cast<const float4*>(Ck + 4 * (j / 2)); Cv = (j & 1) ? make_float2(c4.z, c4.w) : make_float2(c4.x, c4.y); }
+          if (kOut) { const float4 c4 = *reinterpret_cast<const float4*>(Ck + 4 * (j / 2)); Cv = (j & 1) ? make_float2(c4.z, c4.w) : make_float2(c4.x, c4.y); }
         } else {
           Bv = *reinterpret_cast<const float2*>(Bk + 2 * j);
-          if (!kSummary) Cv = *reinterpret_cast<const float2*>(Ck + 2 * j);
+          if (kOut) Cv = *reinterpret_cast<const float2*>(Ck + 2 * j);
         }
         const float2 xa = __fmul2_rn(dt2, A2[j]);
         const float2 dA = make_float2(ex2(xa.x), ex2(xa.y));
         h[j] = __ffma2_rn(dA, h[j], __fmul2_rn(w2, Bv));
-        if (!kSummary) { if (j & 1) acc1 = __ffma2_rn(Cv, h[j], acc1); else acc0 = __ffma2_rn(Cv, h[j], acc0); }
+        if (kOut) { if (j & 1) acc1 = __ffma2_rn(Cv, h[j], acc1); else acc0 = __ffma2_rn(Cv, h[j], acc0); }
       }
-      if (!kSummary) {
+      if (kOut) {
         const float2 a = __fadd2_rn(acc0, acc1);
         const float yv = ((e ? du.y : du.x) + (a.x + a.y)) * (e ? g.y : g.x);
         yrow[e * Dn] = from_f32<T>(yv);
@@ -349,7 +352,20 @@ scan_chunk_kernel_1lane(const ScanParams p) {
     cp_async_wait_prev();
     __syncthreads();
     const int64_t ts = t0 + (int64_t)tile * kScanTile;
-    T* yrow = yg + (b * L + ts) * Dn + d;
+    T* yrow = kOut ? yg + (b * L + ts) * Dn + d : nullptr;
+    if constexpr (kCkpt) {  // the state before this tile (chunks start on tile boundaries)
+      if (active) {
+        float* ck = p.ckpt_h + ((b * ((L + kScanTile - 1) / kScanTile) + ts / kScanTile) * Dn + d) * N;
+        if constexpr (N % 4 == 0) {  // whole 16-byte pieces (a channel's row is 16-byte aligned)
+#pragma unroll
+          for (int j = 0; j < NP; j += 2)
+            *reinterpret_cast<float4*>(ck + 2 * j) = make_float4(h[j].x, h[j].y, h[j + 1].x, h[j + 1].y);
+        } else {
+#pragma unroll
+          for (int j = 0; j < NP; j++) { ck[2 * j] = h[j].x; if (2 * j + 1 < N) ck[2 * j + 1] = h[j].y; }
+        }
+      }
+    }
     if (active) {
       if (ts + kScanTile <= t1) {
 #pragma unroll
@@ -369,7 +385,7 @@ scan_chunk_kernel_1lane(const ScanParams p) {
 #pragma unroll
     for (int j = 0; j < NP; j++) { p.ws_h[slot * N + 2 * j] = h[j].x; if (2 * j + 1 < N) p.ws_h[slot * N + 2 * j + 1] = h[j].y; }
     allow_main_pass();
-  } else if (c == p.n_chunks - 1 && p.last_state) {
+  } else if (kOut && c == p.n_chunks - 1 && p.last_state) {
     float* ls = p.last_state + (b * Dn + d) * N;
 #pragma unroll
     for (int j = 0; j < NP; j++) { ls[2 * j] = h[j].x; if (2 * j + 1 < N) ls[2 * j + 1] = h[j].y; }
@@ -795,16 +811,16 @@ static cudaError_t launch_scan_t(const ScanParams& p, cudaStream_t stream) {
       return launch_passes(scan_chunk_kernel_2lane<N, T, true, true>,
                            scan_chunk_kernel_2lane<N, T, false, true>, p, kScanThreads, sblocks,
                            mblocks, stream);
-    return launch_passes(scan_chunk_kernel_1lane<N, T, true, true>,
-                         scan_chunk_kernel_1lane<N, T, false, true>, p, kScanCh, sblocks, mblocks,
+    return launch_passes(scan_chunk_kernel_1lane<N, T, true, true, false>,
+                         scan_chunk_kernel_1lane<N, T, false, true, false>, p, kScanCh, sblocks, mblocks,
                          stream);
   } else if (p.lanes == 2) {
     return launch_passes(scan_chunk_kernel_2lane<N, T, true, false>,
                          scan_chunk_kernel_2lane<N, T, false, false>, p, kScanThreads, sblocks,
                          mblocks, stream);
   }
-  return launch_passes(scan_chunk_kernel_1lane<N, T, true, false>,
-                       scan_chunk_kernel_1lane<N, T, false, false>, p, kScanCh, sblocks, mblocks,
+  return launch_passes(scan_chunk_kernel_1lane<N, T, true, false, false>,
+                       scan_chunk_kernel_1lane<N, T, false, false, false>, p, kScanCh, sblocks, mblocks,
                        stream);
 }
 
@@ -836,7 +852,7 @@ static cudaError_t summary_only(const ScanParams& p, cudaStream_t s) {
   const int64_t blocks = (p.d_inner + kScanCh - 1) / kScanCh * (p.n_chunks - 1) * p.batch;
   switch (p.d_state) {
 #define SSM_SUMMARY_CASE(NN) \
-    case NN: scan_chunk_kernel_1lane<NN, T, true, false><<<(unsigned)blocks, kScanCh, 0, s>>>(p); break;
+    case NN: scan_chunk_kernel_1lane<NN, T, true, false, false><<<(unsigned)blocks, kScanCh, 0, s>>>(p); break;
     SSM_SUMMARY_CASE(1) SSM_SUMMARY_CASE(2) SSM_SUMMARY_CASE(3) SSM_SUMMARY_CASE(4)
     SSM_SUMMARY_CASE(5) SSM_SUMMARY_CASE(6) SSM_SUMMARY_CASE(7) SSM_SUMMARY_CASE(8)
     SSM_SUMMARY_CASE(9) SSM_SUMMARY_CASE(10) SSM_SUMMARY_CASE(11) SSM_SUMMARY_CASE(12)
@@ -845,6 +861,26 @@ static cudaError_t summary_only(const ScanParams& p, cudaStream_t s) {
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t ckpt_only(const ScanParams& p, cudaStream_t s) {
+  const int64_t blocks = (p.d_inner + kScanCh - 1) / kScanCh * p.n_chunks * p.batch;
+  switch (p.d_state) {
+#define SSM_CKPT_CASE(NN) \
+    case NN: scan_chunk_kernel_1lane<NN, T, false, false, true><<<(unsigned)blocks, kScanCh, 0, s>>>(p); break;
+    SSM_CKPT_CASE(1) SSM_CKPT_CASE(2) SSM_CKPT_CASE(3) SSM_CKPT_CASE(4)
+    SSM_CKPT_CASE(5) SSM_CKPT_CASE(6) SSM_CKPT_CASE(7) SSM_CKPT_CASE(8)
+    SSM_CKPT_CASE(9) SSM_CKPT_CASE(10) SSM_CKPT_CASE(11) SSM_CKPT_CASE(12)
+    SSM_CKPT_CASE(13) SSM_CKPT_CASE(14) SSM_CKPT_CASE(15) SSM_CKPT_CASE(16)
+#undef SSM_CKPT_CASE
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scan_ckpt(const ScanParams& p, bool bf16, cudaStream_t stream) {
+  return bf16 ? ckpt_only<__nv_bfloat16>(p, stream) : ckpt_only<float>(p, stream);
 }
 
 cudaError_t launch_scan_summary(const ScanParams& p, bool bf16, cudaStream_t stream) {

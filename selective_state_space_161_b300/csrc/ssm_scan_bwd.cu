@@ -4,9 +4,9 @@
 // The pages describe the backward only as "recompute the intermediate states in the backward
 // pass instead of storing them" (youngju.dev, "Mamba: Linear-Time Sequence Modeling with
 // Selective State Spaces 论文分析", section "解决方案：Kernel Fusion + Recomputation").  Here:
-//  1. forward checkpoints: the forward recurrence (time-chunked exactly like the forward
-//     scan: the forward summary kernel, then the checkpoint kernel below) stores the state
-//     before every 16-step tile — one state per 16 steps, never the per-step states;
+//  1. forward checkpoints: the forward scan's own kernels (its summary pass, then its
+//     one-lane kernel in checkpoint mode) store the state before every 16-step tile — one
+//     state per 16 steps, never the per-step states;
 //  2. reverse summaries: the adjoint lambda_t = ds_t C_t + dA_{t+1} lambda_{t+1} runs
 //     backwards in time with the same chunk decomposition; per chunk, its carry-out from a
 //     zero carry-in and its decay exp(A sum delta);
@@ -43,113 +43,6 @@ __device__ __forceinline__ void tile_step_sizes(const float (&x)[kBwdTile], floa
     const float2 d = sp ? softplus2(v) : v;
     dt[k] = d.x;
     dt[k + 1] = d.y;
-  }
-}
-
-// ---------------------------------------------------------------------------------------
-// 1. Forward checkpoints: chunk c folds the forward summaries of chunks < c into its start
-//    state (from the initial state), then runs the recurrence over its tiles, storing the
-//    state before each tile.
-template <int N, typename T>
-__global__ void __launch_bounds__(kBwdCh) bwd_fwd_ckpt_kernel(const BwdArgs p) {
-  constexpr int NP = (N + 1) / 2;  // state pairs (packed fp32x2 arithmetic)
-  const int64_t n_dtiles = (p.d_inner + kBwdCh - 1) / kBwdCh;
-  int64_t blk = blockIdx.x;
-  const int64_t dtile = blk % n_dtiles;
-  blk /= n_dtiles;
-  const int c = (int)(blk % p.n_chunks);
-  const int64_t b = blk / p.n_chunks;
-  const int lane = threadIdx.x;
-  const int64_t Dn = p.d_inner, L = p.L, d = dtile * kBwdCh + lane;
-  const bool active = d < Dn;
-  const int64_t dc = active ? d : 0;
-  const int64_t t0 = (int64_t)c * p.chunk_len, t1 = min(t0 + p.chunk_len, L);
-  const int64_t tiles = (L + kBwdTile - 1) / kBwdTile;
-  __shared__ __align__(16) float sB[kBwdTile][2 * NP];
-
-  float2 A2[NP], h[NP];
-#pragma unroll
-  for (int j = 0; j < NP; j++) {
-    const int n0 = 2 * j, n1 = n0 + 1;
-    A2[j] = make_float2(p.A[dc * N + n0] * kLog2e, n1 < N ? p.A[dc * N + n1] * kLog2e : 0.f);
-    const float* h0 = p.initial_state ? p.initial_state + (b * Dn + dc) * N : nullptr;
-    h[j] = h0 ? make_float2(h0[n0], n1 < N ? h0[n1] : 0.f) : make_float2(0.f, 0.f);
-  }
-  if (2 * NP != N)
-    for (int i = lane; i < kBwdTile; i += kBwdCh) sB[i][N] = 0.f;
-  const float bias = p.delta_bias ? p.delta_bias[dc] : 0.f;
-  for (int j = 0; j < c; j++) {
-    const int64_t slot = (b * (p.n_chunks - 1) + j) * Dn + dc;
-    const float S = p.fws_S[slot];
-    const float* hs = p.fws_h + slot * N;
-#pragma unroll
-    for (int q = 0; q < NP; q++) {
-      h[q].x = fmaf(ex2(A2[q].x * S), h[q].x, hs[2 * q]);
-      h[q].y = fmaf(ex2(A2[q].y * S), h[q].y, 2 * q + 1 < N ? hs[2 * q + 1] : 0.f);
-    }
-  }
-  // A tile's activations and B rows are loaded into registers all at once (independent
-  // loads), and the next tile's are requested before the current one is computed.
-  constexpr int kBPL = (kBwdTile * N + kBwdCh - 1) / kBwdCh;  // B values per lane per tile
-  float xr[kBwdTile], ur[kBwdTile], br[kBPL];
-  auto load_tile = [&](int64_t ts, float* xa, float* ua, float* ba) {
-    const int steps = (int)min((int64_t)kBwdTile, t1 - ts);
-#pragma unroll
-    for (int k = 0; k < kBwdTile; k++) {
-      const int64_t e = (b * L + ts + min(k, steps - 1)) * Dn + dc;
-      xa[k] = ldf<T>(p.delta, e);
-      ua[k] = ldf<T>(p.u, e);
-    }
-#pragma unroll
-    for (int r = 0; r < kBPL; r++) {
-      const int i = lane + r * kBwdCh;
-      ba[r] = i < steps * N ? ldf<T>(p.B, (b * L + ts) * N + i) : 0.f;
-    }
-  };
-  if (t0 < t1) load_tile(t0, xr, ur, br);
-  for (int64_t ts = t0; ts < t1; ts += kBwdTile) {
-    const int steps = (int)min((int64_t)kBwdTile, t1 - ts);
-    float xn[kBwdTile], un[kBwdTile], bn[kBPL];
-    const bool more = ts + kBwdTile < t1;
-    if (more) load_tile(ts + kBwdTile, xn, un, bn);
-    if (active) {
-      float* ck = p.ckpt_h + ((b * tiles + ts / kBwdTile) * Dn + d) * N;
-#pragma unroll
-      for (int j = 0; j < NP; j++) {
-        ck[2 * j] = h[j].x;
-        if (2 * j + 1 < N) ck[2 * j + 1] = h[j].y;
-      }
-    }
-    __syncwarp();
-#pragma unroll
-    for (int r = 0; r < kBPL; r++) {
-      const int i = lane + r * kBwdCh;
-      if (i < kBwdTile * N) sB[i / N][i % N] = br[r];
-    }
-    __syncwarp();
-    float dts[kBwdTile];
-    tile_step_sizes(xr, bias, p.softplus != 0, dts);
-#pragma unroll
-    for (int k = 0; k < kBwdTile; k++) {
-      if (k < steps) {
-        const float dt = dts[k];
-        const float w = dt * ur[k];
-        const float2 dt2 = make_float2(dt, dt), w2 = make_float2(w, w);
-#pragma unroll
-        for (int j = 0; j < NP; j++) {
-          const float2 xa = __fmul2_rn(dt2, A2[j]);
-          h[j] = __ffma2_rn(make_float2(ex2(xa.x), ex2(xa.y)), h[j],
-                            __fmul2_rn(w2, *reinterpret_cast<const float2*>(&sB[k][2 * j])));
-        }
-      }
-    }
-    __syncwarp();
-    if (more) {
-#pragma unroll
-      for (int k = 0; k < kBwdTile; k++) { xr[k] = xn[k]; ur[k] = un[k]; }
-#pragma unroll
-      for (int r = 0; r < kBPL; r++) br[r] = bn[r];
-    }
   }
 }
 
@@ -706,7 +599,12 @@ static cudaError_t launch_bwd_t(const BwdArgs& a, const ScanParams& fwd, cudaStr
     if (e != cudaSuccess) return e;
     bwd_reverse_summary_kernel<N, T><<<(unsigned)(n_dtiles * (a.n_chunks - 1) * a.batch), kBwdCh, 0, s>>>(a);
   }
-  bwd_fwd_ckpt_kernel<N, T><<<(unsigned)(n_dtiles * a.n_chunks * a.batch), kBwdCh, 0, s>>>(a);
+  {  // forward checkpoints: the forward scan's own kernel in its checkpoint mode
+    ScanParams f = fwd;
+    f.ckpt_h = a.ckpt_h;
+    const cudaError_t e = launch_scan_ckpt(f, sizeof(T) == 2, s);
+    if (e != cudaSuccess) return e;
+  }
   if constexpr (N % 8 == 0) {  // two lanes per channel
     const int64_t n_dtiles2 = (a.d_inner + kBwdCh2 - 1) / kBwdCh2;
     bwd_grad_kernel2<N, T><<<(unsigned)(n_dtiles2 * a.n_chunks * a.batch), 32, 0, s>>>(a);
