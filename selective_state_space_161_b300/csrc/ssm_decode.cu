@@ -15,7 +15,7 @@
 
 namespace ssm {
 
-constexpr int kDecodeThreads = 64;  // swept 64-512 on the 256 x 5120 x 16 decode: smallest was fastest
+constexpr int kDecodeThreads = 64;  // swept 32-512 on the 256 x 5120 x 16 decode: 64 fastest
 
 // SPL consecutive I/O elements -> fp32; multiples of 4 move as 16-byte (fp32) or 8-byte
 // (bf16) pieces.
