@@ -35,8 +35,9 @@
  * - Requirements: every non-NULL pointer 16-byte aligned; d_inner a multiple
  *   of 8 (bf16) or 4 (fp32); 1 <= d_state <= 16; batch, L, d_inner >= 0.
  *   Outputs must not overlap inputs.
- * - The return value reports argument validation and launch errors only
- *   (kernels have no device-side failure mode: there are no inter-block waits).
+ * - The return value reports argument validation and launch errors only.  The one
+ *   device-side failure mode is a time chunk of a scan that waits too long for the
+ *   records of the chunks before it (see ssm_scan_fwd); ssm_get_status reports it.
  * - Calls on different streams are independent if their outputs and
  *   workspaces are distinct.
  */
@@ -65,15 +66,21 @@ typedef enum {
   SSM_ERR_DTYPE = 3,      /* io is neither SSM_F32 nor SSM_BF16 */
   SSM_ERR_ALIGN = 4,      /* a pointer is not 16-byte aligned */
   SSM_ERR_WORKSPACE = 5,  /* workspace NULL or smaller than the size query says */
-  SSM_ERR_CUDA = 6,       /* no usable CUDA device, or a launch failed */
-  SSM_ERR_SCRATCH_LIMIT = 7 /* ssm_scan_fwd_noalloc: the problem needs more scratch than it holds */
+  SSM_ERR_CUDA = 6,       /* no usable CUDA device, a launch failed, or a CUDA error is pending */
+  SSM_ERR_LOOKBACK_TIMEOUT = 7, /* (ssm_get_status) a time chunk gave up waiting for its
+                                   predecessors' records; that call's outputs are invalid */
+  SSM_ERR_SCRATCH_LIMIT = 8 /* ssm_scan_fwd_noalloc: the problem needs more scratch than it holds */
 } ssm_status_t;
 
 /*
- * Bytes of scratch memory ssm_scan_fwd needs for these sizes on the current
- * device (0 when the sequence is processed in a single chunk).  The scratch
- * holds one (sum of delta, end state) pair per time chunk and channel; its
- * contents need no initialisation and are dead after the call completes.
+ * Bytes of workspace the forward scans (ssm_scan_fwd, ssm_scan_fwd_from_state,
+ * ssm_scan_fwd_conv) need for these sizes on the current device; 0 only for an empty
+ * problem (batch * L * d_inner == 0).  The workspace holds a status word (read by
+ * ssm_get_status) and, when the sequence is cut into time chunks, one record per chunk
+ * and channel tile: the chunk's aggregate (sum of delta, end state from zero) and its
+ * inclusive prefix (the true state at its end), each with a flag.  Records carry a tag
+ * unique to the call, so the contents need no initialisation and are dead after the call
+ * completes, except the status word.
  */
 SSM_API size_t ssm_scan_fwd_workspace_size(int64_t batch, int64_t L, int64_t d_inner, int d_state,
                                    ssm_dtype_t io);
@@ -88,7 +95,17 @@ SSM_API size_t ssm_scan_fwd_workspace_size(int64_t batch, int64_t L, int64_t d_i
  *   last_state     : optional fp32 output, h after the last step (before D and the gate);
  *                    zeros when L == 0.
  *   workspace      : device scratch of workspace_bytes >= ssm_scan_fwd_workspace_size(...);
- *                    may be NULL when that size is 0.
+ *                    may be NULL when that size is 0.  Calls that overlap on the GPU need
+ *                    distinct workspaces.
+ *
+ * Time chunks.  When batch * d_inner channels cannot fill the GPU, the sequence is cut
+ * into chunks processed at the same time, joined by a decoupled look-back: a chunk
+ * publishes its aggregate, then folds its predecessors' aggregates until it finds an
+ * inclusive prefix, publishes its own and produces its outputs (the recurrence is
+ * associative: "看懂Mamba，Transformer最强竞争者（一）…", section "3. 状态空间"; the parallel scan
+ * of "Mamba一作最新大發長文！", section "(3) 訓練效率").  Every wait is bounded; a chunk that gives
+ * up records SSM_ERR_LOOKBACK_TIMEOUT for ssm_get_status and finishes (its outputs are then
+ * invalid) instead of hanging.
  */
 SSM_API ssm_status_t ssm_scan_fwd(const void* u, const void* delta, const float* A, const void* B,
                           const void* C, const float* D, const void* z, const float* delta_bias,
@@ -157,19 +174,19 @@ SSM_API ssm_status_t ssm_state_update(float* state, const void* u, const void* d
  * counterpart to this entry point; it exists for such callers only.)
  *
  * Same arguments, results and requirements as ssm_scan_fwd, minus the workspace.  The
- * scratch it needs (one delta sum and one end state per time chunk and channel) comes
- * from an array of SSM_NOALLOC_SCRATCH_BYTES (8 MiB) that the library places in device
- * memory at load time; every GPU that loads the library keeps that array until the
- * process exits.  Problems whose scratch need, as reported by
- * ssm_scan_fwd_workspace_size, exceeds it return SSM_ERR_SCRATCH_LIMIT without launching
- * anything (an fp32 scan of 2 x 2048 x 1536 x 16 needs 5 MiB; a single 1,048,576-token
- * sequence over 2048 channels needs about 10 MiB and is rejected).
- * - The first call on each device looks up the array's device address (with that device
- *   current) and caches it; make that first call before any stream capture.
+ * scratch it needs (the status word and the time chunks' look-back records) comes from an
+ * array of SSM_NOALLOC_SCRATCH_BYTES (8 MiB) that the library places in device memory at
+ * load time; every GPU that loads the library keeps that array until the process exits.
+ * Problems whose scratch need exceeds it return SSM_ERR_SCRATCH_LIMIT without launching
+ * anything.  The need is bounded by one wave of resident CTAs (a few MiB on B300), so
+ * only time-chunk counts forced above the default plan reach the limit.
+ * - The first call on each device (and after a device reset, in each new context) looks
+ *   up the array's device address with that device current and caches it; make that
+ *   first call before any stream capture.
  * - All calls share the one array: calls whose executions overlap on the GPU (on
  *   different streams, or from different threads) race on it and give wrong results.
- *   Serialise them.  The array needs no clearing: every value a call reads was written
- *   earlier in the same call.
+ *   Serialise them.  The array needs no clearing: a call reads only records tagged by
+ *   itself.  ssm_get_status(NULL, stream) reports on the latest call.
  * - It allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  */
 #define SSM_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
@@ -249,10 +266,24 @@ SSM_API ssm_status_t ssm_ssd_fwd(const void* x, const void* dt, const float* A_h
                                  int n_heads, int d_state, ssm_dtype_t io, void* workspace,
                                  size_t workspace_bytes, void* stream);
 
+/*
+ * Device-side status of the most recent forward scan that used `workspace`: waits for
+ * `stream` (a cudaStream_t, NULL = legacy default stream) to finish, then returns
+ *   SSM_ERR_CUDA             if the stream reports a CUDA error (asynchronous or sticky),
+ *   SSM_ERR_LOOKBACK_TIMEOUT if a time chunk of that scan gave up waiting (its y and
+ *                            last_state are invalid),
+ *   SSM_OK                   otherwise.
+ * workspace == NULL checks the scratch of ssm_scan_fwd_noalloc on the current device (if
+ * it has been used), or only the stream when it has not.  The workspace must have been
+ * passed to a forward scan with a non-empty problem before (its status word is written by
+ * every such call).  Synchronises, so it cannot be captured in a CUDA graph.
+ */
+SSM_API ssm_status_t ssm_get_status(const void* workspace, void* stream);
+
 /* Human-readable name of a status code (static string). */
 SSM_API const char* ssm_status_string(ssm_status_t status);
 
-/* Library ABI version (major * 100 + minor). */
+/* Library ABI version (major * 100 + minor): 200. */
 SSM_API int ssm_version(void);
 
 #ifdef __cplusplus

@@ -23,7 +23,7 @@ __all__ = ["SsmError", "ssm_scan_fwd", "ssm_scan_fwd_from_state", "ssm_scan_fwd_
            "ssm_scan_fwd_noalloc", "ssm_state_update", "ssm_state_update_conv", "ssm_scan_bwd",
            "ssm_scan_bwd_workspace_size", "selective_scan_backward", "ssm_ssd_fwd",
            "ssm_ssd_fwd_workspace_size", "selective_scan_ssd",
-           "ssm_scan_fwd_workspace_size",
+           "ssm_scan_fwd_workspace_size", "ssm_get_status",
            "ssm_status_string", "ssm_version", "selective_scan", "selective_state_update",
            "load_library", "build", "SSM_F32", "SSM_BF16", "EXPORTED_SYMBOLS"]
 
@@ -31,8 +31,9 @@ SSM_F32, SSM_BF16 = 0, 1
 EXPORTED_SYMBOLS = ("ssm_scan_fwd_workspace_size", "ssm_scan_fwd", "ssm_scan_fwd_from_state",
                     "ssm_scan_fwd_conv", "ssm_scan_fwd_noalloc", "ssm_state_update",
                     "ssm_state_update_conv", "ssm_scan_bwd", "ssm_scan_bwd_workspace_size",
-                    "ssm_ssd_fwd", "ssm_ssd_fwd_workspace_size",
+                    "ssm_ssd_fwd", "ssm_ssd_fwd_workspace_size", "ssm_get_status",
                     "ssm_status_string", "ssm_version")
+SSM_ERR_LOOKBACK_TIMEOUT, SSM_ERR_SCRATCH_LIMIT = 7, 8
 SSM_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 _lib = None
@@ -83,6 +84,8 @@ def load_library() -> ctypes.CDLL:
         lib.ssm_scan_fwd_noalloc.restype = c_int
         lib.ssm_state_update.argtypes = [vp] * 10 + [c_int, i64, i64, c_int, c_int, vp]
         lib.ssm_state_update.restype = c_int
+        lib.ssm_get_status.argtypes = [vp, vp]
+        lib.ssm_get_status.restype = c_int
         lib.ssm_status_string.argtypes = [c_int]
         lib.ssm_status_string.restype = ctypes.c_char_p
         lib.ssm_version.restype = c_int
@@ -133,6 +136,14 @@ def ssm_version() -> int:
 
 def ssm_scan_fwd_workspace_size(batch: int, L: int, d_inner: int, d_state: int, io: int) -> int:
     return int(load_library().ssm_scan_fwd_workspace_size(batch, L, d_inner, d_state, io))
+
+
+def ssm_get_status(workspace=None, stream=None) -> int:
+    """C-ABI ``ssm_get_status``: waits for ``stream`` and returns the device-side status of the
+    latest forward scan that used ``workspace`` (None: the no-allocation entry point's scratch):
+    0 (SSM_OK), SSM_ERR_LOOKBACK_TIMEOUT or SSM_ERR_CUDA."""
+    _check_dev("workspace", workspace)
+    return int(load_library().ssm_get_status(_ptr(workspace), _stream_handle(stream)))
 
 
 def ssm_scan_fwd(u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, last_state,

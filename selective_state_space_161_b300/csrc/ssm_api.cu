@@ -4,25 +4,61 @@
 #include "ssm.h"
 #include "ssm_internal.h"
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+#include <chrono>
+#include <cstdlib>
 #include <mutex>
+#include <random>
 
 namespace {
 
 constexpr int kMaxState = 16;
 constexpr int kMaxDevices = 64;
-int g_sm_count[kMaxDevices] = {0};
+std::atomic<int> g_sm_count[kMaxDevices];
 
 // SM count of the current device (cached per device), or 0 if there is no usable device.
 int current_sm_count() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
-  if (dev < kMaxDevices && g_sm_count[dev] > 0) return g_sm_count[dev];
+  if (dev < kMaxDevices) {
+    const int c = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  if (dev < kMaxDevices) g_sm_count[dev] = sms;
+  if (dev < kMaxDevices) g_sm_count[dev].store(sms, std::memory_order_relaxed);
   return sms;
+}
+
+// Per-call tags of the look-back records: a 54-bit counter that starts at a random value,
+// so that records left in a reused workspace by earlier calls (or by another process's
+// allocation) never pass for this call's.
+uint64_t next_call_tag() {
+  static std::atomic<uint64_t> counter{[] {
+    std::random_device rd;
+    const uint64_t t = (uint64_t)std::chrono::steady_clock::now().time_since_epoch().count();
+    return (((uint64_t)rd() << 32) ^ (uint64_t)rd() ^ (t * 0x9E3779B97F4A7C15ull));
+  }()};
+  return counter.fetch_add(1, std::memory_order_relaxed) & ((1ull << 54) - 1);
+}
+
+// Look-back polls before a CTA gives up on a predecessor (about a second with the backoff).
+unsigned lookback_max_polls() {
+  if (const char* v = std::getenv("SSM_LOOKBACK_MAX_POLLS")) {
+    const long long x = std::atoll(v);
+    if (x > 0 && x < (1ll << 31)) return (unsigned)x;
+  }
+  return 1u << 20;
+}
+
+// Self-test of the bounded wait: with SSM_LOOKBACK_SELFTEST=1 the look-back waits for
+// records of a tag that no CTA writes, so every wait runs out.
+bool lookback_selftest() {
+  const char* v = std::getenv("SSM_LOOKBACK_SELFTEST");
+  return v != nullptr && v[0] == '1';
 }
 
 bool aligned16(const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -40,12 +76,14 @@ ssm_status_t check_common(int64_t batch, int64_t L, int64_t d_inner, int d_state
   return SSM_OK;
 }
 
-size_t scan_workspace_bytes(int64_t batch, int64_t L, int64_t d_inner, int d_state, int sms,
-                            ssm::ScanPlan* plan) {
-  ssm::plan_scan(batch, L, d_inner, sms, plan);
-  if (plan->n_chunks <= 1) return 0;
-  return (size_t)batch * (size_t)(plan->n_chunks - 1) * (size_t)d_inner * (size_t)(d_state + 1) *
-         sizeof(float);
+// Workspace of a forward scan (0 for an empty problem); false if the plan cannot be made.
+bool fwd_workspace(int64_t batch, int64_t L, int64_t d_inner, int d_state, bool bf16, bool conv,
+                   int sms, ssm::FwdPlan* plan, size_t* bytes) {
+  *bytes = 0;
+  if (batch * d_inner == 0 || L == 0) return true;
+  if (!ssm::plan_scan_fwd(batch, L, d_inner, d_state, bf16, conv, sms, plan)) return false;
+  *bytes = ssm::fwd_workspace_bytes(batch, d_inner, *plan);
+  return true;
 }
 
 }  // namespace
@@ -57,8 +95,12 @@ size_t ssm_scan_fwd_workspace_size(int64_t batch, int64_t L, int64_t d_inner, in
   if (check_common(batch, L, d_inner, d_state, io) != SSM_OK) return 0;
   const int sms = current_sm_count();
   if (sms <= 0) return 0;
-  ssm::ScanPlan plan;
-  return scan_workspace_bytes(batch, L, d_inner, d_state, sms, &plan);
+  ssm::FwdPlan plan;
+  size_t plain = 0, conv = 0;
+  if (!fwd_workspace(batch, L, d_inner, d_state, io == SSM_BF16, false, sms, &plan, &plain) ||
+      !fwd_workspace(batch, L, d_inner, d_state, io == SSM_BF16, true, sms, &plan, &conv))
+    return 0;
+  return plain > conv ? plain : conv;
 }
 
 }  // extern "C"
@@ -108,26 +150,26 @@ ssm_status_t scan_fwd_impl(const void* u, const void* delta, const float* A, con
     return SSM_OK;
   }
 
-  ssm::ScanParams p{};
-  ssm::ScanPlan plan;
-  const size_t need = scan_workspace_bytes(batch, L, d_inner, d_state, sms, &plan);
-  p.chunk_len = plan.chunk_len;
-  p.n_chunks = plan.n_chunks;
-  p.lanes = plan.lanes;
-  if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return SSM_ERR_WORKSPACE;
-  const int64_t cpc = ssm::scan_channels_per_cta();
-  const int64_t n_dtiles = (d_inner + cpc - 1) / cpc;
-  if (n_dtiles * p.n_chunks * batch >= ((int64_t)1 << 31)) return SSM_ERR_SHAPE;
-  p.u = u; p.delta = delta; p.A = A; p.B = B; p.C = C; p.D = D; p.z = z;
-  p.delta_bias = delta_bias; p.softplus = softplus_flag != 0; p.y = y; p.last_state = last_state;
-  p.initial_state = initial_state;
-  p.conv_w = ex.conv_w; p.conv_b = ex.conv_b; p.d_conv = ex.d_conv; p.u_out = ex.u_out;
-  p.batch = batch; p.L = L; p.d_inner = d_inner; p.d_state = d_state;
-  if (p.n_chunks > 1) {
-    p.ws_S = static_cast<float*>(workspace);
-    p.ws_h = p.ws_S + (size_t)batch * (p.n_chunks - 1) * d_inner;
-  }
-  return ssm::launch_scan(p, io == SSM_BF16, s) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+  const bool bf16 = io == SSM_BF16;
+  const bool conv = ex.conv_w != nullptr;
+  ssm::FwdPlan plan;
+  size_t need = 0;
+  if (!fwd_workspace(batch, L, d_inner, d_state, bf16, conv, sms, &plan, &need)) return SSM_ERR_CUDA;
+  if (workspace == nullptr || workspace_bytes < need) return SSM_ERR_WORKSPACE;
+  const int64_t n_dt = (d_inner + ssm::fwd_channels_per_cta() - 1) / ssm::fwd_channels_per_cta();
+  if ((int64_t)plan.G * batch * n_dt >= ((int64_t)1 << 31)) return SSM_ERR_SHAPE;
+  ssm::FwdLaunch f{};
+  f.u = u; f.delta = delta; f.A = A; f.B = B; f.C = C; f.D = D; f.z = z;
+  f.delta_bias = delta_bias; f.softplus = softplus_flag != 0; f.y = y; f.last_state = last_state;
+  f.initial_state = initial_state;
+  f.conv_w = ex.conv_w; f.conv_b = ex.conv_b; f.d_conv = ex.d_conv; f.u_out = ex.u_out;
+  f.batch = batch; f.L = L; f.d_inner = d_inner; f.d_state = d_state;
+  f.plan = plan;
+  f.workspace = workspace;
+  f.tag = next_call_tag();
+  f.wait_tag = lookback_selftest() ? (f.tag ^ 1ull) : f.tag;
+  f.max_polls = lookback_max_polls();
+  return ssm::launch_scan_fwd(f, bf16, s) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
 }  // namespace
@@ -199,7 +241,7 @@ ssm_status_t state_update_impl(float* state, float* conv_state, const void* u,
   for (const void* q : ptrs)
     if (!aligned16(q)) return SSM_ERR_ALIGN;
   if (current_sm_count() <= 0) return SSM_ERR_CUDA;
-  if ((channels * 4 + 255) / 256 >= ((int64_t)1 << 31)) return SSM_ERR_SHAPE;
+  if ((d_inner + 63) / 64 >= ((int64_t)1 << 31)) return SSM_ERR_SHAPE;
   ssm::DecodeParams p{};
   p.state = state; p.u = u; p.delta = delta; p.A = A; p.B = B; p.C = C; p.D = D; p.z = z; p.y = y;
   p.delta_bias = delta_bias; p.softplus = softplus_flag != 0;
@@ -393,40 +435,79 @@ const char* ssm_status_string(ssm_status_t status) {
     case SSM_ERR_ALIGN: return "a pointer is not 16-byte aligned";
     case SSM_ERR_WORKSPACE: return "workspace missing or too small";
     case SSM_ERR_CUDA: return "CUDA error (no device or launch failure)";
+    case SSM_ERR_LOOKBACK_TIMEOUT:
+      return "a time chunk waited too long for its predecessors' records (results are invalid)";
     case SSM_ERR_SCRATCH_LIMIT:
       return "problem needs more scratch than ssm_scan_fwd_noalloc holds (use ssm_scan_fwd)";
   }
   return "unknown status";
 }
 
-int ssm_version(void) { return 100; }
+int ssm_version(void) { return 200; }
 
 }  // extern "C"
 
 // ---------------------------------------------------------------------------------------
 // No-allocation variant of ssm_scan_fwd.  Its scratch is this file-scope device array;
 // host code must not hand the symbol itself to a kernel (on the host it only names a
-// host-side shadow), so its device address is looked up per device, once, below.
+// host-side shadow), so its device address is looked up per device and context, once,
+// below.
 
 static __device__ __align__(256) float g_noalloc_scratch[SSM_NOALLOC_SCRATCH_BYTES / sizeof(float)];
 
 namespace {
 
-std::mutex g_noalloc_mutex;
-float* g_noalloc_addr[kMaxDevices] = {nullptr};
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
 
-// Device address of g_noalloc_scratch on the current device (looked up on first use).
-float* noalloc_scratch_address() {
+// Process-unique id of the current CUDA context (0 if there is none or it cannot be read).
+// The driver entry points are fetched through the runtime, so the library does not link
+// the driver library itself.
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(f);
+  });
+  if (get_current == nullptr || get_id == nullptr) return 0;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  unsigned long long id = 0;
+  return get_id(ctx, &id) == CUDA_SUCCESS ? id : 0;
+}
+
+struct ScratchSlot {
+  unsigned long long ctx_id = 0;
+  float* addr = nullptr;
+};
+std::mutex g_noalloc_mutex;
+ScratchSlot g_noalloc[kMaxDevices];
+
+// Device address of g_noalloc_scratch for the current device and context; looked up on the
+// first use in a context (a device reset creates a new context, whose first use looks it up
+// again).  With lookup == false, only an address already looked up is returned.
+float* noalloc_scratch_address(bool lookup) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-  if (g_noalloc_addr[dev] == nullptr) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
-      return nullptr;
-    g_noalloc_addr[dev] = static_cast<float*>(ptr);
-  }
-  return g_noalloc_addr[dev];
+  ScratchSlot& slot = g_noalloc[dev];
+  const unsigned long long id = current_context_id();
+  if (slot.addr != nullptr && id != 0 && slot.ctx_id == id) return slot.addr;
+  if (!lookup) return nullptr;
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return nullptr;
+  slot.addr = static_cast<float*>(ptr);
+  slot.ctx_id = current_context_id();  // the lookup made the device's context current
+  return slot.addr;
 }
 
 }  // namespace
@@ -443,16 +524,31 @@ ssm_status_t ssm_scan_fwd_noalloc(const void* u, const void* delta, const float*
   if (batch * d_inner == 0) return SSM_OK;
   const int sms = current_sm_count();
   if (sms <= 0) return SSM_ERR_CUDA;
-  ssm::ScanPlan plan;
-  const size_t need = L > 0 ? scan_workspace_bytes(batch, L, d_inner, d_state, sms, &plan) : 0;
+  ssm::FwdPlan plan;
+  size_t need = 0;
+  if (!fwd_workspace(batch, L, d_inner, d_state, io == SSM_BF16, false, sms, &plan, &need))
+    return SSM_ERR_CUDA;
   if (need > SSM_NOALLOC_SCRATCH_BYTES) return SSM_ERR_SCRATCH_LIMIT;
   float* scratch = nullptr;
   if (need > 0) {
-    scratch = noalloc_scratch_address();
+    scratch = noalloc_scratch_address(true);
     if (scratch == nullptr) return SSM_ERR_CUDA;
   }
   return ssm_scan_fwd(u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, last_state, batch, L,
                       d_inner, d_state, io, scratch, need, stream);
+}
+
+ssm_status_t ssm_get_status(const void* workspace, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return SSM_ERR_CUDA;
+  const void* ws = workspace != nullptr ? workspace : noalloc_scratch_address(false);
+  if (ws == nullptr) return SSM_OK;
+  if (!aligned16(ws)) return SSM_ERR_ALIGN;
+  unsigned long long word = 0;
+  if (cudaMemcpyAsync(&word, ws, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return SSM_ERR_CUDA;
+  return (word & 0xFFull) == ssm::kLookbackTimeoutCode ? SSM_ERR_LOOKBACK_TIMEOUT : SSM_OK;
 }
 
 }  // extern "C"

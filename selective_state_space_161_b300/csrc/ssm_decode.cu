@@ -13,6 +13,8 @@
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
 
+#include <algorithm>
+
 namespace ssm {
 
 constexpr int kDecodeThreads = 64;  // swept 32-512 on the 256 x 5120 x 16 decode: 64 fastest
@@ -49,52 +51,77 @@ __device__ __forceinline__ void load_vals(const __nv_bfloat16* g, float* v) {
 
 // LPC lanes per (batch, channel), each owning SPL = N / LPC consecutive states, so that
 // the state row, A row and B/C rows move as coalesced 16-byte (or 8-byte) pieces; the
-// readout sum over states is finished with log2(LPC) shuffles.
+// readout sum over states is finished with log2(LPC) shuffles.  The grid is 2-D (channels,
+// batch rows), so no index needs an integer division; every global load of the step is
+// issued before the first arithmetic that depends on one, and the state math runs on packed
+// fp32 pairs.
 template <int N, typename T, int LPC, bool kConv>
 __global__ void __launch_bounds__(kDecodeThreads) state_update_kernel(const DecodeParams p) {
   constexpr int SPL = N / LPC;
-  const int64_t gid = (int64_t)blockIdx.x * kDecodeThreads + threadIdx.x;
-  const int64_t i = gid / LPC;  // channel index b * d_inner + d
-  const int q = (int)(gid % LPC);
-  const bool valid = i < p.batch * p.d_inner;
-  const int64_t ic = valid ? i : 0;  // lanes past the end still join the shuffles
-  const int64_t b = ic / p.d_inner, d = ic % p.d_inner;
+  constexpr int kChPerCta = kDecodeThreads / LPC;
+  const int64_t d = (int64_t)blockIdx.x * kChPerCta + threadIdx.x / LPC;
+  const int q = (int)(threadIdx.x % LPC);
+  const bool valid = d < p.d_inner;
+  const int64_t dc = valid ? d : 0;  // lanes past the end still join the shuffles
   const T* u = static_cast<const T*>(p.u);
   const T* dl = static_cast<const T*>(p.delta);
   const T* zg = static_cast<const T*>(p.z);
+  for (int64_t b = blockIdx.y; b < p.batch; b += gridDim.y) {  // one pass unless batch > 65535
+  const int64_t ic = b * p.d_inner + dc;
 
-  const float x = to_f32(dl[ic]) + (p.delta_bias ? p.delta_bias[d] : 0.f);
-  const float dt = p.softplus ? softplus(x) : x;
+  // every load of the step first
+  float* st = p.state + ic * N + q * SPL;
+  float h[SPL], A[SPL], Bv[SPL], Cv[SPL];
+  load_vals<SPL>(st, h);
+  load_vals<SPL>(p.A + dc * N + q * SPL, A);
+  load_vals<SPL>(static_cast<const T*>(p.B) + b * N + q * SPL, Bv);
+  load_vals<SPL>(static_cast<const T*>(p.C) + b * N + q * SPL, Cv);
+  const float xraw = to_f32(dl[ic]);
   float uu = to_f32(u[ic]);
+  const float zraw = zg ? to_f32(zg[ic]) : 0.f;
+  const float bias = p.delta_bias ? p.delta_bias[dc] : 0.f;
+  const float Dd = p.D ? p.D[dc] : 0.f;
   float x_new = 0.f;
   if constexpr (kConv) {
     // u = silu(conv_b + sum_{j<K-1} w[j] * x_{t-(K-1)+j} + w[K-1] * x_t), the earlier inputs
-    // coming from conv_state (both lanes of the channel compute it; lane 0 shifts it below)
+    // coming from conv_state (every lane of the channel computes it; lane 0 shifts it below)
     const int K = p.d_conv;
     const float* cs = p.conv_state + ic * (K - 1);
-    float c = p.conv_b ? p.conv_b[d] : 0.f;
-    for (int j = 0; j < K - 1; j++) c = fmaf(p.conv_w[d * K + j], cs[j], c);
+    float c = p.conv_b ? p.conv_b[dc] : 0.f;
+    for (int j = 0; j < K - 1; j++) c = fmaf(p.conv_w[dc * K + j], cs[j], c);
     x_new = uu;
-    uu = silu(fmaf(p.conv_w[d * K + K - 1], x_new, c));
+    uu = silu(fmaf(p.conv_w[dc * K + K - 1], x_new, c));
   }
+  const float x = xraw + bias;
+  const float dt = p.softplus ? softplus(x) : x;
   const float w = dt * uu;
 
-  float h[SPL], A[SPL], Bv[SPL], Cv[SPL];
-  float* st = p.state + ic * N + q * SPL;
-  load_vals<SPL>(st, h);
-  load_vals<SPL>(p.A + d * N + q * SPL, A);
-  load_vals<SPL>(static_cast<const T*>(p.B) + b * N + q * SPL, Bv);
-  load_vals<SPL>(static_cast<const T*>(p.C) + b * N + q * SPL, Cv);
   float acc = 0.f;
+  if constexpr (SPL % 2 == 0) {
+    const float2 dt2 = make_float2(dt * kLog2e, dt * kLog2e), w2 = make_float2(w, w);
+    float2 acc2 = make_float2(0.f, 0.f);
 #pragma unroll
-  for (int n = 0; n < SPL; n++) {
-    const float dA = ex2(dt * (A[n] * kLog2e));
-    h[n] = fmaf(dA, h[n], w * Bv[n]);
-    acc = fmaf(Cv[n], h[n], acc);
+    for (int n = 0; n < SPL; n += 2) {
+      const float2 xa = __fmul2_rn(dt2, make_float2(A[n], A[n + 1]));
+      const float2 dA = make_float2(ex2(xa.x), ex2(xa.y));
+      const float2 hn = __ffma2_rn(dA, make_float2(h[n], h[n + 1]),
+                                   __fmul2_rn(w2, make_float2(Bv[n], Bv[n + 1])));
+      h[n] = hn.x;
+      h[n + 1] = hn.y;
+      acc2 = __ffma2_rn(make_float2(Cv[n], Cv[n + 1]), hn, acc2);
+    }
+    acc = acc2.x + acc2.y;
+  } else {
+#pragma unroll
+    for (int n = 0; n < SPL; n++) {
+      const float dA = ex2(dt * (A[n] * kLog2e));
+      h[n] = fmaf(dA, h[n], w * Bv[n]);
+      acc = fmaf(Cv[n], h[n], acc);
+    }
   }
 #pragma unroll
   for (int o = 1; o < LPC; o <<= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
-  if (!valid) return;
+  if (!valid) continue;
   if constexpr (SPL % 4 == 0) {
 #pragma unroll
     for (int k = 0; k < SPL / 4; k++)
@@ -111,9 +138,10 @@ __global__ void __launch_bounds__(kDecodeThreads) state_update_kernel(const Deco
     }
   }
   if (q == 0) {
-    if (p.D) acc = fmaf(p.D[d], uu, acc);
-    if (zg) acc *= silu(to_f32(zg[ic]));
+    acc = fmaf(Dd, uu, acc);
+    if (zg) acc *= silu(zraw);
     static_cast<T*>(p.y)[ic] = from_f32<T>(acc);
+  }
   }
 }
 
@@ -123,12 +151,13 @@ static cudaError_t launch_t(const DecodeParams& p, cudaStream_t s) {
   // each where d_state allows (measured fastest at d_state 16: enough bytes in flight per
   // thread, 16-byte pieces, and twice the threads of one lane per channel).
   constexpr int LPC = (N % 8 == 0) ? N / 8 : 1;
-  const int64_t threads = p.batch * p.d_inner * LPC;
-  const int64_t blocks = (threads + kDecodeThreads - 1) / kDecodeThreads;
+  constexpr int kChPerCta = kDecodeThreads / LPC;
+  const dim3 grid((unsigned)((p.d_inner + kChPerCta - 1) / kChPerCta),
+                  (unsigned)std::min<int64_t>(p.batch, 65535));
   if (p.conv_w != nullptr)
-    state_update_kernel<N, T, LPC, true><<<(unsigned)blocks, kDecodeThreads, 0, s>>>(p);
+    state_update_kernel<N, T, LPC, true><<<grid, kDecodeThreads, 0, s>>>(p);
   else
-    state_update_kernel<N, T, LPC, false><<<(unsigned)blocks, kDecodeThreads, 0, s>>>(p);
+    state_update_kernel<N, T, LPC, false><<<grid, kDecodeThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -116,6 +116,54 @@ struct SsdParams {
 int ssd_head_dim();
 cudaError_t launch_ssd(const SsdParams& p, cudaStream_t s);
 
+// ---- Single-pass forward scan with a decoupled look-back (ssm_scan_fwd.cu) ----
+
+// Workspace header: one status word, (call tag << 8) | status code.
+constexpr size_t kFwdHeaderBytes = 256;
+constexpr unsigned kLookbackTimeoutCode = 7;  // SSM_ERR_LOOKBACK_TIMEOUT
+
+// How a forward scan of given sizes runs: lanes per channel pair and states per lane (the
+// kernel variant), CTA threads, and the time chunks (G; chunk 0 has len0 steps, the others
+// len, the last possibly fewer).
+struct FwdPlan {
+  int lanes, states_per_lane, threads, G;
+  int64_t len0, len;
+};
+
+struct FwdLaunch {
+  const void* u;
+  const void* delta;
+  const float* A;
+  const void* B;
+  const void* C;
+  const float* D;
+  const void* z;
+  const float* delta_bias;
+  int softplus;
+  void* y;
+  float* last_state;
+  const float* initial_state;
+  const float* conv_w;  // non-null: conv1d + SiLU in front (u holds the block input x)
+  const float* conv_b;
+  int d_conv;
+  void* u_out;
+  int64_t batch, L, d_inner;
+  int d_state;
+  FwdPlan plan;
+  void* workspace;                // header, flags, records (fwd_workspace_bytes)
+  unsigned long long tag;         // per-call tag of the records
+  unsigned long long wait_tag;    // the tag the look-back accepts (tag, except in the wait self-test)
+  unsigned max_polls;             // look-back polls before giving up
+};
+
+bool plan_scan_fwd(int64_t batch, int64_t L, int64_t d_inner, int d_state, bool bf16, bool conv,
+                   int sms, FwdPlan* plan);
+size_t fwd_workspace_bytes(int64_t batch, int64_t d_inner, const FwdPlan& plan);
+cudaError_t launch_scan_fwd(const FwdLaunch& f, bool bf16, cudaStream_t stream);
+int fwd_channels_per_cta();
+
+// ---- Two-pass chunked scan kernels (ssm_scan.cu), used by the backward pass ----
+
 // Channels handled by one CTA of the scan kernels.
 int scan_channels_per_cta();
 

@@ -1,4 +1,8 @@
-"""Shared test helpers: the error metric, and moving generator output to torch."""
+"""Shared test helpers: the error metric, the record of achieved parity margins, and moving
+generator output to torch."""
+import json
+import os
+
 import numpy as np
 
 FP32_TOL = 1e-4   # max relative error, fp32 I/O (fp32 state)
@@ -30,3 +34,19 @@ def to_torch(a, bf16: bool, device="cuda"):
 
 def to_f64(t) -> np.ndarray:
     return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+# Achieved errors of the parity checks of this session (name -> {quantity: error, "tol": bar}).
+# The terminal summary prints them; with SSM_PARITY_LOG=<path> they are also written as JSON.
+MARGINS = {}
+
+
+def record_margin(name: str, tol: float, **errors) -> None:
+    MARGINS[name] = {**{k: float(v) for k, v in errors.items()}, "tol": float(tol)}
+
+
+def dump_margins():
+    path = os.environ.get("SSM_PARITY_LOG")
+    if path and MARGINS:
+        with open(path, "w") as f:
+            json.dump(MARGINS, f, indent=1, sort_keys=True)

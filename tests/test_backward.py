@@ -9,7 +9,7 @@ import inputgen
 import oracle
 import selective_state_space_161_b300 as ssm
 from inputgen import workloads as W
-from tests.helpers import BF16_TOL, FP32_TOL, rel_err, to_f64, to_torch
+from tests.helpers import record_margin, BF16_TOL, FP32_TOL, rel_err, to_f64, to_torch
 
 pytestmark = pytest.mark.gpu
 
@@ -103,5 +103,6 @@ def test_backward_full_size_sampled(key):
                           delta_bias=x["delta_bias"])
     tol = BF16_TOL if w.bf16 else FP32_TOL
     errs = {k: rel_err(v, ref[k]) for k, v in got.items()}
+    record_margin(f"backward {w.key} (full size, sampled)", tol, **errs)
     bad = {k: e for k, e in errs.items() if e > tol}
     assert not bad, f"gradient errors above {tol}: {bad} (all: {errs})"

@@ -7,7 +7,7 @@ import torch
 import oracle
 import selective_state_space_161_b300 as ssm
 from inputgen import workloads as W
-from tests.helpers import BF16_TOL, FP32_TOL, rel_err, to_f64, to_torch
+from tests.helpers import record_margin, BF16_TOL, FP32_TOL, rel_err, to_f64, to_torch
 
 pytestmark = pytest.mark.gpu
 
@@ -119,14 +119,15 @@ def test_scan_conv_full_size_sampled(key):
                                       delta_bias=x["delta_bias"])
     tol = BF16_TOL if w.bf16 else FP32_TOL
     eu, ey, el = rel_err(got_u, u_ref), rel_err(got_y, y_ref), rel_err(got_last, last_ref)
+    record_margin(f"conv+scan {key} (full size, sampled)", tol, u=eu, y=ey, last_state=el)
     assert eu <= tol and ey <= tol and el <= tol, f"u err {eu:.3g}, y err {ey:.3g}, last err {el:.3g}"
 
 
-@pytest.mark.parametrize("lanes", ["1", "2"])
+@pytest.mark.parametrize("lanes", ["1", "2", "4"])
 @pytest.mark.parametrize("bf16,batch,L,d_inner,d_state,d_conv", [
     (False, 2, 3000, 96, 16, 4), (True, 1, 4100, 64, 16, 3), (False, 3, 700, 40, 5, 4)])
 def test_scan_conv_both_kernels_from_state(lanes, bf16, batch, L, d_inner, d_state, d_conv, monkeypatch):
-    """The conv path in both kernels (one or two lanes per channel), over many ragged time
+    """The conv path in every kernel variant (one, two or four lanes per channel pair), over many ragged time
     chunks (each chunk after the first starts its window from the inputs before it), from a
     given initial state."""
     monkeypatch.setenv("SSM_SCAN_LANES", lanes)

@@ -19,7 +19,7 @@ def _case(batch, L, d_inner, d_state, bf16, seed):
     return w, raw, h0
 
 
-@pytest.mark.parametrize("lanes", ["1", "2"])
+@pytest.mark.parametrize("lanes", ["1", "2", "4"])
 @pytest.mark.parametrize("bf16,batch,L,d_inner,d_state", [
     (False, 2, 1500, 64, 16), (True, 1, 3000, 32, 16), (False, 2, 40, 24, 5), (True, 3, 1, 16, 3)])
 def test_from_state_matches_oracle(lanes, bf16, batch, L, d_inner, d_state, monkeypatch):

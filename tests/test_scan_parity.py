@@ -8,7 +8,7 @@ import torch
 import oracle
 import selective_state_space_161_b300 as ssm
 from inputgen import workloads as W
-from tests.helpers import BF16_TOL, FP32_TOL, rel_err, to_f64, to_torch
+from tests.helpers import BF16_TOL, FP32_TOL, record_margin, rel_err, to_f64, to_torch
 
 pytestmark = pytest.mark.gpu
 
@@ -37,11 +37,13 @@ def _run_oracle(w, raw, use_D=True, use_z=True, use_bias=True, softplus=True):
                            delta_bias=x["delta_bias"] if use_bias else None, softplus_flag=softplus)
 
 
-def _check(w, raw, **flags):
+def _check(w, raw, name=None, **flags):
     y, last = _run_gpu(raw, w.bf16, **flags)
     y_ref, last_ref = _run_oracle(w, raw, **flags)
     tol = BF16_TOL if w.bf16 else FP32_TOL
     ey, el = rel_err(y, y_ref), rel_err(last, last_ref)
+    if name:
+        record_margin(name, tol, y=ey, last_state=el)
     assert ey <= tol and el <= tol, f"y err {ey:.3g}, last_state err {el:.3g} (tol {tol})"
     return ey, el
 
@@ -49,7 +51,7 @@ def _check(w, raw, **flags):
 def test_tiny_workload_full():
     w = W.WORKLOADS["tiny"]
     raw = W.host_scan_inputs(w, raw=True)
-    _check(w, raw)
+    _check(w, raw, name="scan tiny (1x64x16x4 fp32)")
 
 
 @pytest.mark.parametrize("bf16", [False, True])
@@ -133,6 +135,7 @@ def test_full_size_workload_sampled(key):
     ds = torch.from_numpy(d_sel).cuda()
     ey = rel_err(to_f64(y.index_select(2, ds)), y_ref)
     el = rel_err(to_f64(last.index_select(1, ds)), last_ref)
+    record_margin(f"scan {key} (full size, sampled channels)", tol, y=ey, last_state=el)
     assert ey <= tol and el <= tol, f"y err {ey:.3g}, last_state err {el:.3g}"
 
 
@@ -153,6 +156,7 @@ def test_long_context_sampled():
     y_ref, last_ref = oracle.scan_fwd(raw["u"], raw["delta"], raw["A"], raw["B"], raw["C"],
                                       D=raw["D"], z=raw["z"], delta_bias=raw["delta_bias"])
     ey, el = rel_err(y_s, y_ref), rel_err(last_s, last_ref)
+    record_margin("scan long (1x1048576x2048x16 bf16, sampled channels)", BF16_TOL, y=ey, last_state=el)
     assert ey <= BF16_TOL and el <= BF16_TOL, f"y err {ey:.3g}, last_state err {el:.3g}"
 
 
@@ -167,11 +171,12 @@ def test_bad_arguments_raise():
         ssm.ssm_scan_fwd(xs, x, A, Bm, Bm, None, None, None, True, y, None, None)
 
 
-@pytest.mark.parametrize("lanes", ["1", "2"])
+@pytest.mark.parametrize("lanes", ["1", "2", "4"])
 @pytest.mark.parametrize("bf16,d_state,batch,L,d_inner", [
     (False, 16, 2, 3000, 96), (True, 16, 1, 4100, 64), (False, 5, 3, 700, 40), (True, 1, 2, 257, 24)])
 def test_both_kernels(lanes, bf16, d_state, batch, L, d_inner, monkeypatch):
-    """Both kernels (one or two lanes per channel), chunked and ragged, against the oracle."""
+    """Every kernel variant (the states of a channel pair on one, two or four lanes), chunked
+    and ragged, against the oracle."""
     monkeypatch.setenv("SSM_SCAN_LANES", lanes)
     w, raw = _random_case(batch, L, d_inner, d_state, bf16, seed=900 + d_state + int(lanes))
-    _check(w, raw)
+    _check(w, raw, name=f"scan {batch}x{L}x{d_inner}x{d_state} {'bf16' if bf16 else 'fp32'}, {lanes} lane(s)")

@@ -7,7 +7,7 @@ import torch
 import oracle
 import selective_state_space_161_b300 as ssm
 from inputgen import workloads as W
-from tests.helpers import BF16_TOL, rel_err, to_f64
+from tests.helpers import record_margin, BF16_TOL, rel_err, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -26,6 +26,8 @@ def _run(w, use_D=True, use_z=True, use_bias=True, d_sel=None):
         ds = torch.from_numpy(np.asarray(d_sel)).cuda()
         y, last = y.index_select(2, ds), last.index_select(1, ds)
     ey, el = rel_err(to_f64(y), y_ref), rel_err(to_f64(last), last_ref)
+    record_margin(f"ssd {w.batch}x{w.L}x{w.d_inner}x{w.d_state}, {w.heads} heads", BF16_TOL, y=ey,
+                  last_state=el)
     assert ey <= BF16_TOL and el <= BF16_TOL, f"y err {ey:.3g}, last_state err {el:.3g}"
 
 
@@ -65,6 +67,7 @@ def test_ssd_without_softplus():
     y_ref, last_ref = oracle.scan_fwd(x["u"], np.abs(x["delta"]) / 8, x["A"], x["B"], x["C"], D=x["D"],
                                       z=x["z"], delta_bias=None, softplus_flag=False)
     ey, el = rel_err(to_f64(y), y_ref), rel_err(to_f64(last), last_ref)
+    record_margin(f"ssd {w.batch}x{w.L}x{w.d_inner}x{w.d_state}, {w.heads} heads", BF16_TOL, y=ey, last_state=el)
     assert ey <= BF16_TOL and el <= BF16_TOL, f"y err {ey:.3g}, last_state err {el:.3g}"
 
 
