@@ -52,6 +52,10 @@ WORKLOADS = {
                           8, 2048, 5120, 16, True, 2, 0.5),
     "long": Workload("long", "long-context scan, 1,048,576 tokens, bf16 I/O",
                      1, 1 << 20, 2048, 16, True, 3, 0.5),
+    # the long-context scan's first 65,536 tokens (same seed and layout, so the same values):
+    # the size its profiler captures run on
+    "long64k": Workload("long64k", "long-context scan, first 65,536 of 1,048,576 tokens, bf16 I/O",
+                        1, 1 << 16, 2048, 16, True, 3, 0.5),
     "decode": Workload("decode", "selective_state_update, 1024 sequential steps, bf16 I/O",
                        256, 1024, 5120, 16, True, 4, 0.5, decode=True, state_sd=0.1),
     "ssd2p7b": Workload("ssd2p7b", "Mamba-2-2.7B-layer-shaped chunked SSD scan (80 heads of 64, "

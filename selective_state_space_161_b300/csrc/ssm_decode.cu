@@ -49,12 +49,20 @@ __device__ __forceinline__ void load_vals(const __nv_bfloat16* g, float* v) {
   }
 }
 
+// One batch row's operands of a thread's share of a step, loaded before any arithmetic.
+template <int SPL>
+struct RowOperands {
+  float h[SPL], Bv[SPL], Cv[SPL];
+  float xraw, uu, zraw;
+};
+
 // LPC lanes per (batch, channel), each owning SPL = N / LPC consecutive states, so that
 // the state row, A row and B/C rows move as coalesced 16-byte (or 8-byte) pieces; the
 // readout sum over states is finished with log2(LPC) shuffles.  The grid is 2-D (channels,
-// batch rows), so no index needs an integer division; every global load of the step is
-// issued before the first arithmetic that depends on one, and the state math runs on packed
-// fp32 pairs.
+// batch rows), so no index needs an integer division.  A thread serves the same channel of
+// two batch rows (b and b + gridDim.y): the A row is loaded once for both, and every load of
+// both rows is issued before the first arithmetic that depends on one, so twice the state
+// bytes are in flight per thread.  The state math runs on packed fp32 pairs.
 template <int N, typename T, int LPC, bool kConv>
 __global__ void __launch_bounds__(kDecodeThreads) state_update_kernel(const DecodeParams p) {
   constexpr int SPL = N / LPC;
@@ -66,82 +74,95 @@ __global__ void __launch_bounds__(kDecodeThreads) state_update_kernel(const Deco
   const T* u = static_cast<const T*>(p.u);
   const T* dl = static_cast<const T*>(p.delta);
   const T* zg = static_cast<const T*>(p.z);
-  for (int64_t b = blockIdx.y; b < p.batch; b += gridDim.y) {  // one pass unless batch > 65535
-  const int64_t ic = b * p.d_inner + dc;
-
-  // every load of the step first
-  float* st = p.state + ic * N + q * SPL;
-  float h[SPL], A[SPL], Bv[SPL], Cv[SPL];
-  load_vals<SPL>(st, h);
+  float A[SPL];
   load_vals<SPL>(p.A + dc * N + q * SPL, A);
-  load_vals<SPL>(static_cast<const T*>(p.B) + b * N + q * SPL, Bv);
-  load_vals<SPL>(static_cast<const T*>(p.C) + b * N + q * SPL, Cv);
-  const float xraw = to_f32(dl[ic]);
-  float uu = to_f32(u[ic]);
-  const float zraw = zg ? to_f32(zg[ic]) : 0.f;
   const float bias = p.delta_bias ? p.delta_bias[dc] : 0.f;
   const float Dd = p.D ? p.D[dc] : 0.f;
-  float x_new = 0.f;
-  if constexpr (kConv) {
-    // u = silu(conv_b + sum_{j<K-1} w[j] * x_{t-(K-1)+j} + w[K-1] * x_t), the earlier inputs
-    // coming from conv_state (every lane of the channel computes it; lane 0 shifts it below)
-    const int K = p.d_conv;
-    const float* cs = p.conv_state + ic * (K - 1);
-    float c = p.conv_b ? p.conv_b[dc] : 0.f;
-    for (int j = 0; j < K - 1; j++) c = fmaf(p.conv_w[dc * K + j], cs[j], c);
-    x_new = uu;
-    uu = silu(fmaf(p.conv_w[dc * K + K - 1], x_new, c));
-  }
-  const float x = xraw + bias;
-  const float dt = p.softplus ? softplus(x) : x;
-  const float w = dt * uu;
 
-  float acc = 0.f;
-  if constexpr (SPL % 2 == 0) {
-    const float2 dt2 = make_float2(dt * kLog2e, dt * kLog2e), w2 = make_float2(w, w);
-    float2 acc2 = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int n = 0; n < SPL; n += 2) {
-      const float2 xa = __fmul2_rn(dt2, make_float2(A[n], A[n + 1]));
-      const float2 dA = make_float2(ex2(xa.x), ex2(xa.y));
-      const float2 hn = __ffma2_rn(dA, make_float2(h[n], h[n + 1]),
-                                   __fmul2_rn(w2, make_float2(Bv[n], Bv[n + 1])));
-      h[n] = hn.x;
-      h[n + 1] = hn.y;
-      acc2 = __ffma2_rn(make_float2(Cv[n], Cv[n + 1]), hn, acc2);
+  auto load_row = [&](int64_t b, RowOperands<SPL>& r) {
+    const int64_t ic = b * p.d_inner + dc;
+    load_vals<SPL>(p.state + ic * N + q * SPL, r.h);
+    load_vals<SPL>(static_cast<const T*>(p.B) + b * N + q * SPL, r.Bv);
+    load_vals<SPL>(static_cast<const T*>(p.C) + b * N + q * SPL, r.Cv);
+    r.xraw = to_f32(dl[ic]);
+    r.uu = to_f32(u[ic]);
+    r.zraw = zg ? to_f32(zg[ic]) : 0.f;
+  };
+  auto step_row = [&](int64_t b, RowOperands<SPL>& r) {
+    const int64_t ic = b * p.d_inner + dc;
+    float uu = r.uu;
+    float x_new = 0.f;
+    if constexpr (kConv) {
+      // u = silu(conv_b + sum_{j<K-1} w[j] * x_{t-(K-1)+j} + w[K-1] * x_t), the earlier inputs
+      // coming from conv_state (every lane of the channel computes it; lane 0 shifts it below)
+      const int K = p.d_conv;
+      const float* cs = p.conv_state + ic * (K - 1);
+      float c = p.conv_b ? p.conv_b[dc] : 0.f;
+      for (int j = 0; j < K - 1; j++) c = fmaf(p.conv_w[dc * K + j], cs[j], c);
+      x_new = uu;
+      uu = silu(fmaf(p.conv_w[dc * K + K - 1], x_new, c));
     }
-    acc = acc2.x + acc2.y;
-  } else {
+    const float x = r.xraw + bias;
+    const float dt = p.softplus ? softplus(x) : x;
+    const float w = dt * uu;
+    float acc = 0.f;
+    if constexpr (SPL % 2 == 0) {
+      const float2 dt2 = make_float2(dt * kLog2e, dt * kLog2e), w2 = make_float2(w, w);
+      float2 acc2 = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int n = 0; n < SPL; n++) {
-      const float dA = ex2(dt * (A[n] * kLog2e));
-      h[n] = fmaf(dA, h[n], w * Bv[n]);
-      acc = fmaf(Cv[n], h[n], acc);
+      for (int n = 0; n < SPL; n += 2) {
+        const float2 xa = __fmul2_rn(dt2, make_float2(A[n], A[n + 1]));
+        const float2 dA = make_float2(ex2(xa.x), ex2(xa.y));
+        const float2 hn = __ffma2_rn(dA, make_float2(r.h[n], r.h[n + 1]),
+                                     __fmul2_rn(w2, make_float2(r.Bv[n], r.Bv[n + 1])));
+        r.h[n] = hn.x;
+        r.h[n + 1] = hn.y;
+        acc2 = __ffma2_rn(make_float2(r.Cv[n], r.Cv[n + 1]), hn, acc2);
+      }
+      acc = acc2.x + acc2.y;
+    } else {
+#pragma unroll
+      for (int n = 0; n < SPL; n++) {
+        const float dA = ex2(dt * (A[n] * kLog2e));
+        r.h[n] = fmaf(dA, r.h[n], w * r.Bv[n]);
+        acc = fmaf(r.Cv[n], r.h[n], acc);
+      }
     }
-  }
 #pragma unroll
-  for (int o = 1; o < LPC; o <<= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
-  if (!valid) continue;
-  if constexpr (SPL % 4 == 0) {
+    for (int o = 1; o < LPC; o <<= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+    if (!valid) return;
+    float* st = p.state + ic * N + q * SPL;
+    if constexpr (SPL % 4 == 0) {
 #pragma unroll
-    for (int k = 0; k < SPL / 4; k++)
-      reinterpret_cast<float4*>(st)[k] = make_float4(h[4 * k], h[4 * k + 1], h[4 * k + 2], h[4 * k + 3]);
-  } else {
+      for (int k = 0; k < SPL / 4; k++)
+        reinterpret_cast<float4*>(st)[k] = make_float4(r.h[4 * k], r.h[4 * k + 1], r.h[4 * k + 2], r.h[4 * k + 3]);
+    } else {
 #pragma unroll
-    for (int n = 0; n < SPL; n++) st[n] = h[n];
-  }
-  if constexpr (kConv) {
-    if (q == 0 && p.d_conv > 1) {  // after the shuffle: every lane has read conv_state
-      float* cs = p.conv_state + ic * (p.d_conv - 1);
-      for (int j = 0; j < p.d_conv - 2; j++) cs[j] = cs[j + 1];
-      cs[p.d_conv - 2] = x_new;
+      for (int n = 0; n < SPL; n++) st[n] = r.h[n];
     }
-  }
-  if (q == 0) {
-    acc = fmaf(Dd, uu, acc);
-    if (zg) acc *= silu(zraw);
-    static_cast<T*>(p.y)[ic] = from_f32<T>(acc);
-  }
+    if constexpr (kConv) {
+      if (q == 0 && p.d_conv > 1) {  // after the shuffle: every lane has read conv_state
+        float* cs = p.conv_state + ic * (p.d_conv - 1);
+        for (int j = 0; j < p.d_conv - 2; j++) cs[j] = cs[j + 1];
+        cs[p.d_conv - 2] = x_new;
+      }
+    }
+    if (q == 0) {
+      acc = fmaf(Dd, uu, acc);
+      if (zg) acc *= silu(r.zraw);
+      static_cast<T*>(p.y)[ic] = from_f32<T>(acc);
+    }
+  };
+
+  // rows b0 and b0 + gridDim.y together (one pass unless batch > 2 * 65535)
+  for (int64_t b0 = blockIdx.y; b0 < p.batch; b0 += 2 * (int64_t)gridDim.y) {
+    const int64_t b1 = b0 + gridDim.y;
+    const bool two = b1 < p.batch;  // CTA-uniform
+    RowOperands<SPL> r0, r1;
+    load_row(b0, r0);
+    if (two) load_row(b1, r1);
+    step_row(b0, r0);
+    if (two) step_row(b1, r1);
   }
 }
 
@@ -153,7 +174,7 @@ static cudaError_t launch_t(const DecodeParams& p, cudaStream_t s) {
   constexpr int LPC = (N % 8 == 0) ? N / 8 : 1;
   constexpr int kChPerCta = kDecodeThreads / LPC;
   const dim3 grid((unsigned)((p.d_inner + kChPerCta - 1) / kChPerCta),
-                  (unsigned)std::min<int64_t>(p.batch, 65535));
+                  (unsigned)std::min<int64_t>((p.batch + 1) / 2, 65535));
   if (p.conv_w != nullptr)
     state_update_kernel<N, T, LPC, true><<<grid, kDecodeThreads, 0, s>>>(p);
   else

@@ -9,18 +9,11 @@
 namespace ssm {
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
 
 // 2^x on the SFU (MUFU.EX2); subnormal results flush to zero.
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-__device__ __forceinline__ float lg2(float x) {
-  float y;
-  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 
@@ -30,31 +23,48 @@ __device__ __forceinline__ float rcp(float x) {
   return y;
 }
 
-// softplus(x) = log(1 + e^x) = max(x, 0) + log1p(e^-|x|).
-// With e = e^-|x| in (0, 1]: for e < 1/16 the Taylor series of log1p,
-// e - e^2/2 + ... - e^6/6 (truncation below 1e-8 relative), keeps full
-// relative accuracy where 1 + e would round away the small term; otherwise
-// log2(1 + e) on the SFU, scaled by ln 2.
-__device__ __forceinline__ float softplus(float x) {
-  float e = ex2(-fabsf(x) * kLog2e);
-  float series = e * (1.f - e * (0.5f - e * (1.f / 3.f - e * (0.25f - e * (0.2f - e * (1.f / 6.f))))));
-  float viaLog = lg2(1.f + e) * kLn2;
-  return fmaxf(x, 0.f) + (e < 0.0625f ? series : viaLog);
+// log1p(e) for e in [0, 1], as e * q(e): q is a degree-9 polynomial from Chebyshev
+// interpolation of log1p(e)/e on [0, 1] (nodes cos((2k+1)pi/20), k = 0..9, mapped to [0, 1];
+// the power-basis coefficients rounded to float).  Evaluated by Horner's rule with fused
+// multiply-adds in float it is within 1.4e-7 relative error of log1p on the whole interval,
+// small e included (e * q(e) keeps full relative precision where 1 + e would lose it), and
+// it needs no MUFU operation.
+__device__ __forceinline__ float log1p_unit(float e) {
+  float q = -0.0031760570127516985f;
+  q = fmaf(q, e, 0.019542526453733444f);
+  q = fmaf(q, e, -0.056373611092567444f);
+  q = fmaf(q, e, 0.10543623566627502f);
+  q = fmaf(q, e, -0.1526966691017151f);
+  q = fmaf(q, e, 0.1966327428817749f);
+  q = fmaf(q, e, -0.24951615929603577f);
+  q = fmaf(q, e, 0.33329710364341736f);
+  q = fmaf(q, e, -0.49999892711639404f);
+  q = fmaf(q, e, 1.0f);
+  return e * q;
+}
+__device__ __forceinline__ float2 log1p_unit2(float2 e) {
+  float2 q = make_float2(-0.0031760570127516985f, -0.0031760570127516985f);
+  q = __ffma2_rn(q, e, make_float2(0.019542526453733444f, 0.019542526453733444f));
+  q = __ffma2_rn(q, e, make_float2(-0.056373611092567444f, -0.056373611092567444f));
+  q = __ffma2_rn(q, e, make_float2(0.10543623566627502f, 0.10543623566627502f));
+  q = __ffma2_rn(q, e, make_float2(-0.1526966691017151f, -0.1526966691017151f));
+  q = __ffma2_rn(q, e, make_float2(0.1966327428817749f, 0.1966327428817749f));
+  q = __ffma2_rn(q, e, make_float2(-0.24951615929603577f, -0.24951615929603577f));
+  q = __ffma2_rn(q, e, make_float2(0.33329710364341736f, 0.33329710364341736f));
+  q = __ffma2_rn(q, e, make_float2(-0.49999892711639404f, -0.49999892711639404f));
+  q = __ffma2_rn(q, e, make_float2(1.f, 1.f));
+  return __fmul2_rn(e, q);
 }
 
-// softplus on two values at once (packed fp32x2 arithmetic; same steps as above,
-// with the log1p series as Horner in e: e * (1 + e(-1/2 + e(1/3 + e(-1/4 + e/5))))).
+// softplus(x) = log(1 + e^x) = max(x, 0) + log1p(e^-|x|), e^-|x| in (0, 1] on the SFU.
+__device__ __forceinline__ float softplus(float x) {
+  return fmaxf(x, 0.f) + log1p_unit(ex2(-fabsf(x) * kLog2e));
+}
+
+// softplus on two values at once (packed fp32x2 arithmetic).
 __device__ __forceinline__ float2 softplus2(float2 x) {
   const float2 e = make_float2(ex2(-fabsf(x.x) * kLog2e), ex2(-fabsf(x.y) * kLog2e));
-  float2 q = __ffma2_rn(e, make_float2(0.2f, 0.2f), make_float2(-0.25f, -0.25f));
-  q = __ffma2_rn(e, q, make_float2(1.f / 3.f, 1.f / 3.f));
-  q = __ffma2_rn(e, q, make_float2(-0.5f, -0.5f));
-  q = __ffma2_rn(e, q, make_float2(1.f, 1.f));
-  const float2 series = __fmul2_rn(e, q);
-  const float2 ope = __fadd2_rn(e, make_float2(1.f, 1.f));
-  const float2 viaLog = __fmul2_rn(make_float2(lg2(ope.x), lg2(ope.y)), make_float2(kLn2, kLn2));
-  const float2 l = make_float2(e.x < 0.0625f ? series.x : viaLog.x, e.y < 0.0625f ? series.y : viaLog.y);
-  return __fadd2_rn(make_float2(fmaxf(x.x, 0.f), fmaxf(x.y, 0.f)), l);
+  return __fadd2_rn(make_float2(fmaxf(x.x, 0.f), fmaxf(x.y, 0.f)), log1p_unit2(e));
 }
 
 // silu on two values at once.

@@ -50,8 +50,14 @@
 #include <cstdlib>
 #include <type_traits>
 
+#ifndef SSM_FWD_UNROLL
+#define SSM_FWD_UNROLL 4
+#endif
+
 namespace ssm {
 namespace fwd {
+
+constexpr int kStepUnroll = SSM_FWD_UNROLL;  // steps per iteration of the one-lane step loop
 
 constexpr int kCh = 64;   // channels per CTA
 constexpr int kCP = 32;   // channel pairs per CTA
@@ -113,9 +119,9 @@ struct Cfg {
   static constexpr int kInclF = 2 * S;                    // floats per thread of an inclusive record
   static constexpr int kXB = 2 * 3 * kRows * kRowB;
   static constexpr int kBCB = 2 * 2 * kT * kNP * 4;
-  static constexpr int kDWB = kT * kCP * 16;
-  static constexpr int kPB = L > 1 ? kOG * kRS * 4 : 0;
-  static constexpr int kSmem = kXB + kBCB + 2 * kDWB + kPB + 16;
+  static constexpr int kDWB = L > 1 ? kT * kCP * 16 : 0;  // (delta, delta*u) pairs per step (L > 1)
+  static constexpr int kPB = L > 1 ? kOG * kRS * 4 : 0;    // partial readouts per step group (L > 1)
+  static constexpr int kSmem = kXB + kBCB + kDWB + kPB + 16;
   static_assert(S % 4 == 0 && kNP <= 16, "states per lane must be a multiple of 4, at most 16 per pair");
 };
 
@@ -149,16 +155,18 @@ struct Args {
   unsigned max_polls;           // look-back polls before giving up
 };
 
+// Register allocation: 12 resident warps per SM for one lane per pair (three per scheduler,
+// up to 168 registers: its 16 state pairs, A and B/C live at once), 16 for two lanes, 20 for
+// four.
 template <int L, int S, typename T, bool kConv>
-__global__ void __launch_bounds__(32 * L) scan_fwd_kernel(const Args a) {
+__global__ void __launch_bounds__(32 * L, L == 1 ? 12 : (L == 2 ? 8 : 5)) scan_fwd_kernel(const Args a) {
   using K = Cfg<L, S, T, kConv>;
   extern __shared__ __align__(16) unsigned char smem[];
   unsigned char* sX = smem;                                                  // [2][3][kRows][kRowB]
   float* sBC = reinterpret_cast<float*>(smem + K::kXB);                      // [2][2][kT][kNP]
   float4* sDW = reinterpret_cast<float4*>(smem + K::kXB + K::kBCB);          // [kT][kCP]
-  float4* sGD = sDW + kT * kCP;                                              // [kT][kCP]
-  float* sP = reinterpret_cast<float*>(smem + K::kXB + K::kBCB + 2 * K::kDWB);  // [kOG][kRS]
-  int* sInfo = reinterpret_cast<int*>(smem + K::kXB + K::kBCB + 2 * K::kDWB + K::kPB);
+  float* sP = reinterpret_cast<float*>(smem + K::kXB + K::kBCB + K::kDWB);    // [kOG][kRS]
+  int* sInfo = reinterpret_cast<int*>(smem + K::kXB + K::kBCB + K::kDWB + K::kPB);
 
   const int64_t Dn = a.d_inner, Ls = a.L;
   const int N = a.N;
@@ -181,14 +189,18 @@ __global__ void __launch_bounds__(32 * L) scan_fwd_kernel(const Args a) {
 
   if (blockIdx.x == 0 && tid == 0 && a.header != nullptr) atomicExch(a.header, a.tag << 8);
 
-  // Per-lane constants: A * log2(e) for the lane's states of both channels (0 for padding
-  // states and inactive channels), the bias, the skip weight.
+  // Per-lane constants: A * log2(e) for the lane's states (0 for padding states and inactive
+  // channels).  Index s = c * (S/2) + j holds channel d + c, states n0 + 2j and n0 + 2j + 1 as
+  // one fp32 pair, so that a state pair meets a (B_n, B_n+1) or (C_n, C_n+1) pair read
+  // straight from shared memory.
+  constexpr int kHP = S / 2;  // state pairs per channel
+  const int n0 = S * l;
   float2 A2[S], h[S];
 #pragma unroll
   for (int s = 0; s < S; s++) {
-    const int n = S * l + s;
-    const bool ok = active && n < N;
-    A2[s] = make_float2(ok ? a.A[d * N + n] * kLog2e : 0.f, ok ? a.A[(d + 1) * N + n] * kLog2e : 0.f);
+    const int c = s / kHP, n = n0 + 2 * (s % kHP);
+    const float* Ar = a.A + (d + c) * N;
+    A2[s] = make_float2((active && n < N) ? Ar[n] * kLog2e : 0.f, (active && n + 1 < N) ? Ar[n + 1] * kLog2e : 0.f);
     h[s] = make_float2(0.f, 0.f);
   }
   const float2 bias2 = (active && a.delta_bias) ? make_float2(a.delta_bias[d], a.delta_bias[d + 1])
@@ -258,13 +270,27 @@ __global__ void __launch_bounds__(32 * L) scan_fwd_kernel(const Args a) {
       }
     };
 
-    // B/C rows of a tile: global -> registers (a tile ahead) -> fp32 shared memory.
+    // B/C rows of a tile: global -> registers (a tile ahead) -> fp32 shared memory.  Which
+    // elements a thread moves is the same for every tile; their offsets are worked out once.
     constexpr int kVec = 16 / K::kTS;
     constexpr int kMaxEl = 2 * kT * K::kNP;
     constexpr int kVecPT = (kMaxEl / kVec + K::kThreads - 1) / K::kThreads;
     constexpr int kScPT = (kMaxEl + K::kThreads - 1) / K::kThreads;
     const bool vec_bc = (N * K::kTS) % 16 == 0;
     const int bc_el = nbc * kT * N;
+    // vector path (d_state a multiple of 16 bytes): per-thread offsets fixed for every tile
+    int bc_src[kVecPT], bc_dst[kVecPT], bc_row[kVecPT];  // element in the B (or C) rows, smem slot, row
+    bool bc_isC[kVecPT];
+#pragma unroll
+    for (int j = 0; j < kVecPT; j++) {
+      const int e = (tid + j * K::kThreads) * kVec;
+      const int which = e / (kT * N), ew = e % (kT * N);
+      const bool ok = vec_bc && e < bc_el;
+      bc_src[j] = ew;
+      bc_row[j] = ok ? ew / N : kT;  // kT: never loaded
+      bc_dst[j] = ok ? ((which * kT + ew / N) * K::kNP + ew % N) : -1;
+      bc_isC[j] = which != 0;
+    }
     uint4 bcv[kVecPT];
     float bcs[kScPT];
     auto load_bc = [&](int tile) {
@@ -274,16 +300,12 @@ __global__ void __launch_bounds__(32 * L) scan_fwd_kernel(const Args a) {
       if (vec_bc) {
 #pragma unroll
         for (int j = 0; j < kVecPT; j++) {
-          const int q = tid + j * K::kThreads;
-          const int e = q * kVec;  // element within [which][kT][N]
-          const int which = e / (kT * N), ew = e % (kT * N);
           bcv[j] = make_uint4(0, 0, 0, 0);
-          if (e < bc_el && ew / N < rows_left)
-            bcv[j] = __ldg(reinterpret_cast<const uint4*>((which ? Cg : Bg) + e0 + ew));
+          if (bc_row[j] < rows_left) bcv[j] = __ldg(reinterpret_cast<const uint4*>((bc_isC[j] ? Cg : Bg) + e0 + bc_src[j]));
         }
       } else {
 #pragma unroll
-        for (int j = 0; j < kScPT; j++) {
+        for (int j = 0; j < kScPT; j++) {  // any d_state: element by element
           const int e = tid + j * K::kThreads;
           const int which = e / (kT * N), ew = e % (kT * N);
           bcs[j] = 0.f;
@@ -292,14 +314,12 @@ __global__ void __launch_bounds__(32 * L) scan_fwd_kernel(const Args a) {
       }
     };
     auto store_bc = [&](int stage) {
+      float* base = sBC + stage * 2 * kT * K::kNP;
       if (vec_bc) {
 #pragma unroll
         for (int j = 0; j < kVecPT; j++) {
-          const int q = tid + j * K::kThreads;
-          const int e = q * kVec;
-          if (e < bc_el) {
-            const int which = e / (kT * N), ew = e % (kT * N);
-            float* dst = sBC + ((stage * 2 + which) * kT + ew / N) * K::kNP + ew % N;
+          if (bc_dst[j] >= 0) {
+            float* dst = base + bc_dst[j];
             const uint4 v = bcv[j];
             if constexpr (K::kTS == 4) {
               *reinterpret_cast<float4*>(dst) = make_float4(__uint_as_float(v.x), __uint_as_float(v.y),
@@ -320,7 +340,7 @@ __global__ void __launch_bounds__(32 * L) scan_fwd_kernel(const Args a) {
           const int e = tid + j * K::kThreads;
           if (e < bc_el) {
             const int which = e / (kT * N), ew = e % (kT * N);
-            sBC[((stage * 2 + which) * kT + ew / N) * K::kNP + ew % N] = bcs[j];
+            base[(which * kT + ew / N) * K::kNP + ew % N] = bcs[j];
           }
         }
       }
@@ -345,17 +365,17 @@ __global__ void __launch_bounds__(32 * L) scan_fwd_kernel(const Args a) {
       const int64_t ts = t0 + (int64_t)tile * kT;
       const int steps = (int)min((int64_t)kT, t1 - ts);
 
-      // Pre-phase: the per-element work of the steps k = l (mod L), once per element.
-#pragma unroll
-      for (int i = 0; i < kT / L; i++) {
-        const int k = i * L + l;
+      // The per-element work of step k for this lane's channel pair (step size, delta*u, and
+      // for the main pass the gate and D*u*gate), from the staged rows of stage `stage`.
+      auto element = [&](int k, float2& dlt, float2& w, float2& g, float2& dug) {
         const int kp = k + K::kHalo;  // physical row of step k
         auto xrow = [&](int x, int rp) {  // this pair's bytes in row rp of input x
           return sX + ((stage * 3 + x) * K::kRows + rp) * K::kRowB +
                  (((pchunk ^ ((rp % L) * K::kSwz)) * 16) + pwithin);
         };
-        float2 xr = __fadd2_rn(PairIO<T>::load(xrow(0, kp)), bias2);
-        const float2 dlt = sp ? softplus2(xr) : xr;
+        const float2 xr = __fadd2_rn(PairIO<T>::load(xrow(0, kp)), bias2);
+        const float2 spx = softplus2(xr);  // computed either way, selected without a branch
+        dlt = make_float2(sp ? spx.x : xr.x, sp ? spx.y : xr.y);
         float2 uu = PairIO<T>::load(xrow(1, kp));
         if constexpr (kConv) {  // u = silu(conv_b + sum_j cw[j] x[t - 3 + j])
           float2 pre = __ffma2_rn(cw[3], uu, cb2);
@@ -366,82 +386,128 @@ __global__ void __launch_bounds__(32 * L) scan_fwd_kernel(const Args a) {
           if (kMain && a.u_out != nullptr && active && k < steps)
             PairIO<T>::store(static_cast<T*>(a.u_out) + (b * Ls + ts + k) * Dn + d, uu);
         }
-        const float2 w = __fmul2_rn(dlt, uu);
-        const int slot = k * kCP + (P ^ (l * K::kSwz));
-        sDW[slot] = make_float4(dlt.x, dlt.y, w.x, w.y);
+        w = __fmul2_rn(dlt, uu);
         if constexpr (kMain) {
-          const float2 g = has_z ? silu2(PairIO<T>::load(xrow(2, kp))) : make_float2(1.f, 1.f);
-          const float2 dug = __fmul2_rn(__fmul2_rn(D2, uu), g);
-          sGD[slot] = make_float4(g.x, g.y, dug.x, dug.y);
-        } else {
-          if (k < steps) {  // compensated (Kahan) sum of delta over the chunk
-            const float2 yk = sub2(dlt, Scomp);
-            const float2 tk = make_float2(Ssum.x + yk.x, Ssum.y + yk.y);
-            Scomp = sub2(sub2(tk, Ssum), yk);
-            Ssum = tk;
-          }
-        }
-      }
-      __syncwarp();
-
-      // Output of the steps k0 .. k0+kOG-1 (L > 1): lane l sums the partial readouts of its
-      // own steps over the pair's L lanes and applies the skip term and the gate.
-      auto output_group = [&](int k0) {
-#pragma unroll
-        for (int i = 0; i < kOG / L; i++) {
-          const int k = k0 + i * L + l;
-          if (k < steps && active) {
-            const float* pr = sP + (k - k0) * K::kRS + 2 * P;
-            float2 sum = *reinterpret_cast<const float2*>(pr);
-#pragma unroll
-            for (int m = 1; m < L; m++) sum = __fadd2_rn(sum, *reinterpret_cast<const float2*>(pr + m * K::kLS));
-            const float4 gd = sGD[k * kCP + (P ^ (l * K::kSwz))];
-            const float2 yv = __ffma2_rn(sum, make_float2(gd.x, gd.y), make_float2(gd.z, gd.w));
-            PairIO<T>::store(yg + (b * Ls + ts + k) * Dn + d, yv);
-          }
+          // without z the row was never staged; silu of whatever it holds is computed and
+          // discarded by the select
+          const float2 sz = silu2(PairIO<T>::load(xrow(2, kp)));
+          g = make_float2(has_z ? sz.x : 1.f, has_z ? sz.y : 1.f);
+          dug = __fmul2_rn(__fmul2_rn(D2, uu), g);
+        } else if (k < steps) {  // compensated (Kahan) sum of delta over the chunk
+          const float2 yk = sub2(dlt, Scomp);
+          const float2 tk = make_float2(Ssum.x + yk.x, Ssum.y + yk.y);
+          Scomp = sub2(sub2(tk, Ssum), yk);
+          Ssum = tk;
         }
       };
 
-      // Recurrence over the tile's steps on this lane's states.
-      auto recur = [&](auto guarded) {
-        constexpr bool kGuard = decltype(guarded)::value;
+      // One recurrence step on this lane's S states of the pair; returns the partial readout
+      // (main pass), summed over independent accumulators to keep the chains short.
+      auto advance = [&](int k, float2 dt2, float2 w2) {
+        constexpr int kAcc = S >= 8 ? 2 : 1;  // accumulators per channel
+        const float* Bk = sBC + ((stage * 2 + 0) * kT + k) * K::kNP + n0;
+        const float* Ck = sBC + ((stage * 2 + 1) * kT + k) * K::kNP + n0;
+        float2 acc[2][kAcc];
 #pragma unroll
-        for (int k = 0; k < kT; k++) {
-          if (kGuard && k >= steps) break;
-          const float4 dw = sDW[k * kCP + (P ^ ((k % L) * K::kSwz))];
-          const float2 dt2 = make_float2(dw.x, dw.y), w2 = make_float2(dw.z, dw.w);
-          const float* Bk = sBC + ((stage * 2 + 0) * kT + k) * K::kNP + S * l;
-          float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+        for (int c = 0; c < 2; c++)
 #pragma unroll
-          for (int q = 0; q < S / 4; q++) {
-            const float4 b4 = *reinterpret_cast<const float4*>(Bk + 4 * q);
-            const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
-            float cc[4] = {0.f, 0.f, 0.f, 0.f};
-            if constexpr (kMain) {
-              const float4 c4 = *reinterpret_cast<const float4*>(sBC + ((stage * 2 + 1) * kT + k) * K::kNP + S * l + 4 * q);
-              cc[0] = c4.x; cc[1] = c4.y; cc[2] = c4.z; cc[3] = c4.w;
-            }
+          for (int m = 0; m < kAcc; m++) acc[c][m] = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int e = 0; e < 4; e++) {
-              const int s = 4 * q + e;
-              const float2 xa = __fmul2_rn(dt2, A2[s]);
+        for (int q = 0; q < S / 4; q++) {
+          const float4 b4 = *reinterpret_cast<const float4*>(Bk + 4 * q);
+          const float2 bp[2] = {make_float2(b4.x, b4.y), make_float2(b4.z, b4.w)};
+          float2 cp[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+          if constexpr (kMain) {
+            const float4 c4 = *reinterpret_cast<const float4*>(Ck + 4 * q);
+            cp[0] = make_float2(c4.x, c4.y);
+            cp[1] = make_float2(c4.z, c4.w);
+          }
+#pragma unroll
+          for (int c = 0; c < 2; c++) {
+            const float2 dtc = c ? make_float2(dt2.y, dt2.y) : make_float2(dt2.x, dt2.x);
+            const float2 wc = c ? make_float2(w2.y, w2.y) : make_float2(w2.x, w2.x);
+#pragma unroll
+            for (int e = 0; e < 2; e++) {
+              const int j = 2 * q + e, s = c * kHP + j;
+              const float2 xa = __fmul2_rn(dtc, A2[s]);
               const float2 dA = make_float2(ex2(xa.x), ex2(xa.y));
-              h[s] = __ffma2_rn(dA, h[s], __fmul2_rn(w2, make_float2(bb[e], bb[e])));
-              if constexpr (kMain) {
-                if (e & 1) acc1 = __ffma2_rn(make_float2(cc[e], cc[e]), h[s], acc1);
-                else acc0 = __ffma2_rn(make_float2(cc[e], cc[e]), h[s], acc0);
-              }
+              h[s] = __ffma2_rn(dA, h[s], __fmul2_rn(wc, bp[e]));
+              if constexpr (kMain) acc[c][j % kAcc] = __ffma2_rn(cp[e], h[s], acc[c][j % kAcc]);
             }
           }
+        }
+        float2 r[2];
+#pragma unroll
+        for (int c = 0; c < 2; c++) {
+#pragma unroll
+          for (int m = 1; m < kAcc; m++) acc[c][0] = __fadd2_rn(acc[c][0], acc[c][m]);
+          r[c] = acc[c][0];
+        }
+        return make_float2(r[0].x + r[0].y, r[1].x + r[1].y);
+      };
+
+      if constexpr (L == 1) {
+        // One lane owns the pair and all of its states: the per-element work inline, step by step.
+        T* yk = yg + (b * Ls + ts) * Dn + d;  // y of step k, advanced by one row per step
+        auto step1 = [&](int k) {
+          float2 dlt, w, g, dug;
+          element(k, dlt, w, g, dug);
+          const float2 part = advance(k, dlt, w);
           if constexpr (kMain) {
-            const float2 part = __fadd2_rn(acc0, acc1);
-            if constexpr (L == 1) {
-              if (active) {
-                const float4 gd = sGD[k * kCP + P];
-                const float2 yv = __ffma2_rn(part, make_float2(gd.x, gd.y), make_float2(gd.z, gd.w));
-                PairIO<T>::store(yg + (b * Ls + ts + k) * Dn + d, yv);
-              }
-            } else {
+            if (active) PairIO<T>::store(yk, __ffma2_rn(part, g, dug));
+            yk += Dn;
+          }
+        };
+        // Four steps per loop iteration: enough independent work for the scheduler, and code
+        // small enough to stay in the instruction cache (a fully unrolled tile does not).
+        if (steps == kT) {
+#pragma unroll kStepUnroll
+          for (int k = 0; k < kT; k++) step1(k);
+        } else {
+          for (int k = 0; k < steps; k++) step1(k);
+        }
+      } else {
+        // Pre-phase: lane l does the per-element work of the steps k = l (mod L) once and leaves
+        // (delta, delta*u) in shared memory for the pair's L lanes; it keeps (gate, D*u*gate) of
+        // its own steps in registers for their outputs.
+        float4 gd[kT / L];
+#pragma unroll
+        for (int i = 0; i < kT / L; i++) {
+          const int k = i * L + l;
+          float2 dlt, w, g, dug;
+          element(k, dlt, w, g, dug);
+          sDW[k * kCP + (P ^ (l * K::kSwz))] = make_float4(dlt.x, dlt.y, w.x, w.y);
+          gd[i] = make_float4(g.x, g.y, dug.x, dug.y);
+        }
+        __syncwarp();
+
+        // Output of the steps k0 .. k0+kOG-1: lane l sums the partial readouts of its own steps
+        // over the pair's L lanes and applies the skip term and the gate.
+        auto output_group = [&](int k0) {
+#pragma unroll
+          for (int i = 0; i < kOG / L; i++) {
+            const int k = k0 + i * L + l;
+            if (k < steps && active) {
+              const float* pr = sP + (k - k0) * K::kRS + 2 * P;
+              float2 sum = *reinterpret_cast<const float2*>(pr);
+#pragma unroll
+              for (int m = 1; m < L; m++) sum = __fadd2_rn(sum, *reinterpret_cast<const float2*>(pr + m * K::kLS));
+              const float4 q = gd[k0 / L + i];
+              PairIO<T>::store(yg + (b * Ls + ts + k) * Dn + d,
+                               __ffma2_rn(sum, make_float2(q.x, q.y), make_float2(q.z, q.w)));
+            }
+          }
+        };
+
+        // Recurrence over the tile's steps on this lane's states.
+        auto recur = [&](auto guarded) {
+          constexpr bool kGuard = decltype(guarded)::value;
+#pragma unroll
+          for (int k = 0; k < kT; k++) {
+            if (kGuard && k >= steps) break;
+            const float4 dw = sDW[k * kCP + (P ^ ((k % L) * K::kSwz))];
+            const float2 part = advance(k, make_float2(dw.x, dw.y), make_float2(dw.z, dw.w));
+            if constexpr (kMain) {
               *reinterpret_cast<float2*>(sP + (k % kOG) * K::kRS + l * K::kLS + 2 * P) = part;
               if (k % kOG == kOG - 1 || (kGuard && k == steps - 1)) {
                 __syncwarp();
@@ -450,10 +516,10 @@ __global__ void __launch_bounds__(32 * L) scan_fwd_kernel(const Args a) {
               }
             }
           }
-        }
-      };
-      if (steps == kT) recur(std::false_type{});
-      else recur(std::true_type{});
+        };
+        if (steps == kT) recur(std::false_type{});
+        else recur(std::true_type{});
+      }
       __syncthreads();  // this stage and the per-tile buffers are free again
       if (tile + 1 < ntiles) store_bc(stage ^ 1);
     }
@@ -563,10 +629,10 @@ __global__ void __launch_bounds__(32 * L) scan_fwd_kernel(const Args a) {
 #pragma unroll
       for (int u = 0; u < kAhead; u++) {
         if (j + u < c) {
-          const float2 Sj = make_float2(v[u][0], v[u][1]);
 #pragma unroll
           for (int s = 0; s < S; s++) {
-            const float2 xa = __fmul2_rn(A2[s], Sj);
+            const float Sc = v[u][s / kHP];  // the chunk's delta sum for this state's channel
+            const float2 xa = __fmul2_rn(A2[s], make_float2(Sc, Sc));
             h[s] = __ffma2_rn(make_float2(ex2(xa.x), ex2(xa.y)), h[s], make_float2(v[u][2 + 2 * s], v[u][3 + 2 * s]));
           }
         }
@@ -577,7 +643,8 @@ __global__ void __launch_bounds__(32 * L) scan_fwd_kernel(const Args a) {
       float* dst = a.incl + (rec * K::kThreads + tid) * K::kInclF;
 #pragma unroll
       for (int s = 0; s < S; s += 2) {
-        const float2 xa0 = __fmul2_rn(A2[s], S2), xa1 = __fmul2_rn(A2[s + 1], S2);
+        const float S0 = s / kHP ? S2.y : S2.x, S1 = (s + 1) / kHP ? S2.y : S2.x;
+        const float2 xa0 = __fmul2_rn(A2[s], make_float2(S0, S0)), xa1 = __fmul2_rn(A2[s + 1], make_float2(S1, S1));
         const float2 e0 = __ffma2_rn(make_float2(ex2(xa0.x), ex2(xa0.y)), h[s], hagg[s]);
         const float2 e1 = __ffma2_rn(make_float2(ex2(xa1.x), ex2(xa1.y)), h[s + 1], hagg[s + 1]);
         *reinterpret_cast<float4*>(dst + 2 * s) = make_float4(e0.x, e0.y, e1.x, e1.y);
@@ -591,8 +658,9 @@ __global__ void __launch_bounds__(32 * L) scan_fwd_kernel(const Args a) {
   } else if (a.initial_state != nullptr && active) {
 #pragma unroll
     for (int s = 0; s < S; s++) {
-      const int n = S * l + s;
-      if (n < N) h[s] = make_float2(a.initial_state[(b * Dn + d) * N + n], a.initial_state[(b * Dn + d + 1) * N + n]);
+      const int c = s / kHP, n = n0 + 2 * (s % kHP);
+      const float* hr = a.initial_state + (b * Dn + d + c) * N;
+      h[s] = make_float2(n < N ? hr[n] : 0.f, n + 1 < N ? hr[n + 1] : 0.f);
     }
   }
 
@@ -613,11 +681,10 @@ __global__ void __launch_bounds__(32 * L) scan_fwd_kernel(const Args a) {
   if (last_chunk && a.last_state != nullptr && active) {
 #pragma unroll
     for (int s = 0; s < S; s++) {
-      const int n = S * l + s;
-      if (n < N) {
-        a.last_state[(b * Dn + d) * N + n] = h[s].x;
-        a.last_state[(b * Dn + d + 1) * N + n] = h[s].y;
-      }
+      const int c = s / kHP, n = n0 + 2 * (s % kHP);
+      float* lr = a.last_state + (b * Dn + d + c) * N;
+      if (n < N) lr[n] = h[s].x;
+      if (n + 1 < N) lr[n + 1] = h[s].y;
     }
   }
 }
@@ -712,9 +779,14 @@ int fwd_channels_per_cta() { return fwd::kCh; }
 
 bool plan_scan_fwd(int64_t batch, int64_t L, int64_t d_inner, int d_state, bool bf16, bool conv,
                    int sms, FwdPlan* plan) {
-  // Lanes per channel pair: the pair's states split over 1, 2 or 4 lanes (4 states each by
-  // default), so that even a GPU-filling batch of channels gives enough warps.
+  // Lanes per channel pair: the pair's states split over 1, 2 or 4 lanes.  Four lanes (4 states
+  // each) give a GPU-filling batch of channels enough warps and keep time chunks long when
+  // chunking is needed; one lane per pair (all states in one thread, no exchange between
+  // lanes) issues the fewest instructions per element and wins when few channels run a long
+  // sequence (measured on B300: 1 x 1,048,576 x 2048 x 16 at 15.2 ms with one lane against
+  // 17.8 ms with four; 8 x 2048 x 5120 x 16 at 0.47 ms with four against 0.60-0.65 with one).
   int lanes = d_state <= 4 ? 1 : d_state <= 8 ? 2 : 4;
+  if (d_state > 8 && L >= 16384 && batch * d_inner < (int64_t)sms * 12 * fwd::kCh / 2) lanes = 1;
   const int forced = (int)env_int("SSM_SCAN_LANES", 0);
   if (forced == 1 || forced == 2 || forced == 4) lanes = forced;
   int S = (d_state + lanes - 1) / lanes;
@@ -736,9 +808,11 @@ bool plan_scan_fwd(int64_t batch, int64_t L, int64_t d_inner, int d_state, bool 
   G = std::max<int64_t>(1, std::min<int64_t>(G, 4096));
   int64_t len0 = L, len = L;
   if (G > 1) {
-    // Chunk 0 runs only its main pass: shorter by the aggregate/main cost ratio, it
-    // finishes about when the others finish their aggregates.
-    const double alpha = env_double("SSM_SCAN_ALPHA", 0.65);
+    // Chunk 0 runs only its main pass.  It is half the length of the others, so that its
+    // inclusive prefix is out before the others finish their aggregates (an aggregate step
+    // costs about 0.7 of a main step): no chunk waits for it, and its early finish idles only
+    // 1/G of the CTAs.
+    const double alpha = env_double("SSM_SCAN_ALPHA", 0.5);
     len = (int64_t)std::ceil((double)L / ((double)(G - 1) + alpha));
     len = (len + fwd::kT - 1) / fwd::kT * fwd::kT;
     len0 = std::max<int64_t>(fwd::kT, (int64_t)(alpha * (double)len) / fwd::kT * fwd::kT);
