@@ -38,13 +38,16 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 # are stale.
 KERNEL_SOURCES = {"scan": ("ssm_scan_fwd.cu", "ssm_device.cuh"),
                   "decode": ("ssm_decode.cu", "ssm_device.cuh"),
-                  "ssd": ("ssm_ssd.cu", "ssm_device.cuh")}
+                  "ssd": ("ssm_ssd.cu", "ssm_ssd_gram.cu", "ssm_device.cuh")}
 FALLBACK_HBM_GBS = 6400.0
 NOMINAL_HBM_GBS = 7700.0  # B300 HBM3e nominal, reported beside the measured-copy fraction
 SM_MAX_MHZ_NOMINAL = 2032.0
-# Per-SM issue rates of the pipes the scan uses (operations per clock), measured on B300
-# with a throughput probe: FP32 FFMA/FMUL/FADD 128, MUFU.EX2 32, MUFU.LG2 / MUFU.RCP 16.
-FP32_PER_CLK, EX2_PER_CLK, MUFU_SLOW_PER_CLK = 128.0, 32.0, 16.0
+# Per-SM rates of the pipes the scan uses (operations per clock), measured on B300 with a
+# throughput probe: FP32 FFMA/FMUL/FADD 128; MUFU ex2 32, lg2 and rcp 16.  The MUFU
+# operations share one pipe (a 1:1 mix of ex2 and rcp runs at 19.9 per clock, what one shared
+# pipe gives, not the 32 of two separate ones), so the bound counts MUFU "slots": an ex2 takes
+# one, a lg2 or rcp two, at 32 slots per clock.
+FP32_PER_CLK, MUFU_SLOTS_PER_CLK = 128.0, 32.0
 L2_FLUSH_BYTES = 512 << 20
 
 
@@ -105,13 +108,13 @@ SSD_Q = 64  # chunk length of the tensor-core form
 
 def ssd_flops(w: W.Workload) -> float:
     """Tensor-core FLOPs of the chunked form, each product counted once (Q = 64, P = 64):
-    per (batch, head, chunk) the local state X^T (w B) (2 Q P N), the intra-chunk scores
-    C B^T (2 Q^2 N), the carried-state readout C H^T (2 Q N P) and the masked mix M X
-    (2 Q^2 P)."""
+    per (batch, chunk) the Gram matrix C B^T (2 Q^2 N; the same for every head, since B and C
+    are shared), and per (batch, head, chunk) the local state X^T (w B) (2 Q P N), the
+    carried-state readout C H^T (2 Q N P) and the masked mix M X (2 Q^2 P)."""
     P, N, Q = w.d_inner // w.heads, w.d_state, SSD_Q
     chunks = -(-w.L // Q)
-    per = 2 * Q * P * N + 2 * Q * Q * N + 2 * Q * N * P + 2 * Q * Q * P
-    return float(w.batch * w.heads * chunks * per)
+    per_head = 2 * Q * P * N + 2 * Q * N * P + 2 * Q * Q * P
+    return float(w.batch * chunks * (2 * Q * Q * N + w.heads * per_head))
 
 
 def bwd_algorithmic_bytes(w: W.Workload) -> float:
@@ -129,23 +132,27 @@ def bwd_alu_clocks_per_element(N: int) -> float:
     """Backward lower bound per element: recomputing the state (4 FP32 + 1 ex2 per state) and
     the reverse step (per state: the adjoint FMA, dA's product and ex2, the two terms of the
     step-size gradient, the A-gradient FMA, the u-gradient FMA, the B and C partials and the
-    carry: 11 FP32 + 1 ex2), plus ~16 FP32, 4 ex2, 4 slow SFU ops per element."""
+    carry: 11 FP32 + 1 ex2), plus ~16 FP32, 4 ex2 and 4 lg2/rcp (two MUFU slots each) per
+    element."""
     fp32 = 15 * N + 16
-    ex2 = 2 * N + 4
-    slow = 4
-    return max(fp32 / FP32_PER_CLK, ex2 / EX2_PER_CLK, slow / MUFU_SLOW_PER_CLK)
+    mufu = 2 * N + 4 + 2 * 4
+    return max(fp32 / FP32_PER_CLK, mufu / MUFU_SLOTS_PER_CLK)
 
 
-def alu_clocks_per_element(N: int) -> float:
+def alu_clocks_per_element(N: int, conv: bool = False) -> float:
     """Lower bound on SM clocks per (b, t, d) element from the arithmetic the method needs:
     per state n: delta*A, exp, (delta u)*B_n, the FMA of the recurrence and the FMA of the
     readout (4 FP32 + 1 ex2); per element: delta*u, bias add, D*u, gate multiply, the sigmoid's
-    1 + e^-z and z * (.) (6 FP32), the exps of softplus and sigmoid (2 ex2), softplus's log and
-    the sigmoid's reciprocal (2 slow MUFU).  Each pipe is taken as independent."""
-    fp32 = 4 * N + 6
-    ex2 = N + 2
-    slow = 2
-    return max(fp32 / FP32_PER_CLK, ex2 / EX2_PER_CLK, slow / MUFU_SLOW_PER_CLK)
+    1 + e^-z and z * (.) (6 FP32), the exps of softplus and sigmoid (2 ex2), the sigmoid's
+    reciprocal (2 MUFU slots), and softplus's log1p, which costs either a MUFU lg2 (2 slots) or
+    about 10 FP32 operations of a polynomial: the bound takes the cheaper assignment.  With the
+    conv1d + SiLU in front: 4 more FMA, 3 more FP32 and one more exp and reciprocal.  FP32 and
+    MUFU are separate pipes; the slower one binds."""
+    fp32 = 4 * N + 6 + (7 if conv else 0)
+    mufu = N + 2 + 2 + (3 if conv else 0)
+    log_on_mufu = max(fp32 / FP32_PER_CLK, (mufu + 2) / MUFU_SLOTS_PER_CLK)
+    log_on_fma = max((fp32 + 10) / FP32_PER_CLK, mufu / MUFU_SLOTS_PER_CLK)
+    return min(log_on_mufu, log_on_fma)
 
 
 def workload_kind(w: W.Workload) -> str:
@@ -318,7 +325,7 @@ class SsdStep(ScanStep):
         self.last = torch.empty((w.batch, w.d_inner, w.d_state), dtype=torch.float32, device="cuda")
         nbytes = ssm.ssm_ssd_fwd_workspace_size(w.batch, w.L, w.d_inner, w.heads, w.d_state)
         self.ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda") if nbytes else None
-        self.launches = 1  # one fused launch per step
+        self.launches = 2  # the chunk Gram matrices (tensor cores), then the heads
 
     def workspace(self):
         return self.ws
@@ -541,10 +548,8 @@ def whole_job_rate(elements_per_rank: int, world: int, ms_max: float) -> float:
 def roofline(w, ms_per_step, hbm_gbs, sm_mhz, sms, peak_src, traffic=None, which="forward"):
     el_rate = w.elements / (ms_per_step * 1e-3)
     nbytes = bwd_algorithmic_bytes(w) if which == "backward" else algorithmic_bytes(w)
-    clocks = (bwd_alu_clocks_per_element if which == "backward" else alu_clocks_per_element)(w.d_state)
-    if which == "conv":  # conv1d (4 FMA) + SiLU (3 FP32, 1 ex2, 1 rcp) more per element
-        clocks = max(clocks, (4 * w.d_state + 13) / FP32_PER_CLK, (w.d_state + 3) / EX2_PER_CLK,
-                     3 / MUFU_SLOW_PER_CLK)
+    clocks = (bwd_alu_clocks_per_element(w.d_state) if which == "backward"
+              else alu_clocks_per_element(w.d_state, conv=which == "conv"))
     if which == "ssd":
         nbytes = ssd_algorithmic_bytes(w)
         achieved = nbytes / (ms_per_step * 1e-3) / 1e9
@@ -567,9 +572,9 @@ def roofline(w, ms_per_step, hbm_gbs, sm_mhz, sms, peak_src, traffic=None, which
     return {"bound": "alu", "achieved": el_rate / 1e9, "peak": peak, "unit": "Gelem/s",
             "frac": el_rate / 1e9 / peak, "traffic": traffic,
             "algorithmic_bytes": algorithmic_bytes(w),
-            "peak_source": (f"{sms} SMs x {sm_mhz:.0f} MHz, per-element FP32/EX2/MUFU op counts at the "
-                            f"measured rates {FP32_PER_CLK:.0f} FP32, {EX2_PER_CLK:.0f} ex2, "
-                            f"{MUFU_SLOW_PER_CLK:.0f} lg2/rcp per clock per SM"),
+            "peak_source": (f"{sms} SMs x {sm_mhz:.0f} MHz, per-element FP32 and MUFU op counts at the "
+                            f"measured rates {FP32_PER_CLK:.0f} FP32 and {MUFU_SLOTS_PER_CLK:.0f} MUFU "
+                            f"slots per clock per SM (ex2 one slot, lg2/rcp two, one shared pipe)"),
             "hbm_frac": algorithmic_bytes(w) / (ms_per_step * 1e-3) / 1e9 / hbm_gbs,
             "hbm_frac_of_nominal": algorithmic_bytes(w) / (ms_per_step * 1e-3) / 1e9 / NOMINAL_HBM_GBS}
 

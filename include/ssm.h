@@ -254,8 +254,11 @@ SSM_API ssm_status_t ssm_scan_bwd(const void* u, const void* delta, const float*
  *   x, z, y [batch][L][d_inner]; dt [batch][L][n_heads]; B, C [batch][L][d_state]: bf16;
  *   A_head, dt_bias [n_heads], D [d_inner], last_state [batch][d_inner][d_state]: fp32.
  * Requirements: io == SSM_BF16; d_inner == 64 * n_heads (head dimension 64); d_state in
- * {16, 32, 64, 128}; D, z, dt_bias, last_state nullable.  ssm_ssd_fwd_workspace_size
- * returns 0 (the form needs no workspace); workspace may be null and is not touched.
+ * {16, 32, 64, 128}; D, z, dt_bias, last_state nullable; batch * L < 2^31.
+ * The chunks' Gram matrices G = C B^T do not depend on the head (B and C are shared by all
+ * heads): a first tensor-core kernel (tcgen05.mma with operands brought in by TMA) computes
+ * them once per batch row and chunk into the workspace (ssm_ssd_fwd_workspace_size bytes:
+ * batch * ceil(L / 64) * 64 * 64 fp32; no initialisation needed), and every head reads them.
  */
 SSM_API size_t ssm_ssd_fwd_workspace_size(int64_t batch, int64_t L, int64_t d_inner, int n_heads,
                                           int d_state);

@@ -381,8 +381,10 @@ ssm_status_t ssm_scan_bwd(const void* u, const void* delta, const float* A, cons
 
 size_t ssm_ssd_fwd_workspace_size(int64_t batch, int64_t L, int64_t d_inner, int n_heads,
                                   int d_state) {
-  (void)batch; (void)L; (void)d_inner; (void)n_heads; (void)d_state;
-  return 0;  // the state stays on chip: one CTA per (batch, head) walks that head's chunks
+  (void)d_inner; (void)n_heads; (void)d_state;
+  if (batch <= 0 || L <= 0) return 0;
+  // the chunk Gram matrices C B^T (shared by every head); the state itself stays on chip
+  return ssm::ssd_gram_bytes(batch, L);
 }
 
 ssm_status_t ssm_ssd_fwd(const void* x, const void* dt, const float* A, const void* B,
@@ -408,7 +410,8 @@ ssm_status_t ssm_ssd_fwd(const void* x, const void* dt, const float* A, const vo
       return SSM_ERR_CUDA;
     return SSM_OK;
   }
-  (void)workspace_bytes;  // none needed
+  if (workspace == nullptr || workspace_bytes < ssm::ssd_gram_bytes(batch, L)) return SSM_ERR_WORKSPACE;
+  if (batch * L >= ((int64_t)1 << 31)) return SSM_ERR_SHAPE;  // rows of the Gram kernel's TMA maps
   ssm::SsdParams p{};
   p.x = static_cast<const __nv_bfloat16*>(x);
   p.dt = static_cast<const __nv_bfloat16*>(dt);
@@ -421,6 +424,7 @@ ssm_status_t ssm_ssd_fwd(const void* x, const void* dt, const float* A, const vo
   p.softplus = softplus_flag != 0;
   p.y = static_cast<__nv_bfloat16*>(y);
   p.last_state = last_state;
+  p.G = static_cast<float*>(workspace);
   p.batch = batch; p.L = L; p.d_inner = d_inner; p.heads = n_heads; p.N = d_state;
   if (batch * n_heads >= ((int64_t)1 << 31)) return SSM_ERR_SHAPE;
   return ssm::launch_ssd(p, s) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;

@@ -110,11 +110,17 @@ struct SsdParams {
   int softplus;
   __nv_bfloat16* y;
   float* last_state;        // [batch][d_inner][N], may be null
+  float* G;                 // workspace: [batch][chunks][64][64] chunk Gram matrices C B^T
   int64_t batch, L, d_inner;
   int heads, N;
 };
 int ssd_head_dim();
 cudaError_t launch_ssd(const SsdParams& p, cudaStream_t s);
+// Chunk Gram matrices G[b][c] = C_c B_c^T (64 x 64 fp32 per batch row and chunk of 64 steps) on
+// the tensor cores (tcgen05, operands by TMA); ssd_gram_bytes is the workspace they take.
+size_t ssd_gram_bytes(int64_t batch, int64_t L);
+cudaError_t launch_ssd_gram(const __nv_bfloat16* C, const __nv_bfloat16* B, float* G, int64_t batch,
+                            int64_t L, int N, cudaStream_t s);
 
 // ---- Single-pass forward scan with a decoupled look-back (ssm_scan_fwd.cu) ----
 

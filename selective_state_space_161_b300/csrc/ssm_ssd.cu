@@ -159,27 +159,29 @@ __host__ __device__ constexpr int g_tile_j(int w, int s) {
   return w == 0 ? s : w == 1 ? (s < 3 ? 5 + s : s - 3) : w == 2 ? s : (s == 0 ? 5 : s - 1);
 }
 
-// G = C B^T on warp WARP's five tiles, masked (j <= i) and decayed into
+// Warp WARP's five tiles of the chunk's Gram matrix G = C B^T (computed for all heads at once
+// by the tensor-core kernel of ssm_ssd_gram.cu), in the m16n8 accumulator layout: G[s][0..1]
+// at row 16 r + g, columns 8 jt + 2 tq (+1); G[s][2..3] eight rows below.  Loaded from L2 at
+// the start of a chunk, so the latency hides behind the chunk's copies and barrier.
+template <int WARP>
+__device__ __forceinline__ void load_g(const float* Gc, int lane, float (&G)[5][4]) {
+  const int g = lane / 4, tq = lane % 4;
+#pragma unroll
+  for (int s = 0; s < 5; s++) {
+    const int r = g_tile_r(WARP, s), jt = g_tile_j(WARP, s);
+    const float* row = Gc + (16 * r + g) * kQ + 8 * jt + 2 * tq;
+    const float2 lo = __ldcg(reinterpret_cast<const float2*>(row));
+    const float2 hi = __ldcg(reinterpret_cast<const float2*>(row + 8 * kQ));
+    G[s][0] = lo.x; G[s][1] = lo.y; G[s][2] = hi.x; G[s][3] = hi.y;
+  }
+}
+
+// Warp WARP's five tiles of G, masked (j <= i) and decayed into
 // M[i][j] = G[i][j] delta_j 2^(S_i - S_j), stored as bf16 hi and lo.
 template <int N, int WARP>
-__device__ __forceinline__ void g_phase(SsdSmem<N>& sm, const float* sS, const float* sDt, int lane) {
+__device__ __forceinline__ void g_phase(SsdSmem<N>& sm, const float* sS, const float* sDt, int lane,
+                                        const float (&G)[5][4]) {
   const int g = lane / 4, tq = lane % 4;
-  float G[5][4];
-#pragma unroll
-  for (int s = 0; s < 5; s++) G[s][0] = G[s][1] = G[s][2] = G[s][3] = 0.f;
-#pragma unroll
-  for (int kk = 0; kk < N / 16; kk++) {
-    uint32_t a[4];
-#pragma unroll
-    for (int s = 0; s < 5; s++) {
-      const int r = g_tile_r(WARP, s), jt = g_tile_j(WARP, s);
-      if (s == 0 || r != g_tile_r(WARP, s - 1))
-        ldsm_x4(a, &sm.C[16 * r + (lane % 16)][kk * 16 + 8 * (lane / 16)]);
-      uint32_t bb[2];  // B operand (k = n, column = j) = B[j][n]
-      ldsm_x2(bb, &sm.B[8 * jt + (lane % 8)][kk * 16 + 8 * ((lane / 8) % 2)]);
-      mma16816(G[s], a, bb[0], bb[1]);
-    }
-  }
 #pragma unroll
   for (int s = 0; s < 5; s++) {
     const int r = g_tile_r(WARP, s), jt = g_tile_j(WARP, s);
@@ -237,6 +239,16 @@ __global__ void __launch_bounds__(kSsdThreads, 3) ssd_fused_kernel(const SsdPara
   int par = 0;  // parity of the current chunk's decay arrays
   for (int64_t t0 = 0; t0 < p.L; t0 += kQ, par ^= 1) {
     const int rows = (int)min((int64_t)kQ, p.L - t0);
+    float G[5][4];  // this warp's tiles of the chunk's Gram matrix
+    {
+      const float* Gc = p.G + (b * ((p.L + kQ - 1) / kQ) + t0 / kQ) * kQ * kQ;
+      switch (warp) {
+        case 0: load_g<0>(Gc, lane, G); break;
+        case 1: load_g<1>(Gc, lane, G); break;
+        case 2: load_g<2>(Gc, lane, G); break;
+        default: load_g<3>(Gc, lane, G); break;
+      }
+    }
     const float* sDt = sm.dt[par];
     const float* sS = sm.S[par];
     const float* sW = sm.W[par];
@@ -251,12 +263,12 @@ __global__ void __launch_bounds__(kSsdThreads, 3) ssd_fused_kernel(const SsdPara
       if (t0 + 2 * kQ < p.L) dt_raw = load_dt_pair(p, b, h, t0 + 2 * kQ, lane);
     }
 
-    // ---- G = C B^T on this warp's five tiles, then M (hi, lo) into shared memory
+    // ---- M (hi, lo) from this warp's tiles of G into shared memory
     switch (warp) {
-      case 0: g_phase<N, 0>(sm, sS, sDt, lane); break;
-      case 1: g_phase<N, 1>(sm, sS, sDt, lane); break;
-      case 2: g_phase<N, 2>(sm, sS, sDt, lane); break;
-      default: g_phase<N, 3>(sm, sS, sDt, lane); break;
+      case 0: g_phase<N, 0>(sm, sS, sDt, lane, G); break;
+      case 1: g_phase<N, 1>(sm, sS, sDt, lane, G); break;
+      case 2: g_phase<N, 2>(sm, sS, sDt, lane, G); break;
+      default: g_phase<N, 3>(sm, sS, sDt, lane, G); break;
     }
 
     // ---- Y = 2^(S_i) C H_in^T: rows i (four 16-row blocks) x this warp's 16 channels
@@ -419,6 +431,9 @@ static cudaError_t launch_ssd_n(const SsdParams& p, cudaStream_t s) {
 int ssd_head_dim() { return kP; }
 
 cudaError_t launch_ssd(const SsdParams& p, cudaStream_t s) {
+  // the chunk Gram matrices of every batch row first (tensor-core kernel), then the heads
+  const cudaError_t e = launch_ssd_gram(p.C, p.B, p.G, p.batch, p.L, p.N, s);
+  if (e != cudaSuccess) return e;
   switch (p.N) {
     case 16: return launch_ssd_n<16>(p, s);
     case 32: return launch_ssd_n<32>(p, s);

@@ -86,4 +86,6 @@ def test_ssd_host_validation_before_any_device_call():
     assert _ssd_rc(L=-1) == 2
     assert _ssd_rc(batch=0) == 0                   # empty problem
     assert _ssd_rc() == 1                          # A (and the tensors) missing
-    assert ssm.ssm_ssd_fwd_workspace_size(8, 2048, 5120, 80, 128) == 0  # state kept on chip
+    # the chunk Gram matrices C B^T, shared by every head: 8 x 32 chunks x 64 x 64 fp32
+    assert ssm.ssm_ssd_fwd_workspace_size(8, 2048, 5120, 80, 128) == 8 * 32 * 64 * 64 * 4
+    assert ssm.ssm_ssd_fwd_workspace_size(8, 0, 5120, 80, 128) == 0
