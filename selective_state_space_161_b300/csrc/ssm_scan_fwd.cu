@@ -117,7 +117,12 @@ struct Cfg {
   static constexpr int kRS = L == 4 ? 296 : L == 2 ? 176 : 64;   // partial buffer: row stride (floats)
   static constexpr int kAggF = (2 + 2 * S + 3) / 4 * 4;  // floats per thread of an aggregate record
   static constexpr int kInclF = 2 * S;                    // floats per thread of an inclusive record
-  static constexpr int kXB = 2 * 3 * kRows * kRowB;
+  // One stage of activation rows: delta (kT rows), u or the conv input (kRows rows: the kHalo
+  // rows before the tile first), z (kT rows).
+  static constexpr int kOffU = kT * kRowB;
+  static constexpr int kOffZ = (kT + kRows) * kRowB;
+  static constexpr int kStageB = (2 * kT + kRows) * kRowB;
+  static constexpr int kXB = 2 * kStageB;
   static constexpr int kBCB = 2 * 2 * kT * kNP * 4;
   static constexpr int kDWB = L > 1 ? kT * kCP * 16 : 0;  // (delta, delta*u) pairs per step (L > 1)
   static constexpr int kPB = L > 1 ? kOG * kRS * 4 : 0;    // partial readouts per step group (L > 1)
@@ -162,7 +167,7 @@ template <int L, int S, typename T, bool kConv>
 __global__ void __launch_bounds__(32 * L, L == 1 ? 12 : (L == 2 ? 8 : 5)) scan_fwd_kernel(const Args a) {
   using K = Cfg<L, S, T, kConv>;
   extern __shared__ __align__(16) unsigned char smem[];
-  unsigned char* sX = smem;                                                  // [2][3][kRows][kRowB]
+  unsigned char* sX = smem;                                                  // [2][kStageB]
   float* sBC = reinterpret_cast<float*>(smem + K::kXB);                      // [2][2][kT][kNP]
   float4* sDW = reinterpret_cast<float4*>(smem + K::kXB + K::kBCB);          // [kT][kCP]
   float* sP = reinterpret_cast<float*>(smem + K::kXB + K::kBCB + K::kDWB);    // [kOG][kRS]
@@ -242,32 +247,34 @@ __global__ void __launch_bounds__(32 * L, L == 1 ? 12 : (L == 2 ? 8 : 5)) scan_f
   auto run = [&](auto mode_tag) {
     constexpr int kMode = decltype(mode_tag)::value;
     constexpr bool kMain = kMode == kModeMain;
-    const int nx = kMain ? (has_z ? 3 : 2) : 2;
     const int nbc = kMain ? 2 : 1;
 
-    // Activation rows of a tile: delta, u (or the conv input x), z, kRows rows each (the
-    // conv input also gets the kHalo rows before the tile); 16-byte piece ch of physical
-    // row rp lands at piece ch ^ ((rp % L) * kSwz).
-    auto issue_x = [&](int tile, int stage) {
-      const int64_t ts = t0 + (int64_t)tile * kT;
-      constexpr int kPieces = 3 * K::kRows * K::kChunks;
+    // Activation rows of a tile: delta and z (kT rows), u or the conv input x (kRows rows,
+    // the kHalo rows before the tile first); 16-byte piece ch of row r of an array lands at
+    // piece ch ^ ((r % L) * kSwz).
+    auto issue_rows = [&](auto rows_tag, const char* base, int off, int64_t tfirst) {
+      constexpr int kR = decltype(rows_tag)::value;
+      constexpr int kPieces = kR * K::kChunks;
+      const char* g0 = base + ((b * Ls + tfirst) * Dn + d0) * K::kTS;  // row tfirst, channel d0
+      const int64_t row_bytes = Dn * K::kTS;
 #pragma unroll
       for (int j = 0; j < (kPieces + K::kThreads - 1) / K::kThreads; j++) {
         const int q = tid + j * K::kThreads;
-        const int x = q / (K::kRows * K::kChunks);
-        if (q < kPieces && x < nx) {
-          const int rp = (q / K::kChunks) % K::kRows;  // physical row; step ts + rp - kHalo
-          const int ch = q % K::kChunks;
-          const int64_t t = ts + rp - K::kHalo;
-          if (rp >= K::kHalo || x == 1) {
-            const bool valid = t >= 0 && t < t1 && d0 + ch * (16 / K::kTS) < Dn;
-            const char* base = x == 0 ? xd : x == 1 ? xu : xz;
-            const char* g = base + ((b * Ls + t) * Dn + d0) * K::kTS + ch * 16;
-            unsigned char* s = sX + ((stage * 3 + x) * K::kRows + rp) * K::kRowB + ((ch ^ ((rp % L) * K::kSwz)) * 16);
-            cp_async16(s, valid ? g : base, valid);
-          }
+        if (kPieces % K::kThreads == 0 || q < kPieces) {
+          const int r = q / K::kChunks, ch = q % K::kChunks;  // kChunks is a power of two
+          const int64_t t = tfirst + r;
+          const bool valid = t >= 0 && t < t1 && d0 + ch * (16 / K::kTS) < Dn;
+          const char* g = g0 + r * row_bytes + ch * 16;
+          cp_async16(sX + off + r * K::kRowB + ((ch ^ ((r % L) * K::kSwz)) * 16), valid ? g : base, valid);
         }
       }
+    };
+    auto issue_x = [&](int tile, int stage) {
+      const int64_t ts = t0 + (int64_t)tile * kT;
+      const int so = stage * K::kStageB;
+      issue_rows(std::integral_constant<int, kT>{}, xd, so, ts);
+      issue_rows(std::integral_constant<int, K::kRows>{}, xu, so + K::kOffU, ts - K::kHalo);
+      if (kMain && has_z) issue_rows(std::integral_constant<int, kT>{}, xz, so + K::kOffZ, ts);
     };
 
     // B/C rows of a tile: global -> registers (a tile ahead) -> fp32 shared memory.  Which
@@ -368,20 +375,19 @@ __global__ void __launch_bounds__(32 * L, L == 1 ? 12 : (L == 2 ? 8 : 5)) scan_f
       // The per-element work of step k for this lane's channel pair (step size, delta*u, and
       // for the main pass the gate and D*u*gate), from the staged rows of stage `stage`.
       auto element = [&](int k, float2& dlt, float2& w, float2& g, float2& dug) {
-        const int kp = k + K::kHalo;  // physical row of step k
-        auto xrow = [&](int x, int rp) {  // this pair's bytes in row rp of input x
-          return sX + ((stage * 3 + x) * K::kRows + rp) * K::kRowB +
-                 (((pchunk ^ ((rp % L) * K::kSwz)) * 16) + pwithin);
+        auto xrow = [&](int off, int r) {  // this pair's bytes in row r of the array at off
+          return sX + stage * K::kStageB + off + r * K::kRowB + (((pchunk ^ ((r % L) * K::kSwz)) * 16) + pwithin);
         };
-        const float2 xr = __fadd2_rn(PairIO<T>::load(xrow(0, kp)), bias2);
+        const int ku = k + K::kHalo;  // row of step k in the u (conv input) array
+        const float2 xr = __fadd2_rn(PairIO<T>::load(xrow(0, k)), bias2);
         const float2 spx = softplus2(xr);  // computed either way, selected without a branch
         dlt = make_float2(sp ? spx.x : xr.x, sp ? spx.y : xr.y);
-        float2 uu = PairIO<T>::load(xrow(1, kp));
+        float2 uu = PairIO<T>::load(xrow(K::kOffU, ku));
         if constexpr (kConv) {  // u = silu(conv_b + sum_j cw[j] x[t - 3 + j])
           float2 pre = __ffma2_rn(cw[3], uu, cb2);
-          pre = __ffma2_rn(cw[2], PairIO<T>::load(xrow(1, kp - 1)), pre);
-          pre = __ffma2_rn(cw[1], PairIO<T>::load(xrow(1, kp - 2)), pre);
-          pre = __ffma2_rn(cw[0], PairIO<T>::load(xrow(1, kp - 3)), pre);
+          pre = __ffma2_rn(cw[2], PairIO<T>::load(xrow(K::kOffU, ku - 1)), pre);
+          pre = __ffma2_rn(cw[1], PairIO<T>::load(xrow(K::kOffU, ku - 2)), pre);
+          pre = __ffma2_rn(cw[0], PairIO<T>::load(xrow(K::kOffU, ku - 3)), pre);
           uu = silu2(pre);
           if (kMain && a.u_out != nullptr && active && k < steps)
             PairIO<T>::store(static_cast<T*>(a.u_out) + (b * Ls + ts + k) * Dn + d, uu);
@@ -390,7 +396,7 @@ __global__ void __launch_bounds__(32 * L, L == 1 ? 12 : (L == 2 ? 8 : 5)) scan_f
         if constexpr (kMain) {
           // without z the row was never staged; silu of whatever it holds is computed and
           // discarded by the select
-          const float2 sz = silu2(PairIO<T>::load(xrow(2, kp)));
+          const float2 sz = silu2(PairIO<T>::load(xrow(K::kOffZ, k)));
           g = make_float2(has_z ? sz.x : 1.f, has_z ? sz.y : 1.f);
           dug = __fmul2_rn(__fmul2_rn(D2, uu), g);
         } else if (k < steps) {  // compensated (Kahan) sum of delta over the chunk
