@@ -347,7 +347,7 @@ ssm_status_t ssm_scan_bwd(const void* u, const void* delta, const float* A, cons
   bwd_plan(batch, L, d_inner, sms, &plan);
   const size_t need = ssm::bwd_workspace_floats(batch, L, d_inner, d_state, plan.n_chunks) * sizeof(float);
   if (workspace == nullptr || workspace_bytes < need) return SSM_ERR_WORKSPACE;
-  const int64_t tiles = (L + 15) / 16;
+  const int64_t tiles = (L + ssm::kCkptSteps - 1) / ssm::kCkptSteps;
   if ((d_inner + 31) / 32 * tiles * batch >= ((int64_t)1 << 31)) return SSM_ERR_SHAPE;
 
   float* ws = static_cast<float*>(workspace);

@@ -37,7 +37,7 @@ struct ScanParams {
   int lanes;  // 1 or 2 lanes per channel (which kernel runs)
   float* ws_S;  // [batch][n_chunks-1][d_inner]
   float* ws_h;  // [batch][n_chunks-1][d_inner][d_state]
-  float* ckpt_h = nullptr;  // checkpoint pass only: [batch][ceil(L/16)][d_inner][d_state]
+  float* ckpt_h = nullptr;  // checkpoint pass only: [batch][ceil(L/kCkptSteps)][d_inner][d_state]
 };
 
 struct DecodeParams {
@@ -93,7 +93,7 @@ struct BwdArgs {
   const float* fws_h;
   float* rws_S;        // reverse chunk summaries [batch][n_chunks][d_inner] (+ [.][d_state])
   float* rws_m;
-  float* ckpt_h;       // [batch][tiles][d_inner][d_state]: state before each tile
+  float* ckpt_h;       // [batch][ceil(L / kCkptSteps)][d_inner][d_state]: state before every kCkptSteps steps
 };
 
 
@@ -126,6 +126,7 @@ cudaError_t launch_ssd_gram(const __nv_bfloat16* C, const __nv_bfloat16* B, floa
 
 // Workspace header: one status word, (call tag << 8) | status code.
 constexpr size_t kFwdHeaderBytes = 256;
+constexpr int kCkptSteps = 8;  // backward checkpoint interval (steps)
 constexpr unsigned kLookbackTimeoutCode = 7;  // SSM_ERR_LOOKBACK_TIMEOUT
 
 // How a forward scan of given sizes runs: lanes per channel pair and states per lane (the
@@ -186,7 +187,7 @@ cudaError_t launch_scan(const ScanParams& p, bool bf16, cudaStream_t stream);
 // Only the forward summary pass (one lane per channel) of a chunked scan plan.
 cudaError_t launch_scan_summary(const ScanParams& p, bool bf16, cudaStream_t stream);
 // The main pass's states from initial_state and the chunk summaries, with no output: the state
-// before every 16-step tile into p.ckpt_h (one lane per channel).
+// before every kCkptSteps steps into p.ckpt_h (one lane per channel).
 cudaError_t launch_scan_ckpt(const ScanParams& p, bool bf16, cudaStream_t stream);
 // Floats of scratch the backward pass needs for n_chunks time chunks.
 size_t bwd_workspace_floats(int64_t batch, int64_t L, int64_t d_inner, int d_state, int n_chunks);

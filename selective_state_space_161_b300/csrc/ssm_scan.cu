@@ -1,5 +1,5 @@
 // Forward states for the training backward pass (ssm_scan_bwd.cu): per-chunk summaries of
-// the recurrence and the state before every tile of 16 steps.  These are the forward
+// the recurrence and the state before every 8 steps (kCkptSteps).  These are the forward
 // recurrence of the selective scan (dA = exp(delta*A), dBu = delta*B*u,
 // h_t = dA_t h_{t-1} + dBu_t; youngju.dev "Mamba: Linear-Time Sequence Modeling with
 // Selective State Spaces 论文分析", "解决方案：Kernel Fusion + Recomputation", whose backward
@@ -14,7 +14,7 @@
 //  - checkpoint mode (every chunk): the chunk from its true start state (the initial state
 //    folded with the summaries of the chunks before it, using the associativity of
 //    (a, b) o (a', b') = (a a', a b' + b) and prod_t exp(delta_t A) = exp(A sum_t delta_t)),
-//    storing the state before each tile.
+//    storing the state before every 8 steps (two per tile).
 
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
@@ -28,6 +28,7 @@ namespace ssm {
 constexpr int kScanCh = 32;                          // channels per CTA
 constexpr int kScanTile = 16;                        // time steps per pipelined tile
 constexpr int kChunkAlign = 32;
+static_assert(kScanTile == 2 * kCkptSteps, "two checkpoints per tile");
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {
   const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
@@ -202,19 +203,20 @@ scan_state_kernel(const ScanParams p) {
     cp_async_wait_prev();
     __syncthreads();
     const int64_t ts = t0 + (int64_t)tile * kScanTile;
-    if constexpr (kCkpt) {  // the state before this tile (chunks start on tile boundaries)
-      if (active) {
-        float* ck = p.ckpt_h + ((b * ((L + kScanTile - 1) / kScanTile) + ts / kScanTile) * Dn + d) * N;
-        if constexpr (N % 4 == 0) {  // whole 16-byte pieces (a channel's row is 16-byte aligned)
+    // checkpoint mode: the state before step ts + q (q = 0 or kCkptSteps; chunks start on
+    // tile boundaries)
+    auto store_ckpt = [&](int q) {
+      float* ck = p.ckpt_h + ((b * ((L + kCkptSteps - 1) / kCkptSteps) + (ts + q) / kCkptSteps) * Dn + d) * N;
+      if constexpr (N % 4 == 0) {  // whole 16-byte pieces (a channel's row is 16-byte aligned)
 #pragma unroll
-          for (int j = 0; j < NP; j += 2)
-            *reinterpret_cast<float4*>(ck + 2 * j) = make_float4(h[j].x, h[j].y, h[j + 1].x, h[j + 1].y);
-        } else {
+        for (int j = 0; j < NP; j += 2)
+          *reinterpret_cast<float4*>(ck + 2 * j) = make_float4(h[j].x, h[j].y, h[j + 1].x, h[j + 1].y);
+      } else {
 #pragma unroll
-          for (int j = 0; j < NP; j++) { ck[2 * j] = h[j].x; if (2 * j + 1 < N) ck[2 * j + 1] = h[j].y; }
-        }
+        for (int j = 0; j < NP; j++) { ck[2 * j] = h[j].x; if (2 * j + 1 < N) ck[2 * j + 1] = h[j].y; }
       }
-    }
+    };
+    if (kCkpt && active) store_ckpt(0);
     if (active) {
       if (ts + kScanTile <= t1) {
         // two steps' step sizes at once in packed fp32x2, then the two recurrence steps
@@ -226,6 +228,7 @@ scan_state_kernel(const ScanParams p) {
           const float2 w = __fmul2_rn(dt, make_float2(to_f32(sX[stage][1][k][tid]), to_f32(sX[stage][1][k + 1][tid])));
           advance(stage, k, dt.x, w.x);
           advance(stage, k + 1, dt.y, w.y);
+          if (kCkpt && k + 2 == kCkptSteps) store_ckpt(kCkptSteps);
         }
       } else {
         const int steps = (int)(t1 - ts);
@@ -233,6 +236,7 @@ scan_state_kernel(const ScanParams p) {
           const float x = to_f32(sX[stage][0][k][tid]) + bias;
           const float dt = sp ? softplus(x) : x;
           advance(stage, k, dt, dt * to_f32(sX[stage][1][k][tid]));
+          if (kCkpt && k + 1 == kCkptSteps && steps > kCkptSteps) store_ckpt(kCkptSteps);
         }
       }
     }

@@ -4,29 +4,27 @@
 // The pages describe the backward only as "recompute the intermediate states in the backward
 // pass instead of storing them" (youngju.dev, "Mamba: Linear-Time Sequence Modeling with
 // Selective State Spaces 论文分析", section "解决方案：Kernel Fusion + Recomputation").  Here:
-//  1. forward checkpoints: the forward scan's own kernels (its summary pass, then its
-//     one-lane kernel in checkpoint mode) store the state before every 16-step tile — one
-//     state per 16 steps, never the per-step states;
-//  2. reverse summaries: the adjoint lambda_t = ds_t C_t + dA_{t+1} lambda_{t+1} runs
-//     backwards in time with the same chunk decomposition; per chunk, its carry-out from a
-//     zero carry-in and its decay exp(A sum delta);
-//  3. gradients: one CTA per (batch row, time chunk, 32 or 16 channels) starts from the
-//     adjoint carry entering its chunk from the right (dL/dlast_state folded with the
-//     summaries of the later chunks) and walks the chunk's tiles backwards: per tile it
-//     recomputes the 16 states into shared memory from the tile's checkpoint, then carries
-//     the adjoint through the tile while forming every gradient.  dB and dC sum over
-//     channels (a warp reduction, then one atomic add per lane).
-// All arithmetic is fp32; one thread per (batch, channel), all d_state states in registers.
+//  1. forward checkpoints: the forward scan's one-lane state kernels (ssm_scan.cu; its summary
+//     pass, then its checkpoint mode) store the state before every 8 steps — never the
+//     per-step states;
+//  2. reverse summaries (time-chunked plans only): the adjoint
+//     lambda_t = ds_t C_t + dA_{t+1} lambda_{t+1} runs backwards over each chunk from a zero
+//     carry; per chunk, its carry-out and its decay exp(A sum delta);
+//  3. gradients: one CTA per (batch row, time chunk, 64 channels) walks the chunk's 8-step
+//     tiles backwards from the adjoint carry entering it from the right, recomputing each
+//     tile's states from its checkpoint (section 3 below).
+// All arithmetic is fp32.
 
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
 
 #include <algorithm>
+#include <type_traits>
 
 namespace ssm {
 
-constexpr int kBwdCh = 32;    // channels per CTA (one warp)
-constexpr int kBwdTile = 16;  // time steps per tile
+constexpr int kBwdCh = 32;    // channels per CTA of the reverse-summary kernel (one warp)
+constexpr int kBwdTile = 16;  // its time steps per tile
 
 template <typename T>
 __device__ __forceinline__ float ldf(const void* p, int64_t i) {
@@ -144,450 +142,587 @@ __global__ void __launch_bounds__(kBwdCh) bwd_reverse_summary_kernel(const BwdAr
 }
 
 // ---------------------------------------------------------------------------------------
-// 3. Gradients for one tile.  Lane = channel; the 2N per-step partials of dB (lambda dt u) and
-//    dC (ds h) are summed over the 32 channels by a reduce-scatter: after five halving
-//    exchanges lane j holds the warp's total of value j, and adds it to global memory.
-template <int N>
-__device__ __forceinline__ void warp_reduce_scatter_add(float (&v)[32], int lane, float* dB_row,
-                                                        float* dC_row) {
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
-    const bool upper = (lane & o) != 0;
-#pragma unroll
-    for (int j = 0; j < o; j++) {
-      const float send = upper ? v[j] : v[j + o];
-      const float keep = upper ? v[j + o] : v[j];
-      v[j] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, o);
-    }
+// 3. Gradients.  A CTA covers 64 consecutive channels of one batch row over one time chunk
+//    and walks the chunk's 8-step tiles backwards, starting from the adjoint carry that
+//    enters the chunk from the right.  Each thread owns a channel pair (d, d+1) and 4 of the
+//    pair's states; the L lanes of a pair (L = 1, 2 or 4) split its 4L >= d_state states, and
+//    state arithmetic runs on packed fp32 pairs of adjacent states.  Per tile:
+//     - delta, u, z and dy rows (64 channels, 8 steps) are in shared memory (cp.async, issued
+//       while the previous tile ran), B/C rows as fp32 (prefetched into registers);
+//     - pre-phase: lane l does the per-element work of the steps k = l (mod L) once: step
+//       size, delta*u, the gated output gradient ds = dy silu(z), and keeps the factors of
+//       dz and of the softplus derivative for its own steps;
+//     - forward recompute from the tile's checkpoint; the states after the odd steps go to
+//       shared memory.  The reverse walk rebuilds each even step's state from the odd one
+//       before it with one recurrence step: it needs that step's exp(delta A) anyway;
+//     - reverse walk: lambda_t = m + ds_t C_t, the gradients of every input, m <- dA_t lambda_t.
+//       Sums over states (delta, u and z gradients) go through shared memory per 4-step group;
+//       dB and dC (sums over channels) through a warp reduce-scatter, then the CTA's warps are
+//       added in shared memory and the tile's rows go to global memory as float4 atomics.
+namespace bwd {
+
+constexpr int kCh = 64;   // channels per CTA
+constexpr int kCP = 32;   // channel pairs per CTA
+constexpr int kT = kCkptSteps;  // steps per tile (one checkpoint per tile)
+constexpr int kOG = 4;    // steps per output group
+static_assert(kT == 8, "the reverse walk is written for 8-step tiles");
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {
+  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  const int n = valid ? 16 : 0;  // n == 0: no global read, 16 zero bytes written
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem), "r"(n));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::); }
+
+template <typename T> struct PairIO;
+template <> struct PairIO<float> {
+  static __device__ __forceinline__ float2 load(const unsigned char* p) {
+    return *reinterpret_cast<const float2*>(p);
   }
-  if (lane < N) atomicAdd(dB_row + lane, v[0]);
-  else if (lane < 2 * N) atomicAdd(dC_row + lane - N, v[0]);
+  static __device__ __forceinline__ void store(void* p, float2 v) { *reinterpret_cast<float2*>(p) = v; }
+};
+template <> struct PairIO<__nv_bfloat16> {
+  static __device__ __forceinline__ float2 load(const unsigned char* p) {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+  }
+  static __device__ __forceinline__ void store(void* p, float2 v) {
+    *reinterpret_cast<__nv_bfloat162*>(p) = __float22bfloat162_rn(v);
+  }
+};
+
+// softplus(x) and its derivative sigmoid(x) from one exponential e = exp(-|x|):
+// softplus = max(x, 0) + log1p(e), sigmoid = (x >= 0 ? 1 : e) / (1 + e).
+__device__ __forceinline__ void softplus_sigmoid2(float2 x, float2& sp, float2& sg) {
+  const float2 e = make_float2(ex2(-fabsf(x.x) * kLog2e), ex2(-fabsf(x.y) * kLog2e));
+  sp = __fadd2_rn(make_float2(fmaxf(x.x, 0.f), fmaxf(x.y, 0.f)), log1p_unit2(e));
+  const float2 r = make_float2(rcp(1.f + e.x), rcp(1.f + e.y));
+  sg = make_float2(x.x >= 0.f ? r.x : e.x * r.x, x.y >= 0.f ? r.y : e.y * r.y);
 }
 
-// The adjoint carry entering chunk c from the right for states nb + 2j, nb + 2j + 1 (j < NP):
-// dL/dlast_state (or zero) folded with the reverse summaries of chunks n_chunks - 1 .. c + 1.
-template <int N, int NP>
-__device__ __forceinline__ void chunk_carry_in(const BwdArgs& p, int64_t b, int64_t dc, int c, int nb,
-                                               const float2 (&A2)[NP], float2 (&m)[NP]) {
-  const int64_t Dn = p.d_inner;
-#pragma unroll
-  for (int j = 0; j < NP; j++) m[j] = make_float2(0.f, 0.f);
-  if (p.dlast) {
-    const float* dl = p.dlast + (b * Dn + dc) * N + nb;
-#pragma unroll
-    for (int j = 0; j < NP; j++) m[j] = make_float2(dl[2 * j], nb + 2 * j + 1 < N ? dl[2 * j + 1] : 0.f);
-  }
-  for (int jc = p.n_chunks - 1; jc > c; jc--) {
-    const int64_t slot = (b * p.n_chunks + jc) * Dn + dc;
-    const float S = p.rws_S[slot];
-    const float* ms = p.rws_m + slot * N + nb;
-#pragma unroll
-    for (int j = 0; j < NP; j++) {
-      m[j].x = fmaf(ex2(A2[j].x * S), m[j].x, ms[2 * j]);
-      m[j].y = fmaf(ex2(A2[j].y * S), m[j].y, nb + 2 * j + 1 < N ? ms[2 * j + 1] : 0.f);
-    }
-  }
-}
+template <int L, typename T>
+struct Cfg {
+  static constexpr int kThreads = 32 * L;
+  static constexpr int kWarps = L;
+  static constexpr int kNP = 4 * L;                 // states held per pair (>= d_state)
+  static constexpr int kTS = (int)sizeof(T);
+  static constexpr int kRowB = kCh * kTS;            // one activation row of the CTA's channels
+  static constexpr int kChunks = kRowB / 16;         // 16-byte pieces per row
+  static constexpr int kPairB = 2 * kTS;
+  static constexpr int kSwz = 8 / L;                 // row swizzle step
+  static constexpr int kXB = 4 * kT * kRowB;         // delta, u, z, dy rows of one tile
+  static constexpr int kBCB = 2 * kT * kNP * 4;      // B, C rows (fp32)
+  static constexpr int kQB = 2 * kT * kCP * 16;      // per step and pair: (dt, dt*u), (ds, u)
+  static constexpr int kHB = (kT / 2) * 2 * kThreads * 16;  // states after the odd steps
+  static constexpr int kP4B = kOG * L * kCP * 16;    // per-lane partial sums (ddt, u-gradient)
+  static constexpr int kP2B = kOG * L * kCP * 8;     // per-lane partial readouts
+  static constexpr int kRB = kT * kWarps * 2 * kNP * 4;  // dB/dC rows per warp
+  static constexpr int kSmem = kXB + kBCB + kQB + kHB + kP4B + kP2B + kRB;
+};
 
-template <int N, typename T>
-__global__ void __launch_bounds__(kBwdCh) bwd_grad_kernel(const BwdArgs p) {
-  static_assert(2 * N <= 32, "dB/dC partials must fit one value per lane");
-  constexpr int NP = (N + 1) / 2;          // state pairs (packed fp32x2 arithmetic)
-  constexpr int NQ = (2 * NP + 3) / 4;     // groups of 4 states in the shared state rows
-  const int64_t n_dtiles = (p.d_inner + kBwdCh - 1) / kBwdCh;
-  const int64_t tiles = (p.L + kBwdTile - 1) / kBwdTile;
+template <int L, typename T>
+__global__ void __launch_bounds__(32 * L, L == 4 ? 3 : (L == 2 ? 6 : 12)) grad_kernel(const BwdArgs p) {
+  using K = Cfg<L, T>;
+  constexpr int kNP = K::kNP;
+  extern __shared__ __align__(16) unsigned char smem[];
+  unsigned char* sX = smem;                                                    // [4][kT][kRowB]
+  float* sBC = reinterpret_cast<float*>(smem + K::kXB);                        // [2][kT][kNP]
+  float4* sQ = reinterpret_cast<float4*>(smem + K::kXB + K::kBCB);              // [kT][2][kCP]
+  float4* sH = reinterpret_cast<float4*>(smem + K::kXB + K::kBCB + K::kQB);     // [kT/2][2][kThreads]
+  float4* sP4 = reinterpret_cast<float4*>(smem + K::kXB + K::kBCB + K::kQB + K::kHB);  // [kOG][L][kCP]
+  float2* sP2 = reinterpret_cast<float2*>(smem + K::kXB + K::kBCB + K::kQB + K::kHB + K::kP4B);
+  float* sR = reinterpret_cast<float*>(smem + K::kXB + K::kBCB + K::kQB + K::kHB + K::kP4B + K::kP2B);
+
+  const int N = p.d_state;
+  const int64_t Dn = p.d_inner, Ls = p.L;
+  const int64_t n_dt = (Dn + kCh - 1) / kCh;
   int64_t blk = blockIdx.x;
-  const int64_t dtile = blk % n_dtiles;
-  blk /= n_dtiles;
+  const int64_t dtile = blk % n_dt;
+  blk /= n_dt;
   const int c = (int)(blk % p.n_chunks);
   const int64_t b = blk / p.n_chunks;
-  const int lane = threadIdx.x;
-  const int64_t Dn = p.d_inner, L = p.L, d = dtile * kBwdCh + lane;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int l = lane % L;
+  const int P = warp * (32 / L) + lane / L;
+  const int64_t d0 = dtile * kCh;
+  const int64_t d = d0 + 2 * P;
   const bool active = d < Dn;
-  const int64_t dc = active ? d : 0;
-  const int64_t t0 = (int64_t)c * p.chunk_len, t1 = min(t0 + p.chunk_len, L);
-  const int64_t tl_lo = t0 / kBwdTile, tl_hi = (t1 - 1) / kBwdTile;  // chunks hold whole tiles
-  __shared__ __align__(16) float sB[kBwdTile][4 * NQ], sC[kBwdTile][4 * NQ];
-  // states after each step of the tile: [step][group of 4 states][lane][4] (16-byte rows)
-  __shared__ __align__(16) float4 sH[kBwdTile][NQ][kBwdCh];
+  const int n0 = 4 * l;
+  const int64_t t0 = (int64_t)c * p.chunk_len, t1 = min(t0 + p.chunk_len, Ls);
+  const int64_t tiles = (Ls + kT - 1) / kT;
+  const int64_t tl_lo = t0 / kT, tl_hi = (t1 - 1) / kT;  // chunks hold whole tiles
 
-  float2 A2[NP], Af[NP], m[NP], dAacc[NP];
+  // Index s = 2c + j: channel d + c, states n0 + 2j, n0 + 2j + 1.
+  float2 A2[4], Af[4], m[4], dAacc[4];
 #pragma unroll
-  for (int j = 0; j < NP; j++) {
-    const int n0 = 2 * j, n1 = 2 * j + 1;
-    const float a0 = p.A[dc * N + n0], a1 = n1 < N ? p.A[dc * N + n1] : 0.f;
-    Af[j] = make_float2(a0, a1);
-    A2[j] = make_float2(a0 * kLog2e, a1 * kLog2e);
-    dAacc[j] = make_float2(0.f, 0.f);
+  for (int s = 0; s < 4; s++) {
+    const int cc = s / 2, n = n0 + 2 * (s % 2);
+    const float* Ar = p.A + (active ? (d + cc) * N : 0);
+    const float a0 = (active && n < N) ? Ar[n] : 0.f, a1 = (active && n + 1 < N) ? Ar[n + 1] : 0.f;
+    Af[s] = make_float2(a0, a1);
+    A2[s] = make_float2(a0 * kLog2e, a1 * kLog2e);
+    dAacc[s] = make_float2(0.f, 0.f);
+    m[s] = make_float2(0.f, 0.f);
+    if (!active) continue;
+    // adjoint carry entering the chunk: dL/dlast_state folded with the reverse summaries of
+    // the chunks after it
+    if (p.dlast) {
+      const float* dl = p.dlast + (b * Dn + d + cc) * N;
+      m[s] = make_float2(n < N ? dl[n] : 0.f, n + 1 < N ? dl[n + 1] : 0.f);
+    }
+    for (int jc = p.n_chunks - 1; jc > c; jc--) {
+      const int64_t slot = (b * p.n_chunks + jc) * Dn + d + cc;
+      const float S = p.rws_S[slot];
+      const float* ms = p.rws_m + slot * N;
+      m[s].x = fmaf(ex2(A2[s].x * S), m[s].x, n < N ? ms[n] : 0.f);
+      m[s].y = fmaf(ex2(A2[s].y * S), m[s].y, n + 1 < N ? ms[n + 1] : 0.f);
+    }
   }
-  chunk_carry_in<N, NP>(p, b, dc, c, 0, A2, m);
-  if (2 * NP != 4 * NQ || 2 * NP != N) {  // zero the padding columns of the B/C rows
-    for (int i = lane; i < kBwdTile * 4 * NQ; i += kBwdCh) { sB[i / (4 * NQ)][i % (4 * NQ)] = 0.f; sC[i / (4 * NQ)][i % (4 * NQ)] = 0.f; }
+  const float2 bias2 = (active && p.delta_bias) ? make_float2(p.delta_bias[d], p.delta_bias[d + 1])
+                                                : make_float2(0.f, 0.f);
+  const float2 D2 = (active && p.D) ? make_float2(p.D[d], p.D[d + 1]) : make_float2(0.f, 0.f);
+  const bool sp = p.softplus != 0;
+  const bool has_z = p.z != nullptr;
+  float2 dDacc = make_float2(0.f, 0.f), dbacc = make_float2(0.f, 0.f);
+
+  if (kNP > N) {  // padding state columns of the B/C rows read as zero
+    for (int i = tid; i < 2 * kT * (kNP - N); i += K::kThreads)
+      sBC[(i / (kNP - N)) * kNP + N + i % (kNP - N)] = 0.f;
   }
-  const float bias = p.delta_bias ? p.delta_bias[dc] : 0.f;
-  const float Dd = p.D ? p.D[dc] : 0.f;
-  float dDacc = 0.f, dbacc = 0.f;
-  auto hrow = [&](int k, int j) -> float2 {
-    const float4 q = sH[k][j / 2][lane];
-    return (j & 1) ? make_float2(q.z, q.w) : make_float2(q.x, q.y);
+
+  const int pchunk = (P * K::kPairB) / 16, pwithin = (P * K::kPairB) % 16;
+  const char* xsrc[4] = {static_cast<const char*>(p.delta), static_cast<const char*>(p.u),
+                         static_cast<const char*>(p.z), static_cast<const char*>(p.dy)};
+  // One tile's activation rows: 16-byte piece ch of row r of array x lands at piece
+  // ch ^ ((r % L) * kSwz), so that the L rows the lanes of a pair read at once hit distinct banks.
+  auto issue_tile = [&](int64_t tl) {
+    const int64_t ts = tl * kT;
+    constexpr int kPieces = kT * K::kChunks;
+#pragma unroll
+    for (int x = 0; x < 4; x++) {
+      if (x == 2 && !has_z) continue;
+      const char* g0 = xsrc[x] + ((b * Ls + ts) * Dn + d0) * K::kTS;
+#pragma unroll
+      for (int j = 0; j < (kPieces + K::kThreads - 1) / K::kThreads; j++) {
+        const int q = tid + j * K::kThreads;
+        if (kPieces % K::kThreads == 0 || q < kPieces) {
+          const int r = q / K::kChunks, ch = q % K::kChunks;
+          const bool valid = ts + r < t1 && d0 + ch * (16 / K::kTS) < Dn;
+          cp_async16(sX + (x * kT + r) * K::kRowB + ((ch ^ ((r % L) * K::kSwz)) * 16),
+                     valid ? g0 + (int64_t)r * Dn * K::kTS + ch * 16 : xsrc[x], valid);
+        }
+      }
+    }
   };
-  auto pair_of = [&](const float* row, int j) -> float2 {
-    return *reinterpret_cast<const float2*>(row + 2 * j);
+  auto xrow = [&](int x, int r) {
+    return sX + (x * kT + r) * K::kRowB + (((pchunk ^ ((r % L) * K::kSwz)) * 16) + pwithin);
   };
 
-  for (int64_t tl = tl_hi; tl >= tl_lo; tl--) {
-    const int64_t ts = tl * kBwdTile;
-    const int steps = (int)min((int64_t)kBwdTile, L - ts);
-    float xs[kBwdTile], us[kBwdTile], dys[kBwdTile], zs[kBwdTile];
+  // B/C rows of a tile: global -> registers -> fp32 shared memory.  Whole 16-byte pieces when
+  // the rows are exactly the padded width and 16-byte multiples, element by element otherwise.
+  const T* __restrict__ Bg = static_cast<const T*>(p.B);
+  const T* __restrict__ Cg = static_cast<const T*>(p.C);
+  constexpr int kVec = 16 / K::kTS;
+  constexpr int kBCVals = 2 * kT * kNP;
+  constexpr int kVecPT = (kBCVals / kVec + K::kThreads - 1) / K::kThreads;
+  constexpr int kScPT = (kBCVals + K::kThreads - 1) / K::kThreads;
+  const bool vec_bc = N == kNP && (N * K::kTS) % 16 == 0;
+  uint4 bcv[kVecPT];
+  float bcs[kScPT];
+  auto load_bc = [&](int64_t tl) {
+    const int64_t ts = tl * kT;
+    const int64_t e0 = (b * Ls + ts) * N;
+    const int64_t rows = min((int64_t)kT, t1 - ts);
+    if (vec_bc) {
 #pragma unroll
-    for (int k = 0; k < kBwdTile; k++) {
-      const int64_t e = (b * L + ts + min(k, steps - 1)) * Dn + dc;
-      xs[k] = ldf<T>(p.delta, e) + bias;
-      us[k] = ldf<T>(p.u, e);
-      dys[k] = ldf<T>(p.dy, e);
-      zs[k] = p.z ? ldf<T>(p.z, e) : 0.f;
+      for (int j = 0; j < kVecPT; j++) {
+        const int e = (tid + j * K::kThreads) * kVec;  // element of [which][k][n]
+        const int which = e / (kT * N), ew = e % (kT * N);
+        bcv[j] = make_uint4(0, 0, 0, 0);
+        if (e < kBCVals && ew / N < rows) bcv[j] = __ldg(reinterpret_cast<const uint4*>((which ? Cg : Bg) + e0 + ew));
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < kScPT; j++) {
+        const int e = tid + j * K::kThreads;
+        const int which = e / (kT * N), ew = e % (kT * N);
+        bcs[j] = 0.f;
+        if (e < 2 * kT * N && ew / N < rows) bcs[j] = to_f32((which ? Cg : Bg)[e0 + ew]);
+      }
     }
-    __syncwarp();
-    for (int i = lane; i < steps * N; i += kBwdCh) {
-      sB[i / N][i % N] = ldf<T>(p.B, (b * L + ts) * N + i);
-      sC[i / N][i % N] = ldf<T>(p.C, (b * L + ts) * N + i);
-    }
-    float2 h0[NP];
-    {
-      const float* hk = p.ckpt_h + ((b * tiles + tl) * Dn + dc) * N;
+  };
+  auto store_bc = [&]() {
+    if (vec_bc) {
 #pragma unroll
-      for (int j = 0; j < NP; j++)
-        h0[j] = active ? make_float2(hk[2 * j], 2 * j + 1 < N ? hk[2 * j + 1] : 0.f) : make_float2(0.f, 0.f);
-    }
-    __syncwarp();
-    float dts[kBwdTile];
-    tile_step_sizes(xs, 0.f, p.softplus != 0, dts);  // xs hold delta_raw + bias
-
-    // forward recompute of the tile's states into shared memory
-    {
-      float2 h[NP];
+      for (int j = 0; j < kVecPT; j++) {
+        const int e = (tid + j * K::kThreads) * kVec;
+        if (e < kBCVals) {
+          float* dst = sBC + e;  // N == kNP: the layouts agree
+          const uint4 v = bcv[j];
+          if constexpr (K::kTS == 4) {
+            *reinterpret_cast<float4*>(dst) = make_float4(__uint_as_float(v.x), __uint_as_float(v.y),
+                                                          __uint_as_float(v.z), __uint_as_float(v.w));
+          } else {
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int j = 0; j < NP; j++) h[j] = h0[j];
-#pragma unroll
-      for (int k = 0; k < kBwdTile; k++) {
-        if (k < steps) {
-          const float2 dt2 = make_float2(dts[k], dts[k]);
-          const float w = dts[k] * us[k];
-          const float2 w2 = make_float2(w, w);
-#pragma unroll
-          for (int j = 0; j < NP; j++) {
-            const float2 xa = __fmul2_rn(dt2, A2[j]);
-            h[j] = __ffma2_rn(make_float2(ex2(xa.x), ex2(xa.y)), h[j], __fmul2_rn(w2, pair_of(sB[k], j)));
+            for (int q = 0; q < 2; q++)
+              *reinterpret_cast<float4*>(dst + 4 * q) = make_float4(
+                  __uint_as_float(w4[2 * q] << 16), __uint_as_float(w4[2 * q] & 0xFFFF0000u),
+                  __uint_as_float(w4[2 * q + 1] << 16), __uint_as_float(w4[2 * q + 1] & 0xFFFF0000u));
           }
+        }
+      }
+    } else {
 #pragma unroll
-          for (int q = 0; q < NQ; q++)
-            sH[k][q][lane] = make_float4(h[2 * q].x, h[2 * q].y, 2 * q + 1 < NP ? h[2 * q + 1].x : 0.f,
-                                         2 * q + 1 < NP ? h[2 * q + 1].y : 0.f);
+      for (int j = 0; j < kScPT; j++) {
+        const int e = tid + j * K::kThreads;
+        if (e < 2 * kT * N) {
+          const int which = e / (kT * N), ew = e % (kT * N);
+          sBC[(which * kT + ew / N) * kNP + ew % N] = bcs[j];
         }
       }
     }
-    __syncwarp();
+  };
 
-    // reverse over the tile; hk holds the state after step k, loaded one step ahead
-    float2 hk[NP];
+  // The state before a tile (its checkpoint) for this thread's 4 states of both channels.
+  float2 h0[4], h0n[4];
+  auto load_ckpt = [&](int64_t tl, float2 (&h)[4]) {
 #pragma unroll
-    for (int j = 0; j < NP; j++) hk[j] = hrow(kBwdTile - 1 < steps ? kBwdTile - 1 : 0, j);
+    for (int s = 0; s < 4; s++) h[s] = make_float2(0.f, 0.f);
+    if (!active) return;
 #pragma unroll
-    for (int k = kBwdTile - 1; k >= 0; k--) {
-      if (k >= steps) {
-        if (k - 1 >= 0 && k - 1 < steps) {
-#pragma unroll
-          for (int j = 0; j < NP; j++) hk[j] = hrow(k - 1, j);
+    for (int cc = 0; cc < 2; cc++) {
+      const float* ck = p.ckpt_h + ((b * tiles + tl) * Dn + d + cc) * N;
+      if (N % 4 == 0) {
+        if (n0 < N) {
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(ck + n0));
+          h[2 * cc] = make_float2(v.x, v.y);
+          h[2 * cc + 1] = make_float2(v.z, v.w);
         }
-        continue;
-      }
-      const int64_t e = (b * L + ts + k) * Dn + dc;
-      float2 hp[NP];
+      } else {
 #pragma unroll
-      for (int j = 0; j < NP; j++) hp[j] = k > 0 ? hrow(k - 1, j) : h0[j];
-      float2 s2 = make_float2(Dd * us[k], 0.f);
-#pragma unroll
-      for (int j = 0; j < NP; j++) s2 = __ffma2_rn(pair_of(sC[k], j), hk[j], s2);
-      const float s = s2.x + s2.y;
-      float g = 1.f;
-      if (p.z) {
-        const float sg = rcp(1.f + ex2(-zs[k] * kLog2e));
-        g = zs[k] * sg;
-        if (active) static_cast<T*>(p.dz)[e] = from_f32<T>(dys[k] * s * sg * fmaf(zs[k], 1.f - sg, 1.f));
+        for (int j = 0; j < 2; j++) {
+          const int n = n0 + 2 * j;
+          h[2 * cc + j] = make_float2(n < N ? ck[n] : 0.f, n + 1 < N ? ck[n + 1] : 0.f);
+        }
       }
-      const float ds = dys[k] * g;
-      dDacc = fmaf(ds, us[k], dDacc);
-      const float dt = dts[k];
-      const float2 dt2 = make_float2(dt, dt), ds2 = make_float2(ds, ds), u2 = make_float2(us[k], us[k]);
-      const float dtu = dt * us[k];
-      const float2 dtu2 = make_float2(active ? dtu : 0.f, active ? dtu : 0.f);
-      const float2 dsa = make_float2(active ? ds : 0.f, active ? ds : 0.f);
-      float2 ddt2 = make_float2(0.f, 0.f), slb2 = make_float2(0.f, 0.f);
-      float v[32];
-#pragma unroll
-      for (int j = 0; j < NP; j++) {
-        const float2 Bv = pair_of(sB[k], j);
-        const float2 lam = __ffma2_rn(ds2, pair_of(sC[k], j), m[j]);
-        const float2 xa = __fmul2_rn(dt2, A2[j]);
-        const float2 dA = make_float2(ex2(xa.x), ex2(xa.y));
-        const float2 t1 = __fmul2_rn(__fmul2_rn(lam, hp[j]), dA);
-        ddt2 = __ffma2_rn(t1, Af[j], __ffma2_rn(lam, __fmul2_rn(Bv, u2), ddt2));
-        dAacc[j] = __ffma2_rn(t1, dt2, dAacc[j]);
-        slb2 = __ffma2_rn(lam, Bv, slb2);
-        const float2 pb = __fmul2_rn(lam, dtu2), pc = __fmul2_rn(dsa, hk[j]);
-        v[2 * j] = pb.x;
-        if (2 * j + 1 < N) v[2 * j + 1] = pb.y;
-        v[N + 2 * j] = pc.x;
-        if (2 * j + 1 < N) v[N + 2 * j + 1] = pc.y;
-        m[j] = __fmul2_rn(dA, lam);
-        hk[j] = hp[j];
-      }
-#pragma unroll
-      for (int j = 2 * N; j < 32; j++) v[j] = 0.f;
-      const float ddt = ddt2.x + ddt2.y;
-      const float dx = p.softplus ? ddt * rcp(1.f + ex2(-xs[k] * kLog2e)) : ddt;
-      dbacc += dx;
-      if (active) {
-        static_cast<T*>(p.du)[e] = from_f32<T>(fmaf(ds, Dd, dt * (slb2.x + slb2.y)));
-        static_cast<T*>(p.ddelta)[e] = from_f32<T>(dx);
-      }
-      warp_reduce_scatter_add<N>(v, lane, p.dB + (b * L + ts + k) * N, p.dC + (b * L + ts + k) * N);
     }
-    __syncwarp();
+  };
+
+  // pair-of-step quantities (both channels) of step k, from the pre-phase
+  auto q_dt = [&](int k) { return sQ[(k * 2 + 0) * kCP + (P ^ ((k % L) * K::kSwz))]; };  // dt0 dt1 dtu0 dtu1
+  auto q_ds = [&](int k) { return sQ[(k * 2 + 1) * kCP + (P ^ ((k % L) * K::kSwz))]; };  // ds0 ds1 u0 u1
+  auto brow = [&](int k) { return *reinterpret_cast<const float4*>(sBC + (0 * kT + k) * kNP + n0); };
+  auto crow = [&](int k) { return *reinterpret_cast<const float4*>(sBC + (1 * kT + k) * kNP + n0); };
+
+  // exp(dt A) for the 4 state pairs at step k
+  auto decays = [&](const float4 q, float2 (&dA)[4]) {
+#pragma unroll
+    for (int s = 0; s < 4; s++) {
+      const float dtc = s < 2 ? q.x : q.y;
+      const float2 xa = __fmul2_rn(make_float2(dtc, dtc), A2[s]);
+      dA[s] = make_float2(ex2(xa.x), ex2(xa.y));
+    }
+  };
+  // one forward step: h <- dA h + dt u B
+  auto fwd_step = [&](const float4 q, const float4 Bq, const float2 (&dA)[4], const float2 (&hin)[4], float2 (&hout)[4]) {
+    const float2 Bp[2] = {make_float2(Bq.x, Bq.y), make_float2(Bq.z, Bq.w)};
+#pragma unroll
+    for (int s = 0; s < 4; s++) {
+      const float w = s < 2 ? q.z : q.w;
+      hout[s] = __ffma2_rn(dA[s], hin[s], __fmul2_rn(make_float2(w, w), Bp[s % 2]));
+    }
+  };
+
+  float4 own[kT / L];  // per own step: (dz factor, softplus derivative) of both channels
+
+  // one reverse step at step k: hk = state after step k, hp = before, dA = exp(dt_k A)
+  auto rev_step = [&](int k, const float2 (&hk)[4], const float2 (&hp)[4], const float2 (&dA)[4]) {
+    const float4 q0 = q_dt(k), q1 = q_ds(k);
+    const float4 Bq = brow(k), Cq = crow(k);
+    const float2 Bp[2] = {make_float2(Bq.x, Bq.y), make_float2(Bq.z, Bq.w)};
+    const float2 Cp[2] = {make_float2(Cq.x, Cq.y), make_float2(Cq.z, Cq.w)};
+    float2 ddt[2], slb[2], rd[2], pbs[2], pcs[2];
+#pragma unroll
+    for (int cc = 0; cc < 2; cc++) {
+      const float dt = cc ? q0.y : q0.x, dtu = cc ? q0.w : q0.z;
+      const float ds = cc ? q1.y : q1.x, uu = cc ? q1.w : q1.z;
+      const float2 dt2 = make_float2(dt, dt), dtu2 = make_float2(dtu, dtu), ds2 = make_float2(ds, ds),
+                   u2 = make_float2(uu, uu);
+      ddt[cc] = slb[cc] = rd[cc] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < 2; j++) {
+        const int s = 2 * cc + j;
+        const float2 lam = __ffma2_rn(ds2, Cp[j], m[s]);
+        const float2 t1 = __fmul2_rn(__fmul2_rn(lam, hp[s]), dA[s]);
+        ddt[cc] = __ffma2_rn(t1, Af[s], __ffma2_rn(lam, __fmul2_rn(Bp[j], u2), ddt[cc]));
+        dAacc[s] = __ffma2_rn(t1, dt2, dAacc[s]);
+        slb[cc] = __ffma2_rn(lam, Bp[j], slb[cc]);
+        rd[cc] = __ffma2_rn(Cp[j], hk[s], rd[cc]);
+        const float2 pb = __fmul2_rn(lam, dtu2), pc = __fmul2_rn(ds2, hk[s]);
+        pbs[j] = cc ? __fadd2_rn(pbs[j], pb) : pb;
+        pcs[j] = cc ? __fadd2_rn(pcs[j], pc) : pc;
+        m[s] = __fmul2_rn(dA[s], lam);
+      }
+    }
+    // this lane's share of the per-channel sums over states
+    const int kg = k % kOG;
+    sP4[(kg * L + l) * kCP + P] = make_float4(ddt[0].x + ddt[0].y, ddt[1].x + ddt[1].y,
+                                              slb[0].x + slb[0].y, slb[1].x + slb[1].y);
+    sP2[(kg * L + l) * kCP + P] = make_float2(rd[0].x + rd[0].y, rd[1].x + rd[1].y);
+    // dB (states n0..n0+3), dC (same): summed over the warp's pairs of this lane's state
+    // slice by a reduce-scatter over the lane bits 4, 3, 2 (which keep l), so that lane holds
+    // value (lane >> 2) & 7; lane bits below 2 that are not l are then summed plainly
+    float v[8] = {pbs[0].x, pbs[0].y, pbs[1].x, pbs[1].y, pcs[0].x, pcs[0].y, pcs[1].x, pcs[1].y};
+#pragma unroll
+    for (int o = 16, h = 4; o >= 4; o >>= 1, h >>= 1) {
+      const bool upper = (lane & o) != 0;
+#pragma unroll
+      for (int j = 0; j < h; j++) {
+        const float send = upper ? v[j] : v[j + h];
+        const float keep = upper ? v[j + h] : v[j];
+        v[j] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, o);
+      }
+    }
+#pragma unroll
+    for (int o = L; o < 4; o <<= 1) v[0] += __shfl_xor_sync(0xFFFFFFFFu, v[0], o);
+    if ((lane & 3 & ~(L - 1)) == 0) {
+      const int vi = (lane >> 2) & 7;
+      const int o = vi < 4 ? n0 + vi : kNP + n0 + vi - 4;
+      sR[(k * K::kWarps + warp) * 2 * kNP + o] = v[0];
+    }
+  };
+
+  // Outputs of the steps k0 .. k0+kOG-1: lane l finishes its own steps from the L lanes'
+  // partial sums.
+  auto output_group = [&](auto k0_tag, int steps, int64_t ts) {
+    constexpr int k0 = decltype(k0_tag)::value;
+#pragma unroll
+    for (int i = 0; i < kOG / L; i++) {
+      const int k = k0 + i * L + l;
+      if (k < steps && active) {
+        float4 a = sP4[((k % kOG) * L + 0) * kCP + P];
+        float2 r = sP2[((k % kOG) * L + 0) * kCP + P];
+#pragma unroll
+        for (int mm = 1; mm < L; mm++) {
+          const float4 a2 = sP4[((k % kOG) * L + mm) * kCP + P];
+          const float2 r2 = sP2[((k % kOG) * L + mm) * kCP + P];
+          a = make_float4(a.x + a2.x, a.y + a2.y, a.z + a2.z, a.w + a2.w);
+          r = make_float2(r.x + r2.x, r.y + r2.y);
+        }
+        const float4 q0 = q_dt(k), q1 = q_ds(k);
+        const float4 f = own[k0 / L + i];
+        const float2 ddt = make_float2(a.x, a.y), slb = make_float2(a.z, a.w);
+        const float2 dx = sp ? __fmul2_rn(ddt, make_float2(f.z, f.w)) : ddt;
+        const float2 ds = make_float2(q1.x, q1.y), uu = make_float2(q1.z, q1.w), dt = make_float2(q0.x, q0.y);
+        const float2 du = __ffma2_rn(ds, D2, __fmul2_rn(dt, slb));
+        const int64_t e = ((b * Ls + ts + k) * Dn + d) * K::kTS;
+        PairIO<T>::store(static_cast<char*>(p.du) + e, du);
+        PairIO<T>::store(static_cast<char*>(p.ddelta) + e, dx);
+        if (has_z) {
+          const float2 s = __ffma2_rn(D2, uu, r);  // the output before the gate
+          PairIO<T>::store(static_cast<char*>(p.dz) + e, __fmul2_rn(s, make_float2(f.x, f.y)));
+        }
+        dbacc = __fadd2_rn(dbacc, dx);
+      }
+    }
+  };
+
+  if (tl_hi >= tl_lo) {
+    issue_tile(tl_hi);
+    cp_async_commit();
+    load_bc(tl_hi);
+    store_bc();
+    load_ckpt(tl_hi, h0);
+  }
+  for (int64_t tl = tl_hi; tl >= tl_lo; tl--) {
+    const int64_t ts = tl * kT;
+    const int steps = (int)min((int64_t)kT, t1 - ts);
+    cp_async_wait_all();
+    __syncthreads();  // this tile's rows and B/C are in shared memory
+
+    // pre-phase: the per-element work of steps k = l (mod L)
+#pragma unroll
+    for (int i = 0; i < kT / L; i++) {
+      const int k = i * L + l;
+      const float2 xr = __fadd2_rn(PairIO<T>::load(xrow(0, k)), bias2);
+      float2 spx, sgx;
+      softplus_sigmoid2(xr, spx, sgx);
+      float2 dt = sp ? spx : xr;
+      if (k >= steps) dt = make_float2(0.f, 0.f);  // steps past the end: identity steps
+      const float2 uu = PairIO<T>::load(xrow(1, k));
+      const float2 dy = PairIO<T>::load(xrow(3, k));
+      float2 ds = dy, zf = make_float2(0.f, 0.f);
+      if (has_z) {
+        const float2 zz = PairIO<T>::load(xrow(2, k));
+        const float2 sz = make_float2(rcp(1.f + ex2(-zz.x * kLog2e)), rcp(1.f + ex2(-zz.y * kLog2e)));
+        ds = __fmul2_rn(dy, __fmul2_rn(zz, sz));  // dy * silu(z)
+        // d silu / dz = sigmoid(z) (1 + z (1 - sigmoid(z)))
+        const float2 one = make_float2(1.f, 1.f);
+        zf = __fmul2_rn(__fmul2_rn(dy, sz), __ffma2_rn(zz, make_float2(1.f - sz.x, 1.f - sz.y), one));
+      }
+      const float2 dtu = __fmul2_rn(dt, uu);
+      sQ[(k * 2 + 0) * kCP + (P ^ (l * K::kSwz))] = make_float4(dt.x, dt.y, dtu.x, dtu.y);
+      sQ[(k * 2 + 1) * kCP + (P ^ (l * K::kSwz))] = make_float4(ds.x, ds.y, uu.x, uu.y);
+      own[i] = make_float4(zf.x, zf.y, sgx.x, sgx.y);
+      dDacc = __ffma2_rn(ds, uu, dDacc);
+    }
+    __syncthreads();  // sQ complete; the staged rows are free
+    if (tl > tl_lo) {
+      issue_tile(tl - 1);
+      cp_async_commit();
+      load_bc(tl - 1);
+      load_ckpt(tl - 1, h0n);
+    }
+
+    // forward recompute: the states after the odd steps to shared memory
+    {
+      float2 h[4];
+#pragma unroll
+      for (int s = 0; s < 4; s++) h[s] = h0[s];
+#pragma unroll 1
+      for (int k = 0; k < kT; k += 2) {
+#pragma unroll
+        for (int e = 0; e < 2; e++) {
+          const float4 q = q_dt(k + e);
+          float2 dA[4];
+          decays(q, dA);
+          fwd_step(q, brow(k + e), dA, h, h);
+        }
+        sH[((k / 2) * 2 + 0) * K::kThreads + tid] = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
+        sH[((k / 2) * 2 + 1) * K::kThreads + tid] = make_float4(h[2].x, h[2].y, h[3].x, h[3].y);
+      }
+    }
+
+    // reverse walk, two steps at a time: (k, k-1) with k odd
+#pragma unroll 1
+    for (int k = kT - 1; k >= 1; k -= 2) {
+      float2 hk[4], hpp[4], hm[4], dAk[4], dAm[4];
+      {
+        const float4 a0 = sH[((k / 2) * 2 + 0) * K::kThreads + tid], a1 = sH[((k / 2) * 2 + 1) * K::kThreads + tid];
+        hk[0] = make_float2(a0.x, a0.y); hk[1] = make_float2(a0.z, a0.w);
+        hk[2] = make_float2(a1.x, a1.y); hk[3] = make_float2(a1.z, a1.w);
+      }
+      if (k >= 3) {
+        const float4 a0 = sH[((k / 2 - 1) * 2 + 0) * K::kThreads + tid], a1 = sH[((k / 2 - 1) * 2 + 1) * K::kThreads + tid];
+        hpp[0] = make_float2(a0.x, a0.y); hpp[1] = make_float2(a0.z, a0.w);
+        hpp[2] = make_float2(a1.x, a1.y); hpp[3] = make_float2(a1.z, a1.w);
+      } else {
+#pragma unroll
+        for (int s = 0; s < 4; s++) hpp[s] = h0[s];
+      }
+      const float4 qm = q_dt(k - 1);
+      decays(qm, dAm);
+      fwd_step(qm, brow(k - 1), dAm, hpp, hm);  // the state after step k-1
+      decays(q_dt(k), dAk);
+      rev_step(k, hk, hm, dAk);
+      rev_step(k - 1, hm, hpp, dAm);
+      if ((k - 1) % kOG == 0) {
+        __syncwarp();
+        if (k - 1 == kOG) output_group(std::integral_constant<int, kOG>{}, steps, ts);
+        else output_group(std::integral_constant<int, 0>{}, steps, ts);
+        __syncwarp();
+      }
+    }
+    __syncthreads();  // sR complete; sBC, sH, sQ free
+
+    // dB, dC rows of this tile: the warps' sums, added to global memory
+    {
+      constexpr int kGroups = kT * 2 * kNP / 4;
+      if (tid < kGroups) {
+        const int k = tid / (2 * kNP / 4), og = tid % (2 * kNP / 4);
+        float4 acc = *reinterpret_cast<const float4*>(sR + (k * K::kWarps + 0) * 2 * kNP + 4 * og);
+#pragma unroll
+        for (int w = 1; w < K::kWarps; w++) {
+          const float4 a2 = *reinterpret_cast<const float4*>(sR + (k * K::kWarps + w) * 2 * kNP + 4 * og);
+          acc = make_float4(acc.x + a2.x, acc.y + a2.y, acc.z + a2.z, acc.w + a2.w);
+        }
+        const bool isC = og >= kNP / 4;
+        const int nb = 4 * (isC ? og - kNP / 4 : og);
+        if (k < steps && nb < N) {
+          float* row = (isC ? p.dC : p.dB) + (b * Ls + ts + k) * N + nb;
+          if (N % 4 == 0) {
+            atomicAdd(reinterpret_cast<float4*>(row), acc);
+          } else {
+            const float vals[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+            for (int q = 0; q < 4; q++)
+              if (nb + q < N) atomicAdd(row + q, vals[q]);
+          }
+        }
+      }
+    }
+    if (tl > tl_lo) {
+      store_bc();
+#pragma unroll
+      for (int s = 0; s < 4; s++) h0[s] = h0n[s];
+    }
+  }
+
+  // per-channel sums over the lanes of the pair, then one atomic per output
+#pragma unroll
+  for (int o = 1; o < L; o <<= 1) {
+    dDacc.x += __shfl_xor_sync(0xFFFFFFFFu, dDacc.x, o);
+    dDacc.y += __shfl_xor_sync(0xFFFFFFFFu, dDacc.y, o);
+    dbacc.x += __shfl_xor_sync(0xFFFFFFFFu, dbacc.x, o);
+    dbacc.y += __shfl_xor_sync(0xFFFFFFFFu, dbacc.y, o);
   }
   if (!active) return;
-#pragma unroll
-  for (int j = 0; j < NP; j++) {
-    atomicAdd(p.dA + d * N + 2 * j, dAacc[j].x);
-    if (2 * j + 1 < N) atomicAdd(p.dA + d * N + 2 * j + 1, dAacc[j].y);
+  if (l == 0) {
+    if (p.dD) { atomicAdd(p.dD + d, dDacc.x); atomicAdd(p.dD + d + 1, dDacc.y); }
+    if (p.dbias) { atomicAdd(p.dbias + d, dbacc.x); atomicAdd(p.dbias + d + 1, dbacc.y); }
   }
-  if (p.dD) atomicAdd(p.dD + d, dDacc);
-  if (p.dbias) atomicAdd(p.dbias + d, dbacc);
-  if (p.dinit && tl_lo == 0) {
 #pragma unroll
-    for (int j = 0; j < NP; j++) {
-      p.dinit[(b * Dn + d) * N + 2 * j] = m[j].x;
-      if (2 * j + 1 < N) p.dinit[(b * Dn + d) * N + 2 * j + 1] = m[j].y;
+  for (int cc = 0; cc < 2; cc++) {
+    float* row = p.dA + (d + cc) * N;
+    if (N % 4 == 0) {
+      if (n0 < N)
+        atomicAdd(reinterpret_cast<float4*>(row + n0),
+                  make_float4(dAacc[2 * cc].x, dAacc[2 * cc].y, dAacc[2 * cc + 1].x, dAacc[2 * cc + 1].y));
+    } else {
+#pragma unroll
+      for (int j = 0; j < 2; j++) {
+        const int n = n0 + 2 * j;
+        if (n < N) atomicAdd(row + n, dAacc[2 * cc + j].x);
+        if (n + 1 < N) atomicAdd(row + n + 1, dAacc[2 * cc + j].y);
+      }
+    }
+  }
+  if (p.dinit && tl_lo == 0) {  // the adjoint carry before step 0
+#pragma unroll
+    for (int cc = 0; cc < 2; cc++) {
+      float* row = p.dinit + (b * Dn + d + cc) * N;
+#pragma unroll
+      for (int j = 0; j < 2; j++) {
+        const int n = n0 + 2 * j;
+        if (n < N) row[n] = m[2 * cc + j].x;
+        if (n + 1 < N) row[n + 1] = m[2 * cc + j].y;
+      }
     }
   }
 }
 
-// ---------------------------------------------------------------------------------------
-// 3b. Gradients with two lanes per channel (d_state a multiple of 8): lane 2c + q of the warp
-//     holds states [q N/2, (q + 1) N/2) of channel c, so a CTA covers 16 channels with half
-//     the per-lane registers and half the shared state tile of the one-lane kernel per warp
-//     (about twice the warps per SM).  The per-step readout and the step-size and u gradients
-//     add the two halves with one shfl.xor each; dB and dC are summed over the 16 channels
-//     through a transpose in shared memory (each lane stores its N partials as one row, then
-//     sums one column over the 16 lanes of its parity) and added atomically, one value per
-//     lane.
-constexpr int kBwdCh2 = 16;  // channels per CTA of the two-lane gradient kernel
-
-template <int N, typename T>
-__global__ void __launch_bounds__(32, 10) bwd_grad_kernel2(const BwdArgs p) {
-  static_assert(N % 8 == 0 && N <= 16, "two lanes of whole float4 state groups");
-  constexpr int NL = N / 2;        // states per lane
-  constexpr int NP = NL / 2;       // state pairs per lane (packed fp32x2 arithmetic)
-  constexpr int NQ = NL / 4;       // float4 groups per lane in the shared state rows
-  constexpr int kPitch = N + 4;    // reduction rows: N partials + padding (16-byte aligned)
-  const int64_t n_dtiles = (p.d_inner + kBwdCh2 - 1) / kBwdCh2;
-  const int64_t tiles = (p.L + kBwdTile - 1) / kBwdTile;
-  int64_t blk = blockIdx.x;
-  const int64_t dtile = blk % n_dtiles;
-  blk /= n_dtiles;
-  const int c = (int)(blk % p.n_chunks);
-  const int64_t b = blk / p.n_chunks;
-  const int lane = threadIdx.x, q = lane & 1;
-  const int64_t Dn = p.d_inner, L = p.L, d = dtile * kBwdCh2 + (lane >> 1);
-  const bool active = d < Dn;
-  const int64_t dc = active ? d : 0;
-  const int nb = q * NL;  // first state of this lane
-  const int64_t t0 = (int64_t)c * p.chunk_len, t1 = min(t0 + p.chunk_len, L);
-  const int64_t tl_lo = t0 / kBwdTile, tl_hi = (t1 - 1) / kBwdTile;  // chunks hold whole tiles
-  __shared__ __align__(16) float sB[kBwdTile][N], sC[kBwdTile][N];
-  __shared__ __align__(16) float4 sH[kBwdTile][NQ][32];  // this lane's states after each step
-  __shared__ __align__(16) float sR[32][kPitch];          // dB/dC partials, one row per lane
-  // the reduced value this lane adds: output o = lane (o < N: dB[o], else dC[o - N]), the sum
-  // over channels of column (o < N ? 0 : NL) + o mod NL of the rows of parity (o mod N) / NL
-  const int o_col = (lane < N ? 0 : NL) + (lane % N) % NL, o_par = (lane % N) / NL;
-
-  float2 A2[NP], Af[NP], m[NP], dAacc[NP];
-#pragma unroll
-  for (int j = 0; j < NP; j++) {
-    const float a0 = p.A[dc * N + nb + 2 * j], a1 = p.A[dc * N + nb + 2 * j + 1];
-    Af[j] = make_float2(a0, a1);
-    A2[j] = make_float2(a0 * kLog2e, a1 * kLog2e);
-    dAacc[j] = make_float2(0.f, 0.f);
-  }
-  chunk_carry_in<N, NP>(p, b, dc, c, nb, A2, m);
-  const float bias = p.delta_bias ? p.delta_bias[dc] : 0.f;
-  const float Dd = p.D ? p.D[dc] : 0.f;
-  float dDacc = 0.f, dbacc = 0.f;
-  auto hrow = [&](int k, int j) -> float2 {
-    const float4 v = sH[k][j / 2][lane];
-    return (j & 1) ? make_float2(v.z, v.w) : make_float2(v.x, v.y);
-  };
-  auto pair_of = [&](const float* row, int j) -> float2 {
-    return *reinterpret_cast<const float2*>(row + nb + 2 * j);
-  };
-
-  for (int64_t tl = tl_hi; tl >= tl_lo; tl--) {
-    const int64_t ts = tl * kBwdTile;
-    const int steps = (int)min((int64_t)kBwdTile, L - ts);
-    float xs[kBwdTile], us[kBwdTile], dys[kBwdTile], zs[kBwdTile];
-#pragma unroll
-    for (int k = 0; k < kBwdTile; k++) {
-      const int64_t e = (b * L + ts + min(k, steps - 1)) * Dn + dc;
-      xs[k] = ldf<T>(p.delta, e) + bias;
-      us[k] = ldf<T>(p.u, e);
-      dys[k] = ldf<T>(p.dy, e);
-      zs[k] = p.z ? ldf<T>(p.z, e) : 0.f;
-    }
-    __syncwarp();
-    for (int i = lane; i < steps * N; i += 32) {
-      sB[i / N][i % N] = ldf<T>(p.B, (b * L + ts) * N + i);
-      sC[i / N][i % N] = ldf<T>(p.C, (b * L + ts) * N + i);
-    }
-    float2 h0[NP];
-    {
-      const float* hk = p.ckpt_h + ((b * tiles + tl) * Dn + dc) * N + nb;
-#pragma unroll
-      for (int j = 0; j < NP; j++) h0[j] = active ? make_float2(hk[2 * j], hk[2 * j + 1]) : make_float2(0.f, 0.f);
-    }
-    __syncwarp();
-    float dts[kBwdTile];
-    tile_step_sizes(xs, 0.f, p.softplus != 0, dts);  // xs hold delta_raw + bias
-
-    // forward recompute of this lane's states over the tile into shared memory
-    {
-      float2 h[NP];
-#pragma unroll
-      for (int j = 0; j < NP; j++) h[j] = h0[j];
-#pragma unroll
-      for (int k = 0; k < kBwdTile; k++) {
-        if (k < steps) {
-          const float2 dt2 = make_float2(dts[k], dts[k]);
-          const float w = dts[k] * us[k];
-          const float2 w2 = make_float2(w, w);
-#pragma unroll
-          for (int j = 0; j < NP; j++) {
-            const float2 xa = __fmul2_rn(dt2, A2[j]);
-            h[j] = __ffma2_rn(make_float2(ex2(xa.x), ex2(xa.y)), h[j], __fmul2_rn(w2, pair_of(sB[k], j)));
-          }
-#pragma unroll
-          for (int g = 0; g < NQ; g++) sH[k][g][lane] = make_float4(h[2 * g].x, h[2 * g].y, h[2 * g + 1].x, h[2 * g + 1].y);
-        }
-      }
-    }
-    __syncwarp();
-
-    // reverse over the tile; hk holds the state after step k
-    float2 hk[NP];
-#pragma unroll
-    for (int j = 0; j < NP; j++) hk[j] = hrow(kBwdTile - 1 < steps ? kBwdTile - 1 : 0, j);
-#pragma unroll
-    for (int k = kBwdTile - 1; k >= 0; k--) {
-      if (k >= steps) {
-        if (k - 1 >= 0 && k - 1 < steps) {
-#pragma unroll
-          for (int j = 0; j < NP; j++) hk[j] = hrow(k - 1, j);
-        }
-        continue;
-      }
-      const int64_t e = (b * L + ts + k) * Dn + dc;
-      float2 hp[NP];
-#pragma unroll
-      for (int j = 0; j < NP; j++) hp[j] = k > 0 ? hrow(k - 1, j) : h0[j];
-      float2 s2 = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int j = 0; j < NP; j++) s2 = __ffma2_rn(pair_of(sC[k], j), hk[j], s2);
-      const float s_half = s2.x + s2.y;
-      const float s = s_half + __shfl_xor_sync(0xFFFFFFFFu, s_half, 1) + Dd * us[k];
-      float g = 1.f;
-      if (p.z) {
-        const float sg = rcp(1.f + ex2(-zs[k] * kLog2e));
-        g = zs[k] * sg;
-        if (active && q == 0) static_cast<T*>(p.dz)[e] = from_f32<T>(dys[k] * s * sg * fmaf(zs[k], 1.f - sg, 1.f));
-      }
-      const float ds = dys[k] * g;
-      dDacc = fmaf(ds, us[k], dDacc);
-      const float dt = dts[k];
-      const float2 dt2 = make_float2(dt, dt), ds2 = make_float2(ds, ds), u2 = make_float2(us[k], us[k]);
-      const float dtu = dt * us[k];
-      const float2 dtu2 = make_float2(active ? dtu : 0.f, active ? dtu : 0.f);
-      const float2 dsa = make_float2(active ? ds : 0.f, active ? ds : 0.f);
-      float2 ddt2 = make_float2(0.f, 0.f), slb2 = make_float2(0.f, 0.f);
-      float v[N];  // dB partials of this lane's states, then dC partials
-#pragma unroll
-      for (int j = 0; j < NP; j++) {
-        const float2 Bv = pair_of(sB[k], j);
-        const float2 lam = __ffma2_rn(ds2, pair_of(sC[k], j), m[j]);
-        const float2 xa = __fmul2_rn(dt2, A2[j]);
-        const float2 dA = make_float2(ex2(xa.x), ex2(xa.y));
-        const float2 t1 = __fmul2_rn(__fmul2_rn(lam, hp[j]), dA);
-        ddt2 = __ffma2_rn(t1, Af[j], __ffma2_rn(lam, __fmul2_rn(Bv, u2), ddt2));
-        dAacc[j] = __ffma2_rn(t1, dt2, dAacc[j]);
-        slb2 = __ffma2_rn(lam, Bv, slb2);
-        const float2 pb = __fmul2_rn(lam, dtu2), pc = __fmul2_rn(dsa, hk[j]);
-        v[2 * j] = pb.x;
-        v[2 * j + 1] = pb.y;
-        v[NL + 2 * j] = pc.x;
-        v[NL + 2 * j + 1] = pc.y;
-        m[j] = __fmul2_rn(dA, lam);
-        hk[j] = hp[j];
-      }
-      const float ddt_half = ddt2.x + ddt2.y, slb_half = slb2.x + slb2.y;
-      const float ddt = ddt_half + __shfl_xor_sync(0xFFFFFFFFu, ddt_half, 1);
-      const float slb = slb_half + __shfl_xor_sync(0xFFFFFFFFu, slb_half, 1);
-      const float dx = p.softplus ? ddt * rcp(1.f + ex2(-xs[k] * kLog2e)) : ddt;
-      dbacc += dx;
-      if (active) {
-        if (q == 0) static_cast<T*>(p.du)[e] = from_f32<T>(fmaf(ds, Dd, dt * slb));
-        else static_cast<T*>(p.ddelta)[e] = from_f32<T>(dx);
-      }
-      // dB / dC: sum the partials over the 16 channels through shared memory
-#pragma unroll
-      for (int c4 = 0; c4 < N / 4; c4++)
-        *reinterpret_cast<float4*>(&sR[lane][4 * c4]) = make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
-      __syncwarp();
-      if (lane < 2 * N) {
-        float acc = 0.f;
-#pragma unroll
-        for (int c = 0; c < kBwdCh2; c++) acc += sR[2 * c + o_par][o_col];
-        float* row = (lane < N ? p.dB : p.dC) + (b * L + ts + k) * N;
-        atomicAdd(row + lane % N, acc);
-      }
-      __syncwarp();
-    }
-    __syncwarp();
-  }
-  if (!active) return;
-#pragma unroll
-  for (int j = 0; j < NP; j++) {
-    atomicAdd(p.dA + d * N + nb + 2 * j, dAacc[j].x);
-    atomicAdd(p.dA + d * N + nb + 2 * j + 1, dAacc[j].y);
-  }
-  if (q == 0) {  // per-channel sums: both lanes hold them
-    if (p.dD) atomicAdd(p.dD + d, dDacc);
-    if (p.dbias) atomicAdd(p.dbias + d, dbacc);
-  }
-  if (p.dinit && tl_lo == 0) {
-#pragma unroll
-    for (int j = 0; j < NP; j++) {
-      p.dinit[(b * Dn + d) * N + nb + 2 * j] = m[j].x;
-      p.dinit[(b * Dn + d) * N + nb + 2 * j + 1] = m[j].y;
-    }
-  }
-}
+}  // namespace bwd
 
 // ---------------------------------------------------------------------------------------
 
 size_t bwd_workspace_floats(int64_t batch, int64_t L, int64_t d_inner, int d_state, int n_chunks) {
-  const int64_t tiles = (L + kBwdTile - 1) / kBwdTile;
+  const int64_t tiles = (L + kCkptSteps - 1) / kCkptSteps;
   const int64_t ck = batch * tiles * d_inner * d_state;                 // forward checkpoints
   const int64_t fws = batch * (int64_t)std::max(n_chunks - 1, 0) * d_inner * (d_state + 1);
   const int64_t rws = batch * (int64_t)n_chunks * d_inner * (d_state + 1);
   return (size_t)(ck + fws + rws);
+}
+
+template <int L, typename T>
+static cudaError_t launch_grad(const BwdArgs& a, cudaStream_t s) {
+  using K = bwd::Cfg<L, T>;
+  const cudaError_t e = cudaFuncSetAttribute(bwd::grad_kernel<L, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, K::kSmem);
+  if (e != cudaSuccess) return e;
+  const int64_t n_dt = (a.d_inner + bwd::kCh - 1) / bwd::kCh;
+  bwd::grad_kernel<L, T><<<(unsigned)(n_dt * a.n_chunks * a.batch), K::kThreads, K::kSmem, s>>>(a);
+  return cudaGetLastError();
 }
 
 template <int N, typename T>
@@ -599,19 +734,14 @@ static cudaError_t launch_bwd_t(const BwdArgs& a, const ScanParams& fwd, cudaStr
     if (e != cudaSuccess) return e;
     bwd_reverse_summary_kernel<N, T><<<(unsigned)(n_dtiles * (a.n_chunks - 1) * a.batch), kBwdCh, 0, s>>>(a);
   }
-  {  // forward checkpoints: the forward scan's own kernel in its checkpoint mode
+  {  // forward checkpoints: the forward states before every kCkptSteps steps
     ScanParams f = fwd;
     f.ckpt_h = a.ckpt_h;
     const cudaError_t e = launch_scan_ckpt(f, sizeof(T) == 2, s);
     if (e != cudaSuccess) return e;
   }
-  if constexpr (N % 8 == 0) {  // two lanes per channel
-    const int64_t n_dtiles2 = (a.d_inner + kBwdCh2 - 1) / kBwdCh2;
-    bwd_grad_kernel2<N, T><<<(unsigned)(n_dtiles2 * a.n_chunks * a.batch), 32, 0, s>>>(a);
-  } else {
-    bwd_grad_kernel<N, T><<<(unsigned)(n_dtiles * a.n_chunks * a.batch), kBwdCh, 0, s>>>(a);
-  }
-  return cudaGetLastError();
+  // lanes per channel pair: 4 states each, 4L >= d_state
+  return N <= 4 ? launch_grad<1, T>(a, s) : N <= 8 ? launch_grad<2, T>(a, s) : launch_grad<4, T>(a, s);
 }
 
 template <typename T>
