@@ -157,8 +157,9 @@ __global__ void __launch_bounds__(kBwdCh) bwd_reverse_summary_kernel(const BwdAr
 //       before it with one recurrence step: it needs that step's exp(delta A) anyway;
 //     - reverse walk: lambda_t = m + ds_t C_t, the gradients of every input, m <- dA_t lambda_t.
 //       Sums over states (delta, u and z gradients) go through shared memory per 4-step group;
-//       dB and dC (sums over channels) through a warp reduce-scatter, then the CTA's warps are
-//       added in shared memory and the tile's rows go to global memory as float4 atomics.
+//       so do dB and dC (sums over channels): per 4-step group each warp sums its pairs' values
+//       in its own block, the warps' sums are added at the end of the tile and the tile's rows
+//       go to global memory as float4 atomics.
 namespace bwd {
 
 constexpr int kCh = 64;   // channels per CTA
@@ -215,10 +216,12 @@ struct Cfg {
   static constexpr int kBCB = 2 * kT * kNP * 4;      // B, C rows (fp32)
   static constexpr int kQB = 2 * kT * kCP * 16;      // per step and pair: (dt, dt*u), (ds, u)
   static constexpr int kHB = (kT / 2) * 2 * kThreads * 16;  // states after the odd steps
-  static constexpr int kP4B = kOG * L * kCP * 16;    // per-lane partial sums (ddt, u-gradient)
-  static constexpr int kP2B = kOG * L * kCP * 8;     // per-lane partial readouts
-  static constexpr int kRB = kT * kWarps * 2 * kNP * 4;  // dB/dC rows per warp
-  static constexpr int kSmem = kXB + kBCB + kQB + kHB + kP4B + kP2B + kRB;
+  // per-lane partial sums, [step of the group][lane of the pair][pair ^ swizzle]
+  static constexpr int kP4B = kOG * L * kCP * 16;    // (ddt, u-gradient) sums
+  static constexpr int kP2B = kOG * L * kCP * 8;     // readouts
+  static constexpr int kWB = kWarps * kOG * 2 * 32 * 16;  // per warp: dB/dC values of its lanes
+  static constexpr int kRB = kT * kWarps * 2 * kNP * 4;   // dB/dC rows per warp
+  static constexpr int kSmem = kXB + kBCB + kQB + kHB + kP4B + kP2B + kWB + kRB;
 };
 
 template <int L, typename T>
@@ -232,7 +235,8 @@ __global__ void __launch_bounds__(32 * L, L == 4 ? 3 : (L == 2 ? 6 : 12)) grad_k
   float4* sH = reinterpret_cast<float4*>(smem + K::kXB + K::kBCB + K::kQB);     // [kT/2][2][kThreads]
   float4* sP4 = reinterpret_cast<float4*>(smem + K::kXB + K::kBCB + K::kQB + K::kHB);  // [kOG][L][kCP]
   float2* sP2 = reinterpret_cast<float2*>(smem + K::kXB + K::kBCB + K::kQB + K::kHB + K::kP4B);
-  float* sR = reinterpret_cast<float*>(smem + K::kXB + K::kBCB + K::kQB + K::kHB + K::kP4B + K::kP2B);
+  float4* sW = reinterpret_cast<float4*>(smem + K::kXB + K::kBCB + K::kQB + K::kHB + K::kP4B + K::kP2B);
+  float* sR = reinterpret_cast<float*>(smem + K::kXB + K::kBCB + K::kQB + K::kHB + K::kP4B + K::kP2B + K::kWB);
 
   const int N = p.d_state;
   const int64_t Dn = p.d_inner, Ls = p.L;
@@ -249,6 +253,10 @@ __global__ void __launch_bounds__(32 * L, L == 4 ? 3 : (L == 2 ? 6 : 12)) grad_k
   const int64_t d = d0 + 2 * P;
   const bool active = d < Dn;
   const int n0 = 4 * l;
+  // partial-sum slot of (step kg of the group, lane mm of the pair, pair P): the XOR keeps both
+  // the writes (lanes of a pair at one step) and the reads (one lane per step) on distinct banks
+  auto p4 = [&](int kg, int mm) { return (kg * L + mm) * kCP + (P ^ (((kg + mm) % L) * (8 / L))); };
+  auto p2 = [&](int kg, int mm) { return (kg * L + mm) * kCP + (P ^ (((kg + mm) % L) * (16 / L))); };
   const int64_t t0 = (int64_t)c * p.chunk_len, t1 = min(t0 + p.chunk_len, Ls);
   const int64_t tiles = (Ls + kT - 1) / kT;
   const int64_t tl_lo = t0 / kT, tl_hi = (t1 - 1) / kT;  // chunks hold whole tiles
@@ -468,29 +476,32 @@ __global__ void __launch_bounds__(32 * L, L == 4 ? 3 : (L == 2 ? 6 : 12)) grad_k
     }
     // this lane's share of the per-channel sums over states
     const int kg = k % kOG;
-    sP4[(kg * L + l) * kCP + P] = make_float4(ddt[0].x + ddt[0].y, ddt[1].x + ddt[1].y,
+    sP4[p4(kg, l)] = make_float4(ddt[0].x + ddt[0].y, ddt[1].x + ddt[1].y,
                                               slb[0].x + slb[0].y, slb[1].x + slb[1].y);
-    sP2[(kg * L + l) * kCP + P] = make_float2(rd[0].x + rd[0].y, rd[1].x + rd[1].y);
-    // dB (states n0..n0+3), dC (same): summed over the warp's pairs of this lane's state
-    // slice by a reduce-scatter over the lane bits 4, 3, 2 (which keep l), so that lane holds
-    // value (lane >> 2) & 7; lane bits below 2 that are not l are then summed plainly
-    float v[8] = {pbs[0].x, pbs[0].y, pbs[1].x, pbs[1].y, pcs[0].x, pcs[0].y, pcs[1].x, pcs[1].y};
+    sP2[p2(kg, l)] = make_float2(rd[0].x + rd[0].y, rd[1].x + rd[1].y);
+    // dB (states n0..n0+3) and dC (same) of the pair, to this warp's block; lane position
+    // XOR-swizzled per (step, dB|dC) so that the group's column sums read distinct banks
 #pragma unroll
-    for (int o = 16, h = 4; o >= 4; o >>= 1, h >>= 1) {
-      const bool upper = (lane & o) != 0;
+    for (int h = 0; h < 2; h++)
+      sW[((warp * kOG + kg) * 2 + h) * 32 + (lane ^ (((2 * kg + h) * L) % 8))] =
+          h ? make_float4(pcs[0].x, pcs[0].y, pcs[1].x, pcs[1].y) : make_float4(pbs[0].x, pbs[0].y, pbs[1].x, pbs[1].y);
+  };
+
+  // dB/dC of the steps k0 .. k0+kOG-1 summed over the warp's pairs: lane o takes (step, dB|dC,
+  // state slice) and adds the 32/L pairs' values; the warps' sums go to sR.
+  auto warp_bc_sums = [&](int k0) {
+    constexpr int kOut = kOG * 2 * L;  // float4 outputs per warp and group
+    if (lane < kOut) {
+      const int kg = lane / (2 * L), h = (lane / L) % 2, lq = lane % L;
+      const float4* src = sW + ((warp * kOG + kg) * 2 + h) * 32;
+      const int sw = ((2 * kg + h) * L) % 8;
+      float4 acc = src[lq ^ sw];
 #pragma unroll
-      for (int j = 0; j < h; j++) {
-        const float send = upper ? v[j] : v[j + h];
-        const float keep = upper ? v[j + h] : v[j];
-        v[j] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, o);
+      for (int pp = 1; pp < 32 / L; pp++) {
+        const float4 v = src[(pp * L + lq) ^ sw];
+        acc = make_float4(acc.x + v.x, acc.y + v.y, acc.z + v.z, acc.w + v.w);
       }
-    }
-#pragma unroll
-    for (int o = L; o < 4; o <<= 1) v[0] += __shfl_xor_sync(0xFFFFFFFFu, v[0], o);
-    if ((lane & 3 & ~(L - 1)) == 0) {
-      const int vi = (lane >> 2) & 7;
-      const int o = vi < 4 ? n0 + vi : kNP + n0 + vi - 4;
-      sR[(k * K::kWarps + warp) * 2 * kNP + o] = v[0];
+      *reinterpret_cast<float4*>(sR + ((k0 + kg) * K::kWarps + warp) * 2 * kNP + h * kNP + 4 * lq) = acc;
     }
   };
 
@@ -502,12 +513,12 @@ __global__ void __launch_bounds__(32 * L, L == 4 ? 3 : (L == 2 ? 6 : 12)) grad_k
     for (int i = 0; i < kOG / L; i++) {
       const int k = k0 + i * L + l;
       if (k < steps && active) {
-        float4 a = sP4[((k % kOG) * L + 0) * kCP + P];
-        float2 r = sP2[((k % kOG) * L + 0) * kCP + P];
+        float4 a = sP4[p4(k % kOG, 0)];
+        float2 r = sP2[p2(k % kOG, 0)];
 #pragma unroll
         for (int mm = 1; mm < L; mm++) {
-          const float4 a2 = sP4[((k % kOG) * L + mm) * kCP + P];
-          const float2 r2 = sP2[((k % kOG) * L + mm) * kCP + P];
+          const float4 a2 = sP4[p4(k % kOG, mm)];
+          const float2 r2 = sP2[p2(k % kOG, mm)];
           a = make_float4(a.x + a2.x, a.y + a2.y, a.z + a2.z, a.w + a2.w);
           r = make_float2(r.x + r2.x, r.y + r2.y);
         }
@@ -596,7 +607,7 @@ __global__ void __launch_bounds__(32 * L, L == 4 ? 3 : (L == 2 ? 6 : 12)) grad_k
     }
 
     // reverse walk, two steps at a time: (k, k-1) with k odd
-#pragma unroll 1
+#pragma unroll
     for (int k = kT - 1; k >= 1; k -= 2) {
       float2 hk[4], hpp[4], hm[4], dAk[4], dAm[4];
       {
@@ -621,7 +632,8 @@ __global__ void __launch_bounds__(32 * L, L == 4 ? 3 : (L == 2 ? 6 : 12)) grad_k
       if ((k - 1) % kOG == 0) {
         __syncwarp();
         if (k - 1 == kOG) output_group(std::integral_constant<int, kOG>{}, steps, ts);
-        else output_group(std::integral_constant<int, 0>{}, steps, ts);
+        else output_group(std::integral_constant<int, 0>{}, steps, ts);  // k - 1 == 0
+        warp_bc_sums(k - 1);
         __syncwarp();
       }
     }
