@@ -495,13 +495,16 @@ __global__ void __launch_bounds__(32 * L, L == 4 ? 3 : (L == 2 ? 6 : 12)) grad_k
       const int kg = lane / (2 * L), h = (lane / L) % 2, lq = lane % L;
       const float4* src = sW + ((warp * kOG + kg) * 2 + h) * 32;
       const int sw = ((2 * kg + h) * L) % 8;
-      float4 acc = src[lq ^ sw];
+      const float4 v0 = src[lq ^ sw];
+      float2 a01 = make_float2(v0.x, v0.y), a23 = make_float2(v0.z, v0.w);
 #pragma unroll
       for (int pp = 1; pp < 32 / L; pp++) {
         const float4 v = src[(pp * L + lq) ^ sw];
-        acc = make_float4(acc.x + v.x, acc.y + v.y, acc.z + v.z, acc.w + v.w);
+        a01 = __fadd2_rn(a01, make_float2(v.x, v.y));
+        a23 = __fadd2_rn(a23, make_float2(v.z, v.w));
       }
-      *reinterpret_cast<float4*>(sR + ((k0 + kg) * K::kWarps + warp) * 2 * kNP + h * kNP + 4 * lq) = acc;
+      *reinterpret_cast<float4*>(sR + ((k0 + kg) * K::kWarps + warp) * 2 * kNP + h * kNP + 4 * lq) =
+          make_float4(a01.x, a01.y, a23.x, a23.y);
     }
   };
 
