@@ -77,11 +77,11 @@ ssm_status_t check_common(int64_t batch, int64_t L, int64_t d_inner, int d_state
 }
 
 // Workspace of a forward scan (0 for an empty problem); false if the plan cannot be made.
-bool fwd_workspace(int64_t batch, int64_t L, int64_t d_inner, int d_state, bool bf16, bool conv,
+bool fwd_workspace(int64_t batch, int64_t L, int64_t d_inner, int d_state, bool bf16, int kind,
                    int sms, ssm::FwdPlan* plan, size_t* bytes) {
   *bytes = 0;
   if (batch * d_inner == 0 || L == 0) return true;
-  if (!ssm::plan_scan_fwd(batch, L, d_inner, d_state, bf16, conv, sms, plan)) return false;
+  if (!ssm::plan_scan_fwd(batch, L, d_inner, d_state, bf16, kind, sms, plan)) return false;
   *bytes = ssm::fwd_workspace_bytes(batch, d_inner, *plan);
   return true;
 }
@@ -97,8 +97,8 @@ size_t ssm_scan_fwd_workspace_size(int64_t batch, int64_t L, int64_t d_inner, in
   if (sms <= 0) return 0;
   ssm::FwdPlan plan;
   size_t plain = 0, conv = 0;
-  if (!fwd_workspace(batch, L, d_inner, d_state, io == SSM_BF16, false, sms, &plan, &plain) ||
-      !fwd_workspace(batch, L, d_inner, d_state, io == SSM_BF16, true, sms, &plan, &conv))
+  if (!fwd_workspace(batch, L, d_inner, d_state, io == SSM_BF16, ssm::kFwdPlain, sms, &plan, &plain) ||
+      !fwd_workspace(batch, L, d_inner, d_state, io == SSM_BF16, ssm::kFwdConv, sms, &plan, &conv))
     return 0;
   return plain > conv ? plain : conv;
 }
@@ -154,7 +154,9 @@ ssm_status_t scan_fwd_impl(const void* u, const void* delta, const float* A, con
   const bool conv = ex.conv_w != nullptr;
   ssm::FwdPlan plan;
   size_t need = 0;
-  if (!fwd_workspace(batch, L, d_inner, d_state, bf16, conv, sms, &plan, &need)) return SSM_ERR_CUDA;
+  if (!fwd_workspace(batch, L, d_inner, d_state, bf16, conv ? ssm::kFwdConv : ssm::kFwdPlain, sms, &plan,
+                     &need))
+    return SSM_ERR_CUDA;
   if (workspace == nullptr || workspace_bytes < need) return SSM_ERR_WORKSPACE;
   const int64_t n_dt = (d_inner + ssm::fwd_channels_per_cta() - 1) / ssm::fwd_channels_per_cta();
   if ((int64_t)plan.G * batch * n_dt >= ((int64_t)1 << 31)) return SSM_ERR_SHAPE;
@@ -280,10 +282,15 @@ ssm_status_t ssm_state_update_conv(float* state, float* conv_state, const void* 
 
 namespace {
 
-// Time chunking of the backward pass: the forward plan's chunks, rounded to whole tiles.
-void bwd_plan(int64_t batch, int64_t L, int64_t d_inner, int sms, ssm::ScanPlan* plan) {
-  ssm::plan_scan(batch, L, d_inner, sms, plan);
-  plan->lanes = 1;
+// Workspace of a backward pass: the checkpoint kernel's look-back region (header first, so that
+// ssm_get_status reads it), then the checkpoints and the reverse chunk summaries.
+bool bwd_workspace(int64_t batch, int64_t L, int64_t d_inner, int d_state, bool bf16, int sms,
+                   ssm::FwdPlan* fplan, ssm::BwdPlan* bplan, size_t* fwd_bytes, size_t* bytes) {
+  ssm::plan_scan_bwd(batch, L, d_inner, sms, bplan);
+  if (!fwd_workspace(batch, L, d_inner, d_state, bf16, ssm::kFwdCkpt, sms, fplan, fwd_bytes)) return false;
+  *fwd_bytes = (*fwd_bytes + 255) / 256 * 256;
+  *bytes = *fwd_bytes + ssm::bwd_workspace_floats(batch, L, d_inner, d_state, bplan->n_chunks) * sizeof(float);
+  return true;
 }
 
 }  // namespace
@@ -295,9 +302,12 @@ size_t ssm_scan_bwd_workspace_size(int64_t batch, int64_t L, int64_t d_inner, in
   if (check_common(batch, L, d_inner, d_state, io) != SSM_OK) return 0;
   const int sms = current_sm_count();
   if (sms <= 0 || batch * d_inner * L == 0) return 0;
-  ssm::ScanPlan plan;
-  bwd_plan(batch, L, d_inner, sms, &plan);
-  return ssm::bwd_workspace_floats(batch, L, d_inner, d_state, plan.n_chunks) * sizeof(float);
+  ssm::FwdPlan fplan;
+  ssm::BwdPlan bplan;
+  size_t fwd_bytes = 0, bytes = 0;
+  if (!bwd_workspace(batch, L, d_inner, d_state, io == SSM_BF16, sms, &fplan, &bplan, &fwd_bytes, &bytes))
+    return 0;
+  return bytes;
 }
 
 ssm_status_t ssm_scan_bwd(const void* u, const void* delta, const float* A, const void* B,
@@ -343,40 +353,43 @@ ssm_status_t ssm_scan_bwd(const void* u, const void* delta, const float* A, cons
   if (cudaMemsetAsync(dB, 0, bc_bytes, s) != cudaSuccess || cudaMemsetAsync(dC, 0, bc_bytes, s) != cudaSuccess)
     return SSM_ERR_CUDA;
 
-  ssm::ScanPlan plan;
-  bwd_plan(batch, L, d_inner, sms, &plan);
-  const size_t need = ssm::bwd_workspace_floats(batch, L, d_inner, d_state, plan.n_chunks) * sizeof(float);
+  const bool bf16 = io == SSM_BF16;
+  ssm::FwdPlan fplan;
+  ssm::BwdPlan bplan;
+  size_t fwd_bytes = 0, need = 0;
+  if (!bwd_workspace(batch, L, d_inner, d_state, bf16, sms, &fplan, &bplan, &fwd_bytes, &need))
+    return SSM_ERR_CUDA;
   if (workspace == nullptr || workspace_bytes < need) return SSM_ERR_WORKSPACE;
-  const int64_t tiles = (L + ssm::kCkptSteps - 1) / ssm::kCkptSteps;
-  if ((d_inner + 31) / 32 * tiles * batch >= ((int64_t)1 << 31)) return SSM_ERR_SHAPE;
+  const int64_t n_dt = (d_inner + ssm::fwd_channels_per_cta() - 1) / ssm::fwd_channels_per_cta();
+  if ((int64_t)std::max<int64_t>(fplan.G, bplan.n_chunks) * batch * ((d_inner + 31) / 32) >= ((int64_t)1 << 31))
+    return SSM_ERR_SHAPE;
+  (void)n_dt;
 
-  float* ws = static_cast<float*>(workspace);
+  float* ws = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + fwd_bytes);
+  const int64_t tiles = (L + ssm::kCkptSteps - 1) / ssm::kCkptSteps;
   const int64_t ck = batch * tiles * d_inner * d_state;
-  const int64_t fws = batch * (int64_t)(plan.n_chunks - 1) * d_inner;
-  const int64_t rws = batch * (int64_t)plan.n_chunks * d_inner;
+  const int64_t rws = batch * (int64_t)bplan.n_chunks * d_inner;
   ssm::BwdArgs a{};
   a.u = u; a.delta = delta; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z; a.delta_bias = delta_bias;
   a.softplus = softplus_flag != 0; a.initial_state = initial_state; a.dy = dy; a.dlast = dlast_state;
   a.du = du; a.ddelta = ddelta; a.dz = dz; a.dA = dA; a.dB = dB; a.dC = dC; a.dD = dD;
   a.dbias = ddelta_bias; a.dinit = dinitial_state;
   a.batch = batch; a.L = L; a.d_inner = d_inner; a.d_state = d_state;
-  a.chunk_len = plan.chunk_len; a.n_chunks = plan.n_chunks;
+  a.chunk_len = bplan.chunk_len; a.n_chunks = bplan.n_chunks;
   a.ckpt_h = ws;
-  float* fS = ws + ck;
-  a.fws_S = fS;
-  a.fws_h = fS + fws;
-  float* rS = fS + fws * (d_state + 1);
-  a.rws_S = rS;
-  a.rws_m = rS + rws;
+  a.rws_S = ws + ck;
+  a.rws_m = ws + ck + rws;
 
-  ssm::ScanParams f{};
+  ssm::FwdLaunch f{};
   f.u = u; f.delta = delta; f.A = A; f.B = B; f.C = C; f.delta_bias = delta_bias;
-  f.softplus = softplus_flag != 0; f.batch = batch; f.L = L; f.d_inner = d_inner;
-  f.d_state = d_state; f.chunk_len = plan.chunk_len; f.n_chunks = plan.n_chunks; f.lanes = 1;
-  f.initial_state = initial_state;
-  f.ws_S = fS;
-  f.ws_h = fS + fws;
-  return ssm::launch_scan_bwd(a, f, io == SSM_BF16, s) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+  f.softplus = softplus_flag != 0; f.initial_state = initial_state; f.ckpt = ws;
+  f.batch = batch; f.L = L; f.d_inner = d_inner; f.d_state = d_state;
+  f.plan = fplan;
+  f.workspace = workspace;
+  f.tag = next_call_tag();
+  f.wait_tag = lookback_selftest() ? (f.tag ^ 1ull) : f.tag;
+  f.max_polls = lookback_max_polls();
+  return ssm::launch_scan_bwd(a, f, bf16, s) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
 size_t ssm_ssd_fwd_workspace_size(int64_t batch, int64_t L, int64_t d_inner, int n_heads,
@@ -530,7 +543,7 @@ ssm_status_t ssm_scan_fwd_noalloc(const void* u, const void* delta, const float*
   if (sms <= 0) return SSM_ERR_CUDA;
   ssm::FwdPlan plan;
   size_t need = 0;
-  if (!fwd_workspace(batch, L, d_inner, d_state, io == SSM_BF16, false, sms, &plan, &need))
+  if (!fwd_workspace(batch, L, d_inner, d_state, io == SSM_BF16, ssm::kFwdPlain, sms, &plan, &need))
     return SSM_ERR_CUDA;
   if (need > SSM_NOALLOC_SCRATCH_BYTES) return SSM_ERR_SCRATCH_LIMIT;
   float* scratch = nullptr;

@@ -7,39 +7,6 @@
 
 namespace ssm {
 
-struct ScanParams {
-  const void* u;
-  const void* delta;
-  const float* A;
-  const void* B;
-  const void* C;
-  const float* D;           // may be null
-  const void* z;            // may be null
-  const float* delta_bias;  // may be null
-  int softplus;
-  void* y;
-  float* last_state;        // may be null
-  const float* initial_state;  // may be null: the state before the first step is zero
-  // Optional causal depthwise conv1d + SiLU in front of the scan (conv_w non-null): the
-  // u operand then holds the block input x, and u = silu(conv_b + sum_k conv_w[d,k] x[t+k-(K-1)]).
-  const float* conv_w;      // [d_inner][d_conv]
-  const float* conv_b;      // [d_inner], may be null
-  int d_conv;               // 1..4
-  void* u_out;              // may be null: the conv output u, I/O dtype
-  int64_t batch, L, d_inner;
-  int d_state;
-  // Time chunking: the sequence is cut into n_chunks chunks of chunk_len steps
-  // (the last one may be shorter).  For n_chunks > 1 the workspace holds, per
-  // (batch, chunk < n_chunks-1, channel), the chunk's delta sum and its end
-  // state started from zero.
-  int64_t chunk_len;
-  int n_chunks;
-  int lanes;  // 1 or 2 lanes per channel (which kernel runs)
-  float* ws_S;  // [batch][n_chunks-1][d_inner]
-  float* ws_h;  // [batch][n_chunks-1][d_inner][d_state]
-  float* ckpt_h = nullptr;  // checkpoint pass only: [batch][ceil(L/kCkptSteps)][d_inner][d_state]
-};
-
 struct DecodeParams {
   float* state;
   const void* u;
@@ -89,8 +56,6 @@ struct BwdArgs {
   int d_state;
   int64_t chunk_len;
   int n_chunks;
-  const float* fws_S;  // forward chunk summaries (written by the forward summary kernel)
-  const float* fws_h;
   float* rws_S;        // reverse chunk summaries [batch][n_chunks][d_inner] (+ [.][d_state])
   float* rws_m;
   float* ckpt_h;       // [batch][ceil(L / kCkptSteps)][d_inner][d_state]: state before every kCkptSteps steps
@@ -154,6 +119,7 @@ struct FwdLaunch {
   const float* conv_b;
   int d_conv;
   void* u_out;
+  float* ckpt;  // non-null: the backward's checkpoint kernel (no outputs; states every kCkptSteps)
   int64_t batch, L, d_inner;
   int d_state;
   FwdPlan plan;
@@ -163,35 +129,27 @@ struct FwdLaunch {
   unsigned max_polls;             // look-back polls before giving up
 };
 
-bool plan_scan_fwd(int64_t batch, int64_t L, int64_t d_inner, int d_state, bool bf16, bool conv,
+// Kernel kinds: the scan, the scan with the conv1d in front, the backward's checkpoints.
+constexpr int kFwdPlain = 0, kFwdConv = 1, kFwdCkpt = 2;
+bool plan_scan_fwd(int64_t batch, int64_t L, int64_t d_inner, int d_state, bool bf16, int kind,
                    int sms, FwdPlan* plan);
 size_t fwd_workspace_bytes(int64_t batch, int64_t d_inner, const FwdPlan& plan);
 cudaError_t launch_scan_fwd(const FwdLaunch& f, bool bf16, cudaStream_t stream);
 int fwd_channels_per_cta();
 
-// ---- Two-pass chunked scan kernels (ssm_scan.cu), used by the backward pass ----
+// ---- Backward pass (ssm_scan_bwd.cu) ----
 
-// Channels handled by one CTA of the scan kernels.
-int scan_channels_per_cta();
-
-// How a scan of these sizes runs on a device with `sms` SMs: the kernel (lanes per
-// channel) and the time chunking.
-struct ScanPlan {
-  int lanes;
+// Time chunks of the backward's gradient kernel (chunk_len a multiple of 32 steps).
+struct BwdPlan {
   int64_t chunk_len;
   int n_chunks;
 };
-void plan_scan(int64_t batch, int64_t L, int64_t d_inner, int sms, ScanPlan* plan);
-
-cudaError_t launch_scan(const ScanParams& p, bool bf16, cudaStream_t stream);
-// Only the forward summary pass (one lane per channel) of a chunked scan plan.
-cudaError_t launch_scan_summary(const ScanParams& p, bool bf16, cudaStream_t stream);
-// The main pass's states from initial_state and the chunk summaries, with no output: the state
-// before every kCkptSteps steps into p.ckpt_h (one lane per channel).
-cudaError_t launch_scan_ckpt(const ScanParams& p, bool bf16, cudaStream_t stream);
-// Floats of scratch the backward pass needs for n_chunks time chunks.
+void plan_scan_bwd(int64_t batch, int64_t L, int64_t d_inner, int sms, BwdPlan* plan);
+// Floats of scratch the backward's checkpoints and reverse summaries take for n_chunks chunks
+// (after the checkpoint kernel's look-back region at the start of the workspace).
 size_t bwd_workspace_floats(int64_t batch, int64_t L, int64_t d_inner, int d_state, int n_chunks);
-cudaError_t launch_scan_bwd(const BwdArgs& a, const ScanParams& fwd, bool bf16, cudaStream_t s);
+// ckpt: the checkpoint kernel's launch (its ckpt pointer set); a: the gradient kernels'.
+cudaError_t launch_scan_bwd(const BwdArgs& a, const FwdLaunch& ckpt, bool bf16, cudaStream_t s);
 cudaError_t launch_state_update(const DecodeParams& p, bool bf16, cudaStream_t stream);
 
 }  // namespace ssm

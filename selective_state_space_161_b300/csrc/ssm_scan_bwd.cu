@@ -4,9 +4,8 @@
 // The pages describe the backward only as "recompute the intermediate states in the backward
 // pass instead of storing them" (youngju.dev, "Mamba: Linear-Time Sequence Modeling with
 // Selective State Spaces 论文分析", section "解决方案：Kernel Fusion + Recomputation").  Here:
-//  1. forward checkpoints: the forward scan's one-lane state kernels (ssm_scan.cu; its summary
-//     pass, then its checkpoint mode) store the state before every 8 steps — never the
-//     per-step states;
+//  1. forward checkpoints: the forward scan's look-back kernel in its checkpoint form
+//     (ssm_scan_fwd.cu) stores the state before every 8 steps — never the per-step states;
 //  2. reverse summaries (time-chunked plans only): the adjoint
 //     lambda_t = ds_t C_t + dA_{t+1} lambda_{t+1} runs backwards over each chunk from a zero
 //     carry; per chunk, its carry-out and its decay exp(A sum delta);
@@ -19,6 +18,7 @@
 #include "ssm_internal.h"
 
 #include <algorithm>
+#include <cstdlib>
 #include <type_traits>
 
 namespace ssm {
@@ -722,12 +722,38 @@ __global__ void __launch_bounds__(32 * L, L == 4 ? 3 : (L == 2 ? 6 : 12)) grad_k
 
 // ---------------------------------------------------------------------------------------
 
+static int64_t env_int(const char* name, int64_t fallback) {
+  if (const char* v = std::getenv(name)) {
+    const long long x = std::atoll(v);
+    if (x > 0) return x;
+  }
+  return fallback;
+}
+
+void plan_scan_bwd(int64_t batch, int64_t L, int64_t d_inner, int sms, BwdPlan* plan) {
+  // Time chunks of the gradient kernel: none when its CTAs (64 channels each, about three
+  // resident per SM) fill the GPU; otherwise about two waves of them, at least 64 steps per
+  // chunk (measured on B300: the 2 x 2048 x 1536 shape at 0.30 ms with 16 chunks against 0.35
+  // with 8 or 32; the 8 x 2048 x 5120 shape fastest unchunked).
+  constexpr int64_t kAlign = 32;
+  const int64_t per_chunk = batch * ((d_inner + bwd::kCh - 1) / bwd::kCh);
+  const int64_t slots = (int64_t)sms * 3;
+  int64_t G = 1;
+  if (per_chunk > 0 && per_chunk < slots) G = (2 * slots + per_chunk - 1) / per_chunk;
+  G = env_int("SSM_BWD_CHUNKS", G);  // tuning override
+  G = std::min<int64_t>(G, std::max<int64_t>(1, L / 64));
+  G = std::min<int64_t>(G, 4096);
+  int64_t len = L > 0 ? (L + G - 1) / G : 1;
+  len = (len + kAlign - 1) / kAlign * kAlign;
+  plan->chunk_len = len;
+  plan->n_chunks = L > 0 ? (int)((L + len - 1) / len) : 1;
+}
+
 size_t bwd_workspace_floats(int64_t batch, int64_t L, int64_t d_inner, int d_state, int n_chunks) {
   const int64_t tiles = (L + kCkptSteps - 1) / kCkptSteps;
   const int64_t ck = batch * tiles * d_inner * d_state;                 // forward checkpoints
-  const int64_t fws = batch * (int64_t)std::max(n_chunks - 1, 0) * d_inner * (d_state + 1);
-  const int64_t rws = batch * (int64_t)n_chunks * d_inner * (d_state + 1);
-  return (size_t)(ck + fws + rws);
+  const int64_t rws = batch * (int64_t)n_chunks * d_inner * (d_state + 1);  // reverse summaries
+  return (size_t)(ck + rws);
 }
 
 template <int L, typename T>
@@ -741,49 +767,36 @@ static cudaError_t launch_grad(const BwdArgs& a, cudaStream_t s) {
 }
 
 template <int N, typename T>
-static cudaError_t launch_bwd_t(const BwdArgs& a, const ScanParams& fwd, cudaStream_t s) {
-  const int64_t n_dtiles = (a.d_inner + kBwdCh - 1) / kBwdCh;
-  if (a.n_chunks > 1) {
-    // forward chunk summaries: the forward scan's own summary pass
-    cudaError_t e = launch_scan_summary(fwd, sizeof(T) == 2, s);
-    if (e != cudaSuccess) return e;
+static cudaError_t launch_bwd_t(const BwdArgs& a, const FwdLaunch& ckpt, cudaStream_t s) {
+  if (a.n_chunks > 1) {  // reverse chunk summaries
+    const int64_t n_dtiles = (a.d_inner + kBwdCh - 1) / kBwdCh;
     bwd_reverse_summary_kernel<N, T><<<(unsigned)(n_dtiles * (a.n_chunks - 1) * a.batch), kBwdCh, 0, s>>>(a);
-  }
-  {  // forward checkpoints: the forward states before every kCkptSteps steps
-    ScanParams f = fwd;
-    f.ckpt_h = a.ckpt_h;
-    const cudaError_t e = launch_scan_ckpt(f, sizeof(T) == 2, s);
+    const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
+  // forward checkpoints: the forward scan's look-back kernel in its checkpoint form
+  const cudaError_t e = launch_scan_fwd(ckpt, sizeof(T) == 2, s);
+  if (e != cudaSuccess) return e;
   // lanes per channel pair: 4 states each, 4L >= d_state
   return N <= 4 ? launch_grad<1, T>(a, s) : N <= 8 ? launch_grad<2, T>(a, s) : launch_grad<4, T>(a, s);
 }
 
 template <typename T>
-static cudaError_t dispatch_bwd(const BwdArgs& a, const ScanParams& fwd, cudaStream_t s) {
+static cudaError_t dispatch_bwd(const BwdArgs& a, const FwdLaunch& ckpt, cudaStream_t s) {
   switch (a.d_state) {
-    case 1: return launch_bwd_t<1, T>(a, fwd, s);
-    case 2: return launch_bwd_t<2, T>(a, fwd, s);
-    case 3: return launch_bwd_t<3, T>(a, fwd, s);
-    case 4: return launch_bwd_t<4, T>(a, fwd, s);
-    case 5: return launch_bwd_t<5, T>(a, fwd, s);
-    case 6: return launch_bwd_t<6, T>(a, fwd, s);
-    case 7: return launch_bwd_t<7, T>(a, fwd, s);
-    case 8: return launch_bwd_t<8, T>(a, fwd, s);
-    case 9: return launch_bwd_t<9, T>(a, fwd, s);
-    case 10: return launch_bwd_t<10, T>(a, fwd, s);
-    case 11: return launch_bwd_t<11, T>(a, fwd, s);
-    case 12: return launch_bwd_t<12, T>(a, fwd, s);
-    case 13: return launch_bwd_t<13, T>(a, fwd, s);
-    case 14: return launch_bwd_t<14, T>(a, fwd, s);
-    case 15: return launch_bwd_t<15, T>(a, fwd, s);
-    case 16: return launch_bwd_t<16, T>(a, fwd, s);
+#define SSM_BWD_CASE(NN) \
+    case NN: return launch_bwd_t<NN, T>(a, ckpt, s);
+    SSM_BWD_CASE(1) SSM_BWD_CASE(2) SSM_BWD_CASE(3) SSM_BWD_CASE(4)
+    SSM_BWD_CASE(5) SSM_BWD_CASE(6) SSM_BWD_CASE(7) SSM_BWD_CASE(8)
+    SSM_BWD_CASE(9) SSM_BWD_CASE(10) SSM_BWD_CASE(11) SSM_BWD_CASE(12)
+    SSM_BWD_CASE(13) SSM_BWD_CASE(14) SSM_BWD_CASE(15) SSM_BWD_CASE(16)
+#undef SSM_BWD_CASE
     default: return cudaErrorInvalidValue;
   }
 }
 
-cudaError_t launch_scan_bwd(const BwdArgs& a, const ScanParams& fwd, bool bf16, cudaStream_t s) {
-  return bf16 ? dispatch_bwd<__nv_bfloat16>(a, fwd, s) : dispatch_bwd<float>(a, fwd, s);
+cudaError_t launch_scan_bwd(const BwdArgs& a, const FwdLaunch& ckpt, bool bf16, cudaStream_t s) {
+  return bf16 ? dispatch_bwd<__nv_bfloat16>(a, ckpt, s) : dispatch_bwd<float>(a, ckpt, s);
 }
 
 }  // namespace ssm

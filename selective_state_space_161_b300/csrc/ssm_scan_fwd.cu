@@ -62,6 +62,7 @@ constexpr int kStepUnroll = SSM_FWD_UNROLL;  // steps per iteration of the one-l
 constexpr int kCh = 64;   // channels per CTA
 constexpr int kCP = 32;   // channel pairs per CTA
 constexpr int kT = 16;    // steps per tile
+static_assert(kT == 2 * kCkptSteps, "two checkpoints per tile");
 constexpr int kOG = 8;    // steps per output group (partial readouts reduced in shared memory)
 constexpr int kModeAgg = 0, kModeMain = 1;
 
@@ -147,6 +148,7 @@ struct Args {
   const float* conv_b;          // [d_inner], may be null
   int d_conv;
   void* u_out;                  // may be null: the conv output u, I/O dtype
+  float* ckpt;                  // checkpoint kernels: [batch][ceil(L/kCkptSteps)][d_inner][d_state]
   int64_t batch, L, d_inner;
   int N;
   int G;                        // time chunks
@@ -163,8 +165,12 @@ struct Args {
 // Register allocation: 12 resident warps per SM for one lane per pair (three per scheduler,
 // up to 168 registers: its 16 state pairs, A and B/C live at once), 16 for two lanes, 20 for
 // four.
-template <int L, int S, typename T, bool kConv>
+// kCkpt: the backward pass's checkpoint kernel.  The same chunks and look-back, but its last
+// pass stores the state before every kCkptSteps steps instead of reading out y (no C, no
+// z, no outputs).
+template <int L, int S, typename T, bool kConv, bool kCkpt = false>
 __global__ void __launch_bounds__(32 * L, L == 1 ? 12 : (L == 2 ? 8 : 5)) scan_fwd_kernel(const Args a) {
+  static_assert(!(kConv && kCkpt), "the checkpoint kernels take the scan input u directly");
   using K = Cfg<L, S, T, kConv>;
   extern __shared__ __align__(16) unsigned char smem[];
   unsigned char* sX = smem;                                                  // [2][kStageB]
@@ -246,7 +252,8 @@ __global__ void __launch_bounds__(32 * L, L == 1 ? 12 : (L == 2 ? 8 : 5)) scan_f
   float2 Ssum = make_float2(0.f, 0.f), Scomp = make_float2(0.f, 0.f);
   auto run = [&](auto mode_tag) {
     constexpr int kMode = decltype(mode_tag)::value;
-    constexpr bool kMain = kMode == kModeMain;
+    constexpr bool kMain = kMode == kModeMain && !kCkpt;  // the pass that reads out y
+    constexpr bool kStore = kMode == kModeMain && kCkpt;  // the pass that stores checkpoints
     const int nbc = kMain ? 2 : 1;
 
     // Activation rows of a tile: delta and z (kT rows), u or the conv input x (kRows rows,
@@ -371,6 +378,29 @@ __global__ void __launch_bounds__(32 * L, L == 1 ? 12 : (L == 2 ? 8 : 5)) scan_f
       __syncthreads();
       const int64_t ts = t0 + (int64_t)tile * kT;
       const int steps = (int)min((int64_t)kT, t1 - ts);
+      // checkpoint kernels: this lane's states of both channels, the state before step t
+      auto store_ckpt = [&](int64_t t) {
+        if (!active) return;
+        const int64_t row0 = (b * ((Ls + kCkptSteps - 1) / kCkptSteps) + t / kCkptSteps) * Dn + d;
+#pragma unroll
+        for (int c = 0; c < 2; c++) {
+          float* dst = a.ckpt + (row0 + c) * N + n0;
+#pragma unroll
+          for (int q = 0; q < S / 4; q++) {
+            const float2 h0 = h[c * kHP + 2 * q], h1 = h[c * kHP + 2 * q + 1];
+            const int n = n0 + 4 * q;
+            if (N % 4 == 0) {
+              if (n < N) *reinterpret_cast<float4*>(dst + 4 * q) = make_float4(h0.x, h0.y, h1.x, h1.y);
+            } else {
+              const float v[4] = {h0.x, h0.y, h1.x, h1.y};
+#pragma unroll
+              for (int e = 0; e < 4; e++)
+                if (n + e < N) dst[4 * q + e] = v[e];
+            }
+          }
+        }
+      };
+      if constexpr (kStore) store_ckpt(ts);
 
       // The per-element work of step k for this lane's channel pair (step size, delta*u, and
       // for the main pass the gate and D*u*gate), from the staged rows of stage `stage`.
@@ -399,7 +429,7 @@ __global__ void __launch_bounds__(32 * L, L == 1 ? 12 : (L == 2 ? 8 : 5)) scan_f
           const float2 sz = silu2(PairIO<T>::load(xrow(K::kOffZ, k)));
           g = make_float2(has_z ? sz.x : 1.f, has_z ? sz.y : 1.f);
           dug = __fmul2_rn(__fmul2_rn(D2, uu), g);
-        } else if (k < steps) {  // compensated (Kahan) sum of delta over the chunk
+        } else if (kMode == kModeAgg && k < steps) {  // compensated (Kahan) sum of delta over the chunk
           const float2 yk = sub2(dlt, Scomp);
           const float2 tk = make_float2(Ssum.x + yk.x, Ssum.y + yk.y);
           Scomp = sub2(sub2(tk, Ssum), yk);
@@ -463,6 +493,9 @@ __global__ void __launch_bounds__(32 * L, L == 1 ? 12 : (L == 2 ? 8 : 5)) scan_f
             if (active) PairIO<T>::store(yk, __ffma2_rn(part, g, dug));
             yk += Dn;
           }
+          if constexpr (kStore) {
+            if (k == kCkptSteps - 1 && steps > kCkptSteps) store_ckpt(ts + kCkptSteps);
+          }
         };
         // Four steps per loop iteration: enough independent work for the scheduler, and code
         // small enough to stay in the instruction cache (a fully unrolled tile does not).
@@ -513,6 +546,9 @@ __global__ void __launch_bounds__(32 * L, L == 1 ? 12 : (L == 2 ? 8 : 5)) scan_f
             if (kGuard && k >= steps) break;
             const float4 dw = sDW[k * kCP + (P ^ ((k % L) * K::kSwz))];
             const float2 part = advance(k, make_float2(dw.x, dw.y), make_float2(dw.z, dw.w));
+            if constexpr (kStore) {
+              if (k == kCkptSteps - 1 && steps > kCkptSteps) store_ckpt(ts + kCkptSteps);
+            }
             if constexpr (kMain) {
               *reinterpret_cast<float2*>(sP + (k % kOG) * K::kRS + l * K::kLS + 2 * P) = part;
               if (k % kOG == kOG - 1 || (kGuard && k == steps - 1)) {
@@ -710,9 +746,9 @@ struct Variant {
   int threads;
 };
 
-template <int L, int S, typename T, bool kConv>
+template <int L, int S, typename T, bool kConv, bool kCkpt>
 Variant make_variant() {
-  return Variant{fwd::scan_fwd_kernel<L, S, T, kConv>, fwd::Cfg<L, S, T, kConv>::kSmem, 32 * L};
+  return Variant{fwd::scan_fwd_kernel<L, S, T, kConv, kCkpt>, fwd::Cfg<L, S, T, kConv>::kSmem, 32 * L};
 }
 
 // The kernel variants: (lanes, states per lane) in {(1,4), (1,8), (1,16), (2,4), (2,8), (4,4)}.
@@ -721,23 +757,29 @@ int ls_index(int L, int S) {
   return L == 1 ? (S == 4 ? 0 : S == 8 ? 1 : S == 16 ? 2 : -1) : L == 2 ? (S == 4 ? 3 : S == 8 ? 4 : -1) : (L == 4 && S == 4) ? 5 : -1;
 }
 
-template <typename T, bool kConv>
+template <typename T, bool kConv, bool kCkpt>
 Variant variant_t(int idx) {
   switch (idx) {
-    case 0: return make_variant<1, 4, T, kConv>();
-    case 1: return make_variant<1, 8, T, kConv>();
-    case 2: return make_variant<1, 16, T, kConv>();
-    case 3: return make_variant<2, 4, T, kConv>();
-    case 4: return make_variant<2, 8, T, kConv>();
-    case 5: return make_variant<4, 4, T, kConv>();
+    case 0: return make_variant<1, 4, T, kConv, kCkpt>();
+    case 1: return make_variant<1, 8, T, kConv, kCkpt>();
+    case 2: return make_variant<1, 16, T, kConv, kCkpt>();
+    case 3: return make_variant<2, 4, T, kConv, kCkpt>();
+    case 4: return make_variant<2, 8, T, kConv, kCkpt>();
+    case 5: return make_variant<4, 4, T, kConv, kCkpt>();
   }
   return Variant{nullptr, 0, 0};
 }
 
-Variant variant(int L, int S, bool bf16, bool conv) {
+template <typename T>
+Variant variant_kind(int idx, int kind) {
+  return kind == kFwdConv ? variant_t<T, true, false>(idx)
+         : kind == kFwdCkpt ? variant_t<T, false, true>(idx)
+                            : variant_t<T, false, false>(idx);
+}
+
+Variant variant(int L, int S, bool bf16, int kind) {
   const int idx = ls_index(L, S);
-  if (bf16) return conv ? variant_t<__nv_bfloat16, true>(idx) : variant_t<__nv_bfloat16, false>(idx);
-  return conv ? variant_t<float, true>(idx) : variant_t<float, false>(idx);
+  return bf16 ? variant_kind<__nv_bfloat16>(idx, kind) : variant_kind<float>(idx, kind);
 }
 
 int64_t env_int(const char* name, int64_t fallback) {
@@ -759,14 +801,14 @@ double env_double(const char* name, double fallback) {
 // Per device and variant: the dynamic shared-memory limit raised once, and the resident CTAs
 // per SM (0: not prepared yet).
 constexpr int kMaxDev = 64;
-std::atomic<int> g_resident[kMaxDev][kNumLS * 4];
+std::atomic<int> g_resident[kMaxDev][kNumLS * 2 * 3];
 
 // Resident CTAs per SM of a kernel variant on the current device (0 on error); the first call
 // per device raises the variant's dynamic shared-memory limit.
-int prepare_variant(const Variant& v, int L, int S, bool bf16, bool conv) {
+int prepare_variant(const Variant& v, int L, int S, bool bf16, int kind) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
-  const int slot = (ls_index(L, S) * 2 + (bf16 ? 1 : 0)) * 2 + (conv ? 1 : 0);
+  const int slot = (ls_index(L, S) * 2 + (bf16 ? 1 : 0)) * 3 + kind;
   if (dev < kMaxDev) {
     const int r = g_resident[dev][slot].load(std::memory_order_relaxed);
     if (r > 0) return r;
@@ -783,7 +825,7 @@ int prepare_variant(const Variant& v, int L, int S, bool bf16, bool conv) {
 
 int fwd_channels_per_cta() { return fwd::kCh; }
 
-bool plan_scan_fwd(int64_t batch, int64_t L, int64_t d_inner, int d_state, bool bf16, bool conv,
+bool plan_scan_fwd(int64_t batch, int64_t L, int64_t d_inner, int d_state, bool bf16, int kind,
                    int sms, FwdPlan* plan) {
   // Lanes per channel pair: the pair's states split over 1, 2 or 4 lanes.  Four lanes (4 states
   // each) give a GPU-filling batch of channels enough warps and keep time chunks long when
@@ -798,9 +840,9 @@ bool plan_scan_fwd(int64_t batch, int64_t L, int64_t d_inner, int d_state, bool 
   int S = (d_state + lanes - 1) / lanes;
   S = S <= 4 ? 4 : S <= 8 ? 8 : 16;
   if (lanes * S > 16) { lanes = 4; S = 4; }
-  const Variant v = variant(lanes, S, bf16, conv);
+  const Variant v = variant(lanes, S, bf16, kind);
   if (v.fn == nullptr) return false;
-  const int per_sm = prepare_variant(v, lanes, S, bf16, conv);
+  const int per_sm = prepare_variant(v, lanes, S, bf16, kind);
   if (per_sm <= 0) return false;
   const int64_t n_dt = (d_inner + fwd::kCh - 1) / fwd::kCh;
   const int64_t per_chunk = batch * n_dt;
@@ -849,9 +891,9 @@ size_t fwd_workspace_bytes(int64_t batch, int64_t d_inner, const FwdPlan& plan) 
 
 cudaError_t launch_scan_fwd(const FwdLaunch& f, bool bf16, cudaStream_t stream) {
   const FwdPlan& plan = f.plan;
-  const bool conv = f.conv_w != nullptr;
-  const Variant v = variant(plan.lanes, plan.states_per_lane, bf16, conv);
-  if (v.fn == nullptr || prepare_variant(v, plan.lanes, plan.states_per_lane, bf16, conv) <= 0)
+  const int kind = f.ckpt != nullptr ? kFwdCkpt : f.conv_w != nullptr ? kFwdConv : kFwdPlain;
+  const Variant v = variant(plan.lanes, plan.states_per_lane, bf16, kind);
+  if (v.fn == nullptr || prepare_variant(v, plan.lanes, plan.states_per_lane, bf16, kind) <= 0)
     return cudaErrorInvalidValue;
   const int64_t n_dt = (f.d_inner + fwd::kCh - 1) / fwd::kCh;
   const int64_t n_rec = (int64_t)(plan.G - 1) * f.batch * n_dt;
@@ -860,7 +902,7 @@ cudaError_t launch_scan_fwd(const FwdLaunch& f, bool bf16, cudaStream_t stream) 
   a.u = f.u; a.delta = f.delta; a.A = f.A; a.B = f.B; a.C = f.C; a.D = f.D; a.z = f.z;
   a.delta_bias = f.delta_bias; a.softplus = f.softplus; a.y = f.y; a.last_state = f.last_state;
   a.initial_state = f.initial_state;
-  a.conv_w = f.conv_w; a.conv_b = f.conv_b; a.d_conv = f.d_conv; a.u_out = f.u_out;
+  a.conv_w = f.conv_w; a.conv_b = f.conv_b; a.d_conv = f.d_conv; a.u_out = f.u_out; a.ckpt = f.ckpt;
   a.batch = f.batch; a.L = f.L; a.d_inner = f.d_inner; a.N = f.d_state;
   a.G = plan.G; a.len0 = plan.len0; a.len = plan.len;
   unsigned char* ws = static_cast<unsigned char*>(f.workspace);
