@@ -255,8 +255,15 @@ __global__ void __launch_bounds__(32 * L, L == 4 ? 3 : (L == 2 ? 6 : 12)) grad_k
   const int n0 = 4 * l;
   // partial-sum slot of (step kg of the group, lane mm of the pair, pair P): the XOR keeps both
   // the writes (lanes of a pair at one step) and the reads (one lane per step) on distinct banks
-  auto p4 = [&](int kg, int mm) { return (kg * L + mm) * kCP + (P ^ (((kg + mm) % L) * (8 / L))); };
-  auto p2 = [&](int kg, int mm) { return (kg * L + mm) * kCP + (P ^ (((kg + mm) % L) * (16 / L))); };
+  //   slot = (kg L + mm) kCP + (P ^ (((kg ^ mm) & (L - 1)) c)), c = 8/L (float4) or 16/L (float2);
+  // the XOR separates, so this lane's part (l c) is folded in once.
+  const int Pl4 = P ^ (l * (8 / L)), Pl2 = P ^ (l * (16 / L));
+  // written by lane l at step kg (compile-time) of the group
+  auto p4w = [&](int kg) { return (kg * L + l) * kCP + (Pl4 ^ ((kg & (L - 1)) * (8 / L))); };
+  auto p2w = [&](int kg) { return (kg * L + l) * kCP + (Pl2 ^ ((kg & (L - 1)) * (16 / L))); };
+  // read by lane l for its own step kg = i L + l of the group, lane mm's part
+  auto p4r = [&](int i, int mm) { return ((i * L + l) * L + mm) * kCP + (Pl4 ^ (mm * (8 / L))); };
+  auto p2r = [&](int i, int mm) { return ((i * L + l) * L + mm) * kCP + (Pl2 ^ (mm * (16 / L))); };
   const int64_t t0 = (int64_t)c * p.chunk_len, t1 = min(t0 + p.chunk_len, Ls);
   const int64_t tiles = (Ls + kT - 1) / kT;
   const int64_t tl_lo = t0 / kT, tl_hi = (t1 - 1) / kT;  // chunks hold whole tiles
@@ -323,9 +330,9 @@ __global__ void __launch_bounds__(32 * L, L == 4 ? 3 : (L == 2 ? 6 : 12)) grad_k
       }
     }
   };
-  auto xrow = [&](int x, int r) {
-    return sX + (x * kT + r) * K::kRowB + (((pchunk ^ ((r % L) * K::kSwz)) * 16) + pwithin);
-  };
+  // this pair's bytes in row i L + l (the pre-phase's rows) of array x
+  const int xl = l * K::kRowB + ((pchunk ^ (l * K::kSwz)) * 16) + pwithin;
+  auto xrow = [&](int x, int i) { return sX + (x * kT + i * L) * K::kRowB + xl; };
 
   // B/C rows of a tile: global -> registers -> fp32 shared memory.  Whole 16-byte pieces when
   // the rows are exactly the padded width and 16-byte multiples, element by element otherwise.
@@ -421,6 +428,9 @@ __global__ void __launch_bounds__(32 * L, L == 4 ? 3 : (L == 2 ? 6 : 12)) grad_k
   // pair-of-step quantities (both channels) of step k, from the pre-phase
   auto q_dt = [&](int k) { return sQ[(k * 2 + 0) * kCP + (P ^ ((k % L) * K::kSwz))]; };  // dt0 dt1 dtu0 dtu1
   auto q_ds = [&](int k) { return sQ[(k * 2 + 1) * kCP + (P ^ ((k % L) * K::kSwz))]; };  // ds0 ds1 u0 u1
+  // the same for this lane's own step i L + l (rows written by this lane in the pre-phase)
+  const int qwl = l * 2 * kCP + (P ^ (l * K::kSwz));
+  auto q_own = [&](int i, int w) { return sQ + (i * L * 2 + w) * kCP + qwl; };
   auto brow = [&](int k) { return *reinterpret_cast<const float4*>(sBC + (0 * kT + k) * kNP + n0); };
   auto crow = [&](int k) { return *reinterpret_cast<const float4*>(sBC + (1 * kT + k) * kNP + n0); };
 
@@ -476,9 +486,9 @@ __global__ void __launch_bounds__(32 * L, L == 4 ? 3 : (L == 2 ? 6 : 12)) grad_k
     }
     // this lane's share of the per-channel sums over states
     const int kg = k % kOG;
-    sP4[p4(kg, l)] = make_float4(ddt[0].x + ddt[0].y, ddt[1].x + ddt[1].y,
+    sP4[p4w(kg)] = make_float4(ddt[0].x + ddt[0].y, ddt[1].x + ddt[1].y,
                                               slb[0].x + slb[0].y, slb[1].x + slb[1].y);
-    sP2[p2(kg, l)] = make_float2(rd[0].x + rd[0].y, rd[1].x + rd[1].y);
+    sP2[p2w(kg)] = make_float2(rd[0].x + rd[0].y, rd[1].x + rd[1].y);
     // dB (states n0..n0+3) and dC (same) of the pair, to this warp's block; lane position
     // XOR-swizzled per (step, dB|dC) so that the group's column sums read distinct banks
 #pragma unroll
@@ -510,28 +520,29 @@ __global__ void __launch_bounds__(32 * L, L == 4 ? 3 : (L == 2 ? 6 : 12)) grad_k
 
   // Outputs of the steps k0 .. k0+kOG-1: lane l finishes its own steps from the L lanes'
   // partial sums.
-  auto output_group = [&](auto k0_tag, int steps, int64_t ts) {
+  int64_t ebase = 0;
+  auto output_group = [&](auto k0_tag, int steps) {
     constexpr int k0 = decltype(k0_tag)::value;
 #pragma unroll
     for (int i = 0; i < kOG / L; i++) {
       const int k = k0 + i * L + l;
       if (k < steps && active) {
-        float4 a = sP4[p4(k % kOG, 0)];
-        float2 r = sP2[p2(k % kOG, 0)];
+        float4 a = sP4[p4r(i, 0)];
+        float2 r = sP2[p2r(i, 0)];
 #pragma unroll
         for (int mm = 1; mm < L; mm++) {
-          const float4 a2 = sP4[p4(k % kOG, mm)];
-          const float2 r2 = sP2[p2(k % kOG, mm)];
+          const float4 a2 = sP4[p4r(i, mm)];
+          const float2 r2 = sP2[p2r(i, mm)];
           a = make_float4(a.x + a2.x, a.y + a2.y, a.z + a2.z, a.w + a2.w);
           r = make_float2(r.x + r2.x, r.y + r2.y);
         }
-        const float4 q0 = q_dt(k), q1 = q_ds(k);
+        const float4 q0 = *q_own(k0 / L + i, 0), q1 = *q_own(k0 / L + i, 1);
         const float4 f = own[k0 / L + i];
         const float2 ddt = make_float2(a.x, a.y), slb = make_float2(a.z, a.w);
         const float2 dx = sp ? __fmul2_rn(ddt, make_float2(f.z, f.w)) : ddt;
         const float2 ds = make_float2(q1.x, q1.y), uu = make_float2(q1.z, q1.w), dt = make_float2(q0.x, q0.y);
         const float2 du = __ffma2_rn(ds, D2, __fmul2_rn(dt, slb));
-        const int64_t e = ((b * Ls + ts + k) * Dn + d) * K::kTS;
+        const int64_t e = ebase + (int64_t)(k0 + i * L) * Dn * K::kTS;
         PairIO<T>::store(static_cast<char*>(p.du) + e, du);
         PairIO<T>::store(static_cast<char*>(p.ddelta) + e, dx);
         if (has_z) {
@@ -556,20 +567,22 @@ __global__ void __launch_bounds__(32 * L, L == 4 ? 3 : (L == 2 ? 6 : 12)) grad_k
     cp_async_wait_all();
     __syncthreads();  // this tile's rows and B/C are in shared memory
 
+    // this lane's output row base: step ts + l, channel d
+    ebase = ((b * Ls + ts + l) * Dn + d) * K::kTS;
     // pre-phase: the per-element work of steps k = l (mod L)
 #pragma unroll
     for (int i = 0; i < kT / L; i++) {
       const int k = i * L + l;
-      const float2 xr = __fadd2_rn(PairIO<T>::load(xrow(0, k)), bias2);
+      const float2 xr = __fadd2_rn(PairIO<T>::load(xrow(0, i)), bias2);
       float2 spx, sgx;
       softplus_sigmoid2(xr, spx, sgx);
       float2 dt = sp ? spx : xr;
       if (k >= steps) dt = make_float2(0.f, 0.f);  // steps past the end: identity steps
-      const float2 uu = PairIO<T>::load(xrow(1, k));
-      const float2 dy = PairIO<T>::load(xrow(3, k));
+      const float2 uu = PairIO<T>::load(xrow(1, i));
+      const float2 dy = PairIO<T>::load(xrow(3, i));
       float2 ds = dy, zf = make_float2(0.f, 0.f);
       if (has_z) {
-        const float2 zz = PairIO<T>::load(xrow(2, k));
+        const float2 zz = PairIO<T>::load(xrow(2, i));
         const float2 sz = make_float2(rcp(1.f + ex2(-zz.x * kLog2e)), rcp(1.f + ex2(-zz.y * kLog2e)));
         ds = __fmul2_rn(dy, __fmul2_rn(zz, sz));  // dy * silu(z)
         // d silu / dz = sigmoid(z) (1 + z (1 - sigmoid(z)))
@@ -577,8 +590,8 @@ __global__ void __launch_bounds__(32 * L, L == 4 ? 3 : (L == 2 ? 6 : 12)) grad_k
         zf = __fmul2_rn(__fmul2_rn(dy, sz), __ffma2_rn(zz, make_float2(1.f - sz.x, 1.f - sz.y), one));
       }
       const float2 dtu = __fmul2_rn(dt, uu);
-      sQ[(k * 2 + 0) * kCP + (P ^ (l * K::kSwz))] = make_float4(dt.x, dt.y, dtu.x, dtu.y);
-      sQ[(k * 2 + 1) * kCP + (P ^ (l * K::kSwz))] = make_float4(ds.x, ds.y, uu.x, uu.y);
+      *q_own(i, 0) = make_float4(dt.x, dt.y, dtu.x, dtu.y);
+      *q_own(i, 1) = make_float4(ds.x, ds.y, uu.x, uu.y);
       own[i] = make_float4(zf.x, zf.y, sgx.x, sgx.y);
       dDacc = __ffma2_rn(ds, uu, dDacc);
     }
@@ -634,8 +647,8 @@ __global__ void __launch_bounds__(32 * L, L == 4 ? 3 : (L == 2 ? 6 : 12)) grad_k
       rev_step(k - 1, hm, hpp, dAm);
       if ((k - 1) % kOG == 0) {
         __syncwarp();
-        if (k - 1 == kOG) output_group(std::integral_constant<int, kOG>{}, steps, ts);
-        else output_group(std::integral_constant<int, 0>{}, steps, ts);  // k - 1 == 0
+        if (k - 1 == kOG) output_group(std::integral_constant<int, kOG>{}, steps);
+        else output_group(std::integral_constant<int, 0>{}, steps);  // k - 1 == 0
         warp_bc_sums(k - 1);
         __syncwarp();
       }
