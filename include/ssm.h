@@ -225,9 +225,12 @@ SSM_API ssm_status_t ssm_state_update_conv(float* state, float* conv_state, cons
  * are the ones the forward call used; no forward output is needed.  The intermediate
  * states are recomputed, not stored by the forward (youngju.dev, "Mamba: Linear-Time
  * Sequence Modeling with Selective State Spaces 论文分析", section "解决方案：Kernel
- * Fusion + Recomputation"): the pass keeps one state per 16 steps and per channel in the
- * workspace (ssm_scan_bwd_workspace_size bytes, about batch * L * d_inner * d_state / 4
- * bytes plus per-chunk summaries; not initialised by the caller).  dB and dC are
+ * Fusion + Recomputation"): the pass keeps one state per 8 steps and per channel in the
+ * workspace (ssm_scan_bwd_workspace_size bytes: a status word and the look-back records of
+ * the forward recompute, as for ssm_scan_fwd, then about batch * L * d_inner * d_state / 2
+ * bytes of states and the per-chunk summaries of the reverse pass; not initialised by the
+ * caller).  The forward recompute waits on its time chunks like ssm_scan_fwd, boundedly;
+ * ssm_get_status(workspace, stream) reports a wait that ran out.  dB and dC are
  * accumulated with atomic additions, so their last bits may vary from run to run.
  */
 SSM_API size_t ssm_scan_bwd_workspace_size(int64_t batch, int64_t L, int64_t d_inner,
@@ -270,15 +273,16 @@ SSM_API ssm_status_t ssm_ssd_fwd(const void* x, const void* dt, const float* A_h
                                  size_t workspace_bytes, void* stream);
 
 /*
- * Device-side status of the most recent forward scan that used `workspace`: waits for
- * `stream` (a cudaStream_t, NULL = legacy default stream) to finish, then returns
+ * Device-side status of the most recent forward scan (or backward pass, whose forward
+ * recompute runs the same chunked kernel) that used `workspace`: waits for `stream` (a
+ * cudaStream_t, NULL = legacy default stream) to finish, then returns
  *   SSM_ERR_CUDA             if the stream reports a CUDA error (asynchronous or sticky),
- *   SSM_ERR_LOOKBACK_TIMEOUT if a time chunk of that scan gave up waiting (its y and
- *                            last_state are invalid),
+ *   SSM_ERR_LOOKBACK_TIMEOUT if a time chunk of that call gave up waiting (its outputs are
+ *                            invalid),
  *   SSM_OK                   otherwise.
  * workspace == NULL checks the scratch of ssm_scan_fwd_noalloc on the current device (if
  * it has been used), or only the stream when it has not.  The workspace must have been
- * passed to a forward scan with a non-empty problem before (its status word is written by
+ * passed to such a call with a non-empty problem before (its status word is written by
  * every such call).  Synchronises, so it cannot be captured in a CUDA graph.
  */
 SSM_API ssm_status_t ssm_get_status(const void* workspace, void* stream);

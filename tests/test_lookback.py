@@ -88,3 +88,40 @@ def test_bounded_wait_reports_timeout_and_gpu_stays_usable(monkeypatch):
 
 def test_get_status_without_workspace_checks_the_stream():
     assert ssm.ssm_get_status(None) == 0
+
+
+def test_backward_recompute_reports_timeout(monkeypatch):
+    """The backward's forward recompute runs the chunked look-back kernel in the backward's
+    workspace: a wait that runs out is reported by ssm_get_status on that workspace, and the
+    next ordinary call gives the same gradients as before."""
+    batch, L, d_inner, d_state, bf16 = 1, 8192, 64, 16, False
+    _, _, t = _inputs(batch, L, d_inner, d_state, bf16, seed=44)
+    dy = torch.randn(batch, L, d_inner, device="cuda")
+
+    def run():
+        g = dict(du=torch.empty_like(t["u"]), ddelta=torch.empty_like(t["u"]), dz=torch.empty_like(t["u"]),
+                 dA=torch.empty((d_inner, d_state), device="cuda"),
+                 dB=torch.empty((batch, L, d_state), device="cuda"),
+                 dC=torch.empty((batch, L, d_state), device="cuda"),
+                 dD=torch.empty(d_inner, device="cuda"), dbias=torch.empty(d_inner, device="cuda"))
+        ws = torch.empty(ssm.ssm_scan_bwd_workspace_size(batch, L, d_inner, d_state, ssm.SSM_F32),
+                         dtype=torch.uint8, device="cuda")
+        ssm.ssm_scan_bwd(t["u"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["delta_bias"],
+                         True, None, dy, None, g["du"], g["ddelta"], g["dA"], g["dB"], g["dC"], g["dD"],
+                         g["dz"], g["dbias"], None, ws)
+        return g, ws
+
+    g0, ws0 = run()
+    assert ssm.ssm_get_status(ws0) == 0
+    monkeypatch.setenv("SSM_LOOKBACK_SELFTEST", "1")
+    monkeypatch.setenv("SSM_LOOKBACK_MAX_POLLS", "64")
+    _, ws1 = run()
+    assert ssm.ssm_get_status(ws1) == ssm.SSM_ERR_LOOKBACK_TIMEOUT
+    monkeypatch.delenv("SSM_LOOKBACK_SELFTEST")
+    monkeypatch.delenv("SSM_LOOKBACK_MAX_POLLS")
+    g2, ws2 = run()
+    assert ssm.ssm_get_status(ws2) == 0
+    for k in ("du", "ddelta", "dz"):  # per element: bit for bit
+        assert torch.equal(g2[k], g0[k]), k
+    for k in ("dA", "dB", "dC", "dD", "dbias"):  # atomic sums over CTAs: the last bits may vary
+        assert torch.allclose(g2[k], g0[k], rtol=1e-5, atol=1e-6), k
