@@ -680,8 +680,9 @@ def main_ours(args, rank, world, local_rank):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": ("bf16 tensor-core products (hi+lo split operands), f32 accumulation"
-                  if w.heads else "bf16 I/O, f32 state and arithmetic" if w.bf16 else "f32"),
+        "dtype": "bf16" if w.heads else "f32",
+        "dtype_note": ("bf16 tensor-core products (hi+lo split operands), f32 accumulation"
+                       if w.heads else "f32 state and arithmetic, " + ("bf16" if w.bf16 else "f32") + " I/O"),
         "data": "synthetic (seeded; recipe in inputgen/workloads.py)",
         "config": bench_config(w, args.which, world),
         "roofline": roofline(w, ms, hbm_gbs, sm_mhz_peak, sms, peak_src,
