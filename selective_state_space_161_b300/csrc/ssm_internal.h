@@ -81,6 +81,8 @@ struct SsdParams {
 };
 int ssd_head_dim();
 cudaError_t launch_ssd(const SsdParams& p, cudaStream_t s);
+// The per-head chain on tcgen05 (ssm_ssd_tc.cu); G must hold the chunk Gram matrices.
+cudaError_t launch_ssd_tc(const SsdParams& p, cudaStream_t s);
 // Chunk Gram matrices G[b][c] = C_c B_c^T (64 x 64 fp32 per batch row and chunk of 64 steps) on
 // the tensor cores (tcgen05, operands by TMA); ssd_gram_bytes is the workspace they take.
 size_t ssd_gram_bytes(int64_t batch, int64_t L);

@@ -29,6 +29,9 @@
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
 
+#include <cstdlib>
+#include <cstring>
+
 namespace ssm {
 
 constexpr int kQ = 64;            // steps per chunk
@@ -431,6 +434,10 @@ static cudaError_t launch_ssd_n(const SsdParams& p, cudaStream_t s) {
 int ssd_head_dim() { return kP; }
 
 cudaError_t launch_ssd(const SsdParams& p, cudaStream_t s) {
+  // SSM_SSD_KERNEL=tc: the per-head chain with every product on tcgen05 (ssm_ssd_tc.cu; measured
+  // slower on B300, 0.72 ms against 0.51 ms at the 8 x 2048 x 5120 x 128 shape)
+  const char* k = std::getenv("SSM_SSD_KERNEL");
+  if (k != nullptr && std::strcmp(k, "tc") == 0) return launch_ssd_tc(p, s);
   // the chunk Gram matrices of every batch row first (tensor-core kernel), then the heads
   const cudaError_t e = launch_ssd_gram(p.C, p.B, p.G, p.batch, p.L, p.N, s);
   if (e != cudaSuccess) return e;

@@ -12,7 +12,7 @@ from tests.helpers import record_margin, BF16_TOL, rel_err, to_f64
 pytestmark = pytest.mark.gpu
 
 
-def _run(w, use_D=True, use_z=True, use_bias=True, d_sel=None):
+def _run(w, use_D=True, use_z=True, use_bias=True, d_sel=None, tag=""):
     dev = W.device_ssd_inputs(w)
     y, last = ssm.selective_scan_ssd(dev["x"], dev["dt"], dev["A_head"], dev["B"], dev["C"],
                                      D=dev["D"] if use_D else None, z=dev["z"] if use_z else None,
@@ -26,7 +26,7 @@ def _run(w, use_D=True, use_z=True, use_bias=True, d_sel=None):
         ds = torch.from_numpy(np.asarray(d_sel)).cuda()
         y, last = y.index_select(2, ds), last.index_select(1, ds)
     ey, el = rel_err(to_f64(y), y_ref), rel_err(to_f64(last), last_ref)
-    record_margin(f"ssd {w.batch}x{w.L}x{w.d_inner}x{w.d_state}, {w.heads} heads", BF16_TOL, y=ey,
+    record_margin(f"ssd {w.batch}x{w.L}x{w.d_inner}x{w.d_state}, {w.heads} heads{tag}", BF16_TOL, y=ey,
                   last_state=el)
     assert ey <= BF16_TOL and el <= BF16_TOL, f"y err {ey:.3g}, last_state err {el:.3g}"
 
@@ -67,7 +67,7 @@ def test_ssd_without_softplus():
     y_ref, last_ref = oracle.scan_fwd(x["u"], np.abs(x["delta"]) / 8, x["A"], x["B"], x["C"], D=x["D"],
                                       z=x["z"], delta_bias=None, softplus_flag=False)
     ey, el = rel_err(to_f64(y), y_ref), rel_err(to_f64(last), last_ref)
-    record_margin(f"ssd {w.batch}x{w.L}x{w.d_inner}x{w.d_state}, {w.heads} heads", BF16_TOL, y=ey, last_state=el)
+    record_margin(f"ssd {w.batch}x{w.L}x{w.d_inner}x{w.d_state}, {w.heads} heads, no softplus", BF16_TOL, y=ey, last_state=el)
     assert ey <= BF16_TOL and el <= BF16_TOL, f"y err {ey:.3g}, last_state err {el:.3g}"
 
 
@@ -80,3 +80,17 @@ def test_ssd_empty_sequence_gives_zero_state():
     y, last = ssm.selective_scan_ssd(x, dt, A, bc, bc)
     torch.cuda.synchronize()
     assert y.shape == (2, 0, 128) and torch.count_nonzero(last).item() == 0
+
+
+@pytest.mark.parametrize("N", [16, 32, 64, 128])
+def test_ssd_tcgen05_chain_ragged(N, monkeypatch):
+    """The opt-in per-head chain with every product on tcgen05 (SSM_SSD_KERNEL=tc), ragged."""
+    monkeypatch.setenv("SSM_SSD_KERNEL", "tc")
+    _run(W.Workload("ssd", "ssd case", 2, 200, 128, N, True, 60 + N, 0.5, heads=2), tag=", tcgen05 chain")
+
+
+def test_ssd_tcgen05_chain_full_size_sampled(monkeypatch):
+    monkeypatch.setenv("SSM_SSD_KERNEL", "tc")
+    w = W.WORKLOADS["ssd2p7b"]
+    d_sel = np.concatenate([np.arange(0, 4), np.arange(64 * 53 + 10, 64 * 53 + 14), np.arange(5100, 5104)])
+    _run(w, d_sel=d_sel, tag=", tcgen05 chain")
