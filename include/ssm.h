@@ -67,8 +67,10 @@ typedef enum {
   SSM_ERR_ALIGN = 4,      /* a pointer is not 16-byte aligned */
   SSM_ERR_WORKSPACE = 5,  /* workspace NULL or smaller than the size query says */
   SSM_ERR_CUDA = 6,       /* no usable CUDA device, a launch failed, or a CUDA error is pending */
-  SSM_ERR_LOOKBACK_TIMEOUT = 7, /* (ssm_get_status) a time chunk gave up waiting for its
-                                   predecessors' records; that call's outputs are invalid */
+  SSM_ERR_LOOKBACK_TIMEOUT = 7, /* (ssm_get_status) a bounded wait in a kernel ran out: a time
+                                   chunk waiting for its predecessors' records, or an SSD kernel
+                                   waiting for its copies or tensor-core products; that call's
+                                   outputs are invalid */
   SSM_ERR_SCRATCH_LIMIT = 8 /* ssm_scan_fwd_noalloc: the problem needs more scratch than it holds */
 } ssm_status_t;
 
@@ -261,7 +263,10 @@ SSM_API ssm_status_t ssm_scan_bwd(const void* u, const void* delta, const float*
  * The chunks' Gram matrices G = C B^T do not depend on the head (B and C are shared by all
  * heads): a first tensor-core kernel (tcgen05.mma with operands brought in by TMA) computes
  * them once per batch row and chunk into the workspace (ssm_ssd_fwd_workspace_size bytes:
- * batch * ceil(L / 64) * 64 * 64 fp32; no initialisation needed), and every head reads them.
+ * a 256-byte status word, then batch * ceil(L / 64) * 64 * 64 fp32; no initialisation
+ * needed), and every head reads them.  The kernels' waits on their copies and tensor-core
+ * products are bounded: a wait that runs out makes ssm_get_status(workspace, stream) return
+ * SSM_ERR_LOOKBACK_TIMEOUT (the outputs are then invalid), never a hang.
  */
 SSM_API size_t ssm_ssd_fwd_workspace_size(int64_t batch, int64_t L, int64_t d_inner, int n_heads,
                                           int d_state);
@@ -273,12 +278,13 @@ SSM_API ssm_status_t ssm_ssd_fwd(const void* x, const void* dt, const float* A_h
                                  size_t workspace_bytes, void* stream);
 
 /*
- * Device-side status of the most recent forward scan (or backward pass, whose forward
- * recompute runs the same chunked kernel) that used `workspace`: waits for `stream` (a
- * cudaStream_t, NULL = legacy default stream) to finish, then returns
+ * Device-side status of the most recent forward scan, backward pass (whose forward
+ * recompute runs the same chunked kernel) or chunked SSD call that used `workspace`: waits
+ * for `stream` (a cudaStream_t, NULL = legacy default stream) to finish, then returns
  *   SSM_ERR_CUDA             if the stream reports a CUDA error (asynchronous or sticky),
- *   SSM_ERR_LOOKBACK_TIMEOUT if a time chunk of that call gave up waiting (its outputs are
- *                            invalid),
+ *   SSM_ERR_LOOKBACK_TIMEOUT if a wait of that call ran out: a time chunk waiting for its
+ *                            predecessors' records, or an SSD kernel waiting for its copies
+ *                            or tensor-core products (the outputs are invalid),
  *   SSM_OK                   otherwise.
  * workspace == NULL checks the scratch of ssm_scan_fwd_noalloc on the current device (if
  * it has been used), or only the stream when it has not.  The workspace must have been

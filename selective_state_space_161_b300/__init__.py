@@ -140,8 +140,8 @@ def ssm_scan_fwd_workspace_size(batch: int, L: int, d_inner: int, d_state: int, 
 
 def ssm_get_status(workspace=None, stream=None) -> int:
     """C-ABI ``ssm_get_status``: waits for ``stream`` and returns the device-side status of the
-    latest forward scan that used ``workspace`` (None: the no-allocation entry point's scratch):
-    0 (SSM_OK), SSM_ERR_LOOKBACK_TIMEOUT or SSM_ERR_CUDA."""
+    latest forward scan, backward pass or chunked SSD call that used ``workspace`` (None: the
+    no-allocation entry point's scratch): 0 (SSM_OK), SSM_ERR_LOOKBACK_TIMEOUT or SSM_ERR_CUDA."""
     _check_dev("workspace", workspace)
     return int(load_library().ssm_get_status(_ptr(workspace), _stream_handle(stream)))
 

@@ -396,8 +396,9 @@ size_t ssm_ssd_fwd_workspace_size(int64_t batch, int64_t L, int64_t d_inner, int
                                   int d_state) {
   (void)d_inner; (void)n_heads; (void)d_state;
   if (batch <= 0 || L <= 0) return 0;
-  // the chunk Gram matrices C B^T (shared by every head); the state itself stays on chip
-  return ssm::ssd_gram_bytes(batch, L);
+  // a status word, then the chunk Gram matrices C B^T (shared by every head); the state itself
+  // stays on chip
+  return ssm::kFwdHeaderBytes + ssm::ssd_gram_bytes(batch, L);
 }
 
 ssm_status_t ssm_ssd_fwd(const void* x, const void* dt, const float* A, const void* B,
@@ -423,7 +424,8 @@ ssm_status_t ssm_ssd_fwd(const void* x, const void* dt, const float* A, const vo
       return SSM_ERR_CUDA;
     return SSM_OK;
   }
-  if (workspace == nullptr || workspace_bytes < ssm::ssd_gram_bytes(batch, L)) return SSM_ERR_WORKSPACE;
+  if (workspace == nullptr || workspace_bytes < ssm::kFwdHeaderBytes + ssm::ssd_gram_bytes(batch, L))
+    return SSM_ERR_WORKSPACE;
   if (batch * L >= ((int64_t)1 << 31)) return SSM_ERR_SHAPE;  // rows of the Gram kernel's TMA maps
   ssm::SsdParams p{};
   p.x = static_cast<const __nv_bfloat16*>(x);
@@ -437,7 +439,9 @@ ssm_status_t ssm_ssd_fwd(const void* x, const void* dt, const float* A, const vo
   p.softplus = softplus_flag != 0;
   p.y = static_cast<__nv_bfloat16*>(y);
   p.last_state = last_state;
-  p.G = static_cast<float*>(workspace);
+  p.header = static_cast<unsigned long long*>(workspace);
+  p.tag = next_call_tag();
+  p.G = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + ssm::kFwdHeaderBytes);
   p.batch = batch; p.L = L; p.d_inner = d_inner; p.heads = n_heads; p.N = d_state;
   if (batch * n_heads >= ((int64_t)1 << 31)) return SSM_ERR_SHAPE;
   return ssm::launch_ssd(p, s) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;

@@ -76,6 +76,8 @@ struct SsdParams {
   __nv_bfloat16* y;
   float* last_state;        // [batch][d_inner][N], may be null
   float* G;                 // workspace: [batch][chunks][64][64] chunk Gram matrices C B^T
+  unsigned long long* header;  // workspace status word: (tag << 8) | code (code 7: a wait ran out)
+  unsigned long long tag;      // this call's tag
   int64_t batch, L, d_inner;
   int heads, N;
 };
@@ -86,8 +88,11 @@ cudaError_t launch_ssd_tc(const SsdParams& p, cudaStream_t s);
 // Chunk Gram matrices G[b][c] = C_c B_c^T (64 x 64 fp32 per batch row and chunk of 64 steps) on
 // the tensor cores (tcgen05, operands by TMA); ssd_gram_bytes is the workspace they take.
 size_t ssd_gram_bytes(int64_t batch, int64_t L);
+// The status word at `header` is set to (tag << 8) by the launch and raised to (tag << 8) | 7 if
+// a wait on the copies or the MMA runs out.
 cudaError_t launch_ssd_gram(const __nv_bfloat16* C, const __nv_bfloat16* B, float* G, int64_t batch,
-                            int64_t L, int N, cudaStream_t s);
+                            int64_t L, int N, unsigned long long* header, unsigned long long tag,
+                            cudaStream_t s);
 
 // ---- Single-pass forward scan with a decoupled look-back (ssm_scan_fwd.cu) ----
 

@@ -439,7 +439,7 @@ cudaError_t launch_ssd(const SsdParams& p, cudaStream_t s) {
   const char* k = std::getenv("SSM_SSD_KERNEL");
   if (k != nullptr && std::strcmp(k, "tc") == 0) return launch_ssd_tc(p, s);
   // the chunk Gram matrices of every batch row first (tensor-core kernel), then the heads
-  const cudaError_t e = launch_ssd_gram(p.C, p.B, p.G, p.batch, p.L, p.N, s);
+  const cudaError_t e = launch_ssd_gram(p.C, p.B, p.G, p.batch, p.L, p.N, p.header, p.tag, s);
   if (e != cudaSuccess) return e;
   switch (p.N) {
     case 16: return launch_ssd_n<16>(p, s);

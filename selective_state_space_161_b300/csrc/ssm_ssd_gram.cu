@@ -14,7 +14,8 @@
 // d_state/16 tcgen05.mma (M = N = 128, K = 16, bf16 in, fp32 accumulate) into tensor memory;
 // the four warps read their 32 rows back (tcgen05.ld) and store the two diagonal 64 x 64 blocks
 // (the off-diagonal blocks pair steps of different chunks and are not needed).  Waits on the
-// copy and MMA barriers are bounded: a wait that runs out leaves G unwritten and never hangs.
+// copy and MMA barriers are bounded: a wait that runs out leaves G unwritten, raises the call's
+// status word to code 7 (read by ssm_get_status) and never hangs.
 
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
@@ -58,6 +59,8 @@ struct Args {
   float* G;      // [batch][chunks][64][64]
   int64_t batch, L;
   int chunks, N;
+  unsigned long long* header;  // status word: (tag << 8) | code
+  unsigned long long tag;
 };
 
 template <int N>
@@ -75,6 +78,7 @@ __global__ void __launch_bounds__(kThreads) gram_kernel(const __grid_constant__ 
   const int c0 = 2 * blockIdx.x;
   const int row0 = (int)(b * a.L + (int64_t)c0 * 64);  // first global row (step) of the pair
 
+  if (blockIdx.x == 0 && blockIdx.y == 0 && tid == 0) atomicExch(a.header, a.tag << 8);  // this call's status: ok
   if (tid == 0) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bars[0])));
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bars[1])));
@@ -128,6 +132,7 @@ __global__ void __launch_bounds__(kThreads) gram_kernel(const __grid_constant__ 
                  : "memory");
   }
   const bool done = loaded && mbar_wait(smem_u32(&bars[1]), 0);
+  if (!done && tid == 0) atomicMax(a.header, (a.tag << 8) | (unsigned long long)kLookbackTimeoutCode);
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 
   // Warp w reads rows 32 w .. 32 w + 31 (TMEM lanes); rows < 64 belong to chunk c0 (columns
@@ -214,11 +219,12 @@ size_t ssd_gram_bytes(int64_t batch, int64_t L) {
 }
 
 cudaError_t launch_ssd_gram(const __nv_bfloat16* C, const __nv_bfloat16* B, float* G, int64_t batch,
-                            int64_t L, int N, cudaStream_t s) {
+                            int64_t L, int N, unsigned long long* header, unsigned long long tag,
+                            cudaStream_t s) {
   CUtensorMap mc, mb;
   if (!gram::make_map(&mc, C, batch * L, N) || !gram::make_map(&mb, B, batch * L, N))
     return cudaErrorInvalidValue;
-  gram::Args a{G, batch, L, (int)((L + 63) / 64), N};
+  gram::Args a{G, batch, L, (int)((L + 63) / 64), N, header, tag};
   switch (N) {
     case 16: return gram::launch_n<16>(mc, mb, a, s);
     case 32: return gram::launch_n<32>(mc, mb, a, s);

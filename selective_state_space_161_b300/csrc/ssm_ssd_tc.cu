@@ -197,6 +197,7 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
   const int qd = warp % 4, ch = warp / 4;      // lane quadrant, column half
   const int rA = 16 * qd + g, rB = rA + 8;     // this thread's rows of every M = 64 product
 
+  if (blockIdx.x == 0 && tid == 0) atomicExch(p.header, p.tag << 8);  // this call's status: ok
   if (tid < kP) sD[tid] = p.D ? p.D[h * kP + tid] : 0.f;
   if (tid == 0) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(bar)));
@@ -349,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
     ok = __syncthreads_and(mbar_wait(smem_u32(bar), phase)) != 0;
     phase ^= 1;
     tc_after_sync();
-    if (!ok) break;
+    if (!ok) break;  // the status word reports it below
     // ---- M = G delta_s 2^{S_t - S_s} (s <= t) as hi / lo, K-major [t][s], from this thread's
     // fragment of G: rows rA, rB, columns s = p0 + 8 j + 2 tq (+1)
     {
@@ -479,6 +480,7 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
     store_state();
   }
   cp_async_wait_all();
+  if (!ok && tid == 0) atomicMax(p.header, (p.tag << 8) | (unsigned long long)kLookbackTimeoutCode);
 
   if (ok && p.last_state) {
 #pragma unroll

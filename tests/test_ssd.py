@@ -94,3 +94,19 @@ def test_ssd_tcgen05_chain_full_size_sampled(monkeypatch):
     w = W.WORKLOADS["ssd2p7b"]
     d_sel = np.concatenate([np.arange(0, 4), np.arange(64 * 53 + 10, 64 * 53 + 14), np.arange(5100, 5104)])
     _run(w, d_sel=d_sel, tag=", tcgen05 chain")
+
+
+@pytest.mark.parametrize("kernel", ["mma", "tc"])
+def test_ssd_status_word_reports_ok(kernel, monkeypatch):
+    """Every chunked SSD call writes its status word at the start of the workspace (the waits
+    that could raise it are bounded); a completed call reads back as SSM_OK."""
+    monkeypatch.setenv("SSM_SSD_KERNEL", kernel)
+    w = W.Workload("ssd", "ssd case", 1, 130, 128, 64, True, 91, 0.5, heads=2)
+    dev = W.device_ssd_inputs(w)
+    y = torch.empty_like(dev["x"])
+    # every byte 7: a status word the call did not write would read as the timeout code
+    ws = torch.full((ssm.ssm_ssd_fwd_workspace_size(1, 130, 128, 2, 64),), 7, dtype=torch.uint8, device="cuda")
+    assert ssm.ssm_get_status(ws) == ssm.SSM_ERR_LOOKBACK_TIMEOUT
+    ssm.ssm_ssd_fwd(dev["x"], dev["dt"], dev["A_head"], dev["B"], dev["C"], dev["D"], dev["z"], dev["dt_bias"],
+                    True, y, None, ws)
+    assert ssm.ssm_get_status(ws) == 0
