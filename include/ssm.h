@@ -262,10 +262,15 @@ SSM_API ssm_status_t ssm_scan_bwd(const void* u, const void* delta, const float*
  * {16, 32, 64, 128}; D, z, dt_bias, last_state nullable; batch * L < 2^31.
  * The chunks' Gram matrices G = C B^T do not depend on the head (B and C are shared by all
  * heads): a first tensor-core kernel (tcgen05.mma with operands brought in by TMA) computes
- * them once per batch row and chunk into the workspace (ssm_ssd_fwd_workspace_size bytes:
- * a 256-byte status word, then batch * ceil(L / 64) * 64 * 64 fp32; no initialisation
- * needed), and every head reads them.  The kernels' waits on their copies and tensor-core
- * products are bounded: a wait that runs out makes ssm_get_status(workspace, stream) return
+ * them once per batch row and chunk into the workspace, and every head reads them.  When the
+ * (batch, head) chains would not spread evenly over the SMs, each chain is run as two time
+ * halves of whole chunks: the first hands its end state to the second through the workspace.
+ * Workspace (ssm_ssd_fwd_workspace_size bytes, caller-owned, no initialisation needed: every
+ * record carries a per-call tag): a 256-byte status word; batch * ceil(L / 64) * 64 * 64 fp32
+ * Gram matrices; one 8-byte flag per (batch, head), padded to a multiple of 256 bytes;
+ * batch * d_inner * d_state fp32 for the handed-over states.  The kernels' waits (on their
+ * copies, their tensor-core products, and the second half's wait for the first half's state)
+ * are bounded: a wait that runs out makes ssm_get_status(workspace, stream) return
  * SSM_ERR_LOOKBACK_TIMEOUT (the outputs are then invalid), never a hang.
  */
 SSM_API size_t ssm_ssd_fwd_workspace_size(int64_t batch, int64_t L, int64_t d_inner, int n_heads,
@@ -283,8 +288,9 @@ SSM_API ssm_status_t ssm_ssd_fwd(const void* x, const void* dt, const float* A_h
  * for `stream` (a cudaStream_t, NULL = legacy default stream) to finish, then returns
  *   SSM_ERR_CUDA             if the stream reports a CUDA error (asynchronous or sticky),
  *   SSM_ERR_LOOKBACK_TIMEOUT if a wait of that call ran out: a time chunk waiting for its
- *                            predecessors' records, or an SSD kernel waiting for its copies
- *                            or tensor-core products (the outputs are invalid),
+ *                            predecessors' records, or an SSD kernel waiting for its copies,
+ *                            its tensor-core products or the state of the first time half
+ *                            (the outputs are invalid),
  *   SSM_OK                   otherwise.
  * workspace == NULL checks the scratch of ssm_scan_fwd_noalloc on the current device (if
  * it has been used), or only the stream when it has not.  The workspace must have been

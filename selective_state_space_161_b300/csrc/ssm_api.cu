@@ -394,11 +394,11 @@ ssm_status_t ssm_scan_bwd(const void* u, const void* delta, const float* A, cons
 
 size_t ssm_ssd_fwd_workspace_size(int64_t batch, int64_t L, int64_t d_inner, int n_heads,
                                   int d_state) {
-  (void)d_inner; (void)n_heads; (void)d_state;
-  if (batch <= 0 || L <= 0) return 0;
-  // a status word, then the chunk Gram matrices C B^T (shared by every head); the state itself
-  // stays on chip
-  return ssm::kFwdHeaderBytes + ssm::ssd_gram_bytes(batch, L);
+  (void)n_heads;
+  if (batch <= 0 || L <= 0 || d_inner < 0) return 0;
+  // a status word, the chunk Gram matrices C B^T (shared by every head), then one flag per
+  // (batch, head) and room for the state handed from the first time half to the second
+  return ssm::ssd_workspace_bytes(batch, L, d_inner, d_state);
 }
 
 ssm_status_t ssm_ssd_fwd(const void* x, const void* dt, const float* A, const void* B,
@@ -424,7 +424,7 @@ ssm_status_t ssm_ssd_fwd(const void* x, const void* dt, const float* A, const vo
       return SSM_ERR_CUDA;
     return SSM_OK;
   }
-  if (workspace == nullptr || workspace_bytes < ssm::kFwdHeaderBytes + ssm::ssd_gram_bytes(batch, L))
+  if (workspace == nullptr || workspace_bytes < ssm::ssd_workspace_bytes(batch, L, d_inner, d_state))
     return SSM_ERR_WORKSPACE;
   if (batch * L >= ((int64_t)1 << 31)) return SSM_ERR_SHAPE;  // rows of the Gram kernel's TMA maps
   ssm::SsdParams p{};
@@ -439,10 +439,16 @@ ssm_status_t ssm_ssd_fwd(const void* x, const void* dt, const float* A, const vo
   p.softplus = softplus_flag != 0;
   p.y = static_cast<__nv_bfloat16*>(y);
   p.last_state = last_state;
-  p.header = static_cast<unsigned long long*>(workspace);
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  p.header = reinterpret_cast<unsigned long long*>(ws);
   p.tag = next_call_tag();
-  p.G = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + ssm::kFwdHeaderBytes);
+  p.wait_tag = lookback_selftest() ? (p.tag ^ 1ull) : p.tag;
+  p.max_polls = lookback_max_polls();
+  p.G = reinterpret_cast<float*>(ws + ssm::kFwdHeaderBytes);
+  p.flags = reinterpret_cast<unsigned long long*>(ws + ssm::ssd_flags_offset(batch, L));
+  p.hand = reinterpret_cast<float*>(ws + ssm::ssd_hand_offset(batch, L, d_inner));
   p.batch = batch; p.L = L; p.d_inner = d_inner; p.heads = n_heads; p.N = d_state;
+  p.sms = current_sm_count();
   if (batch * n_heads >= ((int64_t)1 << 31)) return SSM_ERR_SHAPE;
   return ssm::launch_ssd(p, s) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }

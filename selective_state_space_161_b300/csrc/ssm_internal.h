@@ -78,10 +78,20 @@ struct SsdParams {
   float* G;                 // workspace: [batch][chunks][64][64] chunk Gram matrices C B^T
   unsigned long long* header;  // workspace status word: (tag << 8) | code (code 7: a wait ran out)
   unsigned long long tag;      // this call's tag
+  unsigned long long wait_tag; // the tag the second time half waits for (== tag but in a self-test)
+  unsigned max_polls;          // polls of that wait before it gives up
+  unsigned long long* flags;   // workspace: [batch][heads] the first half's "state is out" tag
+  float* hand;                 // workspace: [batch][d_inner][N] the state at the end of the first half
   int64_t batch, L, d_inner;
   int heads, N;
+  int sms;                     // SMs of the device (the launch picks one or two time halves)
 };
 int ssd_head_dim();
+// Workspace of ssm_ssd_fwd: status word, chunk Gram matrices, the halves' flags and hand-over
+// states.
+size_t ssd_workspace_bytes(int64_t batch, int64_t L, int64_t d_inner, int N);
+size_t ssd_flags_offset(int64_t batch, int64_t L);
+size_t ssd_hand_offset(int64_t batch, int64_t L, int64_t d_inner);
 cudaError_t launch_ssd(const SsdParams& p, cudaStream_t s);
 // The per-head chain on tcgen05 (ssm_ssd_tc.cu); G must hold the chunk Gram matrices.
 cudaError_t launch_ssd_tc(const SsdParams& p, cudaStream_t s);

@@ -25,10 +25,19 @@
 // shared-memory tiles by ldmatrix.  The inputs x, B, C are bf16 already; the computed operands
 // (M, w x, the carried state) go in as a bf16 hi part plus a bf16 lo part (the rounding
 // remainder), two products each, so their rounding error is ~2^-16 rather than bf16's 2^-8.
+//
+// Time parts.  When the (batch, head) chains do not spread evenly over the SMs (a partial
+// wave), each chain is cut into parts of whole chunks, one CTA each: part k walks its chunks
+// from the state part k - 1 hands over through the workspace (a release store of a per-call,
+// per-part tag), after starting its first copies and decays and waiting (acquire loads,
+// bounded) for that tag; part 0 starts from zero.  The work is the same; the parts are finer
+// pieces for the SMs to share.  CTAs are numbered part-major, so the CTA a part waits for was
+// dispatched before it.
 
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
 
+#include <algorithm>
 #include <cstdlib>
 #include <cstring>
 
@@ -209,12 +218,28 @@ __device__ __forceinline__ void g_phase(SsdSmem<N>& sm, const float* sS, const f
   }
 }
 
+__device__ __forceinline__ unsigned long long ssd_ld_acquire(const unsigned long long* q) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(q) : "memory");
+  return v;
+}
+__device__ __forceinline__ void ssd_st_release(unsigned long long* q, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(q), "l"(v) : "memory");
+}
+
+// part_len: steps per time part (a multiple of kQ; >= p.L for one part).
 template <int N>
-__global__ void __launch_bounds__(kSsdThreads, 3) ssd_fused_kernel(const SsdParams p) {
+__global__ void __launch_bounds__(kSsdThreads, 3) ssd_fused_kernel(const SsdParams p, int64_t part_len) {
   extern __shared__ __align__(16) unsigned char ssd_smem[];
   SsdSmem<N>& sm = *reinterpret_cast<SsdSmem<N>*>(ssd_smem);
-  const int h = blockIdx.x % p.heads;
-  const int64_t b = blockIdx.x / p.heads;
+  const int64_t chains = p.batch * p.heads;
+  const int64_t chain = blockIdx.x % chains;
+  const int part = (int)(blockIdx.x / chains);
+  const int64_t t_begin = (int64_t)part * part_len;
+  const int64_t t_end = min(t_begin + part_len, p.L);
+  const bool hands_over = t_end < p.L;  // a later part continues from this one's end state
+  const int h = (int)(chain % p.heads);
+  const int64_t b = chain / p.heads;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int g = lane / 4, tq = lane % 4;
   const int p0 = 16 * warp;  // this warp's channels within the head
@@ -230,17 +255,45 @@ __global__ void __launch_bounds__(kSsdThreads, 3) ssd_fused_kernel(const SsdPara
   // outputs), x, z at the chunk's start; warp 0 computes the next chunk's step sizes and decays
   // (into the other parity's arrays) while the current chunk runs, from raw step sizes loaded
   // a chunk earlier still.
-  load_tile_async<N>(&sm.B[0][0], p.B + b * p.L * N, N, (int)min((int64_t)kQ, p.L));
-  load_tile_async<N>(&sm.C[0][0], p.C + b * p.L * N, N, (int)min((int64_t)kQ, p.L));
+  load_tile_async<N>(&sm.B[0][0], p.B + (b * p.L + t_begin) * N, N, (int)min((int64_t)kQ, p.L - t_begin));
+  load_tile_async<N>(&sm.C[0][0], p.C + (b * p.L + t_begin) * N, N, (int)min((int64_t)kQ, p.L - t_begin));
   ssd_cp_async_commit();
   float2 dt_raw = make_float2(0.f, 0.f);
   if (warp == 0) {
-    chunk_decays(p, h, 0, load_dt_pair(p, b, h, 0, lane), lane, sm.dt[0], sm.S[0], sm.W[0]);
-    if (kQ < p.L) dt_raw = load_dt_pair(p, b, h, kQ, lane);
+    chunk_decays(p, h, t_begin, load_dt_pair(p, b, h, t_begin, lane), lane, sm.dt[0], sm.S[0], sm.W[0]);
+    if (t_begin + kQ < t_end) dt_raw = load_dt_pair(p, b, h, t_begin + kQ, lane);
+  }
+
+  if (part > 0) {
+    // The state at t_begin, from the part before: wait for its tag (bounded: a wait that runs
+    // out records code 7 in the status word, and the walk goes on from what is there).
+    if (threadIdx.x == 0) {
+      bool ok = false;
+      unsigned ns = 32;
+      const unsigned long long want = (p.wait_tag << 8) | (unsigned long long)part;
+      for (unsigned it = 0; it < p.max_polls; it++) {
+        if (ssd_ld_acquire(p.flags + chain) == want) {
+          ok = true;
+          break;
+        }
+        __nanosleep(ns);
+        ns = ns < 1024 ? 2 * ns : 1024;
+      }
+      if (!ok) atomicMax(p.header, (p.tag << 8) | 7ull);
+    }
+    __syncthreads();
+    const float* in = p.hand + (b * p.d_inner + (int64_t)h * kP + p0) * N;
+#pragma unroll
+    for (int nt = 0; nt < N / 8; nt++) {
+      const int col = 8 * nt + 2 * tq;
+      const float2 v0 = __ldcg(reinterpret_cast<const float2*>(in + g * N + col));
+      const float2 v1 = __ldcg(reinterpret_cast<const float2*>(in + (g + 8) * N + col));
+      H[nt][0] = v0.x; H[nt][1] = v0.y; H[nt][2] = v1.x; H[nt][3] = v1.y;
+    }
   }
 
   int par = 0;  // parity of the current chunk's decay arrays
-  for (int64_t t0 = 0; t0 < p.L; t0 += kQ, par ^= 1) {
+  for (int64_t t0 = t_begin; t0 < t_end; t0 += kQ, par ^= 1) {
     const int rows = (int)min((int64_t)kQ, p.L - t0);
     float G[5][4];  // this warp's tiles of the chunk's Gram matrix
     {
@@ -261,9 +314,9 @@ __global__ void __launch_bounds__(kSsdThreads, 3) ssd_fused_kernel(const SsdPara
     ssd_cp_async_commit();
     ssd_cp_async_wait<1>();  // this chunk's B, C have landed (x, z may still be in flight)
     __syncthreads();         // ... and this chunk's decays (written during the previous chunk)
-    if (warp == 0 && t0 + kQ < p.L) {
+    if (warp == 0 && t0 + kQ < t_end) {
       chunk_decays(p, h, t0 + kQ, dt_raw, lane, sm.dt[par ^ 1], sm.S[par ^ 1], sm.W[par ^ 1]);
-      if (t0 + 2 * kQ < p.L) dt_raw = load_dt_pair(p, b, h, t0 + 2 * kQ, lane);
+      if (t0 + 2 * kQ < t_end) dt_raw = load_dt_pair(p, b, h, t0 + 2 * kQ, lane);
     }
 
     // ---- M (hi, lo) from this warp's tiles of G into shared memory
@@ -345,7 +398,7 @@ __global__ void __launch_bounds__(kSsdThreads, 3) ssd_fused_kernel(const SsdPara
       }
     }
     __syncthreads();  // every warp is done with the B and C tiles: request the next chunk's
-    if (t0 + kQ < p.L) {
+    if (t0 + kQ < t_end) {
       const int next_rows = (int)min((int64_t)kQ, p.L - t0 - kQ);
       load_tile_async<N>(&sm.B[0][0], p.B + (b * p.L + t0 + kQ) * N, N, next_rows);
       load_tile_async<N>(&sm.C[0][0], p.C + (b * p.L + t0 + kQ) * N, N, next_rows);
@@ -408,6 +461,21 @@ __global__ void __launch_bounds__(kSsdThreads, 3) ssd_fused_kernel(const SsdPara
   }
   ssd_cp_async_wait<0>();  // nothing left in flight (the last commit is an empty group)
 
+  if (hands_over) {
+    float* out = p.hand + (b * p.d_inner + (int64_t)h * kP + p0) * N;
+#pragma unroll
+    for (int nt = 0; nt < N / 8; nt++) {
+      const int col = 8 * nt + 2 * tq;
+      __stcg(reinterpret_cast<float2*>(out + g * N + col), make_float2(H[nt][0], H[nt][1]));
+      __stcg(reinterpret_cast<float2*>(out + (g + 8) * N + col), make_float2(H[nt][2], H[nt][3]));
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      ssd_st_release(p.flags + chain, (p.tag << 8) | (unsigned long long)(part + 1));
+    }
+    return;
+  }
   if (p.last_state) {
     float* out = p.last_state + (b * p.d_inner + (int64_t)h * kP + p0) * N;
 #pragma unroll
@@ -427,11 +495,41 @@ static cudaError_t launch_ssd_n(const SsdParams& p, cudaStream_t s) {
   e = cudaFuncSetAttribute(ssd_fused_kernel<N>, cudaFuncAttributePreferredSharedMemoryCarveout,
                            cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
-  ssd_fused_kernel<N><<<(unsigned)(p.batch * p.heads), kSsdThreads, smem, s>>>(p);
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ssd_fused_kernel<N>, kSsdThreads, smem);
+  if (e != cudaSuccess) return e;
+  // Two time halves unless the chains already spread evenly: whole waves of resident CTAs, or
+  // one wave with the same number of CTAs on every SM (measured on B300 at 8 x 2048 x 5120 x
+  // 128, 640 chains in 444 slots: see the design notes).
+  const int64_t chains = p.batch * p.heads;
+  const int64_t n_chunks = (p.L + kQ - 1) / kQ;
+  const int64_t slots = (int64_t)std::max(1, p.sms) * std::max(1, per_sm);
+  const bool even = chains % slots == 0 || (chains <= slots && chains % std::max(1, p.sms) == 0);
+  int parts = even ? 1 : 2;
+  if (const char* v = std::getenv("SSM_SSD_PARTS")) {
+    const int f = std::atoi(v);
+    if (f >= 1 && f <= 64) parts = f;
+  }
+  while (parts > 1 && (int64_t)parts * chains > 0x7FFFFFFF) parts--;  // grid size limit
+  const int64_t chunks_per_part = (n_chunks + std::max(1, parts) - 1) / std::max(1, parts);
+  const int64_t part_len = chunks_per_part * kQ;
+  parts = (int)((n_chunks + chunks_per_part - 1) / chunks_per_part);  // none empty
+  ssd_fused_kernel<N><<<(unsigned)(parts * chains), kSsdThreads, smem, s>>>(p, part_len);
   return cudaGetLastError();
 }
 
 int ssd_head_dim() { return kP; }
+
+size_t ssd_flags_offset(int64_t batch, int64_t L) { return kFwdHeaderBytes + ssd_gram_bytes(batch, L); }
+
+size_t ssd_hand_offset(int64_t batch, int64_t L, int64_t d_inner) {
+  const int64_t chains = batch * (d_inner / kP);
+  return ssd_flags_offset(batch, L) + ((size_t)chains * 8 + 255) / 256 * 256;
+}
+
+size_t ssd_workspace_bytes(int64_t batch, int64_t L, int64_t d_inner, int N) {
+  return ssd_hand_offset(batch, L, d_inner) + (size_t)batch * d_inner * N * sizeof(float);
+}
 
 cudaError_t launch_ssd(const SsdParams& p, cudaStream_t s) {
   // SSM_SSD_KERNEL=tc: the per-head chain with every product on tcgen05 (ssm_ssd_tc.cu; measured

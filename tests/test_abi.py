@@ -87,5 +87,8 @@ def test_ssd_host_validation_before_any_device_call():
     assert _ssd_rc(batch=0) == 0                   # empty problem
     assert _ssd_rc() == 1                          # A (and the tensors) missing
     # the chunk Gram matrices C B^T, shared by every head: 8 x 32 chunks x 64 x 64 fp32
-    assert ssm.ssm_ssd_fwd_workspace_size(8, 2048, 5120, 80, 128) == 256 + 8 * 32 * 64 * 64 * 4  # status word + Gram matrices
+    # status word, Gram matrices, one flag per (batch, head) in whole 256-byte blocks, and the
+    # state handed from the first time half to the second
+    assert ssm.ssm_ssd_fwd_workspace_size(8, 2048, 5120, 80, 128) == (
+        256 + 8 * 32 * 64 * 64 * 4 + 5120 + 8 * 5120 * 128 * 4)
     assert ssm.ssm_ssd_fwd_workspace_size(8, 0, 5120, 80, 128) == 0

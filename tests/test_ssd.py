@@ -96,6 +96,50 @@ def test_ssd_tcgen05_chain_full_size_sampled(monkeypatch):
     _run(w, d_sel=d_sel, tag=", tcgen05 chain")
 
 
+def _ssd_call(dev, ws=None):
+    y = torch.empty_like(dev["x"])
+    last = torch.empty((dev["x"].shape[0], dev["x"].shape[2], dev["B"].shape[2]), device="cuda")
+    if ws is None:
+        b, L, d = dev["x"].shape
+        ws = torch.empty((ssm.ssm_ssd_fwd_workspace_size(b, L, d, dev["dt"].shape[2], dev["B"].shape[2]),),
+                         dtype=torch.uint8, device="cuda")
+    ssm.ssm_ssd_fwd(dev["x"], dev["dt"], dev["A_head"], dev["B"], dev["C"], dev["D"], dev["z"], dev["dt_bias"],
+                    True, y, last, ws)
+    return y, last, ws
+
+
+@pytest.mark.parametrize("L,parts", [(130, 2), (200, 2), (200, 3), (2048, 2), (2048, 5), (2048, 32)])
+def test_ssd_time_parts_match_one_walk(L, parts, monkeypatch):
+    """Time parts (each starting from the state the part before hands over) run the same
+    operations in the same order as one walk over all chunks: bit-identical outputs."""
+    w = W.Workload("ssd", "ssd case", 2, L, 192, 64, True, 300 + L, 0.5, heads=3)
+    dev = W.device_ssd_inputs(w)
+    monkeypatch.setenv("SSM_SSD_PARTS", "1")
+    y1, l1, _ = _ssd_call(dev)
+    monkeypatch.setenv("SSM_SSD_PARTS", str(parts))
+    y2, l2, ws = _ssd_call(dev)
+    torch.cuda.synchronize()
+    assert ssm.ssm_get_status(ws) == 0
+    assert torch.equal(y1, y2) and torch.equal(l1, l2)
+
+
+def test_ssd_time_part_wait_reports_timeout(monkeypatch):
+    """A time part's wait for the state of the part before is bounded: with a tag nobody writes
+    and a 64-poll limit it gives up, the call reports SSM_ERR_LOOKBACK_TIMEOUT and the next call
+    is clean again.  No GPU fault is involved: the CTAs just finish."""
+    w = W.Workload("ssd", "ssd case", 1, 256, 128, 32, True, 71, 0.5, heads=2)
+    dev = W.device_ssd_inputs(w)
+    monkeypatch.setenv("SSM_SSD_PARTS", "2")
+    monkeypatch.setenv("SSM_LOOKBACK_SELFTEST", "1")
+    monkeypatch.setenv("SSM_LOOKBACK_MAX_POLLS", "64")
+    _, _, ws = _ssd_call(dev)
+    assert ssm.ssm_get_status(ws) == ssm.SSM_ERR_LOOKBACK_TIMEOUT
+    monkeypatch.delenv("SSM_LOOKBACK_SELFTEST")
+    monkeypatch.delenv("SSM_LOOKBACK_MAX_POLLS")
+    _, _, ws = _ssd_call(dev, ws)
+    assert ssm.ssm_get_status(ws) == 0
+
+
 @pytest.mark.parametrize("kernel", ["mma", "tc"])
 def test_ssd_status_word_reports_ok(kernel, monkeypatch):
     """Every chunked SSD call writes its status word at the start of the workspace (the waits
