@@ -230,8 +230,11 @@ SSM_API ssm_status_t ssm_state_update_conv(float* state, float* conv_state, cons
  * Fusion + Recomputation"): the pass keeps one state per 8 steps and per channel in the
  * workspace (ssm_scan_bwd_workspace_size bytes: a status word and the look-back records of
  * the forward recompute, as for ssm_scan_fwd, then about batch * L * d_inner * d_state / 2
- * bytes of states and the per-chunk summaries of the reverse pass; not initialised by the
- * caller).  The forward recompute waits on its time chunks like ssm_scan_fwd, boundedly;
+ * bytes of states, the per-chunk summaries (or handed-over carries) of the reverse pass and
+ * one 8-byte tag per (batch, chunk, 64 channels); not initialised by the caller: every record
+ * carries a per-call tag).  The forward recompute waits on its time chunks like ssm_scan_fwd,
+ * and when the gradient CTAs run as a chain of time chunks (each handing its adjoint carry to
+ * the chunk before it) each waits for the one after it; all waits are bounded, and
  * ssm_get_status(workspace, stream) reports a wait that ran out.  dB and dC are
  * accumulated with atomic additions, so their last bits may vary from run to run.
  */

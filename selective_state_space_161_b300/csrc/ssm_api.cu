@@ -379,6 +379,9 @@ ssm_status_t ssm_scan_bwd(const void* u, const void* delta, const float* A, cons
   a.ckpt_h = ws;
   a.rws_S = ws + ck;
   a.rws_m = ws + ck + rws;
+  a.handover = bplan.handover;
+  a.hflags = reinterpret_cast<unsigned long long*>(ws + ck + rws * (d_state + 1));
+  a.header = reinterpret_cast<unsigned long long*>(workspace);
 
   ssm::FwdLaunch f{};
   f.u = u; f.delta = delta; f.A = A; f.B = B; f.C = C; f.delta_bias = delta_bias;
@@ -389,6 +392,9 @@ ssm_status_t ssm_scan_bwd(const void* u, const void* delta, const float* A, cons
   f.tag = next_call_tag();
   f.wait_tag = lookback_selftest() ? (f.tag ^ 1ull) : f.tag;
   f.max_polls = lookback_max_polls();
+  a.tag = f.tag;
+  a.wait_tag = f.wait_tag;
+  a.max_polls = f.max_polls;
   return ssm::launch_scan_bwd(a, f, bf16, s) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 

@@ -57,7 +57,12 @@ struct BwdArgs {
   int64_t chunk_len;
   int n_chunks;
   float* rws_S;        // reverse chunk summaries [batch][n_chunks][d_inner] (+ [.][d_state])
-  float* rws_m;
+  float* rws_m;        // (hand-over plans: the carry each chunk hands to the one before it)
+  int handover;        // 1: chunks run as a chain from the last back to the first, no summaries
+  unsigned long long* hflags;  // [batch][n_chunks][64-channel tiles] hand-over tags
+  unsigned long long* header;  // workspace status word (a hand-over wait that runs out: code 7)
+  unsigned long long tag, wait_tag;
+  unsigned max_polls;
   float* ckpt_h;       // [batch][ceil(L / kCkptSteps)][d_inner][d_state]: state before every kCkptSteps steps
 };
 
@@ -160,6 +165,7 @@ int fwd_channels_per_cta();
 struct BwdPlan {
   int64_t chunk_len;
   int n_chunks;
+  int handover;  // chunks as a chain handing the adjoint carry back (no reverse summaries)
 };
 void plan_scan_bwd(int64_t batch, int64_t L, int64_t d_inner, int sms, BwdPlan* plan);
 // Floats of scratch the backward's checkpoints and reverse summaries take for n_chunks chunks

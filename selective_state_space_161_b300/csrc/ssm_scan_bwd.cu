@@ -174,6 +174,14 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool va
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem), "r"(n));
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* q) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(q) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u64(unsigned long long* q, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(q), "l"(v) : "memory");
+}
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::); }
 
 template <typename T> struct PairIO;
@@ -244,8 +252,11 @@ __global__ void __launch_bounds__(32 * L, L == 4 ? 3 : (L == 2 ? 6 : 12)) grad_k
   int64_t blk = blockIdx.x;
   const int64_t dtile = blk % n_dt;
   blk /= n_dt;
-  const int c = (int)(blk % p.n_chunks);
-  const int64_t b = blk / p.n_chunks;
+  // hand-over plans number the CTAs from the last chunk back, so that the CTA a chunk waits
+  // for (the chunk after it) was dispatched before it
+  const int c = p.handover ? p.n_chunks - 1 - (int)(blk / p.batch) : (int)(blk % p.n_chunks);
+  const int64_t b = p.handover ? blk % p.batch : blk / p.n_chunks;
+  const bool wait_carry = p.handover && c + 1 < p.n_chunks;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int l = lane % L;
   const int P = warp * (32 / L) + lane / L;
@@ -282,11 +293,11 @@ __global__ void __launch_bounds__(32 * L, L == 4 ? 3 : (L == 2 ? 6 : 12)) grad_k
     if (!active) continue;
     // adjoint carry entering the chunk: dL/dlast_state folded with the reverse summaries of
     // the chunks after it
-    if (p.dlast) {
+    if (p.dlast && !wait_carry) {
       const float* dl = p.dlast + (b * Dn + d + cc) * N;
       m[s] = make_float2(n < N ? dl[n] : 0.f, n + 1 < N ? dl[n + 1] : 0.f);
     }
-    for (int jc = p.n_chunks - 1; jc > c; jc--) {
+    for (int jc = p.n_chunks - 1; jc > c && !p.handover; jc--) {
       const int64_t slot = (b * p.n_chunks + jc) * Dn + d + cc;
       const float S = p.rws_S[slot];
       const float* ms = p.rws_m + slot * N;
@@ -561,6 +572,34 @@ __global__ void __launch_bounds__(32 * L, L == 4 ? 3 : (L == 2 ? 6 : 12)) grad_k
     store_bc();
     load_ckpt(tl_hi, h0);
   }
+  if (wait_carry) {
+    // hand-over plans: the carry entering this chunk from the right is the one the next chunk
+    // left at its first step; wait for its tag (bounded: a wait that runs out records code 7
+    // in the status word and the walk goes on from what is there), then read it
+    if (tid == 0) {
+      const unsigned long long* f = p.hflags + ((b * p.n_chunks + c + 1) * n_dt + dtile);
+      bool ok = false;
+      unsigned ns = 32;
+      for (unsigned it = 0; it < p.max_polls; it++) {
+        if (ld_acquire_u64(f) == p.wait_tag) {
+          ok = true;
+          break;
+        }
+        __nanosleep(ns);
+        ns = ns < 1024 ? 2 * ns : 1024;
+      }
+      if (!ok && p.header != nullptr) atomicMax(p.header, (p.tag << 8) | 7ull);
+    }
+    __syncthreads();
+    if (active) {
+#pragma unroll
+      for (int s = 0; s < 4; s++) {
+        const int cc = s / 2, n = n0 + 2 * (s % 2);
+        const float* hm = p.rws_m + ((b * p.n_chunks + c + 1) * Dn + d + cc) * N;
+        m[s] = make_float2(n < N ? __ldcg(hm + n) : 0.f, n + 1 < N ? __ldcg(hm + n + 1) : 0.f);
+      }
+    }
+  }
   for (int64_t tl = tl_hi; tl >= tl_lo; tl--) {
     const int64_t ts = tl * kT;
     const int steps = (int)min((int64_t)kT, t1 - ts);
@@ -696,6 +735,23 @@ __global__ void __launch_bounds__(32 * L, L == 4 ? 3 : (L == 2 ? 6 : 12)) grad_k
     dbacc.x += __shfl_xor_sync(0xFFFFFFFFu, dbacc.x, o);
     dbacc.y += __shfl_xor_sync(0xFFFFFFFFu, dbacc.y, o);
   }
+  if (p.handover && c > 0) {
+    // hand the carry before this chunk's first step to the chunk before it
+    if (active) {
+#pragma unroll
+      for (int s = 0; s < 4; s++) {
+        const int cc = s / 2, n = n0 + 2 * (s % 2);
+        float* hm = p.rws_m + ((b * p.n_chunks + c) * Dn + d + cc) * N;
+        if (n < N) __stcg(hm + n, m[s].x);
+        if (n + 1 < N) __stcg(hm + n + 1, m[s].y);
+      }
+    }
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();
+      st_release_u64(p.hflags + ((b * p.n_chunks + c) * n_dt + dtile), p.tag);
+    }
+  }
   if (!active) return;
   if (l == 0) {
     if (p.dD) { atomicAdd(p.dD + d, dDacc.x); atomicAdd(p.dD + d + 1, dDacc.y); }
@@ -744,6 +800,7 @@ static int64_t env_int(const char* name, int64_t fallback) {
 }
 
 void plan_scan_bwd(int64_t batch, int64_t L, int64_t d_inner, int sms, BwdPlan* plan) {
+  plan->handover = 0;
   // Time chunks of the gradient kernel: none when its CTAs (64 channels each, about three
   // resident per SM) fill the GPU; otherwise about two waves of them, at least 64 steps per
   // chunk (measured on B300: the 2 x 2048 x 1536 shape at 0.30 ms with 16 chunks against 0.35
@@ -753,7 +810,15 @@ void plan_scan_bwd(int64_t batch, int64_t L, int64_t d_inner, int sms, BwdPlan* 
   const int64_t slots = (int64_t)sms * 3;
   int64_t G = 1;
   if (per_chunk > 0 && per_chunk < slots) G = (2 * slots + per_chunk - 1) / per_chunk;
+  // More CTAs than one wave, but not whole waves: two chunks run as a chain (the second half
+  // of the sequence first, handing its adjoint carry to the first half), which needs no
+  // reverse summaries and lets the halves fill the SMs the partial wave would leave idle.
+  if (G == 1 && per_chunk > slots && per_chunk % slots != 0 && L >= 128) {
+    G = 2;
+    plan->handover = 1;
+  }
   G = env_int("SSM_BWD_CHUNKS", G);  // tuning override
+  if (const char* v = std::getenv("SSM_BWD_HANDOVER")) plan->handover = std::atoi(v) == 1;
   G = std::min<int64_t>(G, std::max<int64_t>(1, L / 64));
   G = std::min<int64_t>(G, 4096);
   int64_t len = L > 0 ? (L + G - 1) / G : 1;
@@ -766,7 +831,8 @@ size_t bwd_workspace_floats(int64_t batch, int64_t L, int64_t d_inner, int d_sta
   const int64_t tiles = (L + kCkptSteps - 1) / kCkptSteps;
   const int64_t ck = batch * tiles * d_inner * d_state;                 // forward checkpoints
   const int64_t rws = batch * (int64_t)n_chunks * d_inner * (d_state + 1);  // reverse summaries
-  return (size_t)(ck + rws);
+  const int64_t flags = 2 * batch * (int64_t)n_chunks * ((d_inner + bwd::kCh - 1) / bwd::kCh);  // u64 tags
+  return (size_t)(ck + rws + flags);
 }
 
 template <int L, typename T>
@@ -781,7 +847,7 @@ static cudaError_t launch_grad(const BwdArgs& a, cudaStream_t s) {
 
 template <int N, typename T>
 static cudaError_t launch_bwd_t(const BwdArgs& a, const FwdLaunch& ckpt, cudaStream_t s) {
-  if (a.n_chunks > 1) {  // reverse chunk summaries
+  if (a.n_chunks > 1 && !a.handover) {  // reverse chunk summaries
     const int64_t n_dtiles = (a.d_inner + kBwdCh - 1) / kBwdCh;
     bwd_reverse_summary_kernel<N, T><<<(unsigned)(n_dtiles * (a.n_chunks - 1) * a.batch), kBwdCh, 0, s>>>(a);
     const cudaError_t e = cudaGetLastError();

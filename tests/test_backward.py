@@ -70,6 +70,17 @@ def test_backward_single_step():
     _run(2, 1, 16, 4, False, seed=19, with_h0=True)
 
 
+@pytest.mark.parametrize("chunks", ["2", "5"])
+@pytest.mark.parametrize("bf16", [False, True])
+def test_backward_handover_chain(chunks, bf16, monkeypatch):
+    """Time chunks run as a chain from the last back to the first, each handing its adjoint carry
+    to the chunk before it (the plan the 2.8B shape takes), ragged, with an incoming dL/dlast
+    and an initial state."""
+    monkeypatch.setenv("SSM_BWD_CHUNKS", chunks)
+    monkeypatch.setenv("SSM_BWD_HANDOVER", "1")
+    _run(2, 1500, 96, 16, bf16, seed=23 + int(chunks), with_h0=True, with_dlast=True)
+
+
 @pytest.mark.parametrize("key", ["mamba130m", "mamba2p8b"])
 def test_backward_full_size_sampled(key):
     """The bench's backward at full size (inputs and dy ~ N(0, 1) filled on the device, the
