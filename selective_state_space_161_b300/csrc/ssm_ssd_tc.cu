@@ -310,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
     __syncthreads();  // this chunk's B, C, x and decays, and the carried state, are in shared memory
     tc_after_sync();
 
-    // ---- round 1: G = C B^T (into Yd's columns) and Yo = C H^T, which need nothing computed
+    // ---- first MMA group: G = C B^T (into Yd's columns) and Yo = C H^T, which need nothing computed
     if (tid == 0) {
       // G: M = 64 (t), N = 64 (s), K = N (n); A = C K-major, B = the B tile read K-major
       // (its rows s hold 8 consecutive states per 16 bytes: 128 bytes between state groups,
@@ -329,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
       asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                    ::"r"(smem_u32(bar)) : "memory");
     }
-    // ---- w x as hi / lo, in x's layout (MN-major [t][p]), while round 1 runs
+    // ---- w x as hi / lo, in x's layout (MN-major [t][p]), while the first MMA group runs
 #pragma unroll
     for (int i = 0; i < kQ * kP / 8 / kThreads; i++) {
       const int q = tid + i * kThreads;
@@ -381,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
     __syncthreads();  // M and w x are in shared memory; G has been read
     tc_after_sync();
 
-    // ---- round 2: Yd = M x (over G's columns) and S = (w x)^T B
+    // ---- second MMA group: Yd = M x (over G's columns) and S = (w x)^T B
     if (tid == 0) {
       // Yd: M = 64 (t), N = 64 (p), K = 64 (s); A = M K-major, B = x MN-major
 #pragma unroll
