@@ -14,6 +14,7 @@
 #include "ssm_internal.h"
 
 #include <algorithm>
+#include <cstdlib>
 
 namespace ssm {
 
@@ -67,6 +68,12 @@ template <int N, typename T, int LPC, bool kConv>
 __global__ void __launch_bounds__(kDecodeThreads) state_update_kernel(const DecodeParams p) {
   constexpr int SPL = N / LPC;
   constexpr int kChPerCta = kDecodeThreads / LPC;
+  // Launched as a programmatic dependent of the previous kernel in the stream: let the next
+  // step's launch begin now (its CTAs take the SMs this grid's last CTAs leave), and wait until
+  // the previous kernel has finished and its writes are visible before reading anything.
+  // Without the launch attribute both are no-ops.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t d = (int64_t)blockIdx.x * kChPerCta + threadIdx.x / LPC;
   const int q = (int)(threadIdx.x % LPC);
   const bool valid = d < p.d_inner;
@@ -166,6 +173,12 @@ __global__ void __launch_bounds__(kDecodeThreads) state_update_kernel(const Deco
   }
 }
 
+// Programmatic dependent launch of the decode steps (SSM_DECODE_PDL=0 turns it off).
+static bool decode_pdl() {
+  const char* v = std::getenv("SSM_DECODE_PDL");
+  return v == nullptr || std::atoi(v) != 0;
+}
+
 template <int N, typename T>
 static cudaError_t launch_t(const DecodeParams& p, cudaStream_t s) {
   // Lanes per channel: a power of two (the shuffles pair lanes by xor) with 8 states
@@ -175,11 +188,18 @@ static cudaError_t launch_t(const DecodeParams& p, cudaStream_t s) {
   constexpr int kChPerCta = kDecodeThreads / LPC;
   const dim3 grid((unsigned)((p.d_inner + kChPerCta - 1) / kChPerCta),
                   (unsigned)std::min<int64_t>((p.batch + 1) / 2, 65535));
-  if (p.conv_w != nullptr)
-    state_update_kernel<N, T, LPC, true><<<grid, kDecodeThreads, 0, s>>>(p);
-  else
-    state_update_kernel<N, T, LPC, false><<<grid, kDecodeThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kDecodeThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = decode_pdl() ? 1 : 0;
+  return p.conv_w != nullptr ? cudaLaunchKernelEx(&cfg, state_update_kernel<N, T, LPC, true>, p)
+                             : cudaLaunchKernelEx(&cfg, state_update_kernel<N, T, LPC, false>, p);
 }
 
 template <typename T>
