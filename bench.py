@@ -371,9 +371,8 @@ class BackwardStep:
         io = ssm.SSM_BF16 if w.bf16 else ssm.SSM_F32
         nbytes = ssm.ssm_scan_bwd_workspace_size(w.batch, w.L, w.d_inner, N, io)
         self.ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
-        nf = ssm.ssm_scan_fwd_workspace_size(w.batch, w.L, w.d_inner, N, io)
-        # forward and reverse chunk summaries when chunked, checkpoints, gradients
-        self.launches = 4 if nf else 2
+        # the forward recompute, the gradients, and the reverse summaries if the plan needs them
+        self.launches = ssm.ssm_scan_bwd_launches(w.batch, w.L, w.d_inner, N, io)
 
     def __call__(self, stream=None):
         d, g = self.dev, self.g

@@ -240,6 +240,12 @@ SSM_API ssm_status_t ssm_state_update_conv(float* state, float* conv_state, cons
  */
 SSM_API size_t ssm_scan_bwd_workspace_size(int64_t batch, int64_t L, int64_t d_inner,
                                            int d_state, ssm_dtype_t io);
+/* Kernels one ssm_scan_bwd call launches for these sizes on the current device: the forward
+ * recompute and the gradient kernel, plus the reverse-summary kernel when the plan joins its
+ * time chunks by summaries (2 or 3; the zeroing of the accumulated outputs is done by
+ * cudaMemsetAsync and not counted).  0 for invalid arguments, an empty problem or no device. */
+SSM_API int ssm_scan_bwd_launches(int64_t batch, int64_t L, int64_t d_inner, int d_state,
+                                  ssm_dtype_t io);
 SSM_API ssm_status_t ssm_scan_bwd(const void* u, const void* delta, const float* A, const void* B,
                                   const void* C, const float* D, const void* z,
                                   const float* delta_bias, int softplus_flag,

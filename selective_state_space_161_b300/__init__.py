@@ -21,7 +21,7 @@ from .build import LIB_PATH, build
 
 __all__ = ["SsmError", "ssm_scan_fwd", "ssm_scan_fwd_from_state", "ssm_scan_fwd_conv",
            "ssm_scan_fwd_noalloc", "ssm_state_update", "ssm_state_update_conv", "ssm_scan_bwd",
-           "ssm_scan_bwd_workspace_size", "selective_scan_backward", "ssm_ssd_fwd",
+           "ssm_scan_bwd_workspace_size", "ssm_scan_bwd_launches", "selective_scan_backward", "ssm_ssd_fwd",
            "ssm_ssd_fwd_workspace_size", "selective_scan_ssd",
            "ssm_scan_fwd_workspace_size", "ssm_get_status",
            "ssm_status_string", "ssm_version", "selective_scan", "selective_state_update",
@@ -31,6 +31,7 @@ SSM_F32, SSM_BF16 = 0, 1
 EXPORTED_SYMBOLS = ("ssm_scan_fwd_workspace_size", "ssm_scan_fwd", "ssm_scan_fwd_from_state",
                     "ssm_scan_fwd_conv", "ssm_scan_fwd_noalloc", "ssm_state_update",
                     "ssm_state_update_conv", "ssm_scan_bwd", "ssm_scan_bwd_workspace_size",
+                    "ssm_scan_bwd_launches",
                     "ssm_ssd_fwd", "ssm_ssd_fwd_workspace_size", "ssm_get_status",
                     "ssm_status_string", "ssm_version")
 SSM_ERR_LOOKBACK_TIMEOUT, SSM_ERR_SCRATCH_LIMIT = 7, 8
@@ -71,6 +72,8 @@ def load_library() -> ctypes.CDLL:
         lib.ssm_state_update_conv.restype = c_int
         lib.ssm_scan_bwd_workspace_size.argtypes = [i64, i64, i64, c_int, c_int]
         lib.ssm_scan_bwd_workspace_size.restype = ctypes.c_size_t
+        lib.ssm_scan_bwd_launches.argtypes = [i64, i64, i64, c_int, c_int]
+        lib.ssm_scan_bwd_launches.restype = c_int
         lib.ssm_scan_bwd.argtypes = [vp] * 8 + [c_int] + [vp] * 12 + [i64, i64, i64, c_int, c_int, vp,
                                                                    ctypes.c_size_t, vp]
         lib.ssm_scan_bwd.restype = c_int
@@ -238,6 +241,10 @@ def ssm_scan_fwd_noalloc(u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, 
 
 def ssm_scan_bwd_workspace_size(batch: int, L: int, d_inner: int, d_state: int, io: int) -> int:
     return int(load_library().ssm_scan_bwd_workspace_size(batch, L, d_inner, d_state, io))
+
+
+def ssm_scan_bwd_launches(batch: int, L: int, d_inner: int, d_state: int, io: int) -> int:
+    return int(load_library().ssm_scan_bwd_launches(batch, L, d_inner, d_state, io))
 
 
 def ssm_scan_bwd(u, delta, A, B, C, D, z, delta_bias, softplus_flag, initial_state, dy,

@@ -310,6 +310,18 @@ size_t ssm_scan_bwd_workspace_size(int64_t batch, int64_t L, int64_t d_inner, in
   return bytes;
 }
 
+int ssm_scan_bwd_launches(int64_t batch, int64_t L, int64_t d_inner, int d_state, ssm_dtype_t io) {
+  if (check_common(batch, L, d_inner, d_state, io) != SSM_OK) return 0;
+  const int sms = current_sm_count();
+  if (sms <= 0 || batch * d_inner * L == 0) return 0;
+  ssm::FwdPlan fplan;
+  ssm::BwdPlan bplan;
+  size_t fwd_bytes = 0, bytes = 0;
+  if (!bwd_workspace(batch, L, d_inner, d_state, io == SSM_BF16, sms, &fplan, &bplan, &fwd_bytes, &bytes))
+    return 0;
+  return 2 + ((bplan.n_chunks > 1 && !bplan.handover) ? 1 : 0);
+}
+
 ssm_status_t ssm_scan_bwd(const void* u, const void* delta, const float* A, const void* B,
                           const void* C, const float* D, const void* z, const float* delta_bias,
                           int softplus_flag, const float* initial_state, const void* dy,

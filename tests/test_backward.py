@@ -117,3 +117,15 @@ def test_backward_full_size_sampled(key):
     record_margin(f"backward {w.key} (full size, sampled)", tol, **errs)
     bad = {k: e for k, e in errs.items() if e > tol}
     assert not bad, f"gradient errors above {tol}: {bad} (all: {errs})"
+
+
+def test_backward_launch_count():
+    """ssm_scan_bwd_launches: forward recompute + gradients, plus the reverse summaries when the
+    plan joins its chunks by summaries (the 130M shape) rather than a hand-over chain or not at
+    all (the 2.8B shape on a 148-SM B300)."""
+    big = ssm.ssm_scan_bwd_launches(8, 2048, 5120, 16, ssm.SSM_BF16)
+    small = ssm.ssm_scan_bwd_launches(2, 2048, 1536, 16, ssm.SSM_F32)
+    assert big in (2, 3) and small in (2, 3)
+    if torch.cuda.get_device_properties(0).multi_processor_count == 148:
+        assert (big, small) == (2, 3)
+    assert ssm.ssm_scan_bwd_launches(2, 0, 1536, 16, ssm.SSM_F32) == 0
