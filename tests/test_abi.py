@@ -57,6 +57,53 @@ def test_host_validation_before_any_device_call():
     assert lib.ssm_state_update(*([None] * 10), 1, 2, 8, 0, 0, None) == 2
 
 
+def _ssd_rc(**kw):
+    lib = ssm.load_library()
+    args = dict(x=None, dt=None, A=None, B=None, C=None, D=None, z=None, bias=None, sp=1, y=None,
+                last=None, batch=1, L=64, d_inner=128, heads=2, d_state=64, io=1, ws=None, ws_bytes=0,
+                stream=None)
+    args.update(kw)
+    return lib.ssm_ssd_fwd(*args.values())
+
+
+def test_ssd_host_validation_before_any_device_call():
+    assert _ssd_rc(io=0) == 3                      # bf16 only
+    assert _ssd_rc(d_state=48) == 2                # d_state in {16, 32, 64, 128}
+    assert _ssd_rc(d_state=256) == 2
+    assert _ssd_rc(d_inner=192) == 2               # head dimension 64: d_inner == 64 * heads
+    assert _ssd_rc(heads=0) == 2
+    assert _ssd_rc(L=-1) == 2
+    assert _ssd_rc(batch=0) == 0                   # empty problem
+    assert _ssd_rc() == 1                          # A missing
+    assert ssm.ssm_ssd_fwd_workspace_size(2, 64, 128, 2, 64) == (
+        256 + 2 * 1 * 64 * 64 * 4 + 256 + 2 * 128 * 64 * 4)  # status, Gram, flags, hand-over
+
+
+def _bwd_rc(**kw):
+    lib = ssm.load_library()
+    args = dict(u=None, delta=None, A=None, B=None, C=None, D=None, z=None, bias=None, sp=1, h0=None,
+                dy=None, dlast=None, du=None, ddelta=None, dA=None, dB=None, dC=None, dD=None, dz=None,
+                dbias=None, dinit=None, batch=1, L=8, d_inner=8, d_state=4, io=0, ws=None, ws_bytes=0,
+                stream=None)
+    args.update(kw)
+    return lib.ssm_scan_bwd(*args.values())
+
+
+def test_backward_host_validation_before_any_device_call():
+    assert _bwd_rc(io=5) == 3
+    assert _bwd_rc(d_state=17) == 2
+    assert _bwd_rc(d_inner=6) == 2
+    assert _bwd_rc(batch=0) == 0
+    assert _bwd_rc() == 1                          # A and dA missing
+    # D given without dD (and z without dz): every gradient of a given operand must be asked for
+    import ctypes
+    one = ctypes.c_void_p(16)
+    assert _bwd_rc(A=one, dA=one, u=one, delta=one, B=one, C=one, dy=one, du=one, ddelta=one, dB=one,
+                   dC=one, D=one) == 1
+    assert _bwd_rc(A=one, dA=one, u=one, delta=one, B=one, C=one, dy=one, du=one, ddelta=one, dB=one,
+                   dC=one, z=one) == 1
+
+
 def test_product_path_does_not_import_oracle():
     """The package never imports, links or loads the oracle (test infrastructure)."""
     src_dir = os.path.join(ROOT, "selective_state_space_161_b300")
