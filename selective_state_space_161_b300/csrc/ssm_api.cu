@@ -61,6 +61,10 @@ bool lookback_selftest() {
   return v != nullptr && v[0] == '1';
 }
 
+// The tag a call's waits accept: its own, or in the self-test one with bit 54 set, which no
+// call ever writes (tags are 54-bit), whatever an earlier call left in a reused workspace.
+uint64_t wait_tag_for(uint64_t tag) { return lookback_selftest() ? (tag | (1ull << 54)) : tag; }
+
 bool aligned16(const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 ssm_status_t check_common(int64_t batch, int64_t L, int64_t d_inner, int d_state, ssm_dtype_t io) {
@@ -169,7 +173,7 @@ ssm_status_t scan_fwd_impl(const void* u, const void* delta, const float* A, con
   f.plan = plan;
   f.workspace = workspace;
   f.tag = next_call_tag();
-  f.wait_tag = lookback_selftest() ? (f.tag ^ 1ull) : f.tag;
+  f.wait_tag = wait_tag_for(f.tag);
   f.max_polls = lookback_max_polls();
   return ssm::launch_scan_fwd(f, bf16, s) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
@@ -402,7 +406,7 @@ ssm_status_t ssm_scan_bwd(const void* u, const void* delta, const float* A, cons
   f.plan = fplan;
   f.workspace = workspace;
   f.tag = next_call_tag();
-  f.wait_tag = lookback_selftest() ? (f.tag ^ 1ull) : f.tag;
+  f.wait_tag = wait_tag_for(f.tag);
   f.max_polls = lookback_max_polls();
   a.tag = f.tag;
   a.wait_tag = f.wait_tag;
@@ -460,7 +464,7 @@ ssm_status_t ssm_ssd_fwd(const void* x, const void* dt, const float* A, const vo
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   p.header = reinterpret_cast<unsigned long long*>(ws);
   p.tag = next_call_tag();
-  p.wait_tag = lookback_selftest() ? (p.tag ^ 1ull) : p.tag;
+  p.wait_tag = wait_tag_for(p.tag);
   p.max_polls = lookback_max_polls();
   p.G = reinterpret_cast<float*>(ws + ssm::kFwdHeaderBytes);
   p.flags = reinterpret_cast<unsigned long long*>(ws + ssm::ssd_flags_offset(batch, L));

@@ -533,7 +533,7 @@ size_t ssd_workspace_bytes(int64_t batch, int64_t L, int64_t d_inner, int N) {
 
 cudaError_t launch_ssd(const SsdParams& p, cudaStream_t s) {
   // SSM_SSD_KERNEL=tc: the per-head chain with every product on tcgen05 (ssm_ssd_tc.cu; measured
-  // slower on B300, 0.71 ms against 0.44 ms at the 8 x 2048 x 5120 x 128 shape)
+  // slower on B300, 0.57 ms against 0.44 ms at the 8 x 2048 x 5120 x 128 shape)
   const char* k = std::getenv("SSM_SSD_KERNEL");
   if (k != nullptr && std::strcmp(k, "tc") == 0) return launch_ssd_tc(p, s);
   // the chunk Gram matrices of every batch row first (tensor-core kernel), then the heads

@@ -24,6 +24,7 @@
 #include "ssm_internal.h"
 
 #include <algorithm>
+#include <cstdlib>
 
 namespace ssm {
 namespace ssdtc {
@@ -168,8 +169,21 @@ __device__ __forceinline__ void chunk_decays(const SsdParams& p, int h, int64_t 
   sW[2 * lane + 1] = d1 * ex2(s_last - run);
 }
 
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* q) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(q) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u64(unsigned long long* q, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(q), "l"(v) : "memory");
+}
+
+constexpr int kIssuer = 128;  // thread that issues the MMAs: lane 0 of warp 4 (warp 0 computes decays)
+
+// part_len: steps per time part of a chain (a multiple of kQ; >= p.L for one part).  Part k of a
+// chain starts from the state part k - 1 hands over through the workspace, as in ssm_ssd.cu.
 template <int N>
-__global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) {
+__global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p, int64_t part_len) {
   using SM = Smem<N>;
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char* sC = smem + SM::kC;
@@ -190,8 +204,13 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
   uint32_t* taddr = reinterpret_cast<uint32_t*>(smem + SM::kBar + 8);
   __nv_bfloat16* sY = reinterpret_cast<__nv_bfloat16*>(sMh);  // output staging [kQ][kStageRow]
 
-  const int h = blockIdx.x % p.heads;
-  const int64_t b = blockIdx.x / p.heads;
+  const int64_t chains = p.batch * p.heads;
+  const int64_t chain = blockIdx.x % chains;
+  const int part = (int)(blockIdx.x / chains);
+  const int64_t t_begin = (int64_t)part * part_len;
+  const int64_t t_end = min(t_begin + part_len, p.L);
+  const int h = (int)(chain % p.heads);
+  const int64_t b = chain / p.heads;
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int g = lane / 4, tq = lane % 4;
   const int qd = warp % 4, ch = warp / 4;      // lane quadrant, column half
@@ -262,13 +281,45 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
     }
   };
 
-  load_bc(0);
-  load_x(0);
+  load_bc(t_begin);
+  load_x(t_begin);
   cp_async_commit();
   float2 dt_raw = make_float2(0.f, 0.f);
   if (warp == 0) {
-    chunk_decays(p, h, 0, load_dt_pair(p, b, h, 0, lane), lane, sDt, sS, sW);
-    if (kQ < p.L) dt_raw = load_dt_pair(p, b, h, kQ, lane);
+    chunk_decays(p, h, t_begin, load_dt_pair(p, b, h, t_begin, lane), lane, sDt, sS, sW);
+    if (t_begin + kQ < t_end) dt_raw = load_dt_pair(p, b, h, t_begin + kQ, lane);
+  }
+  bool ok = true;
+  if (part > 0) {
+    // the state at t_begin from the part before (bounded wait; a wait that runs out records
+    // code 7 and the walk goes on from what is there)
+    if (tid == 0) {
+      bool got = false;
+      unsigned ns = 32;
+      const unsigned long long want = (p.wait_tag << 8) | (unsigned long long)part;
+      for (unsigned it = 0; it < p.max_polls; it++) {
+        if (ld_acquire_u64(p.flags + chain) == want) {
+          got = true;
+          break;
+        }
+        __nanosleep(ns);
+        ns = ns < 1024 ? 2 * ns : 1024;
+      }
+      if (!got) atomicMax(p.header, (p.tag << 8) | (unsigned long long)kLookbackTimeoutCode);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int half = 0; half < 2; half++) {
+      const int r = half ? rB : rA;
+      const float* in = p.hand + (b * p.d_inner + (int64_t)h * kP + r) * N + n0;
+#pragma unroll
+      for (int j = 0; j < kHJ; j++) {
+        const float2 v = __ldcg(reinterpret_cast<const float2*>(in + 8 * j + 2 * tq));
+        H[j][2 * half] = v.x;
+        H[j][2 * half + 1] = v.y;
+      }
+    }
+    store_state();
   }
   tc_before_sync();
   __syncthreads();
@@ -285,8 +336,7 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
 
   uint32_t phase = 0;
   int par = 0;
-  bool ok = true;
-  for (int64_t t0 = 0; t0 < p.L; t0 += kQ, par ^= 1) {
+  for (int64_t t0 = t_begin; t0 < t_end; t0 += kQ, par ^= 1) {
     const int rows = (int)min((int64_t)kQ, p.L - t0);
     const float* cDt = sDt + par * kQ;
     const float* cS = sS + par * kQ;
@@ -311,20 +361,23 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
     tc_after_sync();
 
     // ---- first MMA group: G = C B^T (into Yd's columns) and Yo = C H^T, which need nothing computed
-    if (tid == 0) {
+    if (tid == kIssuer) {
+      // descriptors of the tiles' first K block; a K step advances the address field (bytes / 16)
+      const uint64_t dC = smem_desc(smem_u32(sC), 1024, 128);
+      const uint64_t dBk = smem_desc(smem_u32(sB), 128, N * 16);
+      const uint64_t dHh = smem_desc(smem_u32(sHh), 1024, 128), dHl = smem_desc(smem_u32(sHl), 1024, 128);
       // G: M = 64 (t), N = 64 (s), K = N (n); A = C K-major, B = the B tile read K-major
       // (its rows s hold 8 consecutive states per 16 bytes: 128 bytes between state groups,
       // N * 16 between row groups)
 #pragma unroll
       for (int kk = 0; kk < N / 16; kk++)
-        mma_f16(tmem + kColYd, smem_desc(smem_u32(sC) + kk * 2048, 1024, 128),
-                smem_desc(smem_u32(sB) + kk * 256, 128, N * 16), kIdYo, kk > 0);
+        mma_f16(tmem + kColYd, dC + kk * (2048 >> 4), dBk + kk * (256 >> 4), kIdYo, kk > 0);
       // Yo: M = 64 (t), N = 64 (p), K = N (n); A = C K-major, B = H K-major
 #pragma unroll
       for (int kk = 0; kk < N / 16; kk++) {
-        const uint64_t da = smem_desc(smem_u32(sC) + kk * 2048, 1024, 128);
-        mma_f16(tmem + kColYo, da, smem_desc(smem_u32(sHh) + kk * 2048, 1024, 128), kIdYo, kk > 0);
-        mma_f16(tmem + kColYo, da, smem_desc(smem_u32(sHl) + kk * 2048, 1024, 128), kIdYo, 1);
+        const uint64_t da = dC + kk * (2048 >> 4);
+        mma_f16(tmem + kColYo, da, dHh + kk * (2048 >> 4), kIdYo, kk > 0);
+        mma_f16(tmem + kColYo, da, dHl + kk * (2048 >> 4), kIdYo, 1);
       }
       asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                    ::"r"(smem_u32(bar)) : "memory");
@@ -382,28 +435,32 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
     tc_after_sync();
 
     // ---- second MMA group: Yd = M x (over G's columns) and S = (w x)^T B
-    if (tid == 0) {
+    if (tid == kIssuer) {
+      const uint64_t dX = smem_desc(smem_u32(sX), 1024, 128);
+      const uint64_t dMh = smem_desc(smem_u32(sMh), 1024, 128), dMl = smem_desc(smem_u32(sMl), 1024, 128);
+      const uint64_t dBm = smem_desc(smem_u32(sB), N * 16, 128);
+      const uint64_t dWh = smem_desc(smem_u32(sWXh), 1024, 128), dWl = smem_desc(smem_u32(sWXl), 1024, 128);
       // Yd: M = 64 (t), N = 64 (p), K = 64 (s); A = M K-major, B = x MN-major
 #pragma unroll
       for (int kk = 0; kk < kQ / 16; kk++) {
-        const uint64_t db = smem_desc(smem_u32(sX) + kk * 2048, 1024, 128);
-        mma_f16(tmem + kColYd, smem_desc(smem_u32(sMh) + kk * 2048, 1024, 128), db, kIdYd, kk > 0);
-        mma_f16(tmem + kColYd, smem_desc(smem_u32(sMl) + kk * 2048, 1024, 128), db, kIdYd, 1);
+        const uint64_t db = dX + kk * (2048 >> 4);
+        mma_f16(tmem + kColYd, dMh + kk * (2048 >> 4), db, kIdYd, kk > 0);
+        mma_f16(tmem + kColYd, dMl + kk * (2048 >> 4), db, kIdYd, 1);
       }
       // S: M = 64 (p), N = N (n), K = 64 (t); A = w x MN-major, B MN-major
 #pragma unroll
       for (int kk = 0; kk < kQ / 16; kk++) {
-        const uint64_t db = smem_desc(smem_u32(sB) + kk * 2 * (N * 16), N * 16, 128);
-        mma_f16(tmem + kColS, smem_desc(smem_u32(sWXh) + kk * 2048, 1024, 128), db, kIdS, kk > 0);
-        mma_f16(tmem + kColS, smem_desc(smem_u32(sWXl) + kk * 2048, 1024, 128), db, kIdS, 1);
+        const uint64_t db = dBm + kk * ((2 * (N * 16)) >> 4);
+        mma_f16(tmem + kColS, dWh + kk * (2048 >> 4), db, kIdS, kk > 0);
+        mma_f16(tmem + kColS, dWl + kk * (2048 >> 4), db, kIdS, 1);
       }
       asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                    ::"r"(smem_u32(bar)) : "memory");
     }
     // the next chunk's decays while the products run
-    if (warp == 0 && t0 + kQ < p.L) {
+    if (warp == 0 && t0 + kQ < t_end) {
       chunk_decays(p, h, t0 + kQ, dt_raw, lane, sDt + (par ^ 1) * kQ, sS + (par ^ 1) * kQ, sW + (par ^ 1) * kQ);
-      if (t0 + 2 * kQ < p.L) dt_raw = load_dt_pair(p, b, h, t0 + 2 * kQ, lane);
+      if (t0 + 2 * kQ < t_end) dt_raw = load_dt_pair(p, b, h, t0 + 2 * kQ, lane);
     }
     ok = __syncthreads_and(mbar_wait(smem_u32(bar), phase)) != 0;  // one decision for the CTA
     phase ^= 1;
@@ -420,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
         xr[half][j] = *reinterpret_cast<const uint32_t*>(sX + (p0 / 8 + j) * 128 + (r / 8) * 1024 + 16 * (r % 8) + 4 * tq);
     }
     __syncthreads();  // every thread has its x pairs
-    if (t0 + kQ < p.L) {
+    if (t0 + kQ < t_end) {
       load_bc(t0 + kQ);
       load_x(t0 + kQ);
     }
@@ -482,7 +539,23 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
   cp_async_wait_all();
   if (!ok && tid == 0) atomicMax(p.header, (p.tag << 8) | (unsigned long long)kLookbackTimeoutCode);
 
-  if (ok && p.last_state) {
+  if (t_end < p.L) {
+    // hand the state over to the next part (also after a wait that ran out: the next part
+    // must not wait in vain; the call's outputs are invalid then anyway)
+#pragma unroll
+    for (int half = 0; half < 2; half++) {
+      const int r = half ? rB : rA;
+      float* out = p.hand + (b * p.d_inner + (int64_t)h * kP + r) * N + n0;
+#pragma unroll
+      for (int j = 0; j < kHJ; j++)
+        __stcg(reinterpret_cast<float2*>(out + 8 * j + 2 * tq), make_float2(H[j][2 * half], H[j][2 * half + 1]));
+    }
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();
+      st_release_u64(p.flags + chain, (p.tag << 8) | (unsigned long long)(part + 1));
+    }
+  } else if (ok && p.last_state) {
 #pragma unroll
     for (int half = 0; half < 2; half++) {
       const int r = half ? rB : rA;
@@ -503,9 +576,25 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
 template <int N>
 cudaError_t launch_n(const SsdParams& p, cudaStream_t s) {
   constexpr int smem = Smem<N>::kAlloc;
-  const cudaError_t e = cudaFuncSetAttribute(ssd_tc_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = cudaFuncSetAttribute(ssd_tc_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  ssd_tc_kernel<N><<<(unsigned)(p.batch * p.heads), kThreads, smem, s>>>(p);
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ssd_tc_kernel<N>, kThreads, smem);
+  if (e != cudaSuccess) return e;
+  // time parts as for the mma.sync chain: two unless the chains spread evenly over the SMs
+  const int64_t chains = p.batch * p.heads;
+  const int64_t n_chunks = (p.L + kQ - 1) / kQ;
+  const int64_t slots = (int64_t)std::max(1, p.sms) * std::max(1, per_sm);
+  const bool even = chains % slots == 0 || (chains <= slots && chains % std::max(1, p.sms) == 0);
+  int parts = even ? 1 : 2;
+  if (const char* v = std::getenv("SSM_SSD_PARTS")) {
+    const int f = std::atoi(v);
+    if (f >= 1 && f <= 64) parts = f;
+  }
+  while (parts > 1 && (int64_t)parts * chains > 0x7FFFFFFF) parts--;
+  const int64_t chunks_per_part = (n_chunks + parts - 1) / parts;
+  parts = (int)((n_chunks + chunks_per_part - 1) / chunks_per_part);
+  ssd_tc_kernel<N><<<(unsigned)(parts * chains), kThreads, smem, s>>>(p, chunks_per_part * kQ);
   return cudaGetLastError();
 }
 

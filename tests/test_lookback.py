@@ -142,5 +142,8 @@ def test_backward_recompute_reports_timeout(monkeypatch):
     assert ssm.ssm_get_status(ws2) == 0
     for k in ("du", "ddelta", "dz"):  # per element: bit for bit
         assert torch.equal(g2[k], g0[k]), k
-    for k in ("dA", "dB", "dC", "dD", "dbias"):  # atomic sums over CTAs: the last bits may vary
-        assert torch.allclose(g2[k], g0[k], rtol=1e-5, atol=1e-6), k
+    for k in ("dA", "dB", "dC", "dD", "dbias"):
+        # atomic sums over 128 time chunks: the order, and with cancellation the last few bits
+        # of a sum relative to its terms, vary from run to run
+        scale = g0[k].abs().max().item()
+        assert torch.allclose(g2[k], g0[k], rtol=1e-5, atol=1e-5 * scale), k

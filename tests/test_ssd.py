@@ -108,10 +108,13 @@ def _ssd_call(dev, ws=None):
     return y, last, ws
 
 
+@pytest.mark.parametrize("kernel", ["mma", "tc"])
 @pytest.mark.parametrize("L,parts", [(130, 2), (200, 2), (200, 3), (2048, 2), (2048, 5), (2048, 32)])
-def test_ssd_time_parts_match_one_walk(L, parts, monkeypatch):
+def test_ssd_time_parts_match_one_walk(L, parts, kernel, monkeypatch):
     """Time parts (each starting from the state the part before hands over) run the same
-    operations in the same order as one walk over all chunks: bit-identical outputs."""
+    operations in the same order as one walk over all chunks: bit-identical outputs, for the
+    mma.sync chain and the tcgen05 chain."""
+    monkeypatch.setenv("SSM_SSD_KERNEL", kernel)
     w = W.Workload("ssd", "ssd case", 2, L, 192, 64, True, 300 + L, 0.5, heads=3)
     dev = W.device_ssd_inputs(w)
     monkeypatch.setenv("SSM_SSD_PARTS", "1")
@@ -123,12 +126,14 @@ def test_ssd_time_parts_match_one_walk(L, parts, monkeypatch):
     assert torch.equal(y1, y2) and torch.equal(l1, l2)
 
 
-def test_ssd_time_part_wait_reports_timeout(monkeypatch):
+@pytest.mark.parametrize("kernel", ["mma", "tc"])
+def test_ssd_time_part_wait_reports_timeout(kernel, monkeypatch):
     """A time part's wait for the state of the part before is bounded: with a tag nobody writes
     and a 64-poll limit it gives up, the call reports SSM_ERR_LOOKBACK_TIMEOUT and the next call
     is clean again.  No GPU fault is involved: the CTAs just finish."""
     w = W.Workload("ssd", "ssd case", 1, 256, 128, 32, True, 71, 0.5, heads=2)
     dev = W.device_ssd_inputs(w)
+    monkeypatch.setenv("SSM_SSD_KERNEL", kernel)
     monkeypatch.setenv("SSM_SSD_PARTS", "2")
     monkeypatch.setenv("SSM_LOOKBACK_SELFTEST", "1")
     monkeypatch.setenv("SSM_LOOKBACK_MAX_POLLS", "64")
