@@ -862,12 +862,16 @@ bool plan_scan_fwd(int64_t batch, int64_t L, int64_t d_inner, int d_state, bool 
   G = std::max<int64_t>(1, std::min<int64_t>(G, 4096));
   int64_t len0 = L, len = L;
   if (G > 1) {
-    // Chunk 0 runs only its main pass.  With three or more chunks it is half the length of
-    // the others, so that its inclusive prefix is out before the others finish their
-    // aggregates (an aggregate step costs about 0.7 of a main step): no chunk waits for it, and
-    // its early finish idles only 1/G of the CTAs.  With two chunks nobody runs an aggregate and
-    // the second chunk waits for the first's end state anyway: equal halves.
-    const double alpha = env_double("SSM_SCAN_ALPHA", G == 2 ? 1.0 : 0.5);
+    // Chunk 0 runs only its main pass.  With three or more chunks it is shorter than the
+    // others, so that its inclusive prefix is out about when the others finish their
+    // aggregates: the others start their main passes then, and the longer chunk 0 the shorter
+    // all chunks.  The best fraction is about the cost of an aggregate step relative to a main
+    // step, which is higher with several lanes per pair (their per-element pre-phase is paid in
+    // both passes): measured on B300, 0.5 for one lane (1 x 1,048,576 x 2048 x 16: 15.25 ms
+    // against 15.41 at 0.7) and 0.8 for four (2 x 2048 x 1536 x 16: 0.0704 ms against 0.0744 at
+    // 0.5).  With two chunks nobody runs an aggregate and the second chunk waits for the
+    // first's end state anyway: equal halves.
+    const double alpha = env_double("SSM_SCAN_ALPHA", G == 2 ? 1.0 : (lanes == 1 ? 0.5 : 0.8));
     len = (int64_t)std::ceil((double)L / ((double)(G - 1) + alpha));
     len = (len + fwd::kT - 1) / fwd::kT * fwd::kT;
     len0 = std::max<int64_t>(fwd::kT, (int64_t)(alpha * (double)len) / fwd::kT * fwd::kT);
