@@ -63,7 +63,6 @@ constexpr int kCh = 64;   // channels per CTA
 constexpr int kCP = 32;   // channel pairs per CTA
 constexpr int kT = 16;    // steps per tile
 static_assert(kT == 2 * kCkptSteps, "two checkpoints per tile");
-constexpr int kOG = 8;    // steps per output group (partial readouts reduced in shared memory)
 constexpr int kModeAgg = 0, kModeMain = 1;
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {
@@ -126,6 +125,9 @@ struct Cfg {
   static constexpr int kXB = 2 * kStageB;
   static constexpr int kBCB = 2 * 2 * kT * kNP * 4;
   static constexpr int kDWB = L > 1 ? kT * kCP * 16 : 0;  // (delta, delta*u) pairs per step (L > 1)
+  // steps per output group (partial readouts reduced in shared memory): 8, or 4 for fp32 I/O
+  // on four lanes, whose larger staging tiles would otherwise allow only 4 CTAs per SM, not 5
+  static constexpr int kOG = (kTS == 4 && L == 4) ? 4 : 8;
   static constexpr int kPB = L > 1 ? kOG * kRS * 4 : 0;    // partial readouts per step group (L > 1)
   static constexpr int kSmem = kXB + kBCB + kDWB + kPB + 16;
   static_assert(S % 4 == 0 && kNP <= 16, "states per lane must be a multiple of 4, at most 16 per pair");
@@ -176,7 +178,7 @@ __global__ void __launch_bounds__(32 * L, L == 1 ? 12 : (L == 2 ? 8 : 5)) scan_f
   unsigned char* sX = smem;                                                  // [2][kStageB]
   float* sBC = reinterpret_cast<float*>(smem + K::kXB);                      // [2][2][kT][kNP]
   float4* sDW = reinterpret_cast<float4*>(smem + K::kXB + K::kBCB);          // [kT][kCP]
-  float* sP = reinterpret_cast<float*>(smem + K::kXB + K::kBCB + K::kDWB);    // [kOG][kRS]
+  float* sP = reinterpret_cast<float*>(smem + K::kXB + K::kBCB + K::kDWB);    // [K::kOG][kRS]
   int* sInfo = reinterpret_cast<int*>(smem + K::kXB + K::kBCB + K::kDWB + K::kPB);
 
   const int64_t Dn = a.d_inner, Ls = a.L;
@@ -520,11 +522,11 @@ __global__ void __launch_bounds__(32 * L, L == 1 ? 12 : (L == 2 ? 8 : 5)) scan_f
         }
         __syncwarp();
 
-        // Output of the steps k0 .. k0+kOG-1: lane l sums the partial readouts of its own steps
+        // Output of the steps k0 .. k0+K::kOG-1: lane l sums the partial readouts of its own steps
         // over the pair's L lanes and applies the skip term and the gate.
         auto output_group = [&](int k0) {
 #pragma unroll
-          for (int i = 0; i < kOG / L; i++) {
+          for (int i = 0; i < K::kOG / L; i++) {
             const int k = k0 + i * L + l;
             if (k < steps && active) {
               const float* pr = sP + (k - k0) * K::kRS + 2 * P;
@@ -550,10 +552,10 @@ __global__ void __launch_bounds__(32 * L, L == 1 ? 12 : (L == 2 ? 8 : 5)) scan_f
               if (k == kCkptSteps - 1 && steps > kCkptSteps) store_ckpt(ts + kCkptSteps);
             }
             if constexpr (kMain) {
-              *reinterpret_cast<float2*>(sP + (k % kOG) * K::kRS + l * K::kLS + 2 * P) = part;
-              if (k % kOG == kOG - 1 || (kGuard && k == steps - 1)) {
+              *reinterpret_cast<float2*>(sP + (k % K::kOG) * K::kRS + l * K::kLS + 2 * P) = part;
+              if (k % K::kOG == K::kOG - 1 || (kGuard && k == steps - 1)) {
                 __syncwarp();
-                output_group(k - k % kOG);
+                output_group(k - k % K::kOG);
                 __syncwarp();
               }
             }
