@@ -84,3 +84,30 @@ def test_decode_workload_full_size_sampled():
                   state=rel_err(st_g, st))
     assert rel_err(y_g, y_ref) <= BF16_TOL
     assert rel_err(st_g, st) <= BF16_TOL
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+def test_decode_more_batch_rows_than_one_grid_column(bf16):
+    """140,001 batch rows: more than the 2 x 65,535 a single pass of the 2-D grid covers (each
+    CTA row serves two batch rows), so the kernel loops over batch rows; the odd count leaves
+    the last pass with a single row.  Every row against the oracle."""
+    batch, d_inner, N = 140001, 8, 4
+    r = np.random.default_rng(140001)
+    rnd = lambda *s: r.standard_normal(s).astype(np.float32)
+    u, delta, z = rnd(batch, d_inner), 0.5 * rnd(batch, d_inner), rnd(batch, d_inner)
+    B, C = rnd(batch, N), rnd(batch, N)
+    state0 = 0.1 * rnd(batch, d_inner, N)
+    A = -np.tile(np.arange(1, N + 1, dtype=np.float32), (d_inner, 1))
+    D, bias = rnd(d_inner), (0.1 * rnd(d_inner)).astype(np.float32)
+    io = lambda a: torch.from_numpy(a).cuda().to(torch.bfloat16 if bf16 else torch.float32)
+    state = torch.from_numpy(state0).cuda()
+    y = ssm.selective_state_update(state, io(u), io(delta), torch.from_numpy(A).cuda(), io(B), io(C),
+                                   D=torch.from_numpy(D).cuda(), z=io(z),
+                                   delta_bias=torch.from_numpy(bias).cuda())
+    torch.cuda.synchronize()
+    q = lambda a: io(a).float().cpu().numpy().astype(np.float64)  # the values the device holds
+    y_ref, st_ref = oracle.state_update(state0, q(u), q(delta), A, q(B), q(C), D=D, z=q(z), delta_bias=bias)
+    tol = BF16_TOL if bf16 else FP32_TOL
+    ey, es = rel_err(to_f64(y), y_ref), rel_err(to_f64(state), st_ref)
+    record_margin(f"decode {batch}x{d_inner}x{N} {'bf16' if bf16 else 'fp32'}, one step", tol, y=ey, state=es)
+    assert ey <= tol and es <= tol, f"y err {ey:.3g}, state err {es:.3g}"
