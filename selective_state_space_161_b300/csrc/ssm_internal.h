@@ -122,6 +122,7 @@ constexpr unsigned kLookbackTimeoutCode = 7;  // SSM_ERR_LOOKBACK_TIMEOUT
 struct FwdPlan {
   int lanes, states_per_lane, threads, G;
   int64_t len0, len;
+  int chain;  // 1: no aggregate passes; each chunk continues from the end state of the one before
 };
 
 struct FwdLaunch {

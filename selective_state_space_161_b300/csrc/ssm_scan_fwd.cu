@@ -154,6 +154,7 @@ struct Args {
   int64_t batch, L, d_inner;
   int N;
   int G;                        // time chunks
+  int chain;                    // 1: no aggregates; every chunk continues from its predecessor's end state
   int64_t len0, len;            // length of chunk 0, of the others (the last may be shorter)
   unsigned long long* header;   // status word: (tag << 8) | error code
   unsigned long long* flags;    // [G-1][batch][channel tiles]: (tag << 2) | 1 aggregate, 2 inclusive
@@ -571,12 +572,15 @@ __global__ void __launch_bounds__(32 * L, L == 1 ? 12 : (L == 2 ? 8 : 5)) scan_f
 
   const bool chunked = a.G > 1;
   const bool last_chunk = c == a.G - 1;
+  // a chain of chunks (the four-lane plain and checkpoint kernels only): no aggregate pass;
+  // every chunk waits for its predecessor's end state, published when its main pass ends
+  const bool chain = !kConv && L == 4 && a.chain != 0;
   float2 S2 = make_float2(0.f, 0.f);  // sum of delta over this chunk (aggregate pass)
   float2 hagg[S];
 #pragma unroll
   for (int s = 0; s < S; s++) hagg[s] = make_float2(0.f, 0.f);
 
-  if (c > 0 && !last_chunk) {
+  if (c > 0 && !last_chunk && !chain) {
     // Aggregate: the chunk from a zero state, published for the chunks after it.
     run(std::integral_constant<int, kModeAgg>{});
     S2 = sub2(Ssum, Scomp);
@@ -682,7 +686,7 @@ __global__ void __launch_bounds__(32 * L, L == 1 ? 12 : (L == 2 ? 8 : 5)) scan_f
         }
       }
     }
-    if (!last_chunk) {
+    if (!last_chunk && !chain) {
       // Inclusive prefix of this chunk: its aggregate applied to the carry.
       float* dst = a.incl + (rec * K::kThreads + tid) * K::kInclF;
 #pragma unroll
@@ -710,7 +714,7 @@ __global__ void __launch_bounds__(32 * L, L == 1 ? 12 : (L == 2 ? 8 : 5)) scan_f
 
   run(std::integral_constant<int, kModeMain>{});
 
-  if (c == 0 && chunked) {
+  if (chain ? (chunked && !last_chunk) : (c == 0 && chunked)) {
     // Chunk 0's inclusive prefix is its true end state.
     float* dst = a.incl + (rec * K::kThreads + tid) * K::kInclF;
 #pragma unroll
@@ -858,10 +862,23 @@ bool plan_scan_fwd(int64_t batch, int64_t L, int64_t d_inner, int d_state, bool 
   // (the second waits for the first's end state), so the work is unchanged, and the halves
   // spread over the SMs as the first ones finish (measured on B300 at 8 x 2048 x 5120 x 16,
   // 640 CTAs in 740 slots: 0.438 ms against 0.476 in one chunk).
-  if (G == 1 && per_chunk > 0 && per_chunk <= slots && per_chunk % sms != 0) G = 2;
+  // The four-lane plain and checkpoint kernels go one step further there: three equal chunks
+  // as a chain, each continuing from its predecessor's end state, with no aggregate pass at
+  // all (0.428 ms against 0.438 for the two-chunk plan, same binary and box); the fused conv
+  // variant keeps two chunks (the chain's branch would push it over its registers).
+  bool chain = false;
+  if (G == 1 && per_chunk > 0 && per_chunk <= slots && per_chunk % sms != 0) {
+    G = 2;
+    if (lanes == 4 && kind != kFwdConv && L >= 3 * 128) {
+      G = 3;
+      chain = true;
+    }
+  }
   G = std::min<int64_t>(G, std::max<int64_t>(1, L / 128));
   G = env_int("SSM_SCAN_CHUNKS", G);
   G = std::max<int64_t>(1, std::min<int64_t>(G, 4096));
+  if (const char* v = std::getenv("SSM_SCAN_CHAIN")) chain = std::atoi(v) == 1;
+  chain = chain && G > 1 && lanes == 4 && kind != kFwdConv;
   int64_t len0 = L, len = L;
   if (G > 1) {
     // Chunk 0 runs only its main pass.  With three or more chunks it is shorter than the
@@ -875,7 +892,7 @@ bool plan_scan_fwd(int64_t batch, int64_t L, int64_t d_inner, int d_state, bool 
     // first's end state anyway; the first chunk's CTAs start at once and the second's fill in as
     // they finish, so a shorter second chunk shortens the tail: 1.5 (8 x 2048 x 5120 x 16:
     // 0.429 ms against 0.439 for equal halves and 0.446 at 3).
-    const double alpha = env_double("SSM_SCAN_ALPHA", G == 2 ? 1.5 : (lanes == 1 ? 0.5 : 0.8));
+    const double alpha = env_double("SSM_SCAN_ALPHA", chain ? 1.0 : G == 2 ? 1.5 : (lanes == 1 ? 0.5 : 0.8));
     len = (int64_t)std::ceil((double)L / ((double)(G - 1) + alpha));
     len = (len + fwd::kT - 1) / fwd::kT * fwd::kT;
     len0 = std::max<int64_t>(fwd::kT, (int64_t)(alpha * (double)len) / fwd::kT * fwd::kT);
@@ -889,6 +906,7 @@ bool plan_scan_fwd(int64_t batch, int64_t L, int64_t d_inner, int d_state, bool 
   plan->lanes = lanes;
   plan->states_per_lane = S;
   plan->G = (int)G;
+  plan->chain = chain && G > 1 ? 1 : 0;
   plan->len0 = len0;
   plan->len = len;
   plan->threads = v.threads;
@@ -919,7 +937,7 @@ cudaError_t launch_scan_fwd(const FwdLaunch& f, bool bf16, cudaStream_t stream) 
   a.initial_state = f.initial_state;
   a.conv_w = f.conv_w; a.conv_b = f.conv_b; a.d_conv = f.d_conv; a.u_out = f.u_out; a.ckpt = f.ckpt;
   a.batch = f.batch; a.L = f.L; a.d_inner = f.d_inner; a.N = f.d_state;
-  a.G = plan.G; a.len0 = plan.len0; a.len = plan.len;
+  a.G = plan.G; a.len0 = plan.len0; a.len = plan.len; a.chain = plan.chain;
   unsigned char* ws = static_cast<unsigned char*>(f.workspace);
   a.header = reinterpret_cast<unsigned long long*>(ws);
   a.flags = reinterpret_cast<unsigned long long*>(ws + kFwdHeaderBytes);

@@ -67,6 +67,25 @@ def test_two_equal_chunks_match_oracle(lanes, monkeypatch):
     assert ey <= FP32_TOL and el <= FP32_TOL, f"y err {ey:.3g}, last_state err {el:.3g}"
 
 
+@pytest.mark.parametrize("chunks", ["3", "5"])
+def test_chunk_chain_matches_oracle(chunks, monkeypatch):
+    """Time chunks as a chain (four lanes per pair): no aggregate passes, every chunk continues
+    from its predecessor's end state; ragged length and channel count."""
+    monkeypatch.setenv("SSM_SCAN_CHUNKS", chunks)
+    monkeypatch.setenv("SSM_SCAN_CHAIN", "1")
+    monkeypatch.setenv("SSM_SCAN_LANES", "4")
+    batch, L, d_inner, d_state, bf16 = 2, 1501, 72, 16, False
+    w, raw, t = _inputs(batch, L, d_inner, d_state, bf16, seed=61 + int(chunks))
+    y, last, ws = _call(t, batch, L, d_inner, d_state, bf16)
+    assert ssm.ssm_get_status(ws) == 0
+    x = {k: v.astype(np.float64) for k, v in raw.items()}
+    y_ref, last_ref = oracle.scan_fwd(x["u"], x["delta"], x["A"], x["B"], x["C"], D=x["D"], z=x["z"],
+                                      delta_bias=x["delta_bias"])
+    ey, el = rel_err(to_f64(y), y_ref), rel_err(to_f64(last), last_ref)
+    record_margin(f"scan 2x1501x72x16 fp32, chain of {chunks} chunks", FP32_TOL, y=ey, last_state=el)
+    assert ey <= FP32_TOL and el <= FP32_TOL, f"y err {ey:.3g}, last_state err {el:.3g}"
+
+
 def test_results_are_deterministic():
     """The carry is folded forward from whichever inclusive prefix the look-back finds, in the
     order the chunks themselves use, so repeated calls agree bit for bit."""
