@@ -105,9 +105,11 @@ SSM_API size_t ssm_scan_fwd_workspace_size(int64_t batch, int64_t L, int64_t d_i
  * publishes its aggregate, then folds its predecessors' aggregates until it finds an
  * inclusive prefix, publishes its own and produces its outputs (the recurrence is
  * associative: "看懂Mamba，Transformer最强竞争者（一）…", section "3. 状态空间"; the parallel scan
- * of "Mamba一作最新大發長文！", section "(3) 訓練效率").  Every wait is bounded; a chunk that gives
- * up records SSM_ERR_LOOKBACK_TIMEOUT for ssm_get_status and finishes (its outputs are then
- * invalid) instead of hanging.
+ * of "Mamba一作最新大發長文！", section "(3) 訓練效率").  When the channels alone fill about
+ * one wave of CTAs but spread unevenly over the SMs, the plan uses two or three chunks with no
+ * aggregate at all, each continuing from its predecessor's end state (a finer division of the
+ * same work).  Every wait is bounded; a chunk that gives up records SSM_ERR_LOOKBACK_TIMEOUT
+ * for ssm_get_status and finishes (its outputs are then invalid) instead of hanging.
  */
 SSM_API ssm_status_t ssm_scan_fwd(const void* u, const void* delta, const float* A, const void* B,
                           const void* C, const float* D, const void* z, const float* delta_bias,
