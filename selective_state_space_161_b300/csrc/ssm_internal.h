@@ -89,10 +89,10 @@ struct SsdParams {
   float* hand;                 // workspace: [batch][d_inner][N] the state at the end of the first half
   int64_t batch, L, d_inner;
   int heads, N;
-  int sms;                     // SMs of the device (the launch picks one or two time halves)
+  int sms;                     // SMs of the device (the launch picks the number of time parts)
 };
 int ssd_head_dim();
-// Workspace of ssm_ssd_fwd: status word, chunk Gram matrices, the halves' flags and hand-over
+// Workspace of ssm_ssd_fwd: status word, chunk Gram matrices, the time parts' flags and hand-over
 // states.
 size_t ssd_workspace_bytes(int64_t batch, int64_t L, int64_t d_inner, int N);
 size_t ssd_flags_offset(int64_t batch, int64_t L);

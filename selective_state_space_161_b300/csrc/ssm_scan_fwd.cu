@@ -858,10 +858,10 @@ bool plan_scan_fwd(int64_t batch, int64_t L, int64_t d_inner, int d_state, bool 
   int64_t G = 1;
   if (per_chunk > 0 && per_chunk < slots) G = slots / per_chunk;
   // One wave that does not spread evenly over the SMs (some hold one CTA more than others, and
-  // those set the time): two chunks of half the sequence.  Two chunks need no aggregate pass
-  // (the second waits for the first's end state), so the work is unchanged, and the halves
-  // spread over the SMs as the first ones finish (measured on B300 at 8 x 2048 x 5120 x 16,
-  // 640 CTAs in 740 slots: 0.438 ms against 0.476 in one chunk).
+  // those set the time): two chunks.  Two chunks need no aggregate pass (the second waits for
+  // the first's end state), so the work is unchanged, and the pieces spread over the SMs as
+  // the first ones finish (measured on B300 at 8 x 2048 x 5120 x 16, 640 CTAs in 740 slots:
+  // 0.438 ms against 0.476 in one chunk).
   // The four-lane plain and checkpoint kernels go one step further there: three equal chunks
   // as a chain, each continuing from its predecessor's end state, with no aggregate pass at
   // all (0.428 ms against 0.438 for the two-chunk plan, same binary and box); the fused conv

@@ -498,7 +498,7 @@ static cudaError_t launch_ssd_n(const SsdParams& p, cudaStream_t s) {
   int per_sm = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ssd_fused_kernel<N>, kSsdThreads, smem);
   if (e != cudaSuccess) return e;
-  // Two time halves unless the chains already spread evenly: whole waves of resident CTAs, or
+  // Two time parts unless the chains already spread evenly: whole waves of resident CTAs, or
   // one wave with the same number of CTAs on every SM (measured on B300 at 8 x 2048 x 5120 x
   // 128, 640 chains in 444 slots: see the design notes).
   const int64_t chains = p.batch * p.heads;
