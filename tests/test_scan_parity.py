@@ -71,6 +71,20 @@ def test_optional_operands(flags):
     _check(w, raw, **flags)
 
 
+@pytest.mark.parametrize("lanes", ["1", "4"])
+def test_positive_and_mixed_A(lanes, monkeypatch):
+    """A is taken as given: positive entries (a growing state, exp(delta A) > 1) and a mix of
+    signs and magnitudes per channel, over a sequence short enough to stay finite, and over
+    several time chunks so that the look-back folds exp(A sum delta) > 1 as well."""
+    monkeypatch.setenv("SSM_SCAN_LANES", lanes)
+    monkeypatch.setenv("SSM_SCAN_CHUNKS", "4")
+    w, raw = _random_case(2, 300, 64, 16, False, seed=211)
+    r = np.random.default_rng(211)
+    raw["A"] = r.uniform(-3.0, 0.05, size=raw["A"].shape).astype(np.float32)
+    raw["A"][:8] = np.abs(raw["A"][:8]) * 0.02 + 0.01  # eight channels with every A positive
+    _check(w, raw, name=f"scan 2x300x64x16 fp32, mixed-sign A, {lanes} lane(s)")
+
+
 @pytest.mark.parametrize("bf16", [False, True])
 def test_many_time_chunks_ragged(bf16):
     # 8 channels and 5000 steps: the GPU is filled by cutting time into many chunks
