@@ -55,7 +55,7 @@ def test_backward_long_sequence_few_channels():
     _run(1, 5000, 32, 16, False, seed=12, with_h0=True, with_dlast=True)
 
 
-@pytest.mark.parametrize("d_state", [1, 3, 8])
+@pytest.mark.parametrize("d_state", [1, 3, 5, 8, 12, 16])
 def test_backward_small_states_ragged(d_state):
     _run(3, 77, 40, d_state, False, seed=13 + d_state, with_dlast=True)
 
